@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of the forward 2-D convolution library on one or more GPUs.
+
+Workload (one "step"): the 4-layer MSCRED signature-matrix encoder in fp32
+NCHW on a batch of 256 time steps of 3x30x30 signature matrices
+(3->32 3x3 s1p1, 32->64 3x3 s2p1, 64->128 2x2 s2p1, 128->256 2x2 s2p0, each
+with bias, each layer fed by the previous one).  Metric: conv2d forward
+TFLOPS = sum over layers of 2*N*K*P*Q*C*R*S / time, plus the roofline
+fraction of the dominant kernel and the extra workspace (always 0 bytes).
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream; L2 is flushed (a 256 MiB write) before every timed step,
+outside its events.  Barrier + synchronize on both sides of the timed region;
+the slowest rank's time is reported.  With --gpus N > 1 (torchrun) every rank
+runs an independent replica of the workload (the layer needs no exchange),
+so the total work grows with N ("weak" scaling).
+
+The same JSON line also carries the tensor-core layers (fp16/bf16 NHWC),
+each timed alone, with their own roofline fractions.
+
+--impl reference times the fp64 CPU oracle on the same workload (a bounded
+sample of it) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "conv2d fwd TFLOPS (2·NKPQCRS/t) and % of GB300 roofline; extra workspace bytes"
+WORKLOAD = "mscred_encoder_4layer_f32_nchw_n256_c3_30x30"
+L2_FLUSH_BYTES = 256 << 20
+SMS = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except OSError:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def fp32_alu_peak_tflops():
+    """FFMA peak from unit counts and the maximum SM clock: SMs x 128 lanes x 2 x f."""
+    return SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+
+def encoder_setup(device):
+    from cnn_convolution_gb300 import conv2d, workloads as wl
+    x = wl.mscred_encoder_input(256)
+    params = wl.mscred_encoder_params()
+    descs, ws, bs, outs = [], [], [], []
+    for spec, (w, b) in zip(wl.MSCRED_ENCODER, params):
+        d = conv2d.Conv2dDesc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S,
+                              spec.stride, spec.pad, spec.dil, torch.float32, "NCHW")
+        descs.append(d)
+        ws.append(w.to(device))
+        bs.append(b.to(device))
+        outs.append(torch.empty(d.y_shape(), dtype=torch.float32, device=device))
+    flops = []
+    for spec, d in zip(wl.MSCRED_ENCODER, descs):
+        P, Q = d.output_dims()
+        flops.append(2.0 * spec.N * spec.K * P * Q * spec.C * spec.R * spec.S)
+    return wl.MSCRED_ENCODER, x, descs, ws, bs, outs, flops
+
+
+def layer_bytes(spec, P, Q):
+    elt = {"f32": 4, "f16": 2, "bf16": 2}[spec.dtype]
+    n = (spec.N * spec.C * spec.H * spec.W + spec.K * spec.C * spec.R * spec.S +
+         (spec.K if spec.bias else 0) + spec.N * spec.K * P * Q)
+    return n * elt
+
+
+def run_encoder(descs, x_dev, ws, bs, outs, events=None):
+    cur = x_dev
+    for i, d in enumerate(descs):
+        if events is not None:
+            events[i].record()
+        d.forward(cur, ws[i], bs[i], y=outs[i])
+        cur = outs[i]
+    if events is not None:
+        events[len(descs)].record()
+    return cur
+
+
+def bench_main(args):
+    rank, world, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    from cnn_convolution_gb300 import conv2d
+    conv2d.load()
+    peaks, peak_src = load_peaks()
+
+    specs, x_host, descs, ws, bs, outs, flops = encoder_setup(device)
+    x_dev = x_host.to(device)
+    step_flops = sum(flops)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        run_encoder(descs, x_dev, ws, bs, outs)
+    torch.cuda.synchronize()
+
+    n_layers = len(descs)
+    step_ms, layer_ms = [], [[] for _ in range(n_layers)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(device.index) as clk:
+        t_wall0 = time.perf_counter()
+        evs_all = []
+        for _ in range(args.steps):
+            flush.zero_()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_layers + 1)]
+            run_encoder(descs, x_dev, ws, bs, outs, evs)
+            evs_all.append(evs)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    for evs in evs_all:
+        step_ms.append(evs[0].elapsed_time(evs[-1]))
+        for i in range(n_layers):
+            layer_ms[i].append(evs[i].elapsed_time(evs[i + 1]))
+    local_ms = statistics.mean(step_ms)
+    ms = max_over_ranks(local_ms, world)
+    value = step_flops * world / (ms * 1e-3) / 1e12
+
+    # per-layer roofline; the dominant kernel is the layer with the largest time
+    alu_peak = fp32_alu_peak_tflops()
+    layers = []
+    for i, (spec, d) in enumerate(zip(specs, descs)):
+        P, Q = d.output_dims()
+        t = statistics.mean(layer_ms[i])
+        tf = flops[i] / (t * 1e-3) / 1e12
+        gbs = layer_bytes(spec, P, Q) / (t * 1e-3) / 1e9
+        layers.append({"layer": spec.name, "plan": d.plan(), "ms": round(t, 5),
+                       "tflops": round(tf, 3), "alu_frac": round(tf / alu_peak, 4),
+                       "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)})
+    dom = max(range(n_layers), key=lambda i: statistics.mean(layer_ms[i]))
+    dom_t = statistics.mean(layer_ms[dom])
+    achieved = flops[dom] / (dom_t * 1e-3) / 1e12
+    roofline = {"kernel": specs[dom].name, "bound": "alu", "achieved": round(achieved, 3),
+                "peak": round(alu_peak, 2), "unit": "TFLOP/s", "frac": round(achieved / alu_peak, 4),
+                "traffic": None,
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz"}
+
+    # end to end through the C ABI: pinned host x -> device, 4 layers, y -> pinned host
+    x_pin = x_host.pin_memory()
+    y_pin = torch.empty(outs[-1].shape, dtype=torch.float32).pin_memory()
+    x_buf = torch.empty_like(x_dev)
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        x_buf.copy_(x_pin, non_blocking=True)
+        run_encoder(descs, x_buf, ws, bs, outs)
+        y_pin.copy_(outs[-1], non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_t = max_over_ranks(statistics.mean(e2e_ms), world)
+    e2e = {"value": round(step_flops * world / (e2e_t * 1e-3) / 1e12, 4), "unit": "TFLOPS",
+           "ms_per_step": round(e2e_t, 5),
+           "h2d_bytes_per_step": x_pin.numel() * 4, "d2h_bytes_per_step": y_pin.numel() * 4}
+
+    extra = []
+    if not args.no_tensor_core and rank == 0:
+        extra = tensor_core_layers(device, peaks, flush, iters=max(5, args.steps))
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x_host, [(w.cpu(), b.cpu()) for w, b in zip(ws, bs)], specs, flops)
+
+    clocks = clk.summary()
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 4), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded random-walk signature matrices; Kaiming-uniform weights)",
+            "config": {"workload": WORKLOAD, "global_batch": 256 * world, "layers": 4,
+                       "layout": "NCHW", "l2": "flushed before every timed step (256 MiB write)",
+                       "parallelism": "replicas" if world > 1 else "single_gpu"},
+            "workspace_bytes": 0,
+            "roofline": roofline,
+            "layers": layers,
+            "e2e": e2e,
+            "gpu_launches": n_layers * args.steps,
+            "clocks": clocks,
+            "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
+                      "bf16_tflops": peaks["bf16_tflops"], "fp32_alu_tflops": round(alu_peak, 2)},
+            "wall_s_timed_region": round(t_wall, 4),
+            "tensor_core_layers": extra,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def time_layer(d, x, w, b, y, flush, iters, warm=3):
+    for _ in range(warm):
+        d.forward(x, w, b, y=y)
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.forward(x, w, b, y=y)
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts), min(ts)
+
+
+def tensor_core_layers(device, peaks, flush, iters=10, names=None):
+    """Time each fp16/bf16 NHWC layer alone (L2 flushed before each launch)."""
+    from cnn_convolution_gb300 import conv2d, workloads as wl
+    res = []
+    tc_peak = peaks["bf16_tflops"]
+    for spec in wl.TENSOR_CORE_WORKLOADS:
+        if names and spec.name not in names:
+            continue
+        x, w, b = wl.workload_inputs(spec)
+        d = conv2d.Conv2dDesc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S,
+                              spec.stride, spec.pad, spec.dil, spec.torch_dtype, spec.layout)
+        xd, wd = x.to(device), w.to(device)
+        bd = None if b is None else b.to(device)
+        y = torch.empty(d.y_shape(), dtype=spec.torch_dtype, device=device)
+        med, mn = time_layer(d, xd, wd, bd, y, flush, iters)
+        P, Q = d.output_dims()
+        fl = 2.0 * spec.N * spec.K * P * Q * spec.C * spec.R * spec.S
+        by = layer_bytes(spec, P, Q)
+        tf = fl / (med * 1e-3) / 1e12
+        gbs = by / (med * 1e-3) / 1e9
+        roof_t = max(fl / (tc_peak * 1e12), by / (peaks["hbm_gbs"] * 1e9)) * 1e3
+        bound = "tensor" if fl / (tc_peak * 1e12) >= by / (peaks["hbm_gbs"] * 1e9) else "hbm"
+        res.append({"layer": spec.name, "plan": d.plan(), "ms_median": round(med, 5),
+                    "ms_min": round(mn, 5), "tflops": round(tf, 2), "hbm_gbs": round(gbs, 1),
+                    "bound": bound, "roofline_frac": round(roof_t / med, 4),
+                    "tensor_frac": round(tf / tc_peak, 4), "workspace_bytes": d.workspace_bytes()})
+        del xd, wd, bd, y
+    return res
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def cpu_baseline(x, params, specs, flops, budget_s=10.0):
+    """The fp64 oracle on the host cores: whole encoder steps, repeated within a budget."""
+    import oracle
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        cur = x
+        for spec, (w, b) in zip(specs, params):
+            y, _ = oracle.conv2d(cur, w, b, spec.stride, spec.pad, spec.dil)
+            cur = y
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 20:
+            break
+    per = el / reps
+    return {"value": round(sum(flops) / per / 1e12, 6), "unit": "TFLOPS", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{reps} full encoder steps (batch 256, 4 layers), fp64 direct loop, "
+                      f"{per:.3f} s per step"}
+
+
+def reference_main(args):
+    """--impl reference: the oracle on the host cores, rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from cnn_convolution_gb300 import workloads as wl
+    oracle.build()
+    x = wl.mscred_encoder_input(256)
+    params = wl.mscred_encoder_params()
+    specs = wl.MSCRED_ENCODER
+    flops = []
+    h = 30
+    for spec in specs:
+        P = oracle.out_extent(spec.H, spec.R, spec.stride, spec.pad, spec.dil)
+        Q = oracle.out_extent(spec.W, spec.S, spec.stride, spec.pad, spec.dil)
+        flops.append(2.0 * spec.N * spec.K * P * Q * spec.C * spec.R * spec.S)
+    # each step: a bounded sample of the batch (n_img images) through the 4 layers
+    n_img = int(os.environ.get("CONV2D_REF_IMAGES", "256"))
+    xs = x[:n_img]
+    sample_flops = sum(flops) * n_img / 256
+    for _ in range(args.warmup):
+        pass   # the oracle has nothing to warm up
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        cur = xs
+        for spec, (w, b) in zip(specs, params):
+            cur, _ = oracle.conv2d(cur, w, b, spec.stride, spec.pad, spec.dil)
+        times.append(time.perf_counter() - t0)
+    per = statistics.mean(times)
+    value = sample_flops / per / 1e12
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "global_batch": 256, "layers": 4, "layout": "NCHW",
+                      "parallelism": "host cores"},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS",
+                            "cores": oracle.max_threads(), "kind": "oracle",
+                            "sample": f"{n_img} of 256 images per step through all 4 layers"},
+           "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-tensor-core", action="store_true", help="skip the fp16/bf16 layers")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layer", default=None,
+                    help="time one named fp16/bf16 layer only (for profiling) and print its line")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and args.layer is None:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return reference_main(args)
+    if args.layer:
+        from cnn_convolution_gb300 import conv2d
+        conv2d.load()
+        peaks, _ = load_peaks()
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        res = tensor_core_layers(torch.device("cuda", 0), peaks, flush, iters=args.steps,
+                                 names={args.layer})
+        print(json.dumps({"layers": res}))
+        return 0
+    return bench_main(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

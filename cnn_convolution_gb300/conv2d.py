@@ -1,0 +1,208 @@
+"""Thin Python binding of libconv2d_gb300 (argument marshalling only).
+
+Every step of the convolution runs in the library's CUDA kernels; this
+module only checks that torch tensors are dense CUDA tensors of one dtype,
+passes their device pointers and the current CUDA stream through the C ABI
+declared in include/conv2d.h, and turns status codes into exceptions.  There
+is no fallback: if the library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+F32, F16, BF16 = 0, 1, 2
+NCHW, NHWC = 0, 1
+ALGO_AUTO, ALGO_CUDA_CORE, ALGO_TENSOR_CORE = 0, 1, 2
+
+_DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+_LAYOUT_CODE = {"NCHW": NCHW, "NHWC": NHWC}
+_ALGO_CODE = {"auto": ALGO_AUTO, "cuda_core": ALGO_CUDA_CORE, "tensor_core": ALGO_TENSOR_CORE}
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "misaligned pointer",
+          4: "CUDA error", 5: "kernel barrier wait timed out", 6: "internal error"}
+
+
+class Conv2dError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, 'unknown')} (status {code})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Load the compiled library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or _build.LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"{p} is missing: build it with cnn_convolution_gb300.build.build() "
+                    "(there is no CPU fallback)")
+            lib = ctypes.CDLL(p)
+            _declare(lib)
+            _lib = lib
+    return _lib
+
+
+def _declare(lib):
+    c_int, vp, i32 = ctypes.c_int, ctypes.c_void_p, ctypes.c_int
+    lib.conv2d_desc_create.restype = c_int
+    lib.conv2d_desc_create.argtypes = [ctypes.POINTER(vp)] + [i32] * 10 + [c_int, c_int]
+    lib.conv2d_desc_destroy.restype = c_int
+    lib.conv2d_desc_destroy.argtypes = [vp]
+    lib.conv2d_output_dims.restype = c_int
+    lib.conv2d_output_dims.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.conv2d_workspace_bytes.restype = c_int
+    lib.conv2d_workspace_bytes.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
+    lib.conv2d_desc_set_algo.restype = c_int
+    lib.conv2d_desc_set_algo.argtypes = [vp, c_int]
+    lib.conv2d_desc_plan.restype = c_int
+    lib.conv2d_desc_plan.argtypes = [vp, ctypes.c_char_p, ctypes.c_size_t]
+    lib.conv2d_forward_desc.restype = c_int
+    lib.conv2d_forward_desc.argtypes = [vp, vp, vp, vp, vp, vp]
+    lib.conv2d_forward.restype = c_int
+    lib.conv2d_forward.argtypes = [vp, vp, vp, vp] + [i32] * 10 + [c_int, c_int, vp]
+    lib.conv2d_status_string.restype = ctypes.c_char_p
+    lib.conv2d_status_string.argtypes = [c_int]
+    lib.conv2d_get_device_status.restype = c_int
+    lib.conv2d_get_device_status.argtypes = []
+    lib.conv2d_version.restype = c_int
+    lib.conv2d_version.argtypes = []
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise Conv2dError(code, what)
+
+
+class Conv2dDesc:
+    """A layer descriptor (sizes, dtype, layout) owned by this object."""
+
+    def __init__(self, N, C, H, W, K, R, S, stride=1, pad=0, dil=1,
+                 dtype: torch.dtype = torch.float32, layout: str = "NCHW"):
+        self._lib = load()
+        self.sizes = (N, C, H, W, K, R, S, stride, pad, dil)
+        self.dtype, self.layout = dtype, layout
+        h = ctypes.c_void_p()
+        _check(self._lib.conv2d_desc_create(ctypes.byref(h), N, C, H, W, K, R, S, stride, pad, dil,
+                                            _DTYPE_CODE[dtype], _LAYOUT_CODE[layout]),
+               "conv2d_desc_create")
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.conv2d_desc_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def output_dims(self) -> Tuple[int, int]:
+        P, Q = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.conv2d_output_dims(self._h, ctypes.byref(P), ctypes.byref(Q)),
+               "conv2d_output_dims")
+        return P.value, Q.value
+
+    def workspace_bytes(self) -> int:
+        b = ctypes.c_size_t()
+        _check(self._lib.conv2d_workspace_bytes(self._h, ctypes.byref(b)), "conv2d_workspace_bytes")
+        return b.value
+
+    def set_algo(self, algo: str):
+        _check(self._lib.conv2d_desc_set_algo(self._h, _ALGO_CODE[algo]), "conv2d_desc_set_algo")
+
+    def plan(self) -> str:
+        buf = ctypes.create_string_buffer(256)
+        _check(self._lib.conv2d_desc_plan(self._h, buf, 256), "conv2d_desc_plan")
+        return buf.value.decode()
+
+    def y_shape(self):
+        N, C, H, W, K = self.sizes[:5]
+        P, Q = self.output_dims()
+        return (N, K, P, Q) if self.layout == "NCHW" else (N, P, Q, K)
+
+    def forward(self, x, w, bias=None, y=None, stream=None):
+        if y is None:
+            y = torch.empty(self.y_shape(), dtype=self.dtype, device=x.device)
+        _validate(x, w, bias, y, self.dtype)
+        st = _stream_handle(stream, x.device)
+        _check(self._lib.conv2d_forward_desc(self._h, x.data_ptr(), w.data_ptr(),
+                                             None if bias is None else bias.data_ptr(),
+                                             y.data_ptr(), st), "conv2d_forward_desc")
+        return y
+
+
+def _validate(x, w, bias, y, dtype):
+    for name, t in (("x", x), ("w", w), ("y", y)) + ((("bias", bias),) if bias is not None else ()):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def output_dims(H, W, R, S, stride=1, pad=0, dil=1) -> Tuple[int, int]:
+    d = Conv2dDesc(1, 1, H, W, 1, R, S, stride, pad, dil)
+    return d.output_dims()
+
+
+def forward(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None,
+            stride: int = 1, pad: int = 0, dil: int = 1, layout: str = "NCHW",
+            y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y = conv2d(x, w) + bias through conv2d_forward (plan chosen per shape).
+
+    layout "NCHW": x [N,C,H,W], w [K,C,R,S] -> y [N,K,P,Q];
+    layout "NHWC": x [N,H,W,C], w [K,R,S,C] -> y [N,P,Q,K].
+    """
+    lib = load()
+    if layout == "NCHW":
+        N, C, H, W = x.shape
+        K, C2, R, S = w.shape
+    elif layout == "NHWC":
+        N, H, W, C = x.shape
+        K, R, S, C2 = w.shape
+    else:
+        raise ValueError(layout)
+    if C2 != C:
+        raise ValueError("x and w disagree on C")
+    if y is None:
+        d = Conv2dDesc(N, C, H, W, K, R, S, stride, pad, dil, x.dtype, layout)
+        y = torch.empty(d.y_shape(), dtype=x.dtype, device=x.device)
+    _validate(x, w, bias, y, x.dtype)
+    st = _stream_handle(stream, x.device)
+    _check(lib.conv2d_forward(x.data_ptr(), w.data_ptr(),
+                              None if bias is None else bias.data_ptr(), y.data_ptr(),
+                              N, C, H, W, K, R, S, stride, pad, dil,
+                              _DTYPE_CODE[x.dtype], _LAYOUT_CODE[layout], st), "conv2d_forward")
+    return y
+
+
+def get_device_status() -> int:
+    return load().conv2d_get_device_status()
+
+
+def version() -> int:
+    return load().conv2d_version()

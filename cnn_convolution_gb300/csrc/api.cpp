@@ -1,0 +1,374 @@
+// Host side of the C ABI: argument validation, output shape, the per-shape
+// kernel chooser, the plan cache and the launches.
+//
+// The checks follow the integration concerns listed in "GPU-Accelerating
+// MSCRED with CUDA, im2col, GEMM, and a Custom PyTorch Extension" (section
+// "Integrating the CUDA Implementation with PyTorch": tensor dimensions,
+// device placement, data types, contiguity, error handling): every one of
+// them is decided here, before anything is launched, and reported as a
+// status code.  The chooser is the per-shape counterpart of the page's
+// tile/thread-block tuning (sections "Global Memory and Shared Memory" and
+// "Engineering Challenges", kernel configuration).
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <string>
+#include <tuple>
+
+#include "internal.h"
+
+using namespace conv2d;
+
+struct conv2d_desc {
+    Shape s;
+    conv2d_algo_t algo = CONV2D_ALGO_AUTO;
+};
+
+namespace {
+
+constexpr int64_t kMaxElems = (int64_t)1 << 40;
+
+int elt_size(conv2d_dtype_t d) { return d == CONV2D_F32 ? 4 : 2; }
+
+int64_t out_extent(int64_t in, int64_t k, int64_t st, int64_t pad, int64_t dil) {
+    const int64_t span = in + 2 * pad - dil * (k - 1) - 1;
+    return span < 0 ? 0 : span / st + 1;
+}
+
+conv2d_status_t make_shape(Shape *s, int N, int C, int H, int W, int K, int R, int S, int stride,
+                           int pad, int dil, conv2d_dtype_t dtype, conv2d_layout_t layout) {
+    if (N < 1 || C < 1 || H < 1 || W < 1 || K < 1 || R < 1 || S < 1 || stride < 1 || dil < 1 ||
+        pad < 0)
+        return CONV2D_ERR_INVALID_ARG;
+    if (dtype != CONV2D_F32 && dtype != CONV2D_F16 && dtype != CONV2D_BF16)
+        return CONV2D_ERR_INVALID_ARG;
+    if (layout != CONV2D_NCHW && layout != CONV2D_NHWC) return CONV2D_ERR_INVALID_ARG;
+    const int64_t P = out_extent(H, R, stride, pad, dil);
+    const int64_t Q = out_extent(W, S, stride, pad, dil);
+    if (P < 1 || Q < 1 || P > INT32_MAX || Q > INT32_MAX) return CONV2D_ERR_INVALID_ARG;
+    const int64_t xe = (int64_t)N * C * H * W, we = (int64_t)K * C * R * S,
+                  ye = (int64_t)N * K * P * Q;
+    if (xe >= kMaxElems || we >= kMaxElems || ye >= kMaxElems) return CONV2D_ERR_INVALID_ARG;
+    s->N = N; s->C = C; s->H = H; s->W = W; s->K = K; s->R = R; s->S = S;
+    s->stride = stride; s->pad = pad; s->dil = dil;
+    s->P = (int)P; s->Q = (int)Q;
+    s->dtype = dtype; s->layout = layout;
+    s->M = (int64_t)N * P * Q;
+    s->Kg = (int64_t)C * R * S;
+    s->elt = elt_size(dtype);
+    return CONV2D_OK;
+}
+
+// ------------------------------------------------------------ device info
+
+struct DevInfo {
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;
+};
+
+std::mutex g_dev_mu;
+std::map<int, DevInfo> g_dev;
+
+conv2d_status_t device_info(int *dev_out, DevInfo *info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    auto it = g_dev.find(dev);
+    if (it == g_dev.end()) {
+        DevInfo d;
+        int v = 0;
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return CONV2D_ERR_CUDA;
+        d.smem_optin = (size_t)v;
+        it = g_dev.emplace(dev, d).first;
+    }
+    *dev_out = dev;
+    *info = it->second;
+    return CONV2D_OK;
+}
+
+// ------------------------------------------------------------ chooser
+
+// Estimated time (arbitrary units) of a CUDA-core tile on this layer: the
+// busiest SM's share of tile work divided by a per-tile FFMA efficiency that
+// also falls when too few warps are resident to hide latency.
+double cc_cost(const Shape &s, const CudaCoreTile &t, int sms, size_t smem) {
+    const int64_t tiles = ((s.M + t.BM - 1) / t.BM) * ((s.K + t.BN - 1) / t.BN);
+    const int64_t kt = (s.Kg + t.BK - 1) / t.BK;
+    const double work = (double)t.BM * t.BN * kt * t.BK;       // FMAs per tile incl. padding
+    int occ = 2048 / t.threads;
+    const int regs = t.TM * t.TN + 48;                          // rough registers per thread
+    occ = std::min(occ, 65536 / (t.threads * regs));
+    occ = std::min(occ, (int)((228 * 1024) / (smem + 1024)));
+    occ = std::max(occ, 1);
+    const double per_sm_tiles = (double)((tiles + sms - 1) / sms);
+    const double resident = std::min<double>(per_sm_tiles, occ);
+    const double warps = resident * t.threads / 32.0;
+    // FFMA share of the inner loop: TM*TN FMAs per (TM+TN)/4 shared loads.
+    const double inner = (double)(t.TM * t.TN) / (t.TM * t.TN + (t.TM + t.TN) / 4.0 + 2.0);
+    const double latency = std::min(1.0, warps / 16.0);
+    const double rate = 128.0 * inner * (0.25 + 0.75 * latency);
+    return per_sm_tiles * work / rate;
+}
+
+conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
+    if (!cc_shape_ok(s)) return CONV2D_ERR_UNSUPPORTED;
+    int forced = -1;
+    if (const char *e = std::getenv("CONV2D_CC_TILE")) forced = std::atoi(e);
+    double best = 1e300;
+    int best_id = -1;
+    for (int id = 0; id < cc_num_tiles(); ++id) {
+        const CudaCoreTile t = cc_tile(id);
+        const size_t smem = cc_smem_bytes(s, t);
+        if (smem > d.smem_optin) continue;
+        if (forced >= 0 && id != forced) continue;
+        const double c = cc_cost(s, t, d.sm_count, smem);
+        if (c < best) { best = c; best_id = id; }
+    }
+    if (best_id < 0) return CONV2D_ERR_UNSUPPORTED;
+    p->algo = Algo::CudaCore;
+    p->cc = cc_tile(best_id);
+    p->smem_bytes = cc_smem_bytes(s, p->cc);
+    p->grid = (int)(((s.M + p->cc.BM - 1) / p->cc.BM) * ((s.K + p->cc.BN - 1) / p->cc.BN));
+    p->sm_count = d.sm_count;
+    return CONV2D_OK;
+}
+
+conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) return CONV2D_ERR_UNSUPPORTED;
+    // Output-channel tile: the widest of 256/128/64 that wastes little of K,
+    // then shrink while the grid would leave most SMs idle.
+    int bn = s.K >= 256 ? 256 : (s.K > 64 ? 128 : 64);
+    while (bn > 64 && (s.K % bn) != 0 && (s.K % (bn / 2)) == 0) bn /= 2;
+    auto tiles_for = [&](int b) { return ((s.M + 127) / 128) * ((s.K + b - 1) / b); };
+    while (bn > 64 && tiles_for(bn) < d.sm_count) bn /= 2;
+    if (const char *e = std::getenv("CONV2D_TC_BN")) bn = std::atoi(e);
+    TcTile t;
+    t.BN = bn;
+    t.tma_store = false;
+    const size_t stage = (size_t)128 * 64 * 2 + (size_t)bn * 64 * 2;
+    const size_t budget = d.smem_optin - 4096;
+    t.stages = (int)std::min<size_t>(8, budget / stage);
+    if (const char *e = std::getenv("CONV2D_TC_STAGES")) t.stages = std::atoi(e);
+    if (t.stages < 2) return CONV2D_ERR_UNSUPPORTED;
+    p->algo = Algo::TensorCore;
+    p->tc = t;
+    p->smem_bytes = tc_smem_bytes(t);
+    if (p->smem_bytes > d.smem_optin) return CONV2D_ERR_UNSUPPORTED;
+    const int64_t tiles = tiles_for(bn);
+    p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
+    p->sm_count = d.sm_count;
+    return CONV2D_OK;
+}
+
+bool aligned16(const Tensors &t) {
+    auto a = [](const void *p) { return ((uintptr_t)p & 15) == 0; };
+    return a(t.x) && a(t.w) && a(t.y) && (t.bias == nullptr || ((uintptr_t)t.bias & 1) == 0);
+}
+
+// Plans are cached per (device, shape, dtype, layout, algo, alignment class).
+using PlanKey = std::tuple<int, int, int, int, int, int, int, int, int, int, int, int, int, int, int>;
+std::mutex g_plan_mu;
+std::map<PlanKey, Plan> g_plans;
+
+conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, Plan *out) {
+    int dev = 0;
+    DevInfo d;
+    conv2d_status_t st = device_info(&dev, &d);
+    if (st != CONV2D_OK) return st;
+    const bool al = t == nullptr || aligned16(*t);
+    const PlanKey key{dev, s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
+                      (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0};
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) { *out = it->second; return CONV2D_OK; }
+    }
+    Plan p{};
+    const bool tc_ok = tc_shape_ok(s, t);
+    if (algo == CONV2D_ALGO_TENSOR_CORE) {
+        if (!tc_ok) return CONV2D_ERR_UNSUPPORTED;
+        st = choose_tc(s, d, &p);
+    } else if (algo == CONV2D_ALGO_CUDA_CORE) {
+        st = choose_cc(s, d, &p);
+    } else {
+        st = tc_ok ? choose_tc(s, d, &p) : CONV2D_ERR_UNSUPPORTED;
+        if (st != CONV2D_OK) st = choose_cc(s, d, &p);
+    }
+    if (st != CONV2D_OK) return st;
+    if (std::getenv("CONV2D_LOG")) {
+        if (p.algo == Algo::TensorCore)
+            std::fprintf(stderr, "[conv2d] tensor-core BM=128 BN=%d stages=%d grid=%d smem=%zu\n",
+                         p.tc.BN, p.tc.stages, p.grid, p.smem_bytes);
+        else
+            std::fprintf(stderr, "[conv2d] cuda-core tile=%d (%dx%dx%d, %dx%d/thread) grid=%d smem=%zu\n",
+                         p.cc.id, p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.grid, p.smem_bytes);
+    }
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    g_plans[key] = p;
+    *out = p;
+    return CONV2D_OK;
+}
+
+// ------------------------------------------------------------ pointer checks
+
+// The pointer must be device (or managed) memory of `dev`; returns false for
+// host memory, which a kernel could not (or should not) dereference.
+bool is_device_ptr(const void *p, int dev) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice) return a.device == dev;
+    if (a.type == cudaMemoryTypeManaged) return true;
+    return false;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b) return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+conv2d_status_t check_tensors(const Shape &s, const Tensors &t, cudaStream_t stream) {
+    if (!t.x || !t.w || !t.y) return CONV2D_ERR_INVALID_ARG;
+    const uintptr_t mask = (uintptr_t)s.elt - 1;
+    if (((uintptr_t)t.x & mask) || ((uintptr_t)t.w & mask) || ((uintptr_t)t.y & mask) ||
+        (t.bias && ((uintptr_t)t.bias & mask)))
+        return CONV2D_ERR_MISALIGNED;
+    const size_t xb = (size_t)s.x_elems() * s.elt, wb = (size_t)s.w_elems() * s.elt,
+                 yb = (size_t)s.y_elems() * s.elt, bb = (size_t)s.K * s.elt;
+    if (overlaps(t.y, yb, t.x, xb) || overlaps(t.y, yb, t.w, wb) ||
+        (t.bias && overlaps(t.y, yb, t.bias, bb)))
+        return CONV2D_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (stream) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) {
+            cudaGetLastError();
+            return CONV2D_ERR_INVALID_ARG;
+        }
+        if (sdev != dev) return CONV2D_ERR_INVALID_ARG;
+    }
+    if (!is_device_ptr(t.x, dev) || !is_device_ptr(t.w, dev) || !is_device_ptr(t.y, dev) ||
+        (t.bias && !is_device_ptr(t.bias, dev)))
+        return CONV2D_ERR_INVALID_ARG;
+    return CONV2D_OK;
+}
+
+conv2d_status_t run(const Shape &s, conv2d_algo_t algo, const Tensors &t, cudaStream_t stream) {
+    conv2d_status_t st = check_tensors(s, t, stream);
+    if (st != CONV2D_OK) return st;
+    Plan p;
+    st = get_plan(s, algo, &t, &p);
+    if (st != CONV2D_OK) return st;
+    if (p.algo == Algo::TensorCore) return tc_launch(s, p, t, stream);
+    return cc_launch(s, p, t, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+conv2d_status_t conv2d_desc_create(conv2d_desc_t *out, int N, int C, int H, int W, int K, int R,
+                                   int S, int stride, int pad, int dil, conv2d_dtype_t dtype,
+                                   conv2d_layout_t layout) {
+    if (!out) return CONV2D_ERR_INVALID_ARG;
+    Shape s;
+    conv2d_status_t st = make_shape(&s, N, C, H, W, K, R, S, stride, pad, dil, dtype, layout);
+    if (st != CONV2D_OK) return st;
+    conv2d_desc *d = new (std::nothrow) conv2d_desc;
+    if (!d) return CONV2D_ERR_INTERNAL;
+    d->s = s;
+    *out = d;
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_desc_destroy(conv2d_desc_t desc) {
+    delete desc;
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_output_dims(conv2d_desc_t desc, int *P, int *Q) {
+    if (!desc || !P || !Q) return CONV2D_ERR_INVALID_ARG;
+    *P = desc->s.P;
+    *Q = desc->s.Q;
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_workspace_bytes(conv2d_desc_t desc, size_t *bytes) {
+    if (!desc || !bytes) return CONV2D_ERR_INVALID_ARG;
+    *bytes = 0;
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_desc_set_algo(conv2d_desc_t desc, conv2d_algo_t algo) {
+    if (!desc) return CONV2D_ERR_INVALID_ARG;
+    if (algo != CONV2D_ALGO_AUTO && algo != CONV2D_ALGO_CUDA_CORE && algo != CONV2D_ALGO_TENSOR_CORE)
+        return CONV2D_ERR_INVALID_ARG;
+    if (algo == CONV2D_ALGO_TENSOR_CORE && !tc_shape_ok(desc->s, nullptr))
+        return CONV2D_ERR_UNSUPPORTED;
+    if (algo == CONV2D_ALGO_CUDA_CORE && !cc_shape_ok(desc->s)) return CONV2D_ERR_UNSUPPORTED;
+    desc->algo = algo;
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
+    if (!desc || !buf || len == 0) return CONV2D_ERR_INVALID_ARG;
+    Plan p;
+    conv2d_status_t st = get_plan(desc->s, desc->algo, nullptr, &p);
+    if (st != CONV2D_OK) return st;
+    if (p.algo == Algo::TensorCore)
+        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 stages=%d grid=%d smem=%zu",
+                      p.tc.BN, p.tc.stages, p.grid, p.smem_bytes);
+    else
+        std::snprintf(buf, len, "cuda_core ffma BM=%d BN=%d BK=%d TM=%d TN=%d threads=%d grid=%d smem=%zu",
+                      p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.threads, p.grid,
+                      p.smem_bytes);
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_forward_desc(conv2d_desc_t desc, const void *x, const void *w,
+                                    const void *bias, void *y, cudaStream_t stream) {
+    if (!desc) return CONV2D_ERR_INVALID_ARG;
+    return run(desc->s, desc->algo, Tensors{x, w, bias, y}, stream);
+}
+
+conv2d_status_t conv2d_forward(const void *x, const void *w, const void *bias, void *y, int N,
+                               int C, int H, int W, int K, int R, int S, int stride, int pad,
+                               int dil, conv2d_dtype_t dtype, conv2d_layout_t layout,
+                               cudaStream_t stream) {
+    Shape s;
+    conv2d_status_t st = make_shape(&s, N, C, H, W, K, R, S, stride, pad, dil, dtype, layout);
+    if (st != CONV2D_OK) return st;
+    return run(s, CONV2D_ALGO_AUTO, Tensors{x, w, bias, y}, stream);
+}
+
+const char *conv2d_status_string(conv2d_status_t status) {
+    switch (status) {
+        case CONV2D_OK: return "ok";
+        case CONV2D_ERR_INVALID_ARG: return "invalid argument";
+        case CONV2D_ERR_UNSUPPORTED: return "unsupported configuration";
+        case CONV2D_ERR_MISALIGNED: return "misaligned pointer";
+        case CONV2D_ERR_CUDA: return "CUDA error";
+        case CONV2D_ERR_TIMEOUT: return "kernel barrier wait timed out";
+        case CONV2D_ERR_INTERNAL: return "internal error";
+    }
+    return "unknown status";
+}
+
+conv2d_status_t conv2d_get_device_status(void) { return status_read_and_clear(); }
+
+int conv2d_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,391 @@
+// CUDA-core (FFMA) implicit-GEMM convolution: every dtype and layout.
+//
+// This is the full-precision CUDA-core path of "Enabling Memory-efficient
+// Im2win Convolution with Multi-precision Support on GPU CUDA and Tensor
+// Cores" (abstract) and the shared-memory kernel of "GPU-Accelerating MSCRED
+// with CUDA, im2col, GEMM, and a Custom PyTorch Extension" (section "Global
+// Memory and Shared Memory": stage reusable tiles in shared memory and reuse
+// them across the threads of a block).  The GEMM view is the page's
+// "Output matrix = Weight matrix x im2col(Input)" (section "Transforming
+// Conv2D into im2col and GEMM"), but the im2col matrix is never built: each
+// CTA gathers the BM x BK slice of it that it needs straight from x into
+// shared memory, with zero fill for padding taps.
+//
+// GEMM view:  D[m, k] = sum_j A[m, j] * B[k, j]
+//   m = (n, p, q) flattened output pixel, k = output channel,
+//   j = reduction index; NCHW orders j as (c, r, s) (matching KCRS weights),
+//   NHWC as (r, s, c) (matching KRSC weights), so B rows are contiguous.
+//
+// Per CTA: a BM x BN output tile; per thread: TM x TN accumulators in fp32.
+// A per-layer table in shared memory maps each j to (element offset of the
+// tap relative to the window origin, r*dil, s*dil), so a gathered element
+// costs one table read, two bounds compares and one predicated load.
+// Operands are widened to fp32 on the way into shared memory; the epilogue
+// adds the bias, rounds once to the output type and stores through shared
+// memory so that global writes are coalesced.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdio>
+
+#include "internal.h"
+
+namespace conv2d {
+namespace {
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+struct CcParams {
+    const void *x, *w, *bias;
+    void *y;
+    int N, C, H, W, K, R, S, stride, pad, dil, P, Q;
+    int Kg;        // C*R*S (fits int: checked on the host)
+    int64_t M;     // N*P*Q
+};
+
+// Table entry for reduction index j: offset of x[.., c, h0+dh, w0+dw] from
+// x[.., 0, h0, w0] within one image, and the tap's (dh, dw).
+struct Tap {
+    int delta;
+    short dh, dw;
+};
+
+// Taps held in shared memory at once (32 KB); a multiple of every BK.
+constexpr int kTableChunk = 4096;
+
+template <typename T, int LAYOUT, int BM, int BN, int BK, int TM, int TN>
+struct CcCfg {
+    static constexpr int NT = (BM / TM) * (BN / TN);
+    static constexpr int TPB = NT / BM;               // threads per output row m
+    static constexpr int A_PER = BK / TPB;            // A elements per thread per tile
+    static constexpr int B_PER = (BN * BK) / NT;      // B elements per thread per tile
+    static constexpr int AS = BM + 4;                 // padded row lengths (floats)
+    static constexpr int BS = BN + 4;
+    static constexpr int TMV = TM / 4, TNV = TN / 4;  // float4 groups per thread
+    static_assert(NT % BM == 0, "one output row per thread for the gather");
+    static_assert(BK % TPB == 0, "");
+    static_assert((BN * BK) % NT == 0, "");
+    static_assert(TM % 4 == 0 && TN % 4 == 0, "");
+    static constexpr size_t tile_floats = 2 * (size_t)BK * AS + 2 * (size_t)BK * BS;
+    static constexpr size_t epi_floats =
+        LAYOUT == CONV2D_NCHW ? (size_t)BN * (BM + 1) : (size_t)BM * (BN + 1);
+    static constexpr size_t main_floats = tile_floats > epi_floats ? tile_floats : epi_floats;
+};
+
+template <typename T, int LAYOUT, int BM, int BN, int BK, int TM, int TN>
+__global__ void __launch_bounds__(CcCfg<T, LAYOUT, BM, BN, BK, TM, TN>::NT)
+cc_conv_kernel(const CcParams p) {
+    using Cfg = CcCfg<T, LAYOUT, BM, BN, BK, TM, TN>;
+    constexpr int NT = Cfg::NT, TPB = Cfg::TPB, A_PER = Cfg::A_PER, B_PER = Cfg::B_PER;
+    constexpr int AS = Cfg::AS, BS = Cfg::BS, TMV = Cfg::TMV, TNV = Cfg::TNV;
+
+    extern __shared__ __align__(16) float smem[];
+    float *As = smem;                          // [2][BK][AS]
+    float *Bs = smem + 2 * BK * AS;            // [2][BK][BS]
+    Tap *taps = reinterpret_cast<Tap *>(smem + Cfg::main_floats);   // [Kg]
+
+    const T *__restrict__ x = static_cast<const T *>(p.x);
+    const T *__restrict__ w = static_cast<const T *>(p.w);
+    const int tid = threadIdx.x;
+    const int64_t m0 = (int64_t)blockIdx.x * BM;
+    const int n0 = blockIdx.y * BN;
+    const int Kg = p.Kg;
+    const int PQ = p.P * p.Q;
+
+    // Reduction-index table, built for kTableChunk indices at a time.
+    auto build_taps = [&](int jbase) {
+        const int jend = min(Kg, jbase + kTableChunk);
+        for (int j = jbase + tid; j < jend; j += NT) {
+            int c, r, s;
+            if (LAYOUT == CONV2D_NCHW) {
+                c = j / (p.R * p.S);
+                int rs = j - c * p.R * p.S;
+                r = rs / p.S;
+                s = rs - r * p.S;
+            } else {
+                r = j / (p.S * p.C);
+                int sc = j - r * p.S * p.C;
+                s = sc / p.C;
+                c = sc - s * p.C;
+            }
+            Tap t;
+            t.dh = (short)(r * p.dil);
+            t.dw = (short)(s * p.dil);
+            t.delta = LAYOUT == CONV2D_NCHW ? (c * p.H + t.dh) * p.W + t.dw
+                                            : (t.dh * p.W + t.dw) * p.C + c;
+            taps[j - jbase] = t;
+        }
+    };
+    build_taps(0);
+
+    // This thread gathers A rows for output pixel m_ld.
+    const int ml = tid % BM;
+    const int kl0 = tid / BM;
+    const int64_t m_ld = m0 + ml;
+    const bool m_ok = m_ld < p.M;
+    int ih0 = 0, iw0 = 0;
+    int64_t xbase = 0;       // element offset of the window origin (may be "negative")
+    int64_t ybase = 0;       // NCHW: offset of y[n, 0, p, q]
+    if (m_ok) {
+        int n = (int)(m_ld / PQ);
+        int pq = (int)(m_ld - (int64_t)n * PQ);
+        int pp = pq / p.Q, qq = pq - pp * p.Q;
+        ih0 = pp * p.stride - p.pad;
+        iw0 = qq * p.stride - p.pad;
+        if (LAYOUT == CONV2D_NCHW) {
+            xbase = (int64_t)n * p.C * p.H * p.W + (int64_t)ih0 * p.W + iw0;
+            ybase = (int64_t)n * p.K * PQ + pq;
+        } else {
+            xbase = ((int64_t)n * p.H * p.W + (int64_t)ih0 * p.W + iw0) * p.C;
+        }
+    }
+    __syncthreads();
+
+    float a_reg[A_PER];
+    float b_reg[B_PER];
+
+    auto load_tile = [&](int kt) {
+        const int j0 = kt * BK;
+#pragma unroll
+        for (int i = 0; i < A_PER; ++i) {
+            const int j = j0 + kl0 + i * TPB;
+            float v = 0.f;
+            if (m_ok && j < Kg) {
+                const Tap t = taps[j % kTableChunk];
+                const int h = ih0 + t.dh, ww = iw0 + t.dw;
+                if ((unsigned)h < (unsigned)p.H && (unsigned)ww < (unsigned)p.W)
+                    v = to_f32<T>(__ldg(x + (xbase + t.delta)));
+            }
+            a_reg[i] = v;
+        }
+#pragma unroll
+        for (int i = 0; i < B_PER; ++i) {
+            const int e = tid + i * NT;
+            const int kl = e % BK, nl = e / BK;
+            const int j = j0 + kl, k = n0 + nl;
+            float v = 0.f;
+            if (j < Kg && k < p.K) v = to_f32<T>(__ldg(w + ((int64_t)k * Kg + j)));
+            b_reg[i] = v;
+        }
+    };
+    auto store_tile = [&](int buf) {
+        float *as = As + buf * BK * AS;
+        float *bs = Bs + buf * BK * BS;
+#pragma unroll
+        for (int i = 0; i < A_PER; ++i) as[(kl0 + i * TPB) * AS + ml] = a_reg[i];
+#pragma unroll
+        for (int i = 0; i < B_PER; ++i) {
+            const int e = tid + i * NT;
+            bs[(e % BK) * BS + e / BK] = b_reg[i];
+        }
+    };
+
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+    const int tx = tid % (BN / TN);
+    const int ty = tid / (BN / TN);
+    const int KT = (Kg + BK - 1) / BK;
+
+    load_tile(0);
+    store_tile(0);
+    __syncthreads();
+    for (int kt = 0; kt < KT; ++kt) {
+        const int cur = kt & 1;
+        if (kt + 1 < KT) {
+            if (((kt + 1) * BK) % kTableChunk == 0) {   // next tile starts a new table chunk
+                __syncthreads();
+                build_taps((kt + 1) * BK);
+                __syncthreads();
+            }
+            load_tile(kt + 1);
+        }
+        const float *as = As + cur * BK * AS;
+        const float *bs = Bs + cur * BK * BS;
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            float a[TM], b[TN];
+#pragma unroll
+            for (int v = 0; v < TMV; ++v) {
+                const float4 t = *reinterpret_cast<const float4 *>(as + kk * AS + v * (BM / TMV) + ty * 4);
+                a[4 * v] = t.x; a[4 * v + 1] = t.y; a[4 * v + 2] = t.z; a[4 * v + 3] = t.w;
+            }
+#pragma unroll
+            for (int v = 0; v < TNV; ++v) {
+                const float4 t = *reinterpret_cast<const float4 *>(bs + kk * BS + v * (BN / TNV) + tx * 4);
+                b[4 * v] = t.x; b[4 * v + 1] = t.y; b[4 * v + 2] = t.z; b[4 * v + 3] = t.w;
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        if (kt + 1 < KT) store_tile(cur ^ 1);
+        __syncthreads();
+    }
+
+    // Epilogue: stage the tile in shared memory, then write coalesced rows.
+    float *cs = smem;
+    const T *bias = static_cast<const T *>(p.bias);
+    T *y = static_cast<T *>(p.y);
+    if (LAYOUT == CONV2D_NCHW) {
+        // cs[nl][ml]: m contiguous, as in y[n][k][p][q].
+        constexpr int CS = BM + 1;
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const int mi = (i / 4) * (BM / TMV) + ty * 4 + (i % 4);
+                const int nj = (j / 4) * (BN / TNV) + tx * 4 + (j % 4);
+                cs[nj * CS + mi] = acc[i][j];
+            }
+        __syncthreads();
+        if (m_ok) {
+            for (int nl = kl0; nl < BN; nl += TPB) {
+                const int k = n0 + nl;
+                if (k >= p.K) break;
+                float v = cs[nl * CS + ml];
+                if (bias) v += to_f32<T>(bias[k]);
+                y[ybase + (int64_t)k * PQ] = from_f32<T>(v);
+            }
+        }
+    } else {
+        // cs[ml][nl]: k contiguous, as in y[n][p][q][k].
+        constexpr int CS = BN + 1;
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const int mi = (i / 4) * (BM / TMV) + ty * 4 + (i % 4);
+                const int nj = (j / 4) * (BN / TNV) + tx * 4 + (j % 4);
+                cs[mi * CS + nj] = acc[i][j];
+            }
+        __syncthreads();
+        for (int e = tid; e < BM * BN; e += NT) {
+            const int mi = e / BN, nl = e % BN;
+            const int64_t m = m0 + mi;
+            const int k = n0 + nl;
+            if (m < p.M && k < p.K) {
+                float v = cs[mi * CS + nl];
+                if (bias) v += to_f32<T>(bias[k]);
+                y[m * p.K + k] = from_f32<T>(v);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- tile table
+
+struct TileEntry {
+    int BM, BN, BK, TM, TN;
+};
+// Kept in sync with the dispatch switch below.
+constexpr TileEntry kTiles[] = {
+    {128, 64, 8, 8, 8},    // 0: 128 threads, 64 acc/thread
+    {128, 128, 8, 8, 8},   // 1: 256 threads
+    {64, 64, 16, 4, 4},    // 2: 256 threads, 16 acc/thread
+    {128, 32, 16, 8, 4},   // 3: 128 threads (narrow K, e.g. 32 output channels)
+    {64, 32, 16, 4, 4},    // 4: 128 threads
+    {32, 32, 16, 4, 4},    // 5: 64 threads (tiny layers)
+};
+constexpr int kNumTiles = sizeof(kTiles) / sizeof(kTiles[0]);
+
+template <typename T, int LAYOUT, int BM, int BN, int BK, int TM, int TN>
+conv2d_status_t launch_one(const Shape &s, const Tensors &t, int grid_m, int grid_n,
+                           size_t smem, cudaStream_t st) {
+    using Cfg = CcCfg<T, LAYOUT, BM, BN, BK, TM, TN>;
+    auto kern = cc_conv_kernel<T, LAYOUT, BM, BN, BK, TM, TN>;
+    // Opt in to >48 KB dynamic shared memory (idempotent, cheap).
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return CONV2D_ERR_CUDA;
+    }
+    CcParams p;
+    p.x = t.x; p.w = t.w; p.bias = t.bias; p.y = t.y;
+    p.N = s.N; p.C = s.C; p.H = s.H; p.W = s.W; p.K = s.K; p.R = s.R; p.S = s.S;
+    p.stride = s.stride; p.pad = s.pad; p.dil = s.dil; p.P = s.P; p.Q = s.Q;
+    p.Kg = (int)s.Kg; p.M = s.M;
+    dim3 grid(grid_m, grid_n);
+    kern<<<grid, Cfg::NT, smem, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
+template <typename T, int LAYOUT>
+conv2d_status_t dispatch_tile(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    const CudaCoreTile &c = pl.cc;
+    const int gm = (int)((s.M + c.BM - 1) / c.BM);
+    const int gn = (s.K + c.BN - 1) / c.BN;
+    switch (c.id) {
+        case 0: return launch_one<T, LAYOUT, 128, 64, 8, 8, 8>(s, t, gm, gn, pl.smem_bytes, st);
+        case 1: return launch_one<T, LAYOUT, 128, 128, 8, 8, 8>(s, t, gm, gn, pl.smem_bytes, st);
+        case 2: return launch_one<T, LAYOUT, 64, 64, 16, 4, 4>(s, t, gm, gn, pl.smem_bytes, st);
+        case 3: return launch_one<T, LAYOUT, 128, 32, 16, 8, 4>(s, t, gm, gn, pl.smem_bytes, st);
+        case 4: return launch_one<T, LAYOUT, 64, 32, 16, 4, 4>(s, t, gm, gn, pl.smem_bytes, st);
+        case 5: return launch_one<T, LAYOUT, 32, 32, 16, 4, 4>(s, t, gm, gn, pl.smem_bytes, st);
+        default: return CONV2D_ERR_INTERNAL;
+    }
+}
+
+template <int LAYOUT>
+conv2d_status_t dispatch_dtype(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    switch (s.dtype) {
+        case CONV2D_F32: return dispatch_tile<float, LAYOUT>(s, pl, t, st);
+        case CONV2D_F16: return dispatch_tile<__half, LAYOUT>(s, pl, t, st);
+        case CONV2D_BF16: return dispatch_tile<__nv_bfloat16, LAYOUT>(s, pl, t, st);
+    }
+    return CONV2D_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+int cc_num_tiles() { return kNumTiles; }
+
+CudaCoreTile cc_tile(int id) {
+    const TileEntry &e = kTiles[id];
+    CudaCoreTile t;
+    t.id = id;
+    t.BM = e.BM; t.BN = e.BN; t.BK = e.BK; t.TM = e.TM; t.TN = e.TN;
+    t.threads = (e.BM / e.TM) * (e.BN / e.TN);
+    return t;
+}
+
+// Tap offsets must fit in 32 bits (they are relative to one image).
+bool cc_shape_ok(const Shape &s) {
+    if (s.Kg >= (int64_t)1 << 31) return false;
+    if ((int64_t)s.C * s.H * s.W >= (int64_t)1 << 31) return false;
+    if ((int64_t)s.dil * (s.R - 1) > 32767 || (int64_t)s.dil * (s.S - 1) > 32767) return false;
+    if ((int64_t)s.P * s.Q >= (int64_t)1 << 31) return false;
+    return true;
+}
+
+size_t cc_smem_bytes(const Shape &s, const CudaCoreTile &t) {
+    const size_t tile = 2 * (size_t)t.BK * (t.BM + 4) + 2 * (size_t)t.BK * (t.BN + 4);
+    const size_t epi = s.layout == CONV2D_NCHW ? (size_t)t.BN * (t.BM + 1) : (size_t)t.BM * (t.BN + 1);
+    const size_t main = tile > epi ? tile : epi;
+    const size_t taps = s.Kg < kTableChunk ? (size_t)s.Kg : (size_t)kTableChunk;
+    return main * sizeof(float) + taps * sizeof(Tap);
+}
+
+conv2d_status_t cc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st) {
+    if (s.layout == CONV2D_NCHW) return dispatch_dtype<CONV2D_NCHW>(s, p, t, st);
+    return dispatch_dtype<CONV2D_NHWC>(s, p, t, st);
+}
+
+}  // namespace conv2d

@@ -1,0 +1,76 @@
+// Internal declarations shared by the host API and the kernel files of
+// libconv2d_gb300.  Not part of the public ABI (see include/conv2d.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "conv2d.h"
+
+namespace conv2d {
+
+// One layer, fully validated; all derived sizes precomputed in 64 bits.
+struct Shape {
+    int N, C, H, W, K, R, S, stride, pad, dil;
+    int P, Q;
+    conv2d_dtype_t dtype;
+    conv2d_layout_t layout;
+    int64_t M;    // N*P*Q output pixels (GEMM rows)
+    int64_t Kg;   // C*R*S reduction length
+    int elt;      // element size in bytes
+    int64_t x_elems() const { return (int64_t)N * C * H * W; }
+    int64_t w_elems() const { return (int64_t)K * C * R * S; }
+    int64_t y_elems() const { return (int64_t)N * K * P * Q; }
+    double flops() const { return 2.0 * (double)M * K * (double)Kg; }
+};
+
+// Tile configurations of the CUDA-core implicit GEMM (index into a fixed table).
+struct CudaCoreTile {
+    int id;          // index into the kernel table
+    int BM, BN, BK, TM, TN;
+    int threads;
+};
+
+// Tile configurations of the tensor-core kernel.
+struct TcTile {
+    int BN;          // output channels per tile (multiple of 16, <= 256)
+    int stages;      // smem pipeline depth
+    bool tma_store;  // epilogue through shared memory + TMA store
+};
+
+enum class Algo { CudaCore, TensorCore };
+
+struct Plan {
+    Algo algo;
+    CudaCoreTile cc;
+    TcTile tc;
+    int grid;        // CTAs launched
+    int sm_count;
+    size_t smem_bytes;
+};
+
+struct Tensors {
+    const void *x;
+    const void *w;
+    const void *bias;
+    void *y;
+};
+
+// CUDA-core path (any dtype / layout).  Returns CONV2D_OK or an error code.
+int cc_num_tiles();
+CudaCoreTile cc_tile(int id);
+bool cc_shape_ok(const Shape &s);
+size_t cc_smem_bytes(const Shape &s, const CudaCoreTile &t);
+conv2d_status_t cc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
+
+// Tensor-core path (f16/bf16, NHWC).
+bool tc_shape_ok(const Shape &s, const Tensors *t);
+size_t tc_smem_bytes(const TcTile &t);
+conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
+
+// Device status word (bounded-wait failures).
+conv2d_status_t status_read_and_clear();
+unsigned int *status_word_ptr();   // device address, per current device
+
+}  // namespace conv2d

@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -31,7 +32,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "conv2d_ref.c")
-_BUILD_DIR = os.path.join(_HERE, "_build")
+_BUILD_DIR = os.path.join(_HERE, "_build", platform.machine())
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_conv2d.so")
 _lock = threading.Lock()
 _lib = None

@@ -1,0 +1,63 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path, run the oracle
+on the same seeded inputs, and compare with the tolerance of the method.
+
+Tolerance (per output): |y_gpu - y_oracle| / (sum over taps of |x||w| + |bias|)
+must not exceed 1e-6 for fp32 and 4e-3 for fp16 / bf16 inputs (fp32
+accumulation, one round-to-nearest-even of the output).  Outputs whose taps
+all fall in the padding with no bias must be exactly zero.
+"""
+import numpy as np
+import torch
+
+import oracle
+from cnn_convolution_gb300 import conv2d
+
+TOL = {"f32": 1e-6, "f16": 4e-3, "bf16": 4e-3}
+
+
+def run_gpu(spec, x, w, b, algo="auto", stream=None):
+    d = conv2d.Conv2dDesc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride,
+                          spec.pad, spec.dil, spec.torch_dtype, spec.layout)
+    if algo != "auto":
+        d.set_algo(algo)
+    xd, wd = x.cuda(), w.cuda()
+    bd = None if b is None else b.cuda()
+    y = d.forward(xd, wd, bd, stream=stream)
+    torch.cuda.synchronize()
+    return y.cpu(), d
+
+
+def full_parity(spec, x, w, b, algo="auto"):
+    """Whole-output comparison; returns the max error ratio."""
+    y, _ = run_gpu(spec, x, w, b, algo)
+    y_ref, den = oracle.conv2d(x, w, b, spec.stride, spec.pad, spec.dil, layout=spec.layout)
+    assert tuple(y.shape) == y_ref.shape
+    return oracle.error_ratio(y, y_ref, den)
+
+
+def sample_indices(spec, P, Q, count, seed):
+    """Random outputs plus every border pixel of the first and last image."""
+    rng = np.random.default_rng(seed)
+    idx = [np.stack([rng.integers(0, d, size=count) for d in (spec.N, spec.K, P, Q)], axis=1)]
+    ks = rng.integers(0, spec.K, size=min(spec.K, 8))
+    for n in {0, spec.N - 1}:
+        for k in ks:
+            for p in range(P):
+                for q in range(Q):
+                    if p in (0, P - 1) or q in (0, Q - 1):
+                        idx.append(np.array([[n, k, p, q]]))
+    return np.concatenate(idx, axis=0)
+
+
+def sampled_parity(spec, x, w, b, y, count=6000, seed=0):
+    """Compare y (CPU tensor in spec.layout) at sampled logical outputs."""
+    if spec.layout == "NCHW":
+        P, Q = y.shape[2], y.shape[3]
+    else:
+        P, Q = y.shape[1], y.shape[2]
+    idx = sample_indices(spec, P, Q, count, seed)
+    y_ref, den = oracle.conv2d_points(x, w, b, idx, spec.stride, spec.pad, spec.dil,
+                                      layout=spec.layout)
+    n, k, p, q = idx.T
+    got = y[n, k, p, q] if spec.layout == "NCHW" else y[n, p, q, k]
+    return oracle.error_ratio(got, y_ref, den)
