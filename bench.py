@@ -111,7 +111,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -210,15 +210,15 @@ def bench_main(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
-    for _ in range(args.warmup):
-        run_encoder(descs, x_dev, ws, bs, outs)
-    torch.cuda.synchronize()
-
     n_layers = len(descs)
     step_ms, layer_ms = [], [[] for _ in range(n_layers)]
-    barrier(world)
-    torch.cuda.synchronize()
+    # the clock sampler runs from the warm-up through the end of the timed region
     with ClockSampler(device.index) as clk:
+        for _ in range(args.warmup):
+            run_encoder(descs, x_dev, ws, bs, outs)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
         t_wall0 = time.perf_counter()
         evs_all = []
         for _ in range(args.steps):
@@ -228,7 +228,7 @@ def bench_main(args):
             evs_all.append(evs)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
-    barrier(world)
+        barrier(world)
     for evs in evs_all:
         step_ms.append(evs[0].elapsed_time(evs[-1]))
         for i in range(n_layers):
@@ -433,7 +433,7 @@ def reference_main(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-tensor-core", action="store_true", help="skip the fp16/bf16 layers")

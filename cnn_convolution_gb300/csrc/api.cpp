@@ -10,6 +10,7 @@
 // tile/thread-block tuning (sections "Global Memory and Shared Memory" and
 // "Engineering Challenges", kernel configuration).
 
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -142,28 +143,37 @@ conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
     return CONV2D_OK;
 }
 
+// Tensor-core tile: BM = 128 output pixels; BN output channels from
+// {64, 128, 256}.  Each k-block (64 channels at one tap) costs about
+// max(2*BN, 128 + BN) SM cycles: 128 x BN x 64 MMAs at 4096 MACs per cycle
+// against 16 KB of A plus BN x 128 B of B read from shared memory at 128 B
+// per cycle.  The chooser minimises rounds-of-persistent-CTAs x that cost,
+// wasting no more than half a tile of K.
 conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     if (!(d.cc_major == 10 && d.cc_minor == 3)) return CONV2D_ERR_UNSUPPORTED;
-    // Output-channel tile: the widest of 256/128/64 that wastes little of K,
-    // then shrink while the grid would leave most SMs idle.
-    int bn = s.K >= 256 ? 256 : (s.K > 64 ? 128 : 64);
-    while (bn > 64 && (s.K % bn) != 0 && (s.K % (bn / 2)) == 0) bn /= 2;
-    auto tiles_for = [&](int b) { return ((s.M + 127) / 128) * ((s.K + b - 1) / b); };
-    while (bn > 64 && tiles_for(bn) < d.sm_count) bn /= 2;
-    if (const char *e = std::getenv("CONV2D_TC_BN")) bn = std::atoi(e);
+    const int64_t m_tiles = (s.M + 127) / 128;
+    const int64_t kb = (int64_t)s.R * s.S * ((s.C + 63) / 64);
+    int best_bn = 0;
+    double best = 1e300;
+    for (int bn : {64, 128, 256}) {
+        const int64_t n_tiles = (s.K + bn - 1) / bn;
+        if (bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1) continue;   // too much padding along K
+        const int64_t tiles = m_tiles * n_tiles;
+        const int64_t rounds = (tiles + d.sm_count - 1) / d.sm_count;
+        const double cost = (double)rounds * kb * std::max(2.0 * bn, 128.0 + bn) + rounds * 64.0;
+        if (cost < best) { best = cost; best_bn = bn; }
+    }
+    if (const char *e = std::getenv("CONV2D_TC_BN")) best_bn = std::atoi(e);
+    if (best_bn != 64 && best_bn != 128 && best_bn != 256) return CONV2D_ERR_UNSUPPORTED;
     TcTile t;
-    t.BN = bn;
+    t.BN = best_bn;
+    t.stages = best_bn == 64 ? 8 : (best_bn == 128 ? 6 : 4);
     t.tma_store = false;
-    const size_t stage = (size_t)128 * 64 * 2 + (size_t)bn * 64 * 2;
-    const size_t budget = d.smem_optin - 4096;
-    t.stages = (int)std::min<size_t>(8, budget / stage);
-    if (const char *e = std::getenv("CONV2D_TC_STAGES")) t.stages = std::atoi(e);
-    if (t.stages < 2) return CONV2D_ERR_UNSUPPORTED;
     p->algo = Algo::TensorCore;
     p->tc = t;
     p->smem_bytes = tc_smem_bytes(t);
     if (p->smem_bytes > d.smem_optin) return CONV2D_ERR_UNSUPPORTED;
-    const int64_t tiles = tiles_for(bn);
+    const int64_t tiles = m_tiles * ((s.K + best_bn - 1) / best_bn);
     p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
     p->sm_count = d.sm_count;
     return CONV2D_OK;
@@ -174,8 +184,16 @@ bool aligned16(const Tensors &t) {
     return a(t.x) && a(t.w) && a(t.y) && (t.bias == nullptr || ((uintptr_t)t.bias & 1) == 0);
 }
 
-// Plans are cached per (device, shape, dtype, layout, algo, alignment class).
-using PlanKey = std::tuple<int, int, int, int, int, int, int, int, int, int, int, int, int, int, int>;
+// Plans are cached per (device, shape, dtype, layout, algo, alignment class,
+// tile overrides).  CONV2D_CC_TILE / CONV2D_TC_BN force a tile (tests and
+// A/B measurements); they are read on every call so they can change.
+using PlanKey = std::tuple<int, int, int, int, int, int, int, int, int, int, int, int, int, int, int,
+                           int, int>;
+
+int env_int(const char *name) {
+    const char *e = std::getenv(name);
+    return e ? std::atoi(e) : -1;
+}
 std::mutex g_plan_mu;
 std::map<PlanKey, Plan> g_plans;
 
@@ -186,7 +204,8 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
     if (st != CONV2D_OK) return st;
     const bool al = t == nullptr || aligned16(*t);
     const PlanKey key{dev, s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
-                      (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0};
+                      (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0,
+                      env_int("CONV2D_CC_TILE"), env_int("CONV2D_TC_BN")};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);

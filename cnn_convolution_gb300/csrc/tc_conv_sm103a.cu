@@ -1,9 +1,584 @@
-// Tensor-core path placeholder (replaced by the tcgen05 kernel).
+// Tensor-core implicit-GEMM convolution for sm_103a (fp16 / bf16, NHWC).
+//
+// The half-precision tensor-core path of "Enabling Memory-efficient Im2win
+// Convolution with Multi-precision Support on GPU CUDA and Tensor Cores"
+// (abstract: hardware half-precision multiply-accumulate fed by asynchronous
+// data movement, with no im2col matrix in memory), written for Blackwell:
+//
+//   * GEMM view as in "GPU-Accelerating MSCRED with CUDA, im2col, GEMM, and a
+//     Custom PyTorch Extension" (section "Transforming Conv2D into im2col and
+//     GEMM"): D[m, k] = sum_{r,s,c} A[m, (r,s,c)] * W[k, (r,s,c)], with
+//     m = (n, p, q) an output pixel and A[m, (r,s,c)] = x[n, p*st-pad+r*dil,
+//     q*st-pad+s*dil, c] (zero outside the image).
+//   * A tiles (128 output pixels x 64 channels at one filter tap (r, s)) are
+//     fetched by TMA in im2col mode straight from x: the tensor map walks the
+//     output pixels of the tile across rows and images, applies the conv
+//     stride, the tap offset (s*dil, r*dil) and zero fill for padding.  B tiles
+//     (BN output channels x 64 channels of w[k][r][s][c]) come from a tiled
+//     tensor map.  Both land in shared memory with the 128-byte swizzle the
+//     MMA descriptors expect.  No workspace exists.
+//   * One thread issues tcgen05.mma (kind::f16, M=128, N=BN, K=16) into a
+//     fp32 accumulator in tensor memory; tcgen05.commit frees each shared
+//     memory stage and signals a finished accumulator.
+//   * Persistent CTAs (one per SM) loop over output tiles; the accumulator is
+//     double-buffered in tensor memory so the epilogue of one tile (tcgen05.ld,
+//     + bias, one round-to-nearest-even cast, 16-byte stores) overlaps the
+//     main loop of the next.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = tensor-memory
+// allocator and MMA issuer, warps 2..5 = epilogue (warp w reads accumulator
+// lanes 32*(w%4) .. 32*(w%4)+31, the lane quarter that warp may access).
+//
+// Every mbarrier wait is bounded: after kWaitLimitNs the waiting thread sets
+// a CTA abort flag and the device status word, every role drains what it
+// started, tensor memory is freed, and the kernel returns.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
 #include "internal.h"
+
 namespace conv2d {
-bool tc_shape_ok(const Shape &, const Tensors *) { return false; }
-size_t tc_smem_bytes(const TcTile &) { return 0; }
-conv2d_status_t tc_launch(const Shape &, const Plan &, const Tensors &, cudaStream_t) {
-    return CONV2D_ERR_UNSUPPORTED;
+namespace {
+
+constexpr int kBM = 128;            // output pixels per tile (MMA M)
+constexpr int kBK = 64;             // channels per k-block (128 bytes of fp16/bf16)
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s for any single wait
+constexpr int kATileBytes = kBM * kBK * 2;
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on phase `parity` of an mbarrier.  Returns false (after setting
+// the abort flag and the status word) if it gave up, or if another thread of
+// the CTA already gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                if (status) atomicOr(status, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                   int c, int w, int h, int n, uint16_t off_w,
+                                                   uint16_t off_h) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar), "h"(off_w),
+        "h"(off_h)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_tile_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T, M=128, N from idesc, K=16.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once all tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive fp32 accumulator columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes,
+// 128-byte swizzle, 8-row core groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);      // start address
+    d |= (uint64_t)1 << 16;                         // leading byte offset (unused for SW128 K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                         // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, A and B K-major.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int n) {
+    return (1u << 4)                                   // D format: f32
+           | ((bf16 ? 1u : 0u) << 7)                   // A format: f16 / bf16
+           | ((bf16 ? 1u : 0u) << 10)                  // B format
+           | ((uint32_t)(n >> 3) << 17)                // N / 8
+           | ((uint32_t)(kBM >> 4) << 24);             // M / 16
+}
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <typename T> __device__ __forceinline__ float load_bias(const T *b, int k);
+template <> __device__ __forceinline__ float load_bias<__half>(const __half *b, int k) {
+    return __half2float(b[k]);
+}
+template <> __device__ __forceinline__ float load_bias<__nv_bfloat16>(const __nv_bfloat16 *b, int k) {
+    return __bfloat162float(b[k]);
+}
+
+struct TcParams {
+    const void *bias;
+    void *y;
+    unsigned int *status;
+    int64_t M;            // N*P*Q
+    int K;                // output channels
+    int PQ, Q;
+    int stride, pad, dil;
+    int S;                // filter width
+    int CB;               // channel blocks of 64
+    int KB;               // k-blocks per tile = R*S*CB
+    int n_tiles_n;        // tiles along K
+    int total_tiles;
+};
+
+template <int BN, int STAGES>
+struct TcSmem {
+    static constexpr int kBTileBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+    static constexpr size_t kBarOffset = (size_t)STAGES * kStageBytes;
+    // full[S], empty[S], acc_full[2], acc_empty[2], drain[1]; then tmem addr, abort flag
+    static constexpr size_t kBarBytes = (2 * STAGES + 5) * 8;
+    static constexpr size_t kBytes = kBarOffset + kBarBytes + 16 + 1024;   // +1024 for alignment
+};
+
+template <typename T, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const TcParams p) {
+    using L = TcSmem<BN, STAGES>;
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
+    constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
+    constexpr uint32_t kTxBytes = kATileBytes + L::kBTileBytes;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t bar_base = smem_base + (uint32_t)L::kBarOffset;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
+    auto a_tile = [&](int s) { return smem_base + (uint32_t)(s * L::kStageBytes); };
+    auto b_tile = [&](int s) { return smem_base + (uint32_t)(s * L::kStageBytes + kATileBytes); };
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), 128);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------- TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_phase[STAGES];
+        bool issued[STAGES];
+        for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            const int tm = tile / p.n_tiles_n;
+            const int tn = tile - tm * p.n_tiles_n;
+            const int64_t m0 = (int64_t)tm * kBM;
+            const int n_img = (int)(m0 / p.PQ);
+            const int pq = (int)(m0 - (int64_t)n_img * p.PQ);
+            const int p0 = pq / p.Q, q0 = pq - p0 * p.Q;
+            const int h0 = p0 * p.stride - p.pad;
+            const int w0 = q0 * p.stride - p.pad;
+            const int k0 = tn * BN;
+            for (int kb = 0; kb < p.KB; ++kb) {
+                const int cb = kb % p.CB;
+                const int rs = kb / p.CB;
+                const int r = rs / p.S, s = rs - r * p.S;
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                mbar_arrive_expect_tx(full_bar(stage), kTxBytes);
+                tma_load_im2col_4d(a_tile(stage), &tmA, full_bar(stage), cb * kBK, w0, h0, n_img,
+                                   (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
+                tma_load_tile_4d(b_tile(stage), &tmB, full_bar(stage), cb * kBK, s, r, k0);
+                issued[stage] = true;
+                issued_phase[stage] = phase;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok) {
+            // Let the copies already in flight land before the CTA goes away
+            // (one time budget for all stages together).
+            const uint64_t t0 = global_timer_ns();
+            for (int s = 0; s < STAGES; ++s) {
+                if (!issued[s]) continue;
+                while (!mbar_try_wait(full_bar(s), issued_phase[s]) &&
+                       global_timer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true, any = false;
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < p.KB; ++kb) {
+                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t ad = smem_desc_sw128(a_tile(stage));
+                const uint64_t bd = smem_desc_sw128(b_tile(stage));
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k) {
+                    // advance 16 elements (32 bytes) along K inside the swizzled rows
+                    mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
+                            (kb | k) != 0 ? 1u : 0u);
+                }
+                any = true;
+                mma_commit(empty_bar(stage));
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit(accf_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (any) {
+            // Make sure every MMA has retired before tensor memory is released.
+            mma_commit(drain_bar);
+            uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const T *bias = static_cast<const T *>(p.bias);
+        T *y = static_cast<T *>(p.y);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+            // one lane waits, the whole warp follows (tcgen05.ld needs a converged warp)
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int tm = tile / p.n_tiles_n;
+            const int tn = tile - tm * p.n_tiles_n;
+            const int64_t m = (int64_t)tm * kBM + row;
+            const int k0 = tn * BN;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32cols(t_row + (uint32_t)c0, v);
+                if (m < p.M && k0 + c0 < p.K) {
+                    uint4 out[4];
+                    uint32_t *o = reinterpret_cast<uint32_t *>(out);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
+                        const int k = k0 + c0 + j;
+                        if (bias != nullptr && k < p.K) {
+                            a += load_bias<T>(bias, k);
+                            b += load_bias<T>(bias, k + 1);
+                        }
+                        o[j / 2] = pack2<T>(a, b);
+                    }
+                    T *dst = y + m * p.K + k0 + c0;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (k0 + c0 + 8 * g < p.K) reinterpret_cast<uint4 *>(dst)[g] = out[g];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            mbar_arrive(acce_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using EncodeIm2colFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                    const cuuint64_t *, const cuuint64_t *, const int *, const int *,
+                                    cuuint32_t, cuuint32_t, const cuuint32_t *, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                    CUtensorMapFloatOOBfill);
+
+std::once_flag g_fn_once;
+EncodeTiledFn g_encode_tiled = nullptr;
+EncodeIm2colFn g_encode_im2col = nullptr;
+
+bool load_driver_fns() {
+    std::call_once(g_fn_once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = reinterpret_cast<EncodeTiledFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_im2col = reinterpret_cast<EncodeIm2colFn>(f);
+    });
+    return g_encode_tiled && g_encode_im2col;
+}
+
+template <typename T, int BN, int STAGES>
+conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    using L = TcSmem<BN, STAGES>;
+    if (!load_driver_fns()) return CONV2D_ERR_CUDA;
+    const CUtensorMapDataType dt =
+        s.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    alignas(64) CUtensorMap tmA, tmB;
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.W * s.C * 2,
+                                       (cuuint64_t)s.H * s.W * s.C * 2};
+        // window origins span [-pad, extent - 1 + pad - dil*(ksize-1)] in W and H
+        const int lower[2] = {-s.pad, -s.pad};
+        const int upper[2] = {s.pad - s.dil * (s.S - 1), s.pad - s.dil * (s.R - 1)};
+        const cuuint32_t estr[4] = {1, (cuuint32_t)s.stride, (cuuint32_t)s.stride, 1};
+        if (g_encode_im2col(&tmA, dt, 4, const_cast<void *>(t.x), dims, strides, lower, upper, kBK,
+                            kBM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.S, (cuuint64_t)s.R, (cuuint64_t)s.K};
+        const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.S * s.C * 2,
+                                       (cuuint64_t)s.R * s.S * s.C * 2};
+        const cuuint32_t box[4] = {kBK, 1, 1, BN};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (g_encode_tiled(&tmB, dt, 4, const_cast<void *>(t.w), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    }
+    TcParams p;
+    p.bias = t.bias;
+    p.y = t.y;
+    p.status = status_word_ptr();
+    p.M = s.M;
+    p.K = s.K;
+    p.PQ = s.P * s.Q;
+    p.Q = s.Q;
+    p.stride = s.stride;
+    p.pad = s.pad;
+    p.dil = s.dil;
+    p.S = s.S;
+    p.CB = (s.C + kBK - 1) / kBK;
+    p.KB = s.R * s.S * p.CB;
+    p.n_tiles_n = (s.K + BN - 1) / BN;
+    const int64_t tiles = ((s.M + kBM - 1) / kBM) * (int64_t)p.n_tiles_n;
+    if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
+    p.total_tiles = (int)tiles;
+    auto kern = tc_conv_kernel<T, BN, STAGES>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes) !=
+        cudaSuccess)
+        return CONV2D_ERR_CUDA;
+    const int grid = pl.grid > 0 ? pl.grid : 1;
+    kern<<<grid, kThreads, L::kBytes, st>>>(tmA, tmB, p);
+    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
+template <typename T>
+conv2d_status_t dispatch_bn(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    // stages: as many as fit in ~200 KB of shared memory
+    switch (pl.tc.BN) {
+        case 64: return launch_tc<T, 64, 8>(s, pl, t, st);
+        case 128: return launch_tc<T, 128, 6>(s, pl, t, st);
+        case 256: return launch_tc<T, 256, 4>(s, pl, t, st);
+    }
+    return CONV2D_ERR_INTERNAL;
+}
+
+}  // namespace
+
+bool tc_shape_ok(const Shape &s, const Tensors *t) {
+    if (s.dtype != CONV2D_F16 && s.dtype != CONV2D_BF16) return false;
+    if (s.layout != CONV2D_NHWC) return false;
+    if (s.C % 8 != 0 || s.K % 8 != 0) return false;               // 16-byte rows for TMA and stores
+    if (s.stride > 8) return false;                               // TMA traversal stride limit
+    if (s.pad > 127) return false;                                // im2col corner range
+    const int64_t up_h = (int64_t)s.pad - (int64_t)s.dil * (s.R - 1);
+    const int64_t up_w = (int64_t)s.pad - (int64_t)s.dil * (s.S - 1);
+    if (up_h < -128 || up_w < -128 || up_h > 127 || up_w > 127) return false;
+    if ((int64_t)s.dil * (s.R - 1) > 255 || (int64_t)s.dil * (s.S - 1) > 255) return false;
+    if ((int64_t)s.N * s.H * s.W >= ((int64_t)1 << 31)) return false;
+    if (t) {
+        auto a16 = [](const void *q) { return ((uintptr_t)q & 15) == 0; };
+        if (!a16(t->x) || !a16(t->w) || !a16(t->y)) return false;
+    }
+    return true;
+}
+
+size_t tc_smem_bytes(const TcTile &t) {
+    switch (t.BN) {
+        case 64: return TcSmem<64, 8>::kBytes;
+        case 128: return TcSmem<128, 6>::kBytes;
+        case 256: return TcSmem<256, 4>::kBytes;
+    }
+    return (size_t)1 << 30;
+}
+
+conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st) {
+    if (s.dtype == CONV2D_BF16) return dispatch_bn<__nv_bfloat16>(s, p, t, st);
+    return dispatch_bn<__half>(s, p, t, st);
+}
+
 }  // namespace conv2d

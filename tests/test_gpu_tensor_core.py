@@ -1,0 +1,97 @@
+"""GPU parity of the tcgen05 / TMA-im2col tensor-core kernel, forced on.
+
+Covers each output-channel tile width (64, 128, 256), channel counts that are
+and are not multiples of the 64-channel k-block, output-channel counts that
+leave a ragged tile, M not a multiple of 128 (tiles running past the last
+image), strides, padding, dilation, non-square filters, bias on and off, and
+several persistent rounds per CTA.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from cnn_convolution_gb300 import conv2d, workloads as wl
+from parity import TOL, full_parity, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from cnn_convolution_gb300 import build
+    import oracle
+    build.build()
+    conv2d.load()
+    oracle.build()
+
+
+@pytest.fixture
+def force_bn():
+    def set_bn(bn):
+        if bn is None:
+            os.environ.pop("CONV2D_TC_BN", None)
+        else:
+            os.environ["CONV2D_TC_BN"] = str(bn)
+    yield set_bn
+    os.environ.pop("CONV2D_TC_BN", None)
+
+
+SHAPES = [
+    # N, C, H, W, K, R, S, stride, pad, dil, bias
+    (1, 64, 8, 8, 64, 3, 3, 1, 1, 1, True),
+    (2, 64, 11, 13, 64, 3, 3, 1, 1, 1, False),
+    (3, 128, 9, 7, 128, 3, 3, 2, 1, 1, True),
+    (2, 8, 10, 10, 8, 3, 3, 1, 1, 1, True),        # C = K = 8: mostly zero-filled k-block
+    (2, 72, 9, 9, 72, 3, 3, 1, 1, 1, True),        # C, K one past a multiple of 64
+    (1, 200, 6, 6, 136, 2, 2, 1, 0, 1, False),
+    (2, 64, 15, 15, 96, 5, 5, 1, 2, 1, True),
+    (2, 32, 12, 14, 48, 1, 5, 1, 2, 1, True),      # non-square filter
+    (2, 32, 14, 12, 48, 5, 1, 1, 2, 1, True),
+    (2, 16, 13, 13, 40, 3, 3, 1, 2, 2, True),      # dilation 2
+    (2, 24, 17, 15, 32, 3, 2, 3, 1, 1, True),      # stride 3
+    (4, 64, 7, 7, 264, 1, 1, 1, 0, 1, True),       # 1x1, ragged K
+    (5, 128, 14, 14, 256, 3, 3, 2, 1, 1, False),
+    (1, 64, 3, 3, 64, 3, 3, 1, 0, 1, True),        # single output pixel per image
+    (9, 64, 30, 30, 64, 3, 3, 1, 1, 1, True),      # many tiles: several persistent rounds
+]
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_forced_tile_widths(dtype, bn, force_bn):
+    force_bn(bn)
+    for i, (N, C, H, W, K, R, S, st, pad, dil, bias) in enumerate(SHAPES):
+        spec = wl.ConvSpec(f"tc{i}", N, C, H, W, K, R, S, st, pad, dil, dtype=dtype,
+                           layout="NHWC", bias=bias)
+        x, w, b = wl.random_inputs(spec, seed=100 + i)
+        err = full_parity(spec, x, w, b, algo="tensor_core")
+        assert err <= TOL[dtype], f"{spec} BN={bn}: err={err}"
+
+
+def test_plan_reports_tensor_core():
+    d = conv2d.Conv2dDesc(2, 64, 8, 8, 64, 3, 3, 1, 1, 1, torch.bfloat16, "NHWC")
+    assert d.plan().startswith("tensor_core")
+    assert d.workspace_bytes() == 0
+
+
+def test_tensor_core_matches_cuda_core():
+    spec = wl.ConvSpec("tc_vs_cc", 3, 64, 20, 20, 128, 3, 3, 1, 1, dtype="bf16", layout="NHWC")
+    x, w, b = wl.random_inputs(spec, seed=5)
+    y_tc, _ = run_gpu(spec, x, w, b, "tensor_core")
+    y_cc, _ = run_gpu(spec, x, w, b, "cuda_core")
+    diff = (y_tc.float() - y_cc.float()).abs().max().item()
+    scale = y_cc.float().abs().max().item()
+    assert diff <= 2 * 2 ** -8 * scale
+
+
+def test_repeated_launches_are_deterministic():
+    spec = wl.ConvSpec("det", 4, 128, 16, 16, 256, 3, 3, 1, 1, dtype="bf16", layout="NHWC")
+    x, w, b = wl.random_inputs(spec, seed=6)
+    y1, _ = run_gpu(spec, x, w, b, "tensor_core")
+    y2, _ = run_gpu(spec, x, w, b, "tensor_core")
+    assert torch.equal(y1, y2)
+    assert conv2d.get_device_status() == 0
