@@ -98,6 +98,11 @@ conv2d_status_t device_info(int *dev_out, DevInfo *info) {
 
 // ------------------------------------------------------------ chooser
 
+int env_int(const char *name) {
+    const char *e = std::getenv(name);
+    return e ? std::atoi(e) : -1;
+}
+
 // Estimated time (arbitrary units) of a CUDA-core tile on this layer: the
 // busiest SM's share of tile work divided by a per-tile FFMA efficiency that
 // also falls when too few warps are resident to hide latency.
@@ -169,6 +174,7 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     t.BN = best_bn;
     t.stages = best_bn == 64 ? 8 : (best_bn == 128 ? 6 : 4);
     t.tma_store = false;
+    t.force_im2col = env_int("CONV2D_TC_IM2COL") == 1;
     p->algo = Algo::TensorCore;
     p->tc = t;
     p->smem_bytes = tc_smem_bytes(t);
@@ -190,10 +196,7 @@ bool aligned16(const Tensors &t) {
 using PlanKey = std::tuple<int, int, int, int, int, int, int, int, int, int, int, int, int, int, int,
                            int, int>;
 
-int env_int(const char *name) {
-    const char *e = std::getenv(name);
-    return e ? std::atoi(e) : -1;
-}
+
 std::mutex g_plan_mu;
 std::map<PlanKey, Plan> g_plans;
 
@@ -205,7 +208,7 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
     const bool al = t == nullptr || aligned16(*t);
     const PlanKey key{dev, s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
                       (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0,
-                      env_int("CONV2D_CC_TILE"), env_int("CONV2D_TC_BN")};
+                      env_int("CONV2D_CC_TILE"), env_int("CONV2D_TC_BN") * 4 + env_int("CONV2D_TC_IM2COL")};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);
@@ -271,7 +274,14 @@ conv2d_status_t check_tensors(const Shape &s, const Tensors &t, cudaStream_t str
         return CONV2D_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
-    if (stream) {
+    // cudaStreamGetDevice invalidates an ongoing stream capture, so the
+    // stream's device is checked only when the stream is not capturing.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (stream && cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV2D_ERR_INVALID_ARG;
+    }
+    if (stream && cap == cudaStreamCaptureStatusNone) {
         int sdev = -1;
         if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) {
             cudaGetLastError();
@@ -348,8 +358,10 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
     conv2d_status_t st = get_plan(desc->s, desc->algo, nullptr, &p);
     if (st != CONV2D_OK) return st;
     if (p.algo == Algo::TensorCore)
-        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 stages=%d grid=%d smem=%zu",
-                      p.tc.BN, p.tc.stages, p.grid, p.smem_bytes);
+        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 stages=%d grid=%d smem=%zu a=%s",
+                      p.tc.BN, p.tc.stages, p.grid, p.smem_bytes,
+                      (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
+                       !p.tc.force_im2col) ? "tile" : "im2col");
     else
         std::snprintf(buf, len, "cuda_core ffma BM=%d BN=%d BK=%d TM=%d TN=%d threads=%d grid=%d smem=%zu",
                       p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.threads, p.grid,

@@ -37,6 +37,7 @@ struct TcTile {
     int BN;          // output channels per tile (multiple of 16, <= 256)
     int stages;      // smem pipeline depth
     bool tma_store;  // epilogue through shared memory + TMA store
+    bool force_im2col = false;   // 1x1 layers: use the im2col map even though a plain one would do
 };
 
 enum class Algo { CudaCore, TensorCore };

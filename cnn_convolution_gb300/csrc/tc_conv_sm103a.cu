@@ -130,6 +130,15 @@ __device__ __forceinline__ void tma_load_tile_4d(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_tile_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -250,7 +259,10 @@ struct TcSmem {
     static constexpr size_t kBytes = kBarOffset + kBarBytes + 16 + 1024;   // +1024 for alignment
 };
 
-template <typename T, int BN, int STAGES>
+// A_TILE: the layer is a 1x1 / stride 1 / no padding convolution, so the A
+// operand is x itself viewed as the [N*H*W, C] matrix and is fetched with a
+// plain 2-D tiled map instead of an im2col one.
+template <typename T, int BN, int STAGES, bool A_TILE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const TcParams p) {
@@ -327,8 +339,11 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int r = rs / p.S, s = rs - r * p.S;
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                 mbar_arrive_expect_tx(full_bar(stage), kTxBytes);
-                tma_load_im2col_4d(a_tile(stage), &tmA, full_bar(stage), cb * kBK, w0, h0, n_img,
-                                   (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
+                if (A_TILE)
+                    tma_load_tile_2d(a_tile(stage), &tmA, full_bar(stage), cb * kBK, (int)m0);
+                else
+                    tma_load_im2col_4d(a_tile(stage), &tmA, full_bar(stage), cb * kBK, w0, h0,
+                                       n_img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
                 tma_load_tile_4d(b_tile(stage), &tmB, full_bar(stage), cb * kBK, s, r, k0);
                 issued[stage] = true;
                 issued_phase[stage] = phase;
@@ -476,14 +491,24 @@ bool load_driver_fns() {
     return g_encode_tiled && g_encode_im2col;
 }
 
-template <typename T, int BN, int STAGES>
+template <typename T, int BN, int STAGES, bool A_TILE>
 conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
     using L = TcSmem<BN, STAGES>;
     if (!load_driver_fns()) return CONV2D_ERR_CUDA;
     const CUtensorMapDataType dt =
         s.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     alignas(64) CUtensorMap tmA, tmB;
-    {
+    if (A_TILE) {
+        const cuuint64_t dims[2] = {(cuuint64_t)s.C, (cuuint64_t)s.N * s.H * s.W};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.C * 2};
+        const cuuint32_t box[2] = {kBK, kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (g_encode_tiled(&tmA, dt, 2, const_cast<void *>(t.x), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    } else {
         const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
         const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.W * s.C * 2,
                                        (cuuint64_t)s.H * s.W * s.C * 2};
@@ -527,7 +552,7 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     const int64_t tiles = ((s.M + kBM - 1) / kBM) * (int64_t)p.n_tiles_n;
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     p.total_tiles = (int)tiles;
-    auto kern = tc_conv_kernel<T, BN, STAGES>;
+    auto kern = tc_conv_kernel<T, BN, STAGES, A_TILE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes) !=
         cudaSuccess)
         return CONV2D_ERR_CUDA;
@@ -536,15 +561,20 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 
-template <typename T>
+template <typename T, bool A_TILE>
 conv2d_status_t dispatch_bn(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
     // stages: as many as fit in ~200 KB of shared memory
     switch (pl.tc.BN) {
-        case 64: return launch_tc<T, 64, 8>(s, pl, t, st);
-        case 128: return launch_tc<T, 128, 6>(s, pl, t, st);
-        case 256: return launch_tc<T, 256, 4>(s, pl, t, st);
+        case 64: return launch_tc<T, 64, 8, A_TILE>(s, pl, t, st);
+        case 128: return launch_tc<T, 128, 6, A_TILE>(s, pl, t, st);
+        case 256: return launch_tc<T, 256, 4, A_TILE>(s, pl, t, st);
     }
     return CONV2D_ERR_INTERNAL;
+}
+
+// 1x1, stride 1, no padding: output pixel m reads input pixel m.
+bool plain_matrix_a(const Shape &s) {
+    return s.R == 1 && s.S == 1 && s.stride == 1 && s.pad == 0;
 }
 
 }  // namespace
@@ -577,8 +607,11 @@ size_t tc_smem_bytes(const TcTile &t) {
 }
 
 conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st) {
-    if (s.dtype == CONV2D_BF16) return dispatch_bn<__nv_bfloat16>(s, p, t, st);
-    return dispatch_bn<__half>(s, p, t, st);
+    const bool a_tile = plain_matrix_a(s) && !p.tc.force_im2col;
+    if (s.dtype == CONV2D_BF16)
+        return a_tile ? dispatch_bn<__nv_bfloat16, true>(s, p, t, st)
+                      : dispatch_bn<__nv_bfloat16, false>(s, p, t, st);
+    return a_tile ? dispatch_bn<__half, true>(s, p, t, st) : dispatch_bn<__half, false>(s, p, t, st);
 }
 
 }  // namespace conv2d

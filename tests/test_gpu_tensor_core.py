@@ -95,3 +95,20 @@ def test_repeated_launches_are_deterministic():
     y2, _ = run_gpu(spec, x, w, b, "tensor_core")
     assert torch.equal(y1, y2)
     assert conv2d.get_device_status() == 0
+
+
+@pytest.mark.parametrize("im2col", ["0", "1"])
+def test_1x1_plain_and_im2col_maps(im2col, force_bn):
+    """1x1 / stride 1 / pad 0 layers read x as a plain [N*H*W, C] matrix; the
+    im2col map must give the same answer."""
+    os.environ["CONV2D_TC_IM2COL"] = im2col
+    try:
+        for i, (N, C, H, W, K) in enumerate([(3, 64, 7, 7, 264), (1, 72, 5, 9, 64),
+                                             (4, 512, 7, 7, 256), (2, 8, 13, 11, 16)]):
+            spec = wl.ConvSpec(f"p1x1_{i}", N, C, H, W, K, 1, 1, 1, 0, 1, dtype="bf16",
+                               layout="NHWC", bias=bool(i % 2))
+            x, w, b = wl.random_inputs(spec, seed=40 + i)
+            err = full_parity(spec, x, w, b, algo="tensor_core")
+            assert err <= TOL["bf16"], f"{spec}: {err}"
+    finally:
+        os.environ.pop("CONV2D_TC_IM2COL", None)
