@@ -317,12 +317,14 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- TMA producer
+        // The k-block coordinates (r, s, channel block) advance incrementally:
+        // this single thread's loop is on the critical path of the pipeline.
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t issued_phase[STAGES];
-        bool issued[STAGES];
-        for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+        uint32_t n_issued = 0;
         bool ok = true;
+        const int dil = p.dil;
+        const int c_end = p.CB * kBK;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
@@ -333,30 +335,33 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int h0 = p0 * p.stride - p.pad;
             const int w0 = q0 * p.stride - p.pad;
             const int k0 = tn * BN;
+            int r = 0, s = 0, c = 0;
             for (int kb = 0; kb < p.KB; ++kb) {
-                const int cb = kb % p.CB;
-                const int rs = kb / p.CB;
-                const int r = rs / p.S, s = rs - r * p.S;
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                mbar_arrive_expect_tx(full_bar(stage), kTxBytes);
+                const uint32_t fb = full_bar(stage);
+                mbar_arrive_expect_tx(fb, kTxBytes);
                 if (A_TILE)
-                    tma_load_tile_2d(a_tile(stage), &tmA, full_bar(stage), cb * kBK, (int)m0);
+                    tma_load_tile_2d(a_tile(stage), &tmA, fb, c, (int)m0);
                 else
-                    tma_load_im2col_4d(a_tile(stage), &tmA, full_bar(stage), cb * kBK, w0, h0,
-                                       n_img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
-                tma_load_tile_4d(b_tile(stage), &tmB, full_bar(stage), cb * kBK, s, r, k0);
-                issued[stage] = true;
-                issued_phase[stage] = phase;
+                    tma_load_im2col_4d(a_tile(stage), &tmA, fb, c, w0, h0, n_img,
+                                       (uint16_t)(s * dil), (uint16_t)(r * dil));
+                tma_load_tile_4d(b_tile(stage), &tmB, fb, c, s, r, k0);
+                ++n_issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                c += kBK;
+                if (c >= c_end) {
+                    c = 0;
+                    if (++s == p.S) { s = 0; ++r; }
+                }
             }
         }
         if (!ok) {
             // Let the copies already in flight land before the CTA goes away
-            // (one time budget for all stages together).
+            // (one time budget for all stages together).  Load i went to stage
+            // i % STAGES with phase (i / STAGES) & 1.
             const uint64_t t0 = global_timer_ns();
-            for (int s = 0; s < STAGES; ++s) {
-                if (!issued[s]) continue;
-                while (!mbar_try_wait(full_bar(s), issued_phase[s]) &&
+            for (uint32_t i = n_issued > (uint32_t)STAGES ? n_issued - STAGES : 0; i < n_issued; ++i) {
+                while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) &&
                        global_timer_ns() - t0 < kWaitLimitNs) {
                 }
             }
@@ -368,6 +373,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true, any = false;
+        const uint64_t a_desc0 = smem_desc_sw128(a_tile(0));
+        const uint64_t b_desc0 = smem_desc_sw128(b_tile(0));
+        constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);   // stage stride, 16-B units
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
@@ -375,8 +383,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int kb = 0; kb < p.KB; ++kb) {
                 if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t ad = smem_desc_sw128(a_tile(stage));
-                const uint64_t bd = smem_desc_sw128(b_tile(stage));
+                const uint64_t ad = a_desc0 + (uint64_t)stage * kStageDesc;
+                const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc;
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k) {
                     // advance 16 elements (32 bytes) along K inside the swizzled rows
