@@ -9,8 +9,11 @@ TFLOPS = sum over layers of 2*N*K*P*Q*C*R*S / time, plus the roofline
 fraction of the dominant kernel and the extra workspace (always 0 bytes).
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream; L2 is flushed (a 256 MiB write) before every timed step,
-outside its events.  Barrier + synchronize on both sides of the timed region;
+launching stream; a step is one replay of a CUDA graph holding the 4 C-ABI
+launches (so host-side validation does not sit inside the kernel timing); L2
+is flushed (a 256 MiB write) before every timed step, outside its events.
+The JSON line also reports the eager (non-graph) step time, the host time of
+one C-ABI call, and an end-to-end time with host<->device copies.  Barrier + synchronize on both sides of the timed region;
 the slowest rank's time is reported.  With --gpus N > 1 (torchrun) every rank
 runs an independent replica of the workload (the layer needs no exchange),
 so the total work grows with N ("weak" scaling).
@@ -193,6 +196,14 @@ def run_encoder(descs, x_dev, ws, bs, outs, events=None):
     return cur
 
 
+def capture(fn):
+    """Capture fn's launches (on a side stream, as torch requires) into a CUDA graph."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
 def bench_main(args):
     rank, world, local = dist_setup(args.gpus)
     if not torch.cuda.is_available():
@@ -208,14 +219,26 @@ def bench_main(args):
     x_dev = x_host.to(device)
     step_flops = sum(flops)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
-
     n_layers = len(descs)
+
+    # Eager warm-up (plans, tensor maps), then one CUDA graph for the whole
+    # 4-layer step and one per layer (per-layer times for the roofline).
+    for _ in range(args.warmup):
+        run_encoder(descs, x_dev, ws, bs, outs)
+    torch.cuda.synchronize()
+    step_graph = capture(lambda: run_encoder(descs, x_dev, ws, bs, outs))
+    layer_graphs = []
+    for i in range(n_layers):
+        src = x_dev if i == 0 else outs[i - 1]
+        layer_graphs.append(capture(lambda i=i, src=src: descs[i].forward(src, ws[i], bs[i], y=outs[i])))
+    torch.cuda.synchronize()
+
     step_ms, layer_ms = [], [[] for _ in range(n_layers)]
     # the clock sampler runs from the warm-up through the end of the timed region
     with ClockSampler(device.index) as clk:
         for _ in range(args.warmup):
-            run_encoder(descs, x_dev, ws, bs, outs)
+            flush.zero_()
+            step_graph.replay()
         torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
@@ -223,19 +246,52 @@ def bench_main(args):
         evs_all = []
         for _ in range(args.steps):
             flush.zero_()
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_layers + 1)]
-            run_encoder(descs, x_dev, ws, bs, outs, evs)
-            evs_all.append(evs)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            step_graph.replay()
+            e1.record()
+            evs_all.append((e0, e1))
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
         barrier(world)
-    for evs in evs_all:
-        step_ms.append(evs[0].elapsed_time(evs[-1]))
-        for i in range(n_layers):
-            layer_ms[i].append(evs[i].elapsed_time(evs[i + 1]))
+        # per-layer launches, each alone after an L2 flush (not part of the step time)
+        lay_evs = []
+        for _ in range(max(3, args.steps // 4)):
+            for i in range(n_layers):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                layer_graphs[i].replay()
+                e1.record()
+                lay_evs.append((i, e0, e1))
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in evs_all]
+    for i, a, b in lay_evs:
+        layer_ms[i].append(a.elapsed_time(b))
     local_ms = statistics.mean(step_ms)
     ms = max_over_ranks(local_ms, world)
     value = step_flops * world / (ms * 1e-3) / 1e12
+
+    # eager step (every call through the C ABI from Python, host overhead included)
+    eager = []
+    for _ in range(max(3, args.steps // 4)):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run_encoder(descs, x_dev, ws, bs, outs)
+        e1.record()
+        e1.synchronize()
+        eager.append(e0.elapsed_time(e1))
+    # host time of one C-ABI call (validation, plan lookup, launch), GPU kept busy meanwhile
+    torch.cuda.synchronize()
+    torch.cuda._sleep(50_000_000)
+    t0 = time.perf_counter()
+    n_calls = 200
+    for _ in range(n_calls // n_layers):
+        run_encoder(descs, x_dev, ws, bs, outs)
+    host_us = (time.perf_counter() - t0) / (n_calls // n_layers * n_layers) * 1e6
+    torch.cuda.synchronize()
 
     # per-layer roofline; the dominant kernel is the layer with the largest time
     alu_peak = fp32_alu_peak_tflops()
@@ -263,6 +319,7 @@ def bench_main(args):
     e2e_ms = []
     for it in range(args.warmup + args.steps):
         flush.zero_()
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         x_buf.copy_(x_pin, non_blocking=True)
@@ -275,11 +332,12 @@ def bench_main(args):
     e2e_t = max_over_ranks(statistics.mean(e2e_ms), world)
     e2e = {"value": round(step_flops * world / (e2e_t * 1e-3) / 1e12, 4), "unit": "TFLOPS",
            "ms_per_step": round(e2e_t, 5),
-           "h2d_bytes_per_step": x_pin.numel() * 4, "d2h_bytes_per_step": y_pin.numel() * 4}
+           "h2d_bytes_per_step": x_pin.numel() * 4, "d2h_bytes_per_step": y_pin.numel() * 4,
+           "launch": "eager C-ABI calls from Python (host overhead included)"}
 
     extra = []
     if not args.no_tensor_core and rank == 0:
-        extra = tensor_core_layers(device, peaks, flush, iters=max(5, args.steps))
+        extra = tensor_core_layers(device, peaks, flush, iters=max(5, args.steps // 4))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -294,10 +352,13 @@ def bench_main(args):
             "data": "synthetic (seeded random-walk signature matrices; Kaiming-uniform weights)",
             "config": {"workload": WORKLOAD, "global_batch": 256 * world, "layers": 4,
                        "layout": "NCHW", "l2": "flushed before every timed step (256 MiB write)",
+                       "launch": "CUDA graph of the 4 C-ABI calls",
                        "parallelism": "replicas" if world > 1 else "single_gpu"},
             "workspace_bytes": 0,
             "roofline": roofline,
             "layers": layers,
+            "eager_ms_per_step": round(statistics.mean(eager), 5),
+            "host_us_per_call": round(host_us, 2),
             "e2e": e2e,
             "gpu_launches": n_layers * args.steps,
             "clocks": clocks,
@@ -315,14 +376,17 @@ def bench_main(args):
 
 
 def time_layer(d, x, w, b, y, flush, iters, warm=3):
+    """Median / min time of one layer launched from a CUDA graph after an L2 flush."""
     for _ in range(warm):
         d.forward(x, w, b, y=y)
+    torch.cuda.synchronize()
+    g = capture(lambda: d.forward(x, w, b, y=y))
     ts = []
     for _ in range(iters):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        d.forward(x, w, b, y=y)
+        g.replay()
         e1.record()
         e1.synchronize()
         ts.append(e0.elapsed_time(e1))

@@ -148,31 +148,43 @@ conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
     return CONV2D_OK;
 }
 
-// Tensor-core tile: BM = 128 output pixels; BN output channels from
-// {64, 128, 256}.  Each k-block (64 channels at one tap) costs about
-// max(2*BN, 128 + BN) SM cycles: 128 x BN x 64 MMAs at 4096 MACs per cycle
-// against 16 KB of A plus BN x 128 B of B read from shared memory at 128 B
-// per cycle.  The chooser minimises rounds-of-persistent-CTAs x that cost,
-// wasting no more than half a tile of K.
+// Tensor-core tile: BM = 128 output pixels, BN output channels from
+// {64, 128, 256}, KSUB 64-channel k-blocks per pipeline stage.  Measured on
+// GB300: a stage hand-off costs about 0.2 us plus about 0.04 us per extra TMA
+// load in the stage, whatever the number of stages in flight; the MMAs of a
+// stage take KSUB x 2 x BN SM cycles (128 x BN x 64 MACs at 4096 per cycle).
+// A stage therefore takes the larger of the two, a tile ceil(KB / KSUB)
+// stages, and the layer (tiles / SMs rounded up) tiles per SM.  The chooser
+// minimises that, wasting no more than half a tile of K.
 conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     if (!(d.cc_major == 10 && d.cc_minor == 3)) return CONV2D_ERR_UNSUPPORTED;
     const int64_t m_tiles = (s.M + 127) / 128;
     const int64_t kb = (int64_t)s.R * s.S * ((s.C + 63) / 64);
-    int best_bn = 0;
+    const int force_bn = env_int("CONV2D_TC_BN"), force_ks = env_int("CONV2D_TC_KSUB");
+    int best_bn = 0, best_ks = 0;
     double best = 1e300;
     for (int bn : {64, 128, 256}) {
-        const int64_t n_tiles = (s.K + bn - 1) / bn;
-        if (bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1) continue;   // too much padding along K
-        const int64_t tiles = m_tiles * n_tiles;
-        const int64_t rounds = (tiles + d.sm_count - 1) / d.sm_count;
-        const double cost = (double)rounds * kb * std::max(2.0 * bn, 128.0 + bn) + rounds * 64.0;
-        if (cost < best) { best = cost; best_bn = bn; }
+        for (int ks : {1, 2, 4}) {
+            if (tc_stages(bn, ks) == 0) continue;
+            if (force_bn > 0 && bn != force_bn) continue;
+            if (force_ks > 0 && ks != force_ks) continue;
+            const int64_t n_tiles = (s.K + bn - 1) / bn;
+            if (force_bn <= 0 && bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1) continue;
+            const int64_t tiles = m_tiles * n_tiles;
+            const int64_t rounds = (tiles + d.sm_count - 1) / d.sm_count;
+            const int64_t stages_per_tile = (kb + ks - 1) / ks;
+            const int loads = 2 * (int)std::min<int64_t>(ks, kb);
+            const double handoff_ns = 200.0 + 40.0 * (loads - 1);
+            const double mma_ns = ks * 2.0 * bn / 1.9;
+            const double cost = (double)rounds * stages_per_tile * std::max(handoff_ns, mma_ns);
+            if (cost < best) { best = cost; best_bn = bn; best_ks = ks; }
+        }
     }
-    if (const char *e = std::getenv("CONV2D_TC_BN")) best_bn = std::atoi(e);
-    if (best_bn != 64 && best_bn != 128 && best_bn != 256) return CONV2D_ERR_UNSUPPORTED;
+    if (best_bn == 0) return CONV2D_ERR_UNSUPPORTED;
     TcTile t;
     t.BN = best_bn;
-    t.stages = best_bn == 64 ? 8 : (best_bn == 128 ? 6 : 4);
+    t.ksub = best_ks;
+    t.stages = tc_stages(best_bn, best_ks);
     t.tma_store = false;
     t.force_im2col = env_int("CONV2D_TC_IM2COL") == 1;
     p->algo = Algo::TensorCore;
@@ -208,7 +220,8 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
     const bool al = t == nullptr || aligned16(*t);
     const PlanKey key{dev, s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
                       (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0,
-                      env_int("CONV2D_CC_TILE"), env_int("CONV2D_TC_BN") * 4 + env_int("CONV2D_TC_IM2COL")};
+                      env_int("CONV2D_CC_TILE"),
+                      (env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 + env_int("CONV2D_TC_IM2COL")};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);
@@ -228,8 +241,8 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
     if (st != CONV2D_OK) return st;
     if (std::getenv("CONV2D_LOG")) {
         if (p.algo == Algo::TensorCore)
-            std::fprintf(stderr, "[conv2d] tensor-core BM=128 BN=%d stages=%d grid=%d smem=%zu\n",
-                         p.tc.BN, p.tc.stages, p.grid, p.smem_bytes);
+            std::fprintf(stderr, "[conv2d] tensor-core BM=128 BN=%d ksub=%d stages=%d grid=%d smem=%zu\n",
+                         p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes);
         else
             std::fprintf(stderr, "[conv2d] cuda-core tile=%d (%dx%dx%d, %dx%d/thread) grid=%d smem=%zu\n",
                          p.cc.id, p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.grid, p.smem_bytes);
@@ -358,8 +371,8 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
     conv2d_status_t st = get_plan(desc->s, desc->algo, nullptr, &p);
     if (st != CONV2D_OK) return st;
     if (p.algo == Algo::TensorCore)
-        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 stages=%d grid=%d smem=%zu a=%s",
-                      p.tc.BN, p.tc.stages, p.grid, p.smem_bytes,
+        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 ksub=%d stages=%d grid=%d smem=%zu a=%s",
+                      p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes,
                       (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
                        !p.tc.force_im2col) ? "tile" : "im2col");
     else

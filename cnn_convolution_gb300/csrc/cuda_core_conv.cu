@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cstdio>
 
 #include "internal.h"
@@ -311,11 +312,21 @@ conv2d_status_t launch_one(const Shape &s, const Tensors &t, int grid_m, int gri
                            size_t smem, cudaStream_t st) {
     using Cfg = CcCfg<T, LAYOUT, BM, BN, BK, TM, TN>;
     auto kern = cc_conv_kernel<T, LAYOUT, BM, BN, BK, TM, TN>;
-    // Opt in to >48 KB dynamic shared memory (idempotent, cheap).
+    // Opt in to >48 KB dynamic shared memory: raise the kernel's limit when a
+    // launch needs more than was set before (per device).
     if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return CONV2D_ERR_CUDA;
+        static std::atomic<int> set_bytes[64];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+        std::atomic<int> &cur = set_bytes[dev & 63];
+        if (cur.load(std::memory_order_acquire) < (int)smem) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+                return CONV2D_ERR_CUDA;
+            int prev = cur.load();
+            while (prev < (int)smem && !cur.compare_exchange_weak(prev, (int)smem)) {
+            }
+        }
     }
     CcParams p;
     p.x = t.x; p.w = t.w; p.bias = t.bias; p.y = t.y;

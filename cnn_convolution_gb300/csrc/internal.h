@@ -36,6 +36,7 @@ struct CudaCoreTile {
 struct TcTile {
     int BN;          // output channels per tile (multiple of 16, <= 256)
     int stages;      // smem pipeline depth
+    int ksub = 1;    // 64-channel k-blocks per pipeline stage
     bool tma_store;  // epilogue through shared memory + TMA store
     bool force_im2col = false;   // 1x1 layers: use the im2col map even though a plain one would do
 };
@@ -68,6 +69,7 @@ conv2d_status_t cc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaS
 // Tensor-core path (f16/bf16, NHWC).
 bool tc_shape_ok(const Shape &s, const Tensors *t);
 size_t tc_smem_bytes(const TcTile &t);
+int tc_stages(int bn, int ksub);   // 0 if the (BN, KSUB) variant does not exist
 conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
 
 // Device status word (bounded-wait failures).

@@ -29,7 +29,7 @@
 // allocator and MMA issuer, warps 2..5 = epilogue (warp w reads accumulator
 // lanes 32*(w%4) .. 32*(w%4)+31, the lane quarter that warp may access).
 //
-// Every mbarrier wait is bounded: after kWaitLimitNs the waiting thread sets
+// Every mbarrier wait is bounded: after kWaitLimitCycles the waiting thread sets
 // a CTA abort flag and the device status word, every role drains what it
 // started, tensor memory is freed, and the kernel returns.
 
@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -50,19 +51,14 @@ namespace {
 constexpr int kBM = 128;            // output pixels per tile (MMA M)
 constexpr int kBK = 64;             // channels per k-block (128 bytes of fp16/bf16)
 constexpr int kThreads = 192;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s for any single wait
+// Any single wait gives up after 4e9 SM cycles (about 2 s at the maximum clock).
+constexpr long long kWaitLimitCycles = 4000000000ll;
 constexpr int kATileBytes = kBM * kBK * 2;
 
 // ------------------------------------------------------------------ PTX wrappers
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -92,16 +88,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait on phase `parity` of an mbarrier.  Returns false (after setting
 // the abort flag and the status word) if it gave up, or if another thread of
-// the CTA already gave up.
+// the CTA already gave up.  The SM cycle counter is read only every 256 failed
+// polls: reading a timer on every poll would slow the pipeline down.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned int *status) {
     if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = global_timer_ns();
+    long long t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            const long long now = clock64();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitCycles) {
                 *abort_flag = 1;
                 if (status) atomicOr(status, 1u);
                 return false;
@@ -109,6 +109,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         }
     }
 }
+
+// Unbounded-looking drain loops are bounded by the same cycle budget.
+__device__ __forceinline__ bool cycles_left(long long t0) { return clock64() - t0 < kWaitLimitCycles; }
 
 __device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                                    int c, int w, int h, int n, uint16_t off_w,
@@ -137,6 +140,36 @@ __device__ __forceinline__ void tma_load_tile_2d(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most one committed bulk store group is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_le1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Wait until every committed bulk store group has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void epilogue_bar_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps only
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
@@ -249,11 +282,20 @@ struct TcParams {
     int total_tiles;
 };
 
-template <int BN, int STAGES>
+// Shared-memory layout: STAGES stages, each holding KSUB k-blocks (A tile then
+// B tile per k-block, every tile 1024-byte aligned), then the barriers.
+// A stage is the unit of producer/consumer hand-off: every hand-off costs a
+// fixed fraction of a microsecond on this hardware, so a stage carries
+// several k-blocks (KSUB) of MMA work.
+template <int BN, int KSUB, int STAGES>
 struct TcSmem {
     static constexpr int kBTileBytes = BN * kBK * 2;
-    static constexpr int kStageBytes = kATileBytes + kBTileBytes;
-    static constexpr size_t kBarOffset = (size_t)STAGES * kStageBytes;
+    static constexpr int kSubBytes = kATileBytes + kBTileBytes;
+    static constexpr int kStageBytes = KSUB * kSubBytes;
+    // epilogue staging: two buffers of 128 rows x 32 outputs (64 B), 64-byte swizzled
+    static constexpr int kEpiBufBytes = kBM * 32 * 2;
+    static constexpr size_t kEpiOffset = (size_t)STAGES * kStageBytes;
+    static constexpr size_t kBarOffset = kEpiOffset + 2 * kEpiBufBytes;
     // full[S], empty[S], acc_full[2], acc_empty[2], drain[1]; then tmem addr, abort flag
     static constexpr size_t kBarBytes = (2 * STAGES + 5) * 8;
     static constexpr size_t kBytes = kBarOffset + kBarBytes + 16 + 1024;   // +1024 for alignment
@@ -262,15 +304,14 @@ struct TcSmem {
 // A_TILE: the layer is a 1x1 / stride 1 / no padding convolution, so the A
 // operand is x itself viewed as the [N*H*W, C] matrix and is fetched with a
 // plain 2-D tiled map instead of an im2col one.
-template <typename T, int BN, int STAGES, bool A_TILE>
+template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const TcParams p) {
-    using L = TcSmem<BN, STAGES>;
+               const __grid_constant__ CUtensorMap tmY, const TcParams p) {
+    using L = TcSmem<BN, KSUB, STAGES>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
     constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
-    constexpr uint32_t kTxBytes = kATileBytes + L::kBTileBytes;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -284,8 +325,12 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
-    auto a_tile = [&](int s) { return smem_base + (uint32_t)(s * L::kStageBytes); };
-    auto b_tile = [&](int s) { return smem_base + (uint32_t)(s * L::kStageBytes + kATileBytes); };
+    auto a_tile = [&](int s, int j) {
+        return smem_base + (uint32_t)(s * L::kStageBytes + j * L::kSubBytes);
+    };
+    auto b_tile = [&](int s, int j) {
+        return smem_base + (uint32_t)(s * L::kStageBytes + j * L::kSubBytes + kATileBytes);
+    };
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -305,6 +350,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -321,7 +367,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // this single thread's loop is on the critical path of the pipeline.
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t n_issued = 0;
+        uint32_t n_issued = 0;       // stages filled so far
         bool ok = true;
         const int dil = p.dil;
         const int c_end = p.CB * kBK;
@@ -336,33 +382,35 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int w0 = q0 * p.stride - p.pad;
             const int k0 = tn * BN;
             int r = 0, s = 0, c = 0;
-            for (int kb = 0; kb < p.KB; ++kb) {
+            for (int kb = 0; kb < p.KB; kb += KSUB) {
+                const int nsub = min(KSUB, p.KB - kb);
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                 const uint32_t fb = full_bar(stage);
-                mbar_arrive_expect_tx(fb, kTxBytes);
-                if (A_TILE)
-                    tma_load_tile_2d(a_tile(stage), &tmA, fb, c, (int)m0);
-                else
-                    tma_load_im2col_4d(a_tile(stage), &tmA, fb, c, w0, h0, n_img,
-                                       (uint16_t)(s * dil), (uint16_t)(r * dil));
-                tma_load_tile_4d(b_tile(stage), &tmB, fb, c, s, r, k0);
+                mbar_arrive_expect_tx(fb, (uint32_t)(nsub * L::kSubBytes));
+                for (int j = 0; j < nsub; ++j) {
+                    if (A_TILE)
+                        tma_load_tile_2d(a_tile(stage, j), &tmA, fb, c, (int)m0);
+                    else
+                        tma_load_im2col_4d(a_tile(stage, j), &tmA, fb, c, w0, h0, n_img,
+                                           (uint16_t)(s * dil), (uint16_t)(r * dil));
+                    tma_load_tile_4d(b_tile(stage, j), &tmB, fb, c, s, r, k0);
+                    c += kBK;
+                    if (c >= c_end) {
+                        c = 0;
+                        if (++s == p.S) { s = 0; ++r; }
+                    }
+                }
                 ++n_issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                c += kBK;
-                if (c >= c_end) {
-                    c = 0;
-                    if (++s == p.S) { s = 0; ++r; }
-                }
             }
         }
         if (!ok) {
             // Let the copies already in flight land before the CTA goes away
-            // (one time budget for all stages together).  Load i went to stage
-            // i % STAGES with phase (i / STAGES) & 1.
-            const uint64_t t0 = global_timer_ns();
+            // (one time budget for all stages together).  Stage fill i went to
+            // stage i % STAGES with phase (i / STAGES) & 1.
+            const long long t0 = clock64();
             for (uint32_t i = n_issued > (uint32_t)STAGES ? n_issued - STAGES : 0; i < n_issued; ++i) {
-                while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) &&
-                       global_timer_ns() - t0 < kWaitLimitNs) {
+                while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) && cycles_left(t0)) {
                 }
             }
         }
@@ -373,23 +421,27 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true, any = false;
-        const uint64_t a_desc0 = smem_desc_sw128(a_tile(0));
-        const uint64_t b_desc0 = smem_desc_sw128(b_tile(0));
-        constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);   // stage stride, 16-B units
+        const uint64_t a_desc0 = smem_desc_sw128(a_tile(0, 0));
+        const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
+        constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);   // 16-byte units
+        constexpr uint64_t kSubDesc = (uint64_t)(L::kSubBytes >> 4);
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < p.KB; ++kb) {
+            for (int kb = 0; kb < p.KB; kb += KSUB) {
+                const int nsub = min(KSUB, p.KB - kb);
                 if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t ad = a_desc0 + (uint64_t)stage * kStageDesc;
-                const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc;
+                for (int j = 0; j < nsub; ++j) {
+                    const uint64_t ad = a_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
+                    const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k) {
-                    // advance 16 elements (32 bytes) along K inside the swizzled rows
-                    mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
-                            (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // advance 16 elements (32 bytes) along K inside the swizzled rows
+                        mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
+                                ((kb + j) | k) != 0 ? 1u : 0u);
+                    }
                 }
                 any = true;
                 mma_commit(empty_bar(stage));
@@ -402,18 +454,26 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (any) {
             // Make sure every MMA has retired before tensor memory is released.
             mma_commit(drain_bar);
-            uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(drain_bar, 0) && cycles_left(t0)) {
             }
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
+        // Per 32-output chunk: tcgen05.ld -> + bias -> one RN cast -> this
+        // thread's 64-byte row segment into a 64-byte-swizzled staging buffer
+        // -> one TMA store of the 128 x 32 box (clipped at M and K).  Two
+        // buffers alternate so a store drains while the next chunk is staged.
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
+        const bool issuer = threadIdx.x == 64;      // warp 2, lane 0
         const T *bias = static_cast<const T *>(p.bias);
-        T *y = static_cast<T *>(p.y);
+        const uint32_t epi_base = smem_base + (uint32_t)L::kEpiOffset;
+        const uint32_t row_off = (uint32_t)row * 64u;
+        const uint32_t swz = (uint32_t)((row >> 1) & 3);
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t chunk = 0;
         for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
             // one lane waits, the whole warp follows (tcgen05.ld needs a converged warp)
             int ok = 1;
@@ -423,38 +483,46 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_after();
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
-            const int64_t m = (int64_t)tm * kBM + row;
+            const int m0 = tm * kBM;
             const int k0 = tn * BN;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32cols(t_row + (uint32_t)c0, v);
-                if (m < p.M && k0 + c0 < p.K) {
-                    uint4 out[4];
-                    uint32_t *o = reinterpret_cast<uint32_t *>(out);
+                if (k0 + c0 >= p.K) continue;       // uniform across the epilogue warps
+                uint32_t o[16];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
-                        const int k = k0 + c0 + j;
-                        if (bias != nullptr && k < p.K) {
-                            a += load_bias<T>(bias, k);
-                            b += load_bias<T>(bias, k + 1);
-                        }
-                        o[j / 2] = pack2<T>(a, b);
+                for (int j = 0; j < 32; j += 2) {
+                    float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
+                    const int k = k0 + c0 + j;
+                    if (bias != nullptr && k < p.K) {
+                        a += load_bias<T>(bias, k);
+                        b += load_bias<T>(bias, k + 1);
                     }
-                    T *dst = y + m * p.K + k0 + c0;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (k0 + c0 + 8 * g < p.K) reinterpret_cast<uint4 *>(dst)[g] = out[g];
-                    }
+                    o[j / 2] = pack2<T>(a, b);
                 }
+                const uint32_t buf = epi_base + (chunk & 1u) * (uint32_t)L::kEpiBufBytes;
+                if (issuer) bulk_wait_read_le1();   // the store that used this buffer has read it
+                epilogue_bar_sync();
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    st_shared_v4(buf + row_off + ((((uint32_t)g) ^ swz) << 4), o[4 * g], o[4 * g + 1],
+                                 o[4 * g + 2], o[4 * g + 3]);
+                fence_proxy_async_smem();
+                epilogue_bar_sync();
+                if (issuer) {
+                    tma_store_2d(&tmY, buf, k0 + c0, m0);
+                    bulk_commit_group();
+                }
+                ++chunk;
             }
             tc_fence_before();
             __syncwarp();
             mbar_arrive(acce_bar(acc));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        if (issuer) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -499,19 +567,21 @@ bool load_driver_fns() {
     return g_encode_tiled && g_encode_im2col;
 }
 
-template <typename T, int BN, int STAGES, bool A_TILE>
-conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
-    using L = TcSmem<BN, STAGES>;
+struct TcMaps {
+    alignas(64) CUtensorMap a, b, y;
+};
+
+// Encode the three tensor maps of a launch (x as im2col or plain matrix, w, y).
+conv2d_status_t encode_maps(const Shape &s, int BN, bool a_tile, const Tensors &t, TcMaps *m) {
     if (!load_driver_fns()) return CONV2D_ERR_CUDA;
     const CUtensorMapDataType dt =
         s.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    alignas(64) CUtensorMap tmA, tmB;
-    if (A_TILE) {
+    if (a_tile) {
         const cuuint64_t dims[2] = {(cuuint64_t)s.C, (cuuint64_t)s.N * s.H * s.W};
         const cuuint64_t strides[1] = {(cuuint64_t)s.C * 2};
         const cuuint32_t box[2] = {kBK, kBM};
         const cuuint32_t estr[2] = {1, 1};
-        if (g_encode_tiled(&tmA, dt, 2, const_cast<void *>(t.x), dims, strides, box, estr,
+        if (g_encode_tiled(&m->a, dt, 2, const_cast<void *>(t.x), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -524,7 +594,7 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
         const int lower[2] = {-s.pad, -s.pad};
         const int upper[2] = {s.pad - s.dil * (s.S - 1), s.pad - s.dil * (s.R - 1)};
         const cuuint32_t estr[4] = {1, (cuuint32_t)s.stride, (cuuint32_t)s.stride, 1};
-        if (g_encode_im2col(&tmA, dt, 4, const_cast<void *>(t.x), dims, strides, lower, upper, kBK,
+        if (g_encode_im2col(&m->a, dt, 4, const_cast<void *>(t.x), dims, strides, lower, upper, kBK,
                             kBM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -534,14 +604,94 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
         const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.S, (cuuint64_t)s.R, (cuuint64_t)s.K};
         const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.S * s.C * 2,
                                        (cuuint64_t)s.R * s.S * s.C * 2};
-        const cuuint32_t box[4] = {kBK, 1, 1, BN};
+        const cuuint32_t box[4] = {kBK, 1, 1, (cuuint32_t)BN};
         const cuuint32_t estr[4] = {1, 1, 1, 1};
-        if (g_encode_tiled(&tmB, dt, 4, const_cast<void *>(t.w), dims, strides, box, estr,
+        if (g_encode_tiled(&m->b, dt, 4, const_cast<void *>(t.w), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return CONV2D_ERR_CUDA;
     }
+    {
+        // y as the [M, K] row-major matrix; boxes of 128 rows x 32 outputs
+        const cuuint64_t dims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.K * 2};
+        const cuuint32_t box[2] = {32, kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (g_encode_tiled(&m->y, dt, 2, t.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    }
+    return CONV2D_OK;
+}
+
+// Maps depend only on the layer, the tile width, the A mode and the three
+// pointers; repeated calls with the same tensors reuse them (host time).
+struct MapKey {
+    int v[14];
+    const void *x, *w, *y;
+    bool operator==(const MapKey &o) const {
+        return std::memcmp(v, o.v, sizeof(v)) == 0 && x == o.x && w == o.w && y == o.y;
+    }
+};
+
+conv2d_status_t cached_maps(const Shape &s, int BN, bool a_tile, const Tensors &t, const TcMaps **out) {
+    constexpr int kSlots = 8;
+    struct Slot {
+        MapKey key;
+        TcMaps maps;
+        bool used = false;
+    };
+    thread_local Slot slots[kSlots];
+    thread_local int next = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    MapKey k;
+    const int vals[14] = {s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
+                          (int)s.dtype, BN, a_tile ? 1 : 0, dev};
+    std::memcpy(k.v, vals, sizeof(vals));
+    k.x = t.x;
+    k.w = t.w;
+    k.y = t.y;
+    for (int i = 0; i < kSlots; ++i) {
+        if (slots[i].used && slots[i].key == k) {
+            *out = &slots[i].maps;
+            return CONV2D_OK;
+        }
+    }
+    Slot &sl = slots[next];
+    next = (next + 1) % kSlots;
+    sl.used = false;
+    conv2d_status_t st = encode_maps(s, BN, a_tile, t, &sl.maps);
+    if (st != CONV2D_OK) return st;
+    sl.key = k;
+    sl.used = true;
+    *out = &sl.maps;
+    return CONV2D_OK;
+}
+
+// cudaFuncSetAttribute once per kernel and device.
+template <typename K>
+bool ensure_smem_attr(K kern, size_t bytes) {
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const uint64_t bit = (uint64_t)1 << (dev & 63);
+    if (done_mask.load(std::memory_order_acquire) & bit) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return false;
+    done_mask.fetch_or(bit, std::memory_order_release);
+    return true;
+}
+
+template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
+conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    using L = TcSmem<BN, KSUB, STAGES>;
+    const TcMaps *maps = nullptr;
+    conv2d_status_t mst = cached_maps(s, BN, A_TILE, t, &maps);
+    if (mst != CONV2D_OK) return mst;
     TcParams p;
     p.bias = t.bias;
     p.y = t.y;
@@ -560,23 +710,29 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     const int64_t tiles = ((s.M + kBM - 1) / kBM) * (int64_t)p.n_tiles_n;
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     p.total_tiles = (int)tiles;
-    auto kern = tc_conv_kernel<T, BN, STAGES, A_TILE>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes) !=
-        cudaSuccess)
-        return CONV2D_ERR_CUDA;
+    auto kern = tc_conv_kernel<T, BN, KSUB, STAGES, A_TILE>;
+    if (!ensure_smem_attr(kern, L::kBytes)) return CONV2D_ERR_CUDA;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    kern<<<grid, kThreads, L::kBytes, st>>>(tmA, tmB, p);
+    kern<<<grid, kThreads, L::kBytes, st>>>(maps->a, maps->b, maps->y, p);
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 
+// Variants: (BN, KSUB, STAGES) with about 192 KB of stages.
+#define CONV2D_TC_VARIANTS(X) \
+    X(64, 1, 8)               \
+    X(64, 2, 4)               \
+    X(64, 4, 2)               \
+    X(128, 1, 6)              \
+    X(128, 2, 3)              \
+    X(256, 1, 4)              \
+    X(256, 2, 2)
+
 template <typename T, bool A_TILE>
 conv2d_status_t dispatch_bn(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
-    // stages: as many as fit in ~200 KB of shared memory
-    switch (pl.tc.BN) {
-        case 64: return launch_tc<T, 64, 8, A_TILE>(s, pl, t, st);
-        case 128: return launch_tc<T, 128, 6, A_TILE>(s, pl, t, st);
-        case 256: return launch_tc<T, 256, 4, A_TILE>(s, pl, t, st);
-    }
+#define CONV2D_TC_CASE(vbn, vks, vst) \
+    if (pl.tc.BN == vbn && pl.tc.ksub == vks) return launch_tc<T, vbn, vks, vst, A_TILE>(s, pl, t, st);
+    CONV2D_TC_VARIANTS(CONV2D_TC_CASE)
+#undef CONV2D_TC_CASE
     return CONV2D_ERR_INTERNAL;
 }
 
@@ -598,6 +754,7 @@ bool tc_shape_ok(const Shape &s, const Tensors *t) {
     if (up_h < -128 || up_w < -128 || up_h > 127 || up_w > 127) return false;
     if ((int64_t)s.dil * (s.R - 1) > 255 || (int64_t)s.dil * (s.S - 1) > 255) return false;
     if ((int64_t)s.N * s.H * s.W >= ((int64_t)1 << 31)) return false;
+    if (s.M >= ((int64_t)1 << 31) - 256) return false;   // row coordinates of the y map are 32-bit
     if (t) {
         auto a16 = [](const void *q) { return ((uintptr_t)q & 15) == 0; };
         if (!a16(t->x) || !a16(t->w) || !a16(t->y)) return false;
@@ -606,12 +763,19 @@ bool tc_shape_ok(const Shape &s, const Tensors *t) {
 }
 
 size_t tc_smem_bytes(const TcTile &t) {
-    switch (t.BN) {
-        case 64: return TcSmem<64, 8>::kBytes;
-        case 128: return TcSmem<128, 6>::kBytes;
-        case 256: return TcSmem<256, 4>::kBytes;
-    }
+#define CONV2D_TC_SMEM(vbn, vks, vst) \
+    if (t.BN == vbn && t.ksub == vks) return TcSmem<vbn, vks, vst>::kBytes;
+    CONV2D_TC_VARIANTS(CONV2D_TC_SMEM)
+#undef CONV2D_TC_SMEM
     return (size_t)1 << 30;
+}
+
+int tc_stages(int bn, int ksub) {
+#define CONV2D_TC_ST(vbn, vks, vst) \
+    if (bn == vbn && ksub == vks) return vst;
+    CONV2D_TC_VARIANTS(CONV2D_TC_ST)
+#undef CONV2D_TC_ST
+    return 0;
 }
 
 conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st) {

@@ -31,13 +31,15 @@ def _lib():
 
 @pytest.fixture
 def force_bn():
-    def set_bn(bn):
-        if bn is None:
-            os.environ.pop("CONV2D_TC_BN", None)
-        else:
-            os.environ["CONV2D_TC_BN"] = str(bn)
+    def set_bn(bn, ksub=None):
+        for name, v in (("CONV2D_TC_BN", bn), ("CONV2D_TC_KSUB", ksub)):
+            if v is None:
+                os.environ.pop(name, None)
+            else:
+                os.environ[name] = str(v)
     yield set_bn
     os.environ.pop("CONV2D_TC_BN", None)
+    os.environ.pop("CONV2D_TC_KSUB", None)
 
 
 SHAPES = [
@@ -60,16 +62,20 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("bn", [64, 128, 256])
+# (BN, k-blocks per pipeline stage): every compiled variant
+VARIANTS = [(64, 1), (64, 2), (64, 4), (128, 1), (128, 2), (256, 1), (256, 2)]
+
+
+@pytest.mark.parametrize("bn,ksub", VARIANTS)
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_forced_tile_widths(dtype, bn, force_bn):
-    force_bn(bn)
+def test_forced_tile_widths(dtype, bn, ksub, force_bn):
+    force_bn(bn, ksub)
     for i, (N, C, H, W, K, R, S, st, pad, dil, bias) in enumerate(SHAPES):
         spec = wl.ConvSpec(f"tc{i}", N, C, H, W, K, R, S, st, pad, dil, dtype=dtype,
                            layout="NHWC", bias=bias)
         x, w, b = wl.random_inputs(spec, seed=100 + i)
         err = full_parity(spec, x, w, b, algo="tensor_core")
-        assert err <= TOL[dtype], f"{spec} BN={bn}: err={err}"
+        assert err <= TOL[dtype], f"{spec} BN={bn} KSUB={ksub}: err={err}"
 
 
 def test_plan_reports_tensor_core():
