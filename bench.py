@@ -10,8 +10,9 @@ fraction of the dominant kernel and the extra workspace (always 0 bytes).
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
 launching stream; a step is one replay of a CUDA graph holding the 4 C-ABI
-launches (so host-side validation does not sit inside the kernel timing); L2
-is flushed (a 256 MiB write) before every timed step, outside its events.
+launches, with the L2 flush (a 256 MiB write) and the two timing events
+captured inside the same graph, so the events bracket only the 4 kernels:
+neither host-side validation nor the graph launch latency sits inside them.
 The JSON line also reports the eager (non-graph) step time, the host time of
 one C-ABI call, and an end-to-end time with host<->device copies.  Barrier + synchronize on both sides of the timed region;
 the slowest rank's time is reported.  With --gpus N > 1 (torchrun) every rank
@@ -204,6 +205,50 @@ def capture(fn):
     return g
 
 
+def timing_event():
+    """A timing event that can be recorded inside a captured CUDA graph."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:   # older torch without graph-external events
+        return None
+
+
+class TimedGraph:
+    """One CUDA graph holding [L2 flush, event, fn's launches, event].
+
+    The events are recorded inside the graph, so a replay's elapsed time covers
+    only fn's kernels: neither the graph launch latency nor the flush.  Where
+    graph-external events are unavailable, the events bracket the replay from
+    outside (launch latency included)."""
+
+    def __init__(self, fn, flush):
+        self.e0, self.e1 = timing_event(), timing_event()
+        self.inside = self.e0 is not None
+        if not self.inside:
+            self.e0 = torch.cuda.Event(enable_timing=True)
+            self.e1 = torch.cuda.Event(enable_timing=True)
+        self.flush = flush
+        self.g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g):
+            if self.inside:
+                flush.zero_()
+                self.e0.record()
+            fn()
+            if self.inside:
+                self.e1.record()
+
+    def replay_ms(self):
+        if self.inside:
+            self.g.replay()
+        else:
+            self.flush.zero_()
+            self.e0.record()
+            self.g.replay()
+            self.e1.record()
+        self.e1.synchronize()
+        return self.e0.elapsed_time(self.e1)
+
+
 def bench_main(args):
     rank, world, local = dist_setup(args.gpus)
     if not torch.cuda.is_available():
@@ -226,48 +271,33 @@ def bench_main(args):
     for _ in range(args.warmup):
         run_encoder(descs, x_dev, ws, bs, outs)
     torch.cuda.synchronize()
-    step_graph = capture(lambda: run_encoder(descs, x_dev, ws, bs, outs))
+    step_graph = TimedGraph(lambda: run_encoder(descs, x_dev, ws, bs, outs), flush)
     layer_graphs = []
     for i in range(n_layers):
         src = x_dev if i == 0 else outs[i - 1]
-        layer_graphs.append(capture(lambda i=i, src=src: descs[i].forward(src, ws[i], bs[i], y=outs[i])))
+        layer_graphs.append(TimedGraph(
+            lambda i=i, src=src: descs[i].forward(src, ws[i], bs[i], y=outs[i]), flush))
     torch.cuda.synchronize()
 
     step_ms, layer_ms = [], [[] for _ in range(n_layers)]
     # the clock sampler runs from the warm-up through the end of the timed region
     with ClockSampler(device.index) as clk:
         for _ in range(args.warmup):
-            flush.zero_()
-            step_graph.replay()
+            step_graph.replay_ms()
         torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         t_wall0 = time.perf_counter()
-        evs_all = []
         for _ in range(args.steps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            step_graph.replay()
-            e1.record()
-            evs_all.append((e0, e1))
+            step_ms.append(step_graph.replay_ms())
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
         barrier(world)
         # per-layer launches, each alone after an L2 flush (not part of the step time)
-        lay_evs = []
         for _ in range(max(3, args.steps // 4)):
             for i in range(n_layers):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                layer_graphs[i].replay()
-                e1.record()
-                lay_evs.append((i, e0, e1))
+                layer_ms[i].append(layer_graphs[i].replay_ms())
         torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in evs_all]
-    for i, a, b in lay_evs:
-        layer_ms[i].append(a.elapsed_time(b))
     local_ms = statistics.mean(step_ms)
     ms = max_over_ranks(local_ms, world)
     value = step_flops * world / (ms * 1e-3) / 1e12
@@ -352,7 +382,7 @@ def bench_main(args):
             "data": "synthetic (seeded random-walk signature matrices; Kaiming-uniform weights)",
             "config": {"workload": WORKLOAD, "global_batch": 256 * world, "layers": 4,
                        "layout": "NCHW", "l2": "flushed before every timed step (256 MiB write)",
-                       "launch": "CUDA graph of the 4 C-ABI calls",
+                       "launch": "CUDA graph of the 4 C-ABI calls; timing events inside the graph",
                        "parallelism": "replicas" if world > 1 else "single_gpu"},
             "workspace_bytes": 0,
             "roofline": roofline,
@@ -376,31 +406,24 @@ def bench_main(args):
 
 
 def time_layer(d, x, w, b, y, flush, iters, warm=3):
-    """Median / min time of one layer launched from a CUDA graph after an L2 flush."""
+    """Median / min kernel time of one layer (L2 flushed before each launch)."""
     for _ in range(warm):
         d.forward(x, w, b, y=y)
     torch.cuda.synchronize()
-    g = capture(lambda: d.forward(x, w, b, y=y))
-    ts = []
-    for _ in range(iters):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        g.replay()
-        e1.record()
-        e1.synchronize()
-        ts.append(e0.elapsed_time(e1))
+    tg = TimedGraph(lambda: d.forward(x, w, b, y=y), flush)
+    ts = [tg.replay_ms() for _ in range(iters)]
     return statistics.median(ts), min(ts)
 
 
 def tensor_core_layers(device, peaks, flush, iters=10, names=None):
-    """Time each fp16/bf16 NHWC layer alone (L2 flushed before each launch)."""
+    """Time each fp16/bf16 NHWC layer alone (L2 flushed before each launch).
+
+    With `names`, time those layers instead (any named layer, fp32 included)."""
     from cnn_convolution_gb300 import conv2d, workloads as wl
     res = []
     tc_peak = peaks["bf16_tflops"]
-    for spec in wl.TENSOR_CORE_WORKLOADS:
-        if names and spec.name not in names:
-            continue
+    specs = [wl.ALL_LAYERS[n] for n in names] if names else wl.TENSOR_CORE_WORKLOADS
+    for spec in specs:
         x, w, b = wl.workload_inputs(spec)
         d = conv2d.Conv2dDesc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S,
                               spec.stride, spec.pad, spec.dil, spec.torch_dtype, spec.layout)
@@ -413,12 +436,14 @@ def tensor_core_layers(device, peaks, flush, iters=10, names=None):
         by = layer_bytes(spec, P, Q)
         tf = fl / (med * 1e-3) / 1e12
         gbs = by / (med * 1e-3) / 1e9
-        roof_t = max(fl / (tc_peak * 1e12), by / (peaks["hbm_gbs"] * 1e9)) * 1e3
-        bound = "tensor" if fl / (tc_peak * 1e12) >= by / (peaks["hbm_gbs"] * 1e9) else "hbm"
+        cpeak = tc_peak if spec.dtype != "f32" else fp32_alu_peak_tflops()
+        roof_t = max(fl / (cpeak * 1e12), by / (peaks["hbm_gbs"] * 1e9)) * 1e3
+        bound = ("tensor" if spec.dtype != "f32" else "alu") \
+            if fl / (cpeak * 1e12) >= by / (peaks["hbm_gbs"] * 1e9) else "hbm"
         res.append({"layer": spec.name, "plan": d.plan(), "ms_median": round(med, 5),
                     "ms_min": round(mn, 5), "tflops": round(tf, 2), "hbm_gbs": round(gbs, 1),
                     "bound": bound, "roofline_frac": round(roof_t / med, 4),
-                    "tensor_frac": round(tf / tc_peak, 4), "workspace_bytes": d.workspace_bytes()})
+                    "compute_frac": round(tf / cpeak, 4), "workspace_bytes": d.workspace_bytes()})
         del xd, wd, bd, y
     return res
 
@@ -503,7 +528,7 @@ def main():
     ap.add_argument("--no-tensor-core", action="store_true", help="skip the fp16/bf16 layers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layer", default=None,
-                    help="time one named fp16/bf16 layer only (for profiling) and print its line")
+                    help="time one named layer only (for profiling) and print its line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.layer is None:
         ap.error("--warmup must be at least 3")

@@ -103,26 +103,22 @@ int env_int(const char *name) {
     return e ? std::atoi(e) : -1;
 }
 
-// Estimated time (arbitrary units) of a CUDA-core tile on this layer: the
-// busiest SM's share of tile work divided by a per-tile FFMA efficiency that
-// also falls when too few warps are resident to hide latency.
-double cc_cost(const Shape &s, const CudaCoreTile &t, int sms, size_t smem) {
+// Estimated time (arbitrary units) of a CUDA-core tile on this layer.
+// Each tile has a whole-GPU FFMA rate, measured on GB300 with enough CTAs
+// resident (`full_ctas` per SM); with fewer CTAs per SM the rate falls in
+// proportion.  Padding of M, K and the reduction to whole tiles is work too.
+double cc_cost(const Shape &s, const CudaCoreTile &t, int sms) {
+    struct Rate {
+        double tflops, full_ctas;
+    };
+    static const Rate kRates[] = {{30, 3}, {30, 1.5}, {27, 2}, {23, 3}, {22, 3}, {20, 6}};
+    const Rate r = kRates[t.id];
     const int64_t tiles = ((s.M + t.BM - 1) / t.BM) * ((s.K + t.BN - 1) / t.BN);
     const int64_t kt = (s.Kg + t.BK - 1) / t.BK;
-    const double work = (double)t.BM * t.BN * kt * t.BK;       // FMAs per tile incl. padding
-    int occ = 2048 / t.threads;
-    const int regs = t.TM * t.TN + 48;                          // rough registers per thread
-    occ = std::min(occ, 65536 / (t.threads * regs));
-    occ = std::min(occ, (int)((228 * 1024) / (smem + 1024)));
-    occ = std::max(occ, 1);
-    const double per_sm_tiles = (double)((tiles + sms - 1) / sms);
-    const double resident = std::min<double>(per_sm_tiles, occ);
-    const double warps = resident * t.threads / 32.0;
-    // FFMA share of the inner loop: TM*TN FMAs per (TM+TN)/4 shared loads.
-    const double inner = (double)(t.TM * t.TN) / (t.TM * t.TN + (t.TM + t.TN) / 4.0 + 2.0);
-    const double latency = std::min(1.0, warps / 16.0);
-    const double rate = 128.0 * inner * (0.25 + 0.75 * latency);
-    return per_sm_tiles * work / rate;
+    const double work = (double)tiles * t.BM * t.BN * kt * t.BK;   // FMAs incl. padding
+    const double per_sm = (double)tiles / sms;
+    const double fill = std::min(1.0, per_sm / r.full_ctas);
+    return work / (r.tflops * fill);
 }
 
 conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
@@ -136,7 +132,7 @@ conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
         const size_t smem = cc_smem_bytes(s, t);
         if (smem > d.smem_optin) continue;
         if (forced >= 0 && id != forced) continue;
-        const double c = cc_cost(s, t, d.sm_count, smem);
+        const double c = cc_cost(s, t, d.sm_count);
         if (c < best) { best = c; best_id = id; }
     }
     if (best_id < 0) return CONV2D_ERR_UNSUPPORTED;

@@ -671,10 +671,9 @@ conv2d_status_t cached_maps(const Shape &s, int BN, bool a_tile, const Tensors &
     return CONV2D_OK;
 }
 
-// cudaFuncSetAttribute once per kernel and device.
-template <typename K>
-bool ensure_smem_attr(K kern, size_t bytes) {
-    static std::atomic<uint64_t> done_mask{0};
+// cudaFuncSetAttribute once per device for one kernel; `done_mask` must be
+// owned by that kernel (one static per template instantiation of the caller).
+bool ensure_smem_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &done_mask) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const uint64_t bit = (uint64_t)1 << (dev & 63);
@@ -711,7 +710,9 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     p.total_tiles = (int)tiles;
     auto kern = tc_conv_kernel<T, BN, KSUB, STAGES, A_TILE>;
-    if (!ensure_smem_attr(kern, L::kBytes)) return CONV2D_ERR_CUDA;
+    static std::atomic<uint64_t> attr_done{0};   // this instantiation's per-device flags
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
+        return CONV2D_ERR_CUDA;
     const int grid = pl.grid > 0 ? pl.grid : 1;
     kern<<<grid, kThreads, L::kBytes, st>>>(maps->a, maps->b, maps->y, p);
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
