@@ -144,49 +144,76 @@ conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
     return CONV2D_OK;
 }
 
-// Tensor-core tile: BM = 128 output pixels, BN output channels from
-// {64, 128, 256}, KSUB 64-channel k-blocks per pipeline stage.  Measured on
-// GB300: a stage hand-off costs about 0.2 us plus about 0.04 us per extra TMA
-// load in the stage, whatever the number of stages in flight; the MMAs of a
-// stage take KSUB x 2 x BN SM cycles (128 x BN x 64 MACs at 4096 per cycle).
-// A stage therefore takes the larger of the two, a tile ceil(KB / KSUB)
-// stages, and the layer (tiles / SMs rounded up) tiles per SM.  The chooser
-// minimises that, wasting no more than half a tile of K.
+// Tensor-core plan: BM = 128 output pixels, BN output channels from
+// {64, 128, 256}, KSUB 64-channel k-blocks per pipeline stage, and the A mode
+// (im2col / plain matrix for 1x1, or padded-row windows for stride-1
+// layers).  Measured on GB300: one pipeline stage hand-off costs about
+// 0.2 us plus 0.04 us per extra TMA load in it, and TMA fills shared memory
+// at about 150 KB/us per SM; the MMAs of one k-block take 2 x BN SM cycles.
+// A tile takes the larger of its MMA time and its load time; the layer takes
+// (tiles / SMs rounded up) tiles per SM.  The chooser minimises that.
+double stage_ns(int loads, double bytes) {
+    return std::max(200.0 + 40.0 * (loads - 1), bytes / 150.0);
+}
+
 conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     if (!(d.cc_major == 10 && d.cc_minor == 3)) return CONV2D_ERR_UNSUPPORTED;
-    const int64_t m_tiles = (s.M + 127) / 128;
-    const int64_t kb = (int64_t)s.R * s.S * ((s.C + 63) / 64);
+    const int64_t cb = (s.C + 63) / 64;
+    const int64_t rs = (int64_t)s.R * s.S;
+    const int64_t kb = rs * cb;
     const int force_bn = env_int("CONV2D_TC_BN"), force_ks = env_int("CONV2D_TC_KSUB");
+    const int force_win = env_int("CONV2D_TC_WINDOW");
+    const bool win_ok = tc_window_ok(s);
+    const int wp = s.W + 2 * s.pad;
+    const int tr = wp > 0 ? 128 / wp : 0;
     int best_bn = 0, best_ks = 0;
+    bool best_win = false;
     double best = 1e300;
-    for (int bn : {64, 128, 256}) {
-        for (int ks : {1, 2, 4}) {
-            if (tc_stages(bn, ks) == 0) continue;
-            if (force_bn > 0 && bn != force_bn) continue;
-            if (force_ks > 0 && ks != force_ks) continue;
-            const int64_t n_tiles = (s.K + bn - 1) / bn;
-            if (force_bn <= 0 && bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1) continue;
-            const int64_t tiles = m_tiles * n_tiles;
-            const int64_t rounds = (tiles + d.sm_count - 1) / d.sm_count;
-            const int64_t stages_per_tile = (kb + ks - 1) / ks;
-            const int loads = 2 * (int)std::min<int64_t>(ks, kb);
-            const double handoff_ns = 200.0 + 40.0 * (loads - 1);
-            const double mma_ns = ks * 2.0 * bn / 1.9;
-            const double cost = (double)rounds * stages_per_tile * std::max(handoff_ns, mma_ns);
-            if (cost < best) { best = cost; best_bn = bn; best_ks = ks; }
+    for (int win = 0; win < 2; ++win) {
+        if (win && !win_ok) continue;
+        if (force_win == 1 && !win) continue;
+        if (force_win == 0 && win) continue;
+        for (int bn : {64, 128, 256}) {
+            for (int ks : {1, 2, 4}) {
+                if ((win ? tc_window_stages(bn, ks) : tc_stages(bn, ks)) == 0) continue;
+                if (force_bn > 0 && bn != force_bn) continue;
+                if (force_ks > 0 && ks != force_ks) continue;
+                const int64_t n_tiles = (s.K + bn - 1) / bn;
+                if (force_bn <= 0 && bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1) continue;
+                const int64_t m_tiles =
+                    win ? (int64_t)s.N * ((s.P + tr - 1) / tr) : (s.M + 127) / 128;
+                const int64_t rounds = (m_tiles * n_tiles + d.sm_count - 1) / d.sm_count;
+                const double b_bytes = (double)bn * 128.0;
+                double mem;
+                if (win) {
+                    const double win_bytes = (double)(tr + (s.R - 1) * s.dil) * wp * 128.0;
+                    const int64_t b_stages = (rs + ks - 1) / ks;
+                    mem = cb * (stage_ns(1, win_bytes) + b_stages * stage_ns(ks, ks * b_bytes));
+                } else {
+                    const int64_t stages = (kb + ks - 1) / ks;
+                    const int loads = 2 * (int)std::min<int64_t>(ks, kb);
+                    mem = stages * stage_ns(loads, std::min<int64_t>(ks, kb) * (16384.0 + b_bytes));
+                }
+                const double mma = kb * 2.0 * bn / 1.9;
+                const double cost = (double)rounds * std::max(mem, mma);
+                if (cost < best) { best = cost; best_bn = bn; best_ks = ks; best_win = win; }
+            }
         }
     }
     if (best_bn == 0) return CONV2D_ERR_UNSUPPORTED;
     TcTile t;
     t.BN = best_bn;
     t.ksub = best_ks;
-    t.stages = tc_stages(best_bn, best_ks);
-    t.tma_store = false;
+    t.window = best_win;
+    t.stages = best_win ? tc_window_stages(best_bn, best_ks) : tc_stages(best_bn, best_ks);
+    t.tma_store = true;
     t.force_im2col = env_int("CONV2D_TC_IM2COL") == 1;
+    t.base_off_mode = std::max(0, env_int("CONV2D_TC_BASEOFF"));
     p->algo = Algo::TensorCore;
     p->tc = t;
-    p->smem_bytes = tc_smem_bytes(t);
+    p->smem_bytes = best_win ? tc_window_smem_bytes(t) : tc_smem_bytes(t);
     if (p->smem_bytes > d.smem_optin) return CONV2D_ERR_UNSUPPORTED;
+    const int64_t m_tiles = best_win ? (int64_t)s.N * ((s.P + tr - 1) / tr) : (s.M + 127) / 128;
     const int64_t tiles = m_tiles * ((s.K + best_bn - 1) / best_bn);
     p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
     p->sm_count = d.sm_count;
@@ -217,7 +244,9 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
     const PlanKey key{dev, s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
                       (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0,
                       env_int("CONV2D_CC_TILE"),
-                      (env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 + env_int("CONV2D_TC_IM2COL")};
+                      (((env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 +
+                        env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW")) * 4 +
+                          env_int("CONV2D_TC_BASEOFF")};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);
@@ -369,8 +398,9 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
     if (p.algo == Algo::TensorCore)
         std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 ksub=%d stages=%d grid=%d smem=%zu a=%s",
                       p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes,
-                      (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
-                       !p.tc.force_im2col) ? "tile" : "im2col");
+                      p.tc.window ? "window"
+                      : (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
+                         !p.tc.force_im2col) ? "tile" : "im2col");
     else
         std::snprintf(buf, len, "cuda_core ffma BM=%d BN=%d BK=%d TM=%d TN=%d threads=%d grid=%d smem=%zu",
                       p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.threads, p.grid,

@@ -39,6 +39,8 @@ struct TcTile {
     int ksub = 1;    // 64-channel k-blocks per pipeline stage
     bool tma_store;  // epilogue through shared memory + TMA store
     bool force_im2col = false;   // 1x1 layers: use the im2col map even though a plain one would do
+    bool window = false;         // stride-1 layers: one padded input window per channel block
+    int base_off_mode = 0;       // descriptor base-offset field for row-shifted operands
 };
 
 enum class Algo { CudaCore, TensorCore };
@@ -70,6 +72,9 @@ conv2d_status_t cc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaS
 bool tc_shape_ok(const Shape &s, const Tensors *t);
 size_t tc_smem_bytes(const TcTile &t);
 int tc_stages(int bn, int ksub);   // 0 if the (BN, KSUB) variant does not exist
+bool tc_window_ok(const Shape &s);
+size_t tc_window_smem_bytes(const TcTile &t);
+int tc_window_stages(int bn, int ksub);   // 0 if the window variant does not exist
 conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
 
 // Device status word (bounded-wait failures).

@@ -148,6 +148,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  "r"(c0), "r"(c1), "r"(src)
                  : "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1,
+                                             int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -280,6 +288,13 @@ struct TcParams {
     int KB;               // k-blocks per tile = R*S*CB
     int n_tiles_n;        // tiles along K
     int total_tiles;
+    // window mode only
+    int P;                // output rows
+    int R;                // filter height
+    int Wp;               // padded row length W + 2*pad (rows of the window)
+    int TR;               // output rows per tile (TR * Wp <= 128)
+    int tiles_per_img;    // ceil(P / TR)
+    int base_off_mode;    // descriptor base-offset field for row-shifted A operands
 };
 
 // Shared-memory layout: STAGES stages, each holding KSUB k-blocks (A tile then
@@ -534,6 +549,276 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 }
 
+// ------------------------------------------------------------------ window (im2win) mode
+//
+// Stride-1 layers.  An M tile is TR whole rows of the *padded* output grid
+// (TR * Wp <= 128 pixels, Wp = W + 2*pad): pixel j of the tile is output
+// (p0 + j / Wp, j % Wp); columns j % Wp >= Q are computed and dropped.  In the
+// padded, row-major flattening of the input, every filter tap (r, s) of such
+// a tile reads the SAME pixels shifted by r*dil*Wp + s*dil rows.  So for each
+// 64-channel block the kernel loads one window of TR + (R-1)*dil padded input
+// rows (a tiled TMA box starting at column -pad: its out-of-image part is
+// zero-filled, which is the padding) and runs the MMAs of all R*S taps on it,
+// moving only the A descriptor's start row.  This is the memory-efficient
+// im2win scheme of "Enabling Memory-efficient Im2win Convolution with
+// Multi-precision Support on GPU CUDA and Tensor Cores" (abstract: windows
+// with contiguous access for all kernel sizes), done by the copy engine:
+// a 3x3 layer loads each input window once per channel block instead of
+// nine 128-pixel im2col tiles.
+//
+// Shared memory: two window slots, STAGES stages of KSUB weight tiles, the
+// epilogue staging buffers, barriers.  Weights stream per (tap, channel block).
+template <int BN, int KSUB, int STAGES>
+struct TcWinSmem {
+    static constexpr int kWinBytes = 48 * 1024;        // (max row shift + 128) rows of 128 B
+    static constexpr int kWinRows = kWinBytes / 128;
+    static constexpr int kBTileBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = KSUB * kBTileBytes;
+    static constexpr size_t kStageOffset = 2 * (size_t)kWinBytes;
+    static constexpr int kEpiBufBytes = kBM * 32 * 2;
+    static constexpr size_t kEpiOffset = kStageOffset + (size_t)STAGES * kStageBytes;
+    static constexpr size_t kBarOffset = kEpiOffset + 2 * kEpiBufBytes;
+    // full[S], empty[S], win_full[2], win_empty[2], acc_full[2], acc_empty[2], drain
+    static constexpr size_t kBarBytes = (2 * STAGES + 9) * 8;
+    static constexpr size_t kBytes = kBarOffset + kBarBytes + 16 + 1024;
+};
+
+template <typename T, int BN, int KSUB, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmY, const TcParams p) {
+    using L = TcWinSmem<BN, KSUB, STAGES>;
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
+    constexpr uint32_t kTmemCols = 2 * BN;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t bar_base = smem_base + (uint32_t)L::kBarOffset;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto wfull_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + w); };
+    auto wempty_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 2 + w); };
+    auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 4 + a); };
+    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 6 + a); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 8);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
+    auto win_slot = [&](int w) { return smem_base + (uint32_t)(w * L::kWinBytes); };
+    auto b_tile = [&](int s, int j) {
+        return smem_base + (uint32_t)(L::kStageOffset + s * L::kStageBytes + j * L::kBTileBytes);
+    };
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int RS = p.R * p.S;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(wfull_bar(a), 1);
+            mbar_init(wempty_bar(a), 1);
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), 128);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmY);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const uint32_t win_tx = (uint32_t)((p.TR + (p.R - 1) * p.dil) * p.Wp * 128);
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------- TMA producer
+        int stage = 0, wslot = 0;
+        uint32_t phase = 0, wphase = 0;
+        uint32_t n_b = 0, n_w = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            const int tm = tile / p.n_tiles_n;
+            const int tn = tile - tm * p.n_tiles_n;
+            const int n_img = tm / p.tiles_per_img;
+            const int p0 = (tm - n_img * p.tiles_per_img) * p.TR;
+            const int k0 = tn * BN;
+            for (int cb = 0; cb < p.CB && ok; ++cb) {
+                if (!mbar_wait(wempty_bar(wslot), wphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                mbar_arrive_expect_tx(wfull_bar(wslot), win_tx);
+                tma_load_tile_4d(win_slot(wslot), &tmA, wfull_bar(wslot), cb * kBK, -p.pad, p0 - p.pad,
+                                 n_img);
+                ++n_w;
+                if (++wslot == 2) { wslot = 0; wphase ^= 1u; }
+                int r = 0, s = 0;
+                for (int t0 = 0; t0 < RS; t0 += KSUB) {
+                    const int nsub = min(KSUB, RS - t0);
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, (uint32_t)(nsub * L::kBTileBytes));
+                    for (int j = 0; j < nsub; ++j) {
+                        tma_load_tile_4d(b_tile(stage, j), &tmB, fb, cb * kBK, s, r, k0);
+                        if (++s == p.S) { s = 0; ++r; }
+                    }
+                    ++n_b;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+        if (!ok) {
+            // Let the copies already in flight land before the CTA goes away.
+            const long long t0 = clock64();
+            for (uint32_t i = n_b > (uint32_t)STAGES ? n_b - STAGES : 0; i < n_b; ++i)
+                while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) && cycles_left(t0)) {
+                }
+            for (uint32_t i = n_w > 2u ? n_w - 2u : 0; i < n_w; ++i)
+                while (!mbar_try_wait(wfull_bar((int)(i % 2)), (i / 2) & 1u) && cycles_left(t0)) {
+                }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        int stage = 0, wslot = 0, acc = 0;
+        uint32_t phase = 0, wphase = 0, acc_phase = 0;
+        bool ok = true, any = false;
+        const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
+        constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);
+        constexpr uint64_t kSubDesc = (uint64_t)(L::kBTileBytes >> 4);
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int cb = 0; cb < p.CB && ok; ++cb) {
+                if (!mbar_wait(wfull_bar(wslot), wphase, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t wbase = win_slot(wslot);
+                int r = 0, s = 0;
+                for (int t0 = 0; t0 < RS; t0 += KSUB) {
+                    const int nsub = min(KSUB, RS - t0);
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int j = 0; j < nsub; ++j) {
+                        // tap (r, s): the window's rows shifted by r*dil*Wp + s*dil pixels
+                        const uint32_t a_start = wbase + (uint32_t)((r * p.dil * p.Wp + s * p.dil) * 128);
+                        uint64_t ad = smem_desc_sw128(a_start);
+                        if (p.base_off_mode) ad |= (uint64_t)((a_start >> 7) & 7u) << 49;
+                        const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k)
+                            mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
+                                    (cb | (t0 + j) | k) != 0 ? 1u : 0u);
+                        if (++s == p.S) { s = 0; ++r; }
+                    }
+                    any = true;
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(wempty_bar(wslot));
+                if (++wslot == 2) { wslot = 0; wphase ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit(accf_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (any) {
+            mma_commit(drain_bar);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(drain_bar, 0) && cycles_left(t0)) {
+            }
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------- epilogue
+        // Accumulator lane j is padded-grid pixel (j / Wp, j % Wp); valid lanes
+        // are compacted into the staging buffer as rows i*Q + q, which is the
+        // layout of a (32 outputs x Q x TR x 1) box of the 4-D y map.
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int ti = row / p.Wp, tq = row - ti * p.Wp;
+        const bool valid = ti < p.TR && tq < p.Q;
+        const int srow = ti * p.Q + tq;
+        const uint32_t row_off = (uint32_t)srow * 64u;
+        const uint32_t swz = (uint32_t)((srow >> 1) & 3);
+        const bool issuer = threadIdx.x == 64;
+        const T *bias = static_cast<const T *>(p.bias);
+        const uint32_t epi_base = smem_base + (uint32_t)L::kEpiOffset;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t chunk = 0;
+        for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int tm = tile / p.n_tiles_n;
+            const int tn = tile - tm * p.n_tiles_n;
+            const int n_img = tm / p.tiles_per_img;
+            const int p0 = (tm - n_img * p.tiles_per_img) * p.TR;
+            const int k0 = tn * BN;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32cols(t_row + (uint32_t)c0, v);
+                if (k0 + c0 >= p.K) continue;
+                uint32_t o[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
+                    const int k = k0 + c0 + j;
+                    if (bias != nullptr && k < p.K) {
+                        a += load_bias<T>(bias, k);
+                        b += load_bias<T>(bias, k + 1);
+                    }
+                    o[j / 2] = pack2<T>(a, b);
+                }
+                const uint32_t buf = epi_base + (chunk & 1u) * (uint32_t)L::kEpiBufBytes;
+                if (issuer) bulk_wait_read_le1();
+                epilogue_bar_sync();
+                if (valid) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        st_shared_v4(buf + row_off + ((((uint32_t)g) ^ swz) << 4), o[4 * g],
+                                     o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
+                }
+                fence_proxy_async_smem();
+                epilogue_bar_sync();
+                if (issuer) {
+                    tma_store_4d(&tmY, buf, k0 + c0, 0, p0, n_img);
+                    bulk_commit_group();
+                }
+                ++chunk;
+            }
+            tc_fence_before();
+            __syncwarp();
+            mbar_arrive(acce_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (issuer) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -572,11 +857,39 @@ struct TcMaps {
 };
 
 // Encode the three tensor maps of a launch (x as im2col or plain matrix, w, y).
-conv2d_status_t encode_maps(const Shape &s, int BN, bool a_tile, const Tensors &t, TcMaps *m) {
+// Window geometry of a stride-1 layer (see the window kernel).
+struct WinGeom {
+    int Wp, TR, TRW, max_shift;
+};
+WinGeom win_geom(const Shape &s) {
+    WinGeom g;
+    g.Wp = s.W + 2 * s.pad;
+    g.TR = g.Wp > 0 ? kBM / g.Wp : 0;
+    g.TRW = g.TR + (s.R - 1) * s.dil;
+    g.max_shift = (s.R - 1) * s.dil * g.Wp + (s.S - 1) * s.dil;
+    return g;
+}
+
+// amode: 0 = im2col A, 1 = plain [N*H*W, C] A, 2 = window A.
+conv2d_status_t encode_maps(const Shape &s, int BN, int amode, const Tensors &t, TcMaps *m) {
     if (!load_driver_fns()) return CONV2D_ERR_CUDA;
     const CUtensorMapDataType dt =
         s.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (a_tile) {
+    const bool a_tile = amode == 1;
+    if (amode == 2) {
+        // x as (C, W, H, N); box = 64 channels x Wp columns x TRW rows x 1 image
+        const WinGeom g = win_geom(s);
+        const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.W * s.C * 2,
+                                       (cuuint64_t)s.H * s.W * s.C * 2};
+        const cuuint32_t box[4] = {kBK, (cuuint32_t)g.Wp, (cuuint32_t)g.TRW, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (g_encode_tiled(&m->a, dt, 4, const_cast<void *>(t.x), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    } else if (a_tile) {
         const cuuint64_t dims[2] = {(cuuint64_t)s.C, (cuuint64_t)s.N * s.H * s.W};
         const cuuint64_t strides[1] = {(cuuint64_t)s.C * 2};
         const cuuint32_t box[2] = {kBK, kBM};
@@ -612,7 +925,19 @@ conv2d_status_t encode_maps(const Shape &s, int BN, bool a_tile, const Tensors &
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return CONV2D_ERR_CUDA;
     }
-    {
+    if (amode == 2) {
+        // y as (K, Q, P, N); boxes of 32 outputs x Q columns x TR rows x 1 image
+        const WinGeom g = win_geom(s);
+        const cuuint64_t dims[4] = {(cuuint64_t)s.K, (cuuint64_t)s.Q, (cuuint64_t)s.P, (cuuint64_t)s.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)s.K * 2, (cuuint64_t)s.Q * s.K * 2,
+                                       (cuuint64_t)s.P * s.Q * s.K * 2};
+        const cuuint32_t box[4] = {32, (cuuint32_t)s.Q, (cuuint32_t)g.TR, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (g_encode_tiled(&m->y, dt, 4, t.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    } else {
         // y as the [M, K] row-major matrix; boxes of 128 rows x 32 outputs
         const cuuint64_t dims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
         const cuuint64_t strides[1] = {(cuuint64_t)s.K * 2};
@@ -636,7 +961,7 @@ struct MapKey {
     }
 };
 
-conv2d_status_t cached_maps(const Shape &s, int BN, bool a_tile, const Tensors &t, const TcMaps **out) {
+conv2d_status_t cached_maps(const Shape &s, int BN, int amode, const Tensors &t, const TcMaps **out) {
     constexpr int kSlots = 8;
     struct Slot {
         MapKey key;
@@ -649,7 +974,7 @@ conv2d_status_t cached_maps(const Shape &s, int BN, bool a_tile, const Tensors &
     cudaGetDevice(&dev);
     MapKey k;
     const int vals[14] = {s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
-                          (int)s.dtype, BN, a_tile ? 1 : 0, dev};
+                          (int)s.dtype, BN, amode, dev};
     std::memcpy(k.v, vals, sizeof(vals));
     k.x = t.x;
     k.w = t.w;
@@ -663,7 +988,7 @@ conv2d_status_t cached_maps(const Shape &s, int BN, bool a_tile, const Tensors &
     Slot &sl = slots[next];
     next = (next + 1) % kSlots;
     sl.used = false;
-    conv2d_status_t st = encode_maps(s, BN, a_tile, t, &sl.maps);
+    conv2d_status_t st = encode_maps(s, BN, amode, t, &sl.maps);
     if (st != CONV2D_OK) return st;
     sl.key = k;
     sl.used = true;
@@ -689,7 +1014,7 @@ template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
 conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
     using L = TcSmem<BN, KSUB, STAGES>;
     const TcMaps *maps = nullptr;
-    conv2d_status_t mst = cached_maps(s, BN, A_TILE, t, &maps);
+    conv2d_status_t mst = cached_maps(s, BN, A_TILE ? 1 : 0, t, &maps);
     if (mst != CONV2D_OK) return mst;
     TcParams p;
     p.bias = t.bias;
@@ -718,6 +1043,46 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 
+template <typename T, int BN, int KSUB, int STAGES>
+conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    using L = TcWinSmem<BN, KSUB, STAGES>;
+    const TcMaps *maps = nullptr;
+    conv2d_status_t mst = cached_maps(s, BN, 2, t, &maps);
+    if (mst != CONV2D_OK) return mst;
+    const WinGeom g = win_geom(s);
+    TcParams p;
+    p.bias = t.bias;
+    p.y = t.y;
+    p.status = status_word_ptr();
+    p.M = s.M;
+    p.K = s.K;
+    p.PQ = s.P * s.Q;
+    p.Q = s.Q;
+    p.stride = s.stride;
+    p.pad = s.pad;
+    p.dil = s.dil;
+    p.S = s.S;
+    p.CB = (s.C + kBK - 1) / kBK;
+    p.KB = s.R * s.S * p.CB;
+    p.n_tiles_n = (s.K + BN - 1) / BN;
+    p.P = s.P;
+    p.R = s.R;
+    p.Wp = g.Wp;
+    p.TR = g.TR;
+    p.tiles_per_img = (s.P + g.TR - 1) / g.TR;
+    p.base_off_mode = pl.tc.base_off_mode;
+    const int64_t tiles = (int64_t)s.N * p.tiles_per_img * p.n_tiles_n;
+    if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
+    p.total_tiles = (int)tiles;
+    auto kern = tc_conv_window_kernel<T, BN, KSUB, STAGES>;
+    static std::atomic<uint64_t> attr_done{0};
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
+        return CONV2D_ERR_CUDA;
+    const int grid = pl.grid > 0 ? pl.grid : 1;
+    kern<<<grid, kThreads, L::kBytes, st>>>(maps->a, maps->b, maps->y, p);
+    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
 // Variants: (BN, KSUB, STAGES) with about 192 KB of stages.
 #define CONV2D_TC_VARIANTS(X) \
     X(64, 1, 8)               \
@@ -727,6 +1092,21 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     X(128, 2, 3)              \
     X(256, 1, 4)              \
     X(256, 2, 2)
+
+// Window-mode variants: 96 KB of window slots + 3 stages of 32 KB weight tiles.
+#define CONV2D_TC_WIN_VARIANTS(X) \
+    X(64, 4, 3)                   \
+    X(128, 2, 3)                  \
+    X(256, 1, 3)
+
+template <typename T>
+conv2d_status_t dispatch_window(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+#define CONV2D_TC_WCASE(vbn, vks, vst) \
+    if (pl.tc.BN == vbn && pl.tc.ksub == vks) return launch_tc_window<T, vbn, vks, vst>(s, pl, t, st);
+    CONV2D_TC_WIN_VARIANTS(CONV2D_TC_WCASE)
+#undef CONV2D_TC_WCASE
+    return CONV2D_ERR_INTERNAL;
+}
 
 template <typename T, bool A_TILE>
 conv2d_status_t dispatch_bn(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
@@ -771,6 +1151,33 @@ size_t tc_smem_bytes(const TcTile &t) {
     return (size_t)1 << 30;
 }
 
+size_t tc_window_smem_bytes(const TcTile &t) {
+#define CONV2D_TC_WSMEM(vbn, vks, vst) \
+    if (t.BN == vbn && t.ksub == vks) return TcWinSmem<vbn, vks, vst>::kBytes;
+    CONV2D_TC_WIN_VARIANTS(CONV2D_TC_WSMEM)
+#undef CONV2D_TC_WSMEM
+    return (size_t)1 << 30;
+}
+
+int tc_window_stages(int bn, int ksub) {
+#define CONV2D_TC_WST(vbn, vks, vst) \
+    if (bn == vbn && ksub == vks) return vst;
+    CONV2D_TC_WIN_VARIANTS(CONV2D_TC_WST)
+#undef CONV2D_TC_WST
+    return 0;
+}
+
+// Window mode needs stride 1, padded rows of at most 128 pixels, and the
+// shifted window (largest tap shift + 128 rows) inside one window slot.
+bool tc_window_ok(const Shape &s) {
+    if (s.stride != 1) return false;
+    const WinGeom g = win_geom(s);
+    if (g.Wp > kBM || g.TR < 1) return false;
+    if (g.TRW > 256) return false;
+    if (g.max_shift + kBM > TcWinSmem<64, 4, 3>::kWinRows) return false;
+    return true;
+}
+
 int tc_stages(int bn, int ksub) {
 #define CONV2D_TC_ST(vbn, vks, vst) \
     if (bn == vbn && ksub == vks) return vst;
@@ -780,6 +1187,11 @@ int tc_stages(int bn, int ksub) {
 }
 
 conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st) {
+    if (p.tc.window) {
+        if (!tc_window_ok(s)) return CONV2D_ERR_INTERNAL;
+        if (s.dtype == CONV2D_BF16) return dispatch_window<__nv_bfloat16>(s, p, t, st);
+        return dispatch_window<__half>(s, p, t, st);
+    }
     const bool a_tile = plain_matrix_a(s) && !p.tc.force_im2col;
     if (s.dtype == CONV2D_BF16)
         return a_tile ? dispatch_bn<__nv_bfloat16, true>(s, p, t, st)
