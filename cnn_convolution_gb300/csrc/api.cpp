@@ -208,7 +208,6 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     t.stages = best_win ? tc_window_stages(best_bn, best_ks) : tc_stages(best_bn, best_ks);
     t.tma_store = true;
     t.force_im2col = env_int("CONV2D_TC_IM2COL") == 1;
-    t.base_off_mode = std::max(0, env_int("CONV2D_TC_BASEOFF"));
     p->algo = Algo::TensorCore;
     p->tc = t;
     p->smem_bytes = best_win ? tc_window_smem_bytes(t) : tc_smem_bytes(t);
@@ -245,8 +244,7 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
                       (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0,
                       env_int("CONV2D_CC_TILE"),
                       (((env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 +
-                        env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW")) * 4 +
-                          env_int("CONV2D_TC_BASEOFF")};
+                        env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW"))};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);

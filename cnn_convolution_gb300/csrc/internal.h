@@ -40,7 +40,6 @@ struct TcTile {
     bool tma_store;  // epilogue through shared memory + TMA store
     bool force_im2col = false;   // 1x1 layers: use the im2col map even though a plain one would do
     bool window = false;         // stride-1 layers: one padded input window per channel block
-    int base_off_mode = 0;       // descriptor base-offset field for row-shifted operands
 };
 
 enum class Algo { CudaCore, TensorCore };

@@ -294,7 +294,6 @@ struct TcParams {
     int Wp;               // padded row length W + 2*pad (rows of the window)
     int TR;               // output rows per tile (TR * Wp <= 128)
     int tiles_per_img;    // ceil(P / TR)
-    int base_off_mode;    // descriptor base-offset field for row-shifted A operands
 };
 
 // Shared-memory layout: STAGES stages, each holding KSUB k-blocks (A tile then
@@ -710,10 +709,12 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
                     for (int j = 0; j < nsub; ++j) {
-                        // tap (r, s): the window's rows shifted by r*dil*Wp + s*dil pixels
+                        // tap (r, s): the window's rows shifted by r*dil*Wp + s*dil pixels.
+                        // The start row need not be a multiple of 8: the 128-byte
+                        // swizzle follows absolute shared-memory address bits, so
+                        // the descriptor's base-offset field stays 0.
                         const uint32_t a_start = wbase + (uint32_t)((r * p.dil * p.Wp + s * p.dil) * 128);
-                        uint64_t ad = smem_desc_sw128(a_start);
-                        if (p.base_off_mode) ad |= (uint64_t)((a_start >> 7) & 7u) << 49;
+                        const uint64_t ad = smem_desc_sw128(a_start);
                         const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k)
@@ -1070,7 +1071,6 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     p.Wp = g.Wp;
     p.TR = g.TR;
     p.tiles_per_img = (s.P + g.TR - 1) / g.TR;
-    p.base_off_mode = pl.tc.base_off_mode;
     const int64_t tiles = (int64_t)s.N * p.tiles_per_img * p.n_tiles_n;
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     p.total_tiles = (int)tiles;

@@ -118,3 +118,45 @@ def test_1x1_plain_and_im2col_maps(im2col, force_bn):
             assert err <= TOL["bf16"], f"{spec}: {err}"
     finally:
         os.environ.pop("CONV2D_TC_IM2COL", None)
+
+
+WINDOW_SHAPES = [
+    # stride-1 layers: N, C, H, W, K, R, S, pad, dil, bias
+    (1, 64, 8, 8, 64, 3, 3, 1, 1, True),
+    (2, 64, 10, 12, 64, 3, 3, 1, 1, False),
+    (2, 128, 9, 7, 128, 3, 3, 1, 1, True),
+    (2, 64, 13, 13, 64, 5, 5, 2, 1, True),
+    (1, 64, 6, 9, 64, 3, 2, 0, 2, True),           # dilation, non-square filter, no padding
+    (3, 72, 11, 10, 136, 3, 3, 1, 1, True),        # channel tails, ragged K
+    (2, 8, 20, 30, 24, 7, 7, 3, 1, False),         # 7x7, tiny C
+    (2, 64, 5, 126, 64, 3, 3, 1, 1, True),         # padded row of 128 pixels: one row per tile
+    (4, 32, 3, 3, 16, 3, 3, 1, 1, True),           # output rows fewer than rows per tile
+    (2, 16, 9, 9, 32, 1, 5, 0, 1, True),           # 1 x 5 filter, no padding
+]
+
+
+@pytest.mark.parametrize("bn,ksub", [(64, 4), (128, 2), (256, 1)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_window_mode(dtype, bn, ksub, force_bn):
+    """Stride-1 layers with one padded input window per channel block, the
+    filter taps taken as row shifts of it."""
+    force_bn(bn, ksub)
+    os.environ["CONV2D_TC_WINDOW"] = "1"
+    try:
+        for i, (N, C, H, W, K, R, S, pad, dil, bias) in enumerate(WINDOW_SHAPES):
+            spec = wl.ConvSpec(f"win{i}", N, C, H, W, K, R, S, 1, pad, dil, dtype=dtype,
+                               layout="NHWC", bias=bias)
+            x, w, b = wl.random_inputs(spec, seed=200 + i)
+            y, d = run_gpu(spec, x, w, b, "tensor_core")
+            assert "a=window" in d.plan(), d.plan()
+            err = full_parity(spec, x, w, b, algo="tensor_core")
+            assert err <= TOL[dtype], f"{spec} BN={bn}: err={err}"
+    finally:
+        os.environ.pop("CONV2D_TC_WINDOW", None)
+
+
+def test_window_mode_not_used_where_it_cannot_apply():
+    # stride 2, and a padded row longer than 128 pixels, stay on im2col
+    for (H, W, st) in [(14, 14, 2), (8, 200, 1)]:
+        d = conv2d.Conv2dDesc(2, 64, H, W, 64, 3, 3, st, 1, 1, torch.bfloat16, "NHWC")
+        assert "a=im2col" in d.plan(), d.plan()
