@@ -147,13 +147,14 @@ conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
 // Tensor-core plan: BM = 128 output pixels, BN output channels from
 // {64, 128, 256}, KSUB 64-channel k-blocks per pipeline stage, and the A mode
 // (im2col / plain matrix for 1x1, or padded-row windows for stride-1
-// layers).  Measured on GB300: one pipeline stage hand-off costs about
-// 0.2 us plus 0.04 us per extra TMA load in it, and TMA fills shared memory
-// at about 150 KB/us per SM; the MMAs of one k-block take 2 x BN SM cycles.
-// A tile takes the larger of its MMA time and its load time; the layer takes
-// (tiles / SMs rounded up) tiles per SM.  The chooser minimises that.
-double stage_ns(int loads, double bytes) {
-    return std::max(200.0 + 40.0 * (loads - 1), bytes / 150.0);
+// layers).  Measured on GB300, a pipeline stage costs about 0.18 us plus
+// 0.09 us per TMA instruction in it, largely independent of the bytes moved
+// (TMA fills shared memory at up to about 150 KB/us per SM); the MMAs of one
+// k-block take 2 x BN SM cycles.  A tile takes the larger of its MMA time and
+// its load time; the layer takes (tiles / SMs rounded up) tiles per SM.  The
+// chooser minimises that.
+double stage_ns(int instructions, double bytes) {
+    return std::max(180.0 + 90.0 * instructions, bytes / 150.0);
 }
 
 conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
@@ -188,11 +189,14 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
                 if (win) {
                     const double win_bytes = (double)(tr + (s.R - 1) * s.dil) * wp * 128.0;
                     const int64_t b_stages = (rs + ks - 1) / ks;
-                    mem = cb * (stage_ns(1, win_bytes) + b_stages * stage_ns(ks, ks * b_bytes));
+                    mem = cb * (stage_ns(1, win_bytes) + b_stages * stage_ns(1, ks * b_bytes));
+                } else if (s.R * s.S == 1 && s.stride == 1 && s.pad == 0 && s.C % 64 == 0) {
+                    const int64_t stages = (cb + ks - 1) / ks;       // one A box + one B box per stage
+                    mem = stages * stage_ns(2, ks * (16384.0 + b_bytes));
                 } else {
-                    const int64_t stages = (kb + ks - 1) / ks;
-                    const int loads = 2 * (int)std::min<int64_t>(ks, kb);
-                    mem = stages * stage_ns(loads, std::min<int64_t>(ks, kb) * (16384.0 + b_bytes));
+                    const int64_t per_cb = (rs + ks - 1) / ks;
+                    const int a_loads = (int)std::min<int64_t>(ks, rs);
+                    mem = cb * per_cb * stage_ns(a_loads + 1, a_loads * 16384.0 + ks * b_bytes);
                 }
                 const double mma = kb * 2.0 * bn / 1.9;
                 const double cost = (double)rounds * std::max(mem, mma);

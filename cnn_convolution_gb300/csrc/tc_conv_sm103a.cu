@@ -124,6 +124,15 @@ __device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorM
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_tile_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_tile_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                                  int c0, int c1, int c2, int c3) {
     asm volatile(
@@ -275,6 +284,27 @@ template <> __device__ __forceinline__ float load_bias<__nv_bfloat16>(const __nv
     return __bfloat162float(b[k]);
 }
 
+// Optional timeline trace of CTA 0 (compile with -DCONV2D_TC_TRACE; off in
+// the library build): SM-cycle timestamps of the pipeline events, read back
+// with conv2d_tc_trace_dump().
+#ifdef CONV2D_TC_TRACE
+__device__ unsigned long long g_tc_trace[4][8192];
+__device__ unsigned int g_tc_trace_n[4];
+#define TC_TRACE(role, tag)                                                                  \
+    do {                                                                                     \
+        if (blockIdx.x == 0) {                                                               \
+            const unsigned i_ = atomicAdd(&g_tc_trace_n[role], 1u);                          \
+            if (i_ < 8192u)                                                                  \
+                g_tc_trace[role][i_] =                                                       \
+                    ((unsigned long long)(tag) << 48) | ((unsigned long long)clock64() & 0xFFFFFFFFFFFFull); \
+        }                                                                                    \
+    } while (0)
+#else
+#define TC_TRACE(role, tag) \
+    do {                    \
+    } while (0)
+#endif
+
 struct TcParams {
     const void *bias;
     void *y;
@@ -286,6 +316,8 @@ struct TcParams {
     int S;                // filter width
     int CB;               // channel blocks of 64
     int KB;               // k-blocks per tile = R*S*CB
+    int n_outer, n_inner; // k-block loop: outer x inner (see the producer)
+    int chunked;          // 1x1 plain layer with C % 64 == 0: inner = channel blocks
     int n_tiles_n;        // tiles along K
     int total_tiles;
     // window mode only
@@ -296,16 +328,16 @@ struct TcParams {
     int tiles_per_img;    // ceil(P / TR)
 };
 
-// Shared-memory layout: STAGES stages, each holding KSUB k-blocks (A tile then
-// B tile per k-block, every tile 1024-byte aligned), then the barriers.
-// A stage is the unit of producer/consumer hand-off: every hand-off costs a
-// fixed fraction of a microsecond on this hardware, so a stage carries
-// several k-blocks (KSUB) of MMA work.
+// Shared-memory layout: STAGES stages, each holding KSUB k-blocks (the KSUB A
+// tiles, then the KSUB B tiles, every tile 1024-byte aligned), the epilogue
+// staging buffers, then the barriers.  A stage is the unit of producer /
+// consumer hand-off.  Measured on GB300, TMA cost is per instruction and per
+// stage rather than per byte, so a stage carries KSUB k-blocks and its B tiles
+// (and, for 1x1 layers, its A tiles) arrive in ONE 3-D box each.
 template <int BN, int KSUB, int STAGES>
 struct TcSmem {
     static constexpr int kBTileBytes = BN * kBK * 2;
-    static constexpr int kSubBytes = kATileBytes + kBTileBytes;
-    static constexpr int kStageBytes = KSUB * kSubBytes;
+    static constexpr int kStageBytes = KSUB * (kATileBytes + kBTileBytes);
     // epilogue staging: two buffers of 128 rows x 32 outputs (64 B), 64-byte swizzled
     static constexpr int kEpiBufBytes = kBM * 32 * 2;
     static constexpr size_t kEpiOffset = (size_t)STAGES * kStageBytes;
@@ -340,10 +372,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
     auto a_tile = [&](int s, int j) {
-        return smem_base + (uint32_t)(s * L::kStageBytes + j * L::kSubBytes);
+        return smem_base + (uint32_t)(s * L::kStageBytes + j * kATileBytes);
     };
     auto b_tile = [&](int s, int j) {
-        return smem_base + (uint32_t)(s * L::kStageBytes + j * L::kSubBytes + kATileBytes);
+        return smem_base + (uint32_t)(s * L::kStageBytes + KSUB * kATileBytes + j * L::kBTileBytes);
     };
 
     const int warp = threadIdx.x / 32;
@@ -377,14 +409,17 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- TMA producer
-        // The k-block coordinates (r, s, channel block) advance incrementally:
-        // this single thread's loop is on the critical path of the pipeline.
+        // k-blocks run as n_outer x n_inner: channel blocks x filter taps, or
+        // (1x1 layers with C % 64 == 0) 1 x channel blocks.  A stage holds up to
+        // KSUB consecutive inner k-blocks; its B tiles are one 3-D box of the
+        // weight map (64 channels x BN outputs x KSUB taps or channel blocks)
+        // and, for 1x1 layers, its A tiles are one 3-D box too.  This single
+        // thread's loop is on the critical path: no divisions per k-block.
         int stage = 0;
         uint32_t phase = 0;
         uint32_t n_issued = 0;       // stages filled so far
         bool ok = true;
         const int dil = p.dil;
-        const int c_end = p.CB * kBK;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
@@ -395,27 +430,32 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int h0 = p0 * p.stride - p.pad;
             const int w0 = q0 * p.stride - p.pad;
             const int k0 = tn * BN;
-            int r = 0, s = 0, c = 0;
-            for (int kb = 0; kb < p.KB; kb += KSUB) {
-                const int nsub = min(KSUB, p.KB - kb);
-                if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                const uint32_t fb = full_bar(stage);
-                mbar_arrive_expect_tx(fb, (uint32_t)(nsub * L::kSubBytes));
-                for (int j = 0; j < nsub; ++j) {
-                    if (A_TILE)
-                        tma_load_tile_2d(a_tile(stage, j), &tmA, fb, c, (int)m0);
-                    else
-                        tma_load_im2col_4d(a_tile(stage, j), &tmA, fb, c, w0, h0, n_img,
-                                           (uint16_t)(s * dil), (uint16_t)(r * dil));
-                    tma_load_tile_4d(b_tile(stage, j), &tmB, fb, c, s, r, k0);
-                    c += kBK;
-                    if (c >= c_end) {
-                        c = 0;
-                        if (++s == p.S) { s = 0; ++r; }
+            for (int o = 0; o < p.n_outer && ok; ++o) {
+                const int cx = p.chunked ? 0 : o * kBK;     // channel offset of this outer block
+                int r = 0, s = 0;                            // tap of inner index i0
+                for (int i0 = 0; i0 < p.n_inner; i0 += KSUB) {
+                    const int nsub = min(KSUB, p.n_inner - i0);
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    const uint32_t fb = full_bar(stage);
+                    const int a_tiles = (A_TILE && p.chunked) ? KSUB : nsub;
+                    mbar_arrive_expect_tx(fb, (uint32_t)(a_tiles * kATileBytes + KSUB * L::kBTileBytes));
+                    if (A_TILE) {
+                        if (p.chunked)
+                            tma_load_tile_3d(a_tile(stage, 0), &tmA, fb, 0, (int)m0, i0);
+                        else
+                            tma_load_tile_2d(a_tile(stage, 0), &tmA, fb, cx, (int)m0);
+                    } else {
+                        for (int j = 0; j < nsub; ++j) {
+                            tma_load_im2col_4d(a_tile(stage, j), &tmA, fb, cx, w0, h0, n_img,
+                                               (uint16_t)(s * dil), (uint16_t)(r * dil));
+                            if (++s == p.S) { s = 0; ++r; }
+                        }
                     }
+                    tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
+                    ++n_issued;
+                    TC_TRACE(0, 1);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                ++n_issued;
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
         if (!ok) {
@@ -438,31 +478,38 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint64_t a_desc0 = smem_desc_sw128(a_tile(0, 0));
         const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
         constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);   // 16-byte units
-        constexpr uint64_t kSubDesc = (uint64_t)(L::kSubBytes >> 4);
+        constexpr uint64_t kADesc = (uint64_t)(kATileBytes >> 4);
+        constexpr uint64_t kBDesc = (uint64_t)(L::kBTileBytes >> 4);
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            TC_TRACE(1, 4);
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < p.KB; kb += KSUB) {
-                const int nsub = min(KSUB, p.KB - kb);
-                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
-                tc_fence_after();
-                for (int j = 0; j < nsub; ++j) {
-                    const uint64_t ad = a_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
-                    const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
+            int kb = 0;                                      // k-blocks accumulated in this tile
+            for (int o = 0; o < p.n_outer && ok; ++o) {
+                for (int i0 = 0; i0 < p.n_inner; i0 += KSUB) {
+                    const int nsub = min(KSUB, p.n_inner - i0);
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                    TC_TRACE(1, 2);
+                    tc_fence_after();
+                    for (int j = 0; j < nsub; ++j, ++kb) {
+                        const uint64_t ad = a_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kADesc;
+                        const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kBDesc;
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // advance 16 elements (32 bytes) along K inside the swizzled rows
-                        mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
-                                ((kb + j) | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            // advance 16 elements (32 bytes) along K inside the swizzled rows
+                            mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
+                                    (kb | k) != 0 ? 1u : 0u);
+                        }
                     }
+                    any = true;
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                any = true;
-                mma_commit(empty_bar(stage));
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
             mma_commit(accf_bar(acc));
+            TC_TRACE(1, 3);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (any) {
@@ -494,6 +541,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (lane == 0) ok = mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
+            if (issuer) TC_TRACE(2, 5);
             tc_fence_after();
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
@@ -534,6 +582,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_before();
             __syncwarp();
             mbar_arrive(acce_bar(acc));
+            if (issuer) TC_TRACE(2, 6);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (issuer) bulk_wait_all();
@@ -662,16 +711,12 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                                  n_img);
                 ++n_w;
                 if (++wslot == 2) { wslot = 0; wphase ^= 1u; }
-                int r = 0, s = 0;
                 for (int t0 = 0; t0 < RS; t0 += KSUB) {
-                    const int nsub = min(KSUB, RS - t0);
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, (uint32_t)(nsub * L::kBTileBytes));
-                    for (int j = 0; j < nsub; ++j) {
-                        tma_load_tile_4d(b_tile(stage, j), &tmB, fb, cb * kBK, s, r, k0);
-                        if (++s == p.S) { s = 0; ++r; }
-                    }
+                    mbar_arrive_expect_tx(fb, (uint32_t)(KSUB * L::kBTileBytes));
+                    // one box: 64 channels x BN outputs x KSUB taps (taps past R*S read as zero)
+                    tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cb * kBK, k0, t0);
                     ++n_b;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -871,8 +916,15 @@ WinGeom win_geom(const Shape &s) {
     return g;
 }
 
+// A 1x1 / stride 1 / no padding layer whose channel count is a multiple of 64:
+// its k-blocks are channel blocks with a uniform 128-byte stride, so KSUB of
+// them can be fetched as one box.
+bool chunked_layer(const Shape &s, int amode) { return amode == 1 && s.C % kBK == 0; }
+
 // amode: 0 = im2col A, 1 = plain [N*H*W, C] A, 2 = window A.
-conv2d_status_t encode_maps(const Shape &s, int BN, int amode, const Tensors &t, TcMaps *m) {
+// B is a 3-D map: (64 channels, K outputs, KSUB taps) boxes over w viewed as
+// (C, K, R*S) -- or, for chunked 1x1 layers, (64, K, C/64 channel blocks).
+conv2d_status_t encode_maps(const Shape &s, int BN, int KSUB, int amode, const Tensors &t, TcMaps *m) {
     if (!load_driver_fns()) return CONV2D_ERR_CUDA;
     const CUtensorMapDataType dt =
         s.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -886,6 +938,17 @@ conv2d_status_t encode_maps(const Shape &s, int BN, int amode, const Tensors &t,
         const cuuint32_t box[4] = {kBK, (cuuint32_t)g.Wp, (cuuint32_t)g.TRW, 1};
         const cuuint32_t estr[4] = {1, 1, 1, 1};
         if (g_encode_tiled(&m->a, dt, 4, const_cast<void *>(t.x), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    } else if (a_tile && chunked_layer(s, amode)) {
+        // x as (64 channels, N*H*W pixels, C/64 channel blocks)
+        const cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)s.N * s.H * s.W, (cuuint64_t)(s.C / kBK)};
+        const cuuint64_t strides[2] = {(cuuint64_t)s.C * 2, (cuuint64_t)kBK * 2};
+        const cuuint32_t box[3] = {kBK, kBM, (cuuint32_t)KSUB};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (g_encode_tiled(&m->a, dt, 3, const_cast<void *>(t.x), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -914,13 +977,24 @@ conv2d_status_t encode_maps(const Shape &s, int BN, int amode, const Tensors &t,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return CONV2D_ERR_CUDA;
     }
-    {
-        const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.S, (cuuint64_t)s.R, (cuuint64_t)s.K};
-        const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.S * s.C * 2,
-                                       (cuuint64_t)s.R * s.S * s.C * 2};
-        const cuuint32_t box[4] = {kBK, 1, 1, (cuuint32_t)BN};
-        const cuuint32_t estr[4] = {1, 1, 1, 1};
-        if (g_encode_tiled(&m->b, dt, 4, const_cast<void *>(t.w), dims, strides, box, estr,
+    if (chunked_layer(s, amode)) {
+        // w as (64 channels, K outputs, C/64 channel blocks)
+        const cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)s.K, (cuuint64_t)(s.C / kBK)};
+        const cuuint64_t strides[2] = {(cuuint64_t)s.C * 2, (cuuint64_t)kBK * 2};
+        const cuuint32_t box[3] = {kBK, (cuuint32_t)BN, (cuuint32_t)KSUB};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (g_encode_tiled(&m->b, dt, 3, const_cast<void *>(t.w), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    } else {
+        // w as (C channels, K outputs, R*S taps); w[k][r][s][c] = tap r*S+s
+        const cuuint64_t dims[3] = {(cuuint64_t)s.C, (cuuint64_t)s.K, (cuuint64_t)s.R * s.S};
+        const cuuint64_t strides[2] = {(cuuint64_t)s.R * s.S * s.C * 2, (cuuint64_t)s.C * 2};
+        const cuuint32_t box[3] = {kBK, (cuuint32_t)BN, (cuuint32_t)KSUB};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (g_encode_tiled(&m->b, dt, 3, const_cast<void *>(t.w), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -955,14 +1029,15 @@ conv2d_status_t encode_maps(const Shape &s, int BN, int amode, const Tensors &t,
 // Maps depend only on the layer, the tile width, the A mode and the three
 // pointers; repeated calls with the same tensors reuse them (host time).
 struct MapKey {
-    int v[14];
+    int v[15];
     const void *x, *w, *y;
     bool operator==(const MapKey &o) const {
         return std::memcmp(v, o.v, sizeof(v)) == 0 && x == o.x && w == o.w && y == o.y;
     }
 };
 
-conv2d_status_t cached_maps(const Shape &s, int BN, int amode, const Tensors &t, const TcMaps **out) {
+conv2d_status_t cached_maps(const Shape &s, int BN, int KSUB, int amode, const Tensors &t,
+                            const TcMaps **out) {
     constexpr int kSlots = 8;
     struct Slot {
         MapKey key;
@@ -974,8 +1049,8 @@ conv2d_status_t cached_maps(const Shape &s, int BN, int amode, const Tensors &t,
     int dev = 0;
     cudaGetDevice(&dev);
     MapKey k;
-    const int vals[14] = {s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
-                          (int)s.dtype, BN, amode, dev};
+    const int vals[15] = {s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
+                          (int)s.dtype, BN, amode, dev, KSUB};
     std::memcpy(k.v, vals, sizeof(vals));
     k.x = t.x;
     k.w = t.w;
@@ -989,7 +1064,7 @@ conv2d_status_t cached_maps(const Shape &s, int BN, int amode, const Tensors &t,
     Slot &sl = slots[next];
     next = (next + 1) % kSlots;
     sl.used = false;
-    conv2d_status_t st = encode_maps(s, BN, amode, t, &sl.maps);
+    conv2d_status_t st = encode_maps(s, BN, KSUB, amode, t, &sl.maps);
     if (st != CONV2D_OK) return st;
     sl.key = k;
     sl.used = true;
@@ -1015,7 +1090,7 @@ template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
 conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
     using L = TcSmem<BN, KSUB, STAGES>;
     const TcMaps *maps = nullptr;
-    conv2d_status_t mst = cached_maps(s, BN, A_TILE ? 1 : 0, t, &maps);
+    conv2d_status_t mst = cached_maps(s, BN, KSUB, A_TILE ? 1 : 0, t, &maps);
     if (mst != CONV2D_OK) return mst;
     TcParams p;
     p.bias = t.bias;
@@ -1031,6 +1106,9 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.S = s.S;
     p.CB = (s.C + kBK - 1) / kBK;
     p.KB = s.R * s.S * p.CB;
+    p.chunked = chunked_layer(s, A_TILE ? 1 : 0) ? 1 : 0;
+    p.n_outer = p.chunked ? 1 : p.CB;
+    p.n_inner = p.chunked ? p.CB : s.R * s.S;
     p.n_tiles_n = (s.K + BN - 1) / BN;
     const int64_t tiles = ((s.M + kBM - 1) / kBM) * (int64_t)p.n_tiles_n;
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
@@ -1048,7 +1126,7 @@ template <typename T, int BN, int KSUB, int STAGES>
 conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
     using L = TcWinSmem<BN, KSUB, STAGES>;
     const TcMaps *maps = nullptr;
-    conv2d_status_t mst = cached_maps(s, BN, 2, t, &maps);
+    conv2d_status_t mst = cached_maps(s, BN, KSUB, 2, t, &maps);
     if (mst != CONV2D_OK) return mst;
     const WinGeom g = win_geom(s);
     TcParams p;
@@ -1085,18 +1163,20 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
 
 // Variants: (BN, KSUB, STAGES) with about 192 KB of stages.
 #define CONV2D_TC_VARIANTS(X) \
-    X(64, 1, 8)               \
     X(64, 2, 4)               \
     X(64, 4, 2)               \
     X(128, 1, 6)              \
     X(128, 2, 3)              \
+    X(128, 3, 2)              \
     X(256, 1, 4)              \
     X(256, 2, 2)
 
-// Window-mode variants: 96 KB of window slots + 3 stages of 32 KB weight tiles.
+// Window-mode variants: 96 KB of window slots + about 96 KB of weight stages.
 #define CONV2D_TC_WIN_VARIANTS(X) \
     X(64, 4, 3)                   \
+    X(64, 6, 2)                   \
     X(128, 2, 3)                  \
+    X(128, 3, 2)                  \
     X(256, 1, 3)
 
 template <typename T>
@@ -1200,3 +1280,14 @@ conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaS
 }
 
 }  // namespace conv2d
+
+#ifdef CONV2D_TC_TRACE
+extern "C" int conv2d_tc_trace_dump(unsigned long long *out, unsigned int *counts) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(counts, conv2d::g_tc_trace_n, sizeof(unsigned int) * 4) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(out, conv2d::g_tc_trace, sizeof(unsigned long long) * 4 * 8192) != cudaSuccess)
+        return -1;
+    const unsigned int zero[4] = {0, 0, 0, 0};
+    return cudaMemcpyToSymbol(conv2d::g_tc_trace_n, zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
+}
+#endif

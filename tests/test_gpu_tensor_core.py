@@ -63,7 +63,7 @@ SHAPES = [
 
 
 # (BN, k-blocks per pipeline stage): every compiled variant
-VARIANTS = [(64, 1), (64, 2), (64, 4), (128, 1), (128, 2), (256, 1), (256, 2)]
+VARIANTS = [(64, 2), (64, 4), (128, 1), (128, 2), (128, 3), (256, 1), (256, 2)]
 
 
 @pytest.mark.parametrize("bn,ksub", VARIANTS)
@@ -135,7 +135,7 @@ WINDOW_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("bn,ksub", [(64, 4), (128, 2), (256, 1)])
+@pytest.mark.parametrize("bn,ksub", [(64, 4), (64, 6), (128, 2), (128, 3), (256, 1)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_window_mode(dtype, bn, ksub, force_bn):
     """Stride-1 layers with one padded input window per channel block, the
