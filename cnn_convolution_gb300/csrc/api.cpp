@@ -164,60 +164,83 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     const int64_t kb = rs * cb;
     const int force_bn = env_int("CONV2D_TC_BN"), force_ks = env_int("CONV2D_TC_KSUB");
     const int force_win = env_int("CONV2D_TC_WINDOW");
+    const int force_wv = env_int("CONV2D_TC_WINVAR");
     const bool win_ok = tc_window_ok(s);
     const int wp = s.W + 2 * s.pad;
     const int tr = wp > 0 ? 128 / wp : 0;
-    int best_bn = 0, best_ks = 0;
-    bool best_win = false;
-    double best = 1e300;
-    for (int win = 0; win < 2; ++win) {
-        if (win && !win_ok) continue;
-        if (force_win == 1 && !win) continue;
-        if (force_win == 0 && win) continue;
+    const bool plain = s.R * s.S == 1 && s.stride == 1 && s.pad == 0 && s.C % 64 == 0;
+    struct Cand {
+        int bn, ks, win_variant;
+        double cost;
+    };
+    Cand best{0, 0, -1, 1e300};
+    auto rounds_for = [&](int64_t m_tiles, int bn) {
+        const int64_t n_tiles = (s.K + bn - 1) / bn;
+        return (m_tiles * n_tiles + d.sm_count - 1) / d.sm_count;
+    };
+    auto wasteful = [&](int bn) {
+        const int64_t n_tiles = (s.K + bn - 1) / bn;
+        return force_bn <= 0 && bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1;
+    };
+    // im2col / plain-matrix variants
+    if (force_win != 1) {
         for (int bn : {64, 128, 256}) {
-            for (int ks : {1, 2, 4}) {
-                if ((win ? tc_window_stages(bn, ks) : tc_stages(bn, ks)) == 0) continue;
+            for (int ks : {1, 2, 3, 4, 6}) {
+                if (tc_stages(bn, ks) == 0) continue;
                 if (force_bn > 0 && bn != force_bn) continue;
                 if (force_ks > 0 && ks != force_ks) continue;
-                const int64_t n_tiles = (s.K + bn - 1) / bn;
-                if (force_bn <= 0 && bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1) continue;
-                const int64_t m_tiles =
-                    win ? (int64_t)s.N * ((s.P + tr - 1) / tr) : (s.M + 127) / 128;
-                const int64_t rounds = (m_tiles * n_tiles + d.sm_count - 1) / d.sm_count;
+                if (wasteful(bn)) continue;
                 const double b_bytes = (double)bn * 128.0;
                 double mem;
-                if (win) {
-                    const double win_bytes = (double)(tr + (s.R - 1) * s.dil) * wp * 128.0;
-                    const int64_t b_stages = (rs + ks - 1) / ks;
-                    mem = cb * (stage_ns(1, win_bytes) + b_stages * stage_ns(1, ks * b_bytes));
-                } else if (s.R * s.S == 1 && s.stride == 1 && s.pad == 0 && s.C % 64 == 0) {
-                    const int64_t stages = (cb + ks - 1) / ks;       // one A box + one B box per stage
-                    mem = stages * stage_ns(2, ks * (16384.0 + b_bytes));
+                if (plain) {
+                    mem = ((cb + ks - 1) / ks) * stage_ns(2, ks * (16384.0 + b_bytes));
                 } else {
-                    const int64_t per_cb = (rs + ks - 1) / ks;
                     const int a_loads = (int)std::min<int64_t>(ks, rs);
-                    mem = cb * per_cb * stage_ns(a_loads + 1, a_loads * 16384.0 + ks * b_bytes);
+                    mem = cb * ((rs + ks - 1) / ks) *
+                          stage_ns(a_loads + 1, a_loads * 16384.0 + ks * b_bytes);
                 }
                 const double mma = kb * 2.0 * bn / 1.9;
-                const double cost = (double)rounds * std::max(mem, mma);
-                if (cost < best) { best = cost; best_bn = bn; best_ks = ks; best_win = win; }
+                const double cost = (double)rounds_for((s.M + 127) / 128, bn) * std::max(mem, mma);
+                if (cost < best.cost) best = Cand{bn, ks, -1, cost};
             }
         }
     }
-    if (best_bn == 0) return CONV2D_ERR_UNSUPPORTED;
+    // window variants (stride-1 layers)
+    if (win_ok && force_win != 0) {
+        for (int id = 0; id < tc_window_variants(); ++id) {
+            if (!tc_window_variant_ok(s, id)) continue;
+            if (force_wv >= 0 && id != force_wv) continue;
+            const TcWinVariant v = tc_window_variant(id);
+            if (force_bn > 0 && v.bn != force_bn) continue;
+            if (force_ks > 0 && v.ksub != force_ks && !v.resident) continue;
+            if (wasteful(v.bn)) continue;
+            const double win_bytes = (double)(tr + (s.R - 1) * s.dil) * wp * 128.0;
+            double mem = cb * stage_ns(1, win_bytes);
+            if (!v.resident) mem += cb * ((rs + v.ksub - 1) / v.ksub) * stage_ns(1, v.ksub * v.bn * 128.0);
+            // few stages in flight: loads are latency-bound unless the weights stay resident
+            if (!v.resident) mem *= 1.25;
+            const double mma = kb * 2.0 * v.bn / 1.9;
+            const double cost = (double)rounds_for((int64_t)s.N * ((s.P + tr - 1) / tr), v.bn) *
+                                std::max(mem, mma);
+            if (cost < best.cost) best = Cand{v.bn, v.ksub, id, cost};
+        }
+    }
+    if (best.bn == 0) return CONV2D_ERR_UNSUPPORTED;
     TcTile t;
-    t.BN = best_bn;
-    t.ksub = best_ks;
-    t.window = best_win;
-    t.stages = best_win ? tc_window_stages(best_bn, best_ks) : tc_stages(best_bn, best_ks);
+    t.BN = best.bn;
+    t.ksub = best.ks;
+    t.window = best.win_variant >= 0;
+    t.win_variant = best.win_variant;
+    t.stages = t.window ? tc_window_variant(best.win_variant).stages : tc_stages(best.bn, best.ks);
     t.tma_store = true;
     t.force_im2col = env_int("CONV2D_TC_IM2COL") == 1;
+    t.rotate = env_int("CONV2D_TC_ROTATE") != 0;
     p->algo = Algo::TensorCore;
     p->tc = t;
-    p->smem_bytes = best_win ? tc_window_smem_bytes(t) : tc_smem_bytes(t);
+    p->smem_bytes = t.window ? tc_window_smem_bytes(t) : tc_smem_bytes(t);
     if (p->smem_bytes > d.smem_optin) return CONV2D_ERR_UNSUPPORTED;
-    const int64_t m_tiles = best_win ? (int64_t)s.N * ((s.P + tr - 1) / tr) : (s.M + 127) / 128;
-    const int64_t tiles = m_tiles * ((s.K + best_bn - 1) / best_bn);
+    const int64_t m_tiles = t.window ? (int64_t)s.N * ((s.P + tr - 1) / tr) : (s.M + 127) / 128;
+    const int64_t tiles = m_tiles * ((s.K + best.bn - 1) / best.bn);
     p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
     p->sm_count = d.sm_count;
     return CONV2D_OK;
@@ -248,7 +271,8 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
                       (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0,
                       env_int("CONV2D_CC_TILE"),
                       (((env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 +
-                        env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW"))};
+                        env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW")) * 4 +
+                          env_int("CONV2D_TC_ROTATE") + 64 * env_int("CONV2D_TC_WINVAR")};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);
@@ -398,8 +422,9 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
     conv2d_status_t st = get_plan(desc->s, desc->algo, nullptr, &p);
     if (st != CONV2D_OK) return st;
     if (p.algo == Algo::TensorCore)
-        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 ksub=%d stages=%d grid=%d smem=%zu a=%s",
+        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 ksub=%d stages=%d grid=%d smem=%zu a=%s%s",
                       p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes,
+                      p.tc.window && tc_window_variant(p.tc.win_variant).resident ? "resident-w " : "",
                       p.tc.window ? "window"
                       : (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
                          !p.tc.force_im2col) ? "tile" : "im2col");

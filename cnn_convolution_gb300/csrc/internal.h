@@ -40,6 +40,8 @@ struct TcTile {
     bool tma_store;  // epilogue through shared memory + TMA store
     bool force_im2col = false;   // 1x1 layers: use the im2col map even though a plain one would do
     bool window = false;         // stride-1 layers: one padded input window per channel block
+    int win_variant = -1;        // index into the window-mode variant table
+    bool rotate = true;          // CTA-dependent start of the k-loop
 };
 
 enum class Algo { CudaCore, TensorCore };
@@ -73,7 +75,14 @@ size_t tc_smem_bytes(const TcTile &t);
 int tc_stages(int bn, int ksub);   // 0 if the (BN, KSUB) variant does not exist
 bool tc_window_ok(const Shape &s);
 size_t tc_window_smem_bytes(const TcTile &t);
-int tc_window_stages(int bn, int ksub);   // 0 if the window variant does not exist
+struct TcWinVariant {
+    int bn, ksub, stages, win_kb, nwin;
+    bool resident;
+    int res_kb;
+};
+int tc_window_variants();
+TcWinVariant tc_window_variant(int id);
+bool tc_window_variant_ok(const Shape &s, int id);
 conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
 
 // Device status word (bounded-wait failures).

@@ -318,6 +318,7 @@ struct TcParams {
     int KB;               // k-blocks per tile = R*S*CB
     int n_outer, n_inner; // k-block loop: outer x inner (see the producer)
     int chunked;          // 1x1 plain layer with C % 64 == 0: inner = channel blocks
+    int rotate;           // start each CTA's k-loop at a different stage
     int n_tiles_n;        // tiles along K
     int total_tiles;
     // window mode only
@@ -430,32 +431,41 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int h0 = p0 * p.stride - p.pad;
             const int w0 = q0 * p.stride - p.pad;
             const int k0 = tn * BN;
-            for (int o = 0; o < p.n_outer && ok; ++o) {
+            // Stages of a tile run in a CTA-dependent rotation, so that CTAs
+            // running at the same time fetch different weight tiles instead of
+            // all hammering the same L2 lines.
+            const int per_o = (p.n_inner + KSUB - 1) / KSUB;
+            const int n_st = p.n_outer * per_o;
+            const int rot = p.rotate ? (int)(blockIdx.x % (unsigned)n_st) : 0;
+            for (int j = 0; j < n_st; ++j) {
+                int sidx = rot + j;
+                if (sidx >= n_st) sidx -= n_st;
+                const int o = sidx / per_o;
+                const int i0 = (sidx - o * per_o) * KSUB;
+                const int nsub = min(KSUB, p.n_inner - i0);
                 const int cx = p.chunked ? 0 : o * kBK;     // channel offset of this outer block
-                int r = 0, s = 0;                            // tap of inner index i0
-                for (int i0 = 0; i0 < p.n_inner; i0 += KSUB) {
-                    const int nsub = min(KSUB, p.n_inner - i0);
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    const uint32_t fb = full_bar(stage);
-                    const int a_tiles = (A_TILE && p.chunked) ? KSUB : nsub;
-                    mbar_arrive_expect_tx(fb, (uint32_t)(a_tiles * kATileBytes + KSUB * L::kBTileBytes));
-                    if (A_TILE) {
-                        if (p.chunked)
-                            tma_load_tile_3d(a_tile(stage, 0), &tmA, fb, 0, (int)m0, i0);
-                        else
-                            tma_load_tile_2d(a_tile(stage, 0), &tmA, fb, cx, (int)m0);
-                    } else {
-                        for (int j = 0; j < nsub; ++j) {
-                            tma_load_im2col_4d(a_tile(stage, j), &tmA, fb, cx, w0, h0, n_img,
-                                               (uint16_t)(s * dil), (uint16_t)(r * dil));
-                            if (++s == p.S) { s = 0; ++r; }
-                        }
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                TC_TRACE(3, 8);
+                const uint32_t fb = full_bar(stage);
+                const int a_tiles = (A_TILE && p.chunked) ? KSUB : nsub;
+                mbar_arrive_expect_tx(fb, (uint32_t)(a_tiles * kATileBytes + KSUB * L::kBTileBytes));
+                if (A_TILE) {
+                    if (p.chunked)
+                        tma_load_tile_3d(a_tile(stage, 0), &tmA, fb, 0, (int)m0, i0);
+                    else
+                        tma_load_tile_2d(a_tile(stage, 0), &tmA, fb, cx, (int)m0);
+                } else {
+                    int r = i0 / p.S, s = i0 - r * p.S;
+                    for (int jj = 0; jj < nsub; ++jj) {
+                        tma_load_im2col_4d(a_tile(stage, jj), &tmA, fb, cx, w0, h0, n_img,
+                                           (uint16_t)(s * dil), (uint16_t)(r * dil));
+                        if (++s == p.S) { s = 0; ++r; }
                     }
-                    tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
-                    ++n_issued;
-                    TC_TRACE(0, 1);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
+                ++n_issued;
+                TC_TRACE(0, 1);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
         if (!ok) {
@@ -485,27 +495,30 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             TC_TRACE(1, 4);
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            int kb = 0;                                      // k-blocks accumulated in this tile
-            for (int o = 0; o < p.n_outer && ok; ++o) {
-                for (int i0 = 0; i0 < p.n_inner; i0 += KSUB) {
-                    const int nsub = min(KSUB, p.n_inner - i0);
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
-                    TC_TRACE(1, 2);
-                    tc_fence_after();
-                    for (int j = 0; j < nsub; ++j, ++kb) {
-                        const uint64_t ad = a_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kADesc;
-                        const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kBDesc;
+            const int per_o = (p.n_inner + KSUB - 1) / KSUB;
+            const int n_st = p.n_outer * per_o;
+            const int rot = p.rotate ? (int)(blockIdx.x % (unsigned)n_st) : 0;
+            for (int j = 0; j < n_st; ++j) {
+                int sidx = rot + j;
+                if (sidx >= n_st) sidx -= n_st;
+                const int o = sidx / per_o;
+                const int nsub = min(KSUB, p.n_inner - (sidx - o * per_o) * KSUB);
+                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                TC_TRACE(1, 2);
+                tc_fence_after();
+                for (int jj = 0; jj < nsub; ++jj) {
+                    const uint64_t ad = a_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)jj * kADesc;
+                    const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)jj * kBDesc;
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k) {
-                            // advance 16 elements (32 bytes) along K inside the swizzled rows
-                            mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
-                                    (kb | k) != 0 ? 1u : 0u);
-                        }
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // advance 16 elements (32 bytes) along K inside the swizzled rows
+                        mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
+                                (j | jj | k) != 0 ? 1u : 0u);
                     }
-                    any = true;
-                    mma_commit(empty_bar(stage));
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                any = true;
+                mma_commit(empty_bar(stage));
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
             mma_commit(accf_bar(acc));
@@ -614,28 +627,34 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // a 3x3 layer loads each input window once per channel block instead of
 // nine 128-pixel im2col tiles.
 //
-// Shared memory: two window slots, STAGES stages of KSUB weight tiles, the
-// epilogue staging buffers, barriers.  Weights stream per (tap, channel block).
-template <int BN, int KSUB, int STAGES>
+// Shared memory: NWIN window slots of WINKB KB, the weight region, the
+// epilogue staging buffers, barriers.  The weight region is either STAGES
+// stages of KSUB weight tiles streamed per (tap group, channel block), or --
+// RES, for layers whose whole weight tensor fits (one output-channel tile) --
+// every weight tile of the layer, loaded once per CTA and kept resident; the
+// pipeline then moves windows only.
+template <int BN, int KSUB, int STAGES, int WINKB, int NWIN, bool RES, int RESKB>
 struct TcWinSmem {
-    static constexpr int kWinBytes = 48 * 1024;        // (max row shift + 128) rows of 128 B
+    static constexpr int kWinBytes = WINKB * 1024;     // (max row shift + 128) rows of 128 B
     static constexpr int kWinRows = kWinBytes / 128;
     static constexpr int kBTileBytes = BN * kBK * 2;
     static constexpr int kStageBytes = KSUB * kBTileBytes;
-    static constexpr size_t kStageOffset = 2 * (size_t)kWinBytes;
+    static constexpr int kResBytes = RESKB * 1024;
+    static constexpr size_t kStageOffset = (size_t)NWIN * kWinBytes;
     static constexpr int kEpiBufBytes = kBM * 32 * 2;
-    static constexpr size_t kEpiOffset = kStageOffset + (size_t)STAGES * kStageBytes;
+    static constexpr size_t kEpiOffset =
+        kStageOffset + (RES ? (size_t)kResBytes : (size_t)STAGES * kStageBytes);
     static constexpr size_t kBarOffset = kEpiOffset + 2 * kEpiBufBytes;
-    // full[S], empty[S], win_full[2], win_empty[2], acc_full[2], acc_empty[2], drain
-    static constexpr size_t kBarBytes = (2 * STAGES + 9) * 8;
+    // full[S], empty[S], win_full[NWIN], win_empty[NWIN], acc_full[2], acc_empty[2], drain, resident
+    static constexpr size_t kBarBytes = (2 * STAGES + 2 * NWIN + 6) * 8;
     static constexpr size_t kBytes = kBarOffset + kBarBytes + 16 + 1024;
 };
 
-template <typename T, int BN, int KSUB, int STAGES>
+template <typename T, int BN, int KSUB, int STAGES, int WINKB, int NWIN, bool RES, int RESKB>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmY, const TcParams p) {
-    using L = TcWinSmem<BN, KSUB, STAGES>;
+    using L = TcWinSmem<BN, KSUB, STAGES, WINKB, NWIN, RES, RESKB>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
     constexpr uint32_t kTmemCols = 2 * BN;
@@ -648,15 +667,20 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto wfull_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + w); };
-    auto wempty_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 2 + w); };
-    auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 4 + a); };
-    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 6 + a); };
-    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 8);
+    auto wempty_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + NWIN + w); };
+    auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * NWIN + a); };
+    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * NWIN + 2 + a); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * NWIN + 4);
+    const uint32_t res_bar = bar_base + 8u * (2 * STAGES + 2 * NWIN + 5);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
     auto win_slot = [&](int w) { return smem_base + (uint32_t)(w * L::kWinBytes); };
     auto b_tile = [&](int s, int j) {
         return smem_base + (uint32_t)(L::kStageOffset + s * L::kStageBytes + j * L::kBTileBytes);
+    };
+    // resident weight tile of (channel block cb, tap t)
+    auto res_tile = [&](int cb, int t) {
+        return smem_base + (uint32_t)(L::kStageOffset + (cb * p.R * p.S + t) * L::kBTileBytes);
     };
 
     const int warp = threadIdx.x / 32;
@@ -668,13 +692,16 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
+        for (int w = 0; w < NWIN; ++w) {
+            mbar_init(wfull_bar(w), 1);
+            mbar_init(wempty_bar(w), 1);
+        }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(wfull_bar(a), 1);
-            mbar_init(wempty_bar(a), 1);
             mbar_init(accf_bar(a), 1);
             mbar_init(acce_bar(a), 128);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(res_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -698,6 +725,14 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         uint32_t phase = 0, wphase = 0;
         uint32_t n_b = 0, n_w = 0;
         bool ok = true;
+        bool res_issued = false;
+        if (RES) {
+            // every weight tile of the layer, one box per channel block
+            mbar_arrive_expect_tx(res_bar, (uint32_t)(p.CB * RS * L::kBTileBytes));
+            for (int cb = 0; cb < p.CB; ++cb)
+                tma_load_tile_3d(res_tile(cb, 0), &tmB, res_bar, cb * kBK, 0, 0);
+            res_issued = true;
+        }
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
@@ -710,13 +745,15 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 tma_load_tile_4d(win_slot(wslot), &tmA, wfull_bar(wslot), cb * kBK, -p.pad, p0 - p.pad,
                                  n_img);
                 ++n_w;
-                if (++wslot == 2) { wslot = 0; wphase ^= 1u; }
+                if (++wslot == NWIN) { wslot = 0; wphase ^= 1u; }
+                if (RES) continue;
                 for (int t0 = 0; t0 < RS; t0 += KSUB) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, (uint32_t)(KSUB * L::kBTileBytes));
                     // one box: 64 channels x BN outputs x KSUB taps (taps past R*S read as zero)
                     tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cb * kBK, k0, t0);
+                    TC_TRACE(0, 1);
                     ++n_b;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -728,8 +765,11 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             for (uint32_t i = n_b > (uint32_t)STAGES ? n_b - STAGES : 0; i < n_b; ++i)
                 while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) && cycles_left(t0)) {
                 }
-            for (uint32_t i = n_w > 2u ? n_w - 2u : 0; i < n_w; ++i)
-                while (!mbar_try_wait(wfull_bar((int)(i % 2)), (i / 2) & 1u) && cycles_left(t0)) {
+            for (uint32_t i = n_w > (uint32_t)NWIN ? n_w - NWIN : 0; i < n_w; ++i)
+                while (!mbar_try_wait(wfull_bar((int)(i % NWIN)), (i / NWIN) & 1u) && cycles_left(t0)) {
+                }
+            if (res_issued)
+                while (!mbar_try_wait(res_bar, 0) && cycles_left(t0)) {
                 }
         }
     } else if (warp == 1 && lane == 0) {
@@ -740,19 +780,24 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
         constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);
         constexpr uint64_t kSubDesc = (uint64_t)(L::kBTileBytes >> 4);
+        if (RES && !mbar_wait(res_bar, 0, abort_flag, p.status)) ok = false;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int cb = 0; cb < p.CB && ok; ++cb) {
                 if (!mbar_wait(wfull_bar(wslot), wphase, abort_flag, p.status)) { ok = false; break; }
+                TC_TRACE(1, 7);
                 tc_fence_after();
                 const uint32_t wbase = win_slot(wslot);
                 int r = 0, s = 0;
                 for (int t0 = 0; t0 < RS; t0 += KSUB) {
                     const int nsub = min(KSUB, RS - t0);
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
-                    tc_fence_after();
+                    if (!RES) {
+                        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                        TC_TRACE(1, 2);
+                        tc_fence_after();
+                    }
                     for (int j = 0; j < nsub; ++j) {
                         // tap (r, s): the window's rows shifted by r*dil*Wp + s*dil pixels.
                         // The start row need not be a multiple of 8: the 128-byte
@@ -760,7 +805,8 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                         // the descriptor's base-offset field stays 0.
                         const uint32_t a_start = wbase + (uint32_t)((r * p.dil * p.Wp + s * p.dil) * 128);
                         const uint64_t ad = smem_desc_sw128(a_start);
-                        const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
+                        const uint64_t bd = RES ? smem_desc_sw128(res_tile(cb, t0 + j))
+                                                : b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k)
                             mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
@@ -768,12 +814,14 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                         if (++s == p.S) { s = 0; ++r; }
                     }
                     any = true;
-                    mma_commit(empty_bar(stage));
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (!RES) {
+                        mma_commit(empty_bar(stage));
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    }
                 }
                 if (!ok) break;
                 mma_commit(wempty_bar(wslot));
-                if (++wslot == 2) { wslot = 0; wphase ^= 1u; }
+                if (++wslot == NWIN) { wslot = 0; wphase ^= 1u; }
             }
             if (!ok) break;
             mma_commit(accf_bar(acc));
@@ -1109,6 +1157,7 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.chunked = chunked_layer(s, A_TILE ? 1 : 0) ? 1 : 0;
     p.n_outer = p.chunked ? 1 : p.CB;
     p.n_inner = p.chunked ? p.CB : s.R * s.S;
+    p.rotate = pl.tc.rotate ? 1 : 0;
     p.n_tiles_n = (s.K + BN - 1) / BN;
     const int64_t tiles = ((s.M + kBM - 1) / kBM) * (int64_t)p.n_tiles_n;
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
@@ -1122,11 +1171,12 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 
-template <typename T, int BN, int KSUB, int STAGES>
+template <typename T, int BN, int KSUB, int STAGES, int WINKB, int NWIN, bool RES, int RESKB>
 conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
-    using L = TcWinSmem<BN, KSUB, STAGES>;
+    using L = TcWinSmem<BN, KSUB, STAGES, WINKB, NWIN, RES, RESKB>;
     const TcMaps *maps = nullptr;
-    conv2d_status_t mst = cached_maps(s, BN, KSUB, 2, t, &maps);
+    // resident weights arrive as one (64, BN, R*S) box per channel block
+    conv2d_status_t mst = cached_maps(s, BN, RES ? s.R * s.S : KSUB, 2, t, &maps);
     if (mst != CONV2D_OK) return mst;
     const WinGeom g = win_geom(s);
     TcParams p;
@@ -1152,7 +1202,7 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     const int64_t tiles = (int64_t)s.N * p.tiles_per_img * p.n_tiles_n;
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     p.total_tiles = (int)tiles;
-    auto kern = tc_conv_window_kernel<T, BN, KSUB, STAGES>;
+    auto kern = tc_conv_window_kernel<T, BN, KSUB, STAGES, WINKB, NWIN, RES, RESKB>;
     static std::atomic<uint64_t> attr_done{0};
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
         return CONV2D_ERR_CUDA;
@@ -1171,18 +1221,23 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     X(256, 1, 4)              \
     X(256, 2, 2)
 
-// Window-mode variants: 96 KB of window slots + about 96 KB of weight stages.
-#define CONV2D_TC_WIN_VARIANTS(X) \
-    X(64, 4, 3)                   \
-    X(64, 6, 2)                   \
-    X(128, 2, 3)                  \
-    X(128, 3, 2)                  \
-    X(256, 1, 3)
+// Window-mode variants: (BN, KSUB, STAGES, window slot KB, window slots,
+// resident weights, resident KB).  Id = position in this list.
+#define CONV2D_TC_WIN_VARIANTS(X)       \
+    X(0, 64, 4, 3, 48, 2, false, 0)     \
+    X(1, 64, 6, 2, 48, 2, false, 0)     \
+    X(2, 128, 2, 3, 48, 2, false, 0)    \
+    X(3, 128, 3, 2, 48, 2, false, 0)    \
+    X(4, 256, 1, 3, 48, 2, false, 0)    \
+    X(5, 64, 4, 4, 32, 2, false, 0)     \
+    X(6, 128, 2, 4, 32, 2, false, 0)    \
+    X(7, 64, 1, 1, 32, 4, true, 72)     \
+    X(8, 128, 1, 1, 32, 4, true, 72)
 
 template <typename T>
 conv2d_status_t dispatch_window(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
-#define CONV2D_TC_WCASE(vbn, vks, vst) \
-    if (pl.tc.BN == vbn && pl.tc.ksub == vks) return launch_tc_window<T, vbn, vks, vst>(s, pl, t, st);
+#define CONV2D_TC_WCASE(vid, vbn, vks, vst, vwk, vnw, vres, vrk) \
+    if (pl.tc.win_variant == vid) return launch_tc_window<T, vbn, vks, vst, vwk, vnw, vres, vrk>(s, pl, t, st);
     CONV2D_TC_WIN_VARIANTS(CONV2D_TC_WCASE)
 #undef CONV2D_TC_WCASE
     return CONV2D_ERR_INTERNAL;
@@ -1232,19 +1287,44 @@ size_t tc_smem_bytes(const TcTile &t) {
 }
 
 size_t tc_window_smem_bytes(const TcTile &t) {
-#define CONV2D_TC_WSMEM(vbn, vks, vst) \
-    if (t.BN == vbn && t.ksub == vks) return TcWinSmem<vbn, vks, vst>::kBytes;
+#define CONV2D_TC_WSMEM(vid, vbn, vks, vst, vwk, vnw, vres, vrk) \
+    if (t.win_variant == vid) return TcWinSmem<vbn, vks, vst, vwk, vnw, vres, vrk>::kBytes;
     CONV2D_TC_WIN_VARIANTS(CONV2D_TC_WSMEM)
 #undef CONV2D_TC_WSMEM
     return (size_t)1 << 30;
 }
 
-int tc_window_stages(int bn, int ksub) {
-#define CONV2D_TC_WST(vbn, vks, vst) \
-    if (bn == vbn && ksub == vks) return vst;
-    CONV2D_TC_WIN_VARIANTS(CONV2D_TC_WST)
-#undef CONV2D_TC_WST
-    return 0;
+int tc_window_variants() {
+    int n = 0;
+#define CONV2D_TC_WCOUNT(vid, vbn, vks, vst, vwk, vnw, vres, vrk) ++n;
+    CONV2D_TC_WIN_VARIANTS(CONV2D_TC_WCOUNT)
+#undef CONV2D_TC_WCOUNT
+    return n;
+}
+
+TcWinVariant tc_window_variant(int id) {
+    TcWinVariant v{};
+#define CONV2D_TC_WGET(vid, vbn, vks, vst, vwk, vnw, vres, vrk) \
+    if (id == vid) v = TcWinVariant{vbn, vks, vst, vwk, vnw, vres, vrk};
+    CONV2D_TC_WIN_VARIANTS(CONV2D_TC_WGET)
+#undef CONV2D_TC_WGET
+    return v;
+}
+
+// Geometry checks of one window variant for a layer: the shifted window must
+// fit its slot; resident weights need one output-channel tile and must fit.
+bool tc_window_variant_ok(const Shape &s, int id) {
+    const TcWinVariant v = tc_window_variant(id);
+    if (v.bn == 0) return false;
+    const WinGeom g = win_geom(s);
+    if (g.max_shift + kBM > v.win_kb * 1024 / 128) return false;
+    if (v.resident) {
+        if (s.K > v.bn) return false;
+        const int64_t cb = (s.C + kBK - 1) / kBK;
+        if (cb * s.R * s.S * v.bn * kBK * 2 > (int64_t)v.res_kb * 1024) return false;
+        if ((int64_t)s.R * s.S > 256) return false;   // box dimension limit
+    }
+    return true;
 }
 
 // Window mode needs stride 1, padded rows of at most 128 pixels, and the
@@ -1254,7 +1334,7 @@ bool tc_window_ok(const Shape &s) {
     const WinGeom g = win_geom(s);
     if (g.Wp > kBM || g.TR < 1) return false;
     if (g.TRW > 256) return false;
-    if (g.max_shift + kBM > TcWinSmem<64, 4, 3>::kWinRows) return false;
+    if (g.max_shift + kBM > 48 * 1024 / 128) return false;
     return true;
 }
 

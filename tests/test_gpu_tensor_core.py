@@ -135,24 +135,59 @@ WINDOW_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("bn,ksub", [(64, 4), (64, 6), (128, 2), (128, 3), (256, 1)])
+# window-mode variants: (BN, window slot KB, resident weights), indexed as in the library
+WINDOW_VARIANTS = {0: (64, 48, False), 1: (64, 48, False), 2: (128, 48, False), 3: (128, 48, False),
+                   4: (256, 48, False), 5: (64, 32, False), 6: (128, 32, False), 7: (64, 32, True),
+                   8: (128, 32, True)}
+
+
+def _window_fits(shape, variant):
+    N, C, H, W, K, R, S, pad, dil, bias = shape
+    bn, win_kb, resident = WINDOW_VARIANTS[variant]
+    wp = W + 2 * pad
+    max_shift = (R - 1) * dil * wp + (S - 1) * dil
+    if max_shift + 128 > win_kb * 1024 // 128:
+        return False
+    if resident:
+        cb = (C + 63) // 64
+        return K <= bn and cb * R * S * bn * 128 <= 72 * 1024
+    return True
+
+
+@pytest.mark.parametrize("variant", sorted(WINDOW_VARIANTS))
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_window_mode(dtype, bn, ksub, force_bn):
+def test_window_mode(dtype, variant):
     """Stride-1 layers with one padded input window per channel block, the
-    filter taps taken as row shifts of it."""
-    force_bn(bn, ksub)
+    filter taps taken as row shifts of it (streamed or resident weights)."""
     os.environ["CONV2D_TC_WINDOW"] = "1"
+    os.environ["CONV2D_TC_WINVAR"] = str(variant)
+    ran = 0
     try:
-        for i, (N, C, H, W, K, R, S, pad, dil, bias) in enumerate(WINDOW_SHAPES):
+        for i, sh in enumerate(WINDOW_SHAPES + RESIDENT_SHAPES):
+            if not _window_fits(sh, variant):
+                continue
+            N, C, H, W, K, R, S, pad, dil, bias = sh
             spec = wl.ConvSpec(f"win{i}", N, C, H, W, K, R, S, 1, pad, dil, dtype=dtype,
                                layout="NHWC", bias=bias)
             x, w, b = wl.random_inputs(spec, seed=200 + i)
             y, d = run_gpu(spec, x, w, b, "tensor_core")
             assert "a=window" in d.plan(), d.plan()
             err = full_parity(spec, x, w, b, algo="tensor_core")
-            assert err <= TOL[dtype], f"{spec} BN={bn}: err={err}"
+            assert err <= TOL[dtype], f"{spec} variant {variant}: err={err}"
+            ran += 1
     finally:
         os.environ.pop("CONV2D_TC_WINDOW", None)
+        os.environ.pop("CONV2D_TC_WINVAR", None)
+    assert ran >= 3
+
+
+RESIDENT_SHAPES = [
+    # layers whose whole weight tensor fits one output-channel tile
+    (3, 64, 14, 14, 64, 3, 3, 1, 1, True),
+    (2, 32, 9, 20, 40, 3, 3, 1, 1, False),
+    (2, 128, 8, 8, 64, 2, 2, 0, 1, True),
+    (1, 64, 30, 40, 128, 2, 2, 1, 1, True),
+]
 
 
 def test_window_mode_not_used_where_it_cannot_apply():
