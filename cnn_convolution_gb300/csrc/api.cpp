@@ -180,7 +180,7 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     };
     auto wasteful = [&](int bn) {
         const int64_t n_tiles = (s.K + bn - 1) / bn;
-        return force_bn <= 0 && bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1;
+        return force_bn <= 0 && force_wv < 0 && bn > 64 && n_tiles * bn >= s.K + bn / 2 + 1;
     };
     // im2col / plain-matrix variants
     if (force_win != 1) {

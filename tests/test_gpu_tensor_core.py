@@ -171,7 +171,7 @@ def test_window_mode(dtype, variant):
                                layout="NHWC", bias=bias)
             x, w, b = wl.random_inputs(spec, seed=200 + i)
             y, d = run_gpu(spec, x, w, b, "tensor_core")
-            assert "a=window" in d.plan(), d.plan()
+            assert "window" in d.plan(), d.plan()
             err = full_parity(spec, x, w, b, algo="tensor_core")
             assert err <= TOL[dtype], f"{spec} variant {variant}: err={err}"
             ran += 1
