@@ -107,39 +107,49 @@ int env_int(const char *name) {
 // Each tile has a whole-GPU FFMA rate, measured on GB300 with enough CTAs
 // resident (`full_ctas` per SM); with fewer CTAs per SM the rate falls in
 // proportion.  Padding of M, K and the reduction to whole tiles is work too.
-double cc_cost(const Shape &s, const CudaCoreTile &t, int sms) {
+// Split-K multiplies the CTAs by `split` (each reduces 1/split of the k-tiles)
+// at the price of a cluster-wide reduction of the partial tiles.
+double cc_cost(const Shape &s, const CudaCoreTile &t, int split, int sms) {
     struct Rate {
         double tflops, full_ctas;
     };
-    static const Rate kRates[] = {{30, 3}, {30, 1.5}, {27, 2}, {23, 3}, {22, 3}, {20, 6}};
+    static const Rate kRates[] = {{30, 3}, {30, 1.5}, {27, 2}, {23, 3},
+                                  {22, 3}, {20, 6},   {32, 1.5}, {32, 3}};
     const Rate r = kRates[t.id];
     const int64_t tiles = ((s.M + t.BM - 1) / t.BM) * ((s.K + t.BN - 1) / t.BN);
     const int64_t kt = (s.Kg + t.BK - 1) / t.BK;
+    if (kt < 4 * split) return 1e300;                      // too little reduction to split
     const double work = (double)tiles * t.BM * t.BN * kt * t.BK;   // FMAs incl. padding
-    const double per_sm = (double)tiles / sms;
+    const double per_sm = (double)tiles * split / sms;
     const double fill = std::min(1.0, per_sm / r.full_ctas);
-    return work / (r.tflops * fill);
+    const double reduce = split > 1 ? 1.0 + 0.06 * split : 1.0;
+    return work * reduce / (r.tflops * fill);
 }
 
 conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
     if (!cc_shape_ok(s)) return CONV2D_ERR_UNSUPPORTED;
-    int forced = -1;
-    if (const char *e = std::getenv("CONV2D_CC_TILE")) forced = std::atoi(e);
+    const int forced = env_int("CONV2D_CC_TILE");
+    const int forced_split = env_int("CONV2D_CC_SPLIT");
     double best = 1e300;
-    int best_id = -1;
+    int best_id = -1, best_split = 1;
     for (int id = 0; id < cc_num_tiles(); ++id) {
-        const CudaCoreTile t = cc_tile(id);
-        const size_t smem = cc_smem_bytes(s, t);
-        if (smem > d.smem_optin) continue;
-        if (forced >= 0 && id != forced) continue;
-        const double c = cc_cost(s, t, d.sm_count);
-        if (c < best) { best = c; best_id = id; }
+        for (int split : {1, 2, 4}) {
+            if (!cc_tile_available(id, s.dtype, split)) continue;
+            if (forced >= 0 && id != forced) continue;
+            if (forced_split > 0 && split != forced_split) continue;
+            const CudaCoreTile t = cc_tile(id);
+            const size_t smem = cc_smem_bytes(s, t);
+            if (smem > d.smem_optin) continue;
+            const double c = cc_cost(s, t, split, d.sm_count);
+            if (c < best) { best = c; best_id = id; best_split = split; }
+        }
     }
     if (best_id < 0) return CONV2D_ERR_UNSUPPORTED;
     p->algo = Algo::CudaCore;
     p->cc = cc_tile(best_id);
+    p->cc.split = best_split;
     p->smem_bytes = cc_smem_bytes(s, p->cc);
-    p->grid = (int)(((s.M + p->cc.BM - 1) / p->cc.BM) * ((s.K + p->cc.BN - 1) / p->cc.BN));
+    p->grid = (int)(((s.M + p->cc.BM - 1) / p->cc.BM) * ((s.K + p->cc.BN - 1) / p->cc.BN)) * best_split;
     p->sm_count = d.sm_count;
     return CONV2D_OK;
 }
@@ -269,7 +279,7 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
     const bool al = t == nullptr || aligned16(*t);
     const PlanKey key{dev, s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
                       (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0,
-                      env_int("CONV2D_CC_TILE"),
+                      env_int("CONV2D_CC_TILE") * 8 + env_int("CONV2D_CC_SPLIT"),
                       (((env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 +
                         env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW")) * 4 +
                           env_int("CONV2D_TC_ROTATE") + 64 * env_int("CONV2D_TC_WINVAR")};
@@ -295,8 +305,8 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
             std::fprintf(stderr, "[conv2d] tensor-core BM=128 BN=%d ksub=%d stages=%d grid=%d smem=%zu\n",
                          p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes);
         else
-            std::fprintf(stderr, "[conv2d] cuda-core tile=%d (%dx%dx%d, %dx%d/thread) grid=%d smem=%zu\n",
-                         p.cc.id, p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.grid, p.smem_bytes);
+            std::fprintf(stderr, "[conv2d] cuda-core tile=%d (%dx%dx%d, %dx%d/thread) split=%d grid=%d smem=%zu\n",
+                         p.cc.id, p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.split, p.grid, p.smem_bytes);
     }
     std::lock_guard<std::mutex> lk(g_plan_mu);
     g_plans[key] = p;
@@ -429,8 +439,8 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
                       : (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
                          !p.tc.force_im2col) ? "tile" : "im2col");
     else
-        std::snprintf(buf, len, "cuda_core ffma BM=%d BN=%d BK=%d TM=%d TN=%d threads=%d grid=%d smem=%zu",
-                      p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.threads, p.grid,
+        std::snprintf(buf, len, "cuda_core ffma BM=%d BN=%d BK=%d TM=%d TN=%d threads=%d split=%d grid=%d smem=%zu",
+                      p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.threads, p.cc.split, p.grid,
                       p.smem_bytes);
     return CONV2D_OK;
 }

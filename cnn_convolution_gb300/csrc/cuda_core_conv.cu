@@ -23,12 +23,21 @@
 // Operands are widened to fp32 on the way into shared memory; the epilogue
 // adds the bias, rounds once to the output type and stores through shared
 // memory so that global writes are coalesced.
+//
+// Split-K (SPLIT = 2 or 4, fp32): layers with few output tiles but a long
+// reduction launch SPLIT CTAs per tile as one thread-block cluster; each CTA
+// reduces a contiguous slice of the k-tiles, parks its partial tile in its
+// shared memory, and after a cluster barrier each CTA sums one slice of rows
+// across the cluster through distributed shared memory and writes it.  No
+// global workspace, and the summation order is fixed (deterministic).
 
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <atomic>
 #include <cstdio>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -86,7 +95,7 @@ struct CcCfg {
     static constexpr size_t main_floats = tile_floats > epi_floats ? tile_floats : epi_floats;
 };
 
-template <typename T, int LAYOUT, int BM, int BN, int BK, int TM, int TN>
+template <typename T, int LAYOUT, int BM, int BN, int BK, int TM, int TN, int SPLIT>
 __global__ void __launch_bounds__(CcCfg<T, LAYOUT, BM, BN, BK, TM, TN>::NT)
 cc_conv_kernel(const CcParams p) {
     using Cfg = CcCfg<T, LAYOUT, BM, BN, BK, TM, TN>;
@@ -105,6 +114,12 @@ cc_conv_kernel(const CcParams p) {
     const int n0 = blockIdx.y * BN;
     const int Kg = p.Kg;
     const int PQ = p.P * p.Q;
+    // k-tiles this CTA reduces (all of them unless split across a cluster)
+    const int KT_all = (Kg + BK - 1) / BK;
+    int split_rank = 0;
+    if (SPLIT > 1) split_rank = (int)cooperative_groups::this_cluster().block_rank();
+    const int kt_begin = (int)((int64_t)KT_all * split_rank / SPLIT);
+    const int kt_end = (int)((int64_t)KT_all * (split_rank + 1) / SPLIT);
 
     // Reduction-index table, built for kTableChunk indices at a time.
     auto build_taps = [&](int jbase) {
@@ -130,7 +145,7 @@ cc_conv_kernel(const CcParams p) {
             taps[j - jbase] = t;
         }
     };
-    build_taps(0);
+    build_taps((kt_begin * BK / kTableChunk) * kTableChunk);
 
     // This thread gathers A rows for output pixel m_ld.
     const int ml = tid % BM;
@@ -202,14 +217,14 @@ cc_conv_kernel(const CcParams p) {
 
     const int tx = tid % (BN / TN);
     const int ty = tid / (BN / TN);
-    const int KT = (Kg + BK - 1) / BK;
-
-    load_tile(0);
-    store_tile(0);
+    if (kt_begin < kt_end) {
+        load_tile(kt_begin);
+        store_tile(0);
+    }
     __syncthreads();
-    for (int kt = 0; kt < KT; ++kt) {
-        const int cur = kt & 1;
-        if (kt + 1 < KT) {
+    for (int kt = kt_begin; kt < kt_end; ++kt) {
+        const int cur = (kt - kt_begin) & 1;
+        if (kt + 1 < kt_end) {
             if (((kt + 1) * BK) % kTableChunk == 0) {   // next tile starts a new table chunk
                 __syncthreads();
                 build_taps((kt + 1) * BK);
@@ -237,12 +252,54 @@ cc_conv_kernel(const CcParams p) {
 #pragma unroll
                 for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
-        if (kt + 1 < KT) store_tile(cur ^ 1);
+        if (kt + 1 < kt_end) store_tile(cur ^ 1);
         __syncthreads();
     }
 
     // Epilogue: stage the tile in shared memory, then write coalesced rows.
     float *cs = smem;
+    if constexpr (SPLIT > 1) {
+        // Partial tile -> own shared memory as cs[nl][ml]; cluster barrier;
+        // CTA `split_rank` sums rows [lo, hi) of every CTA's partial tile.
+        constexpr int CS = BM + 1;
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const int mi = (i / 4) * (BM / TMV) + ty * 4 + (i % 4);
+                const int nj = (j / 4) * (BN / TNV) + tx * 4 + (j % 4);
+                cs[nj * CS + mi] = acc[i][j];
+            }
+        auto cluster = cooperative_groups::this_cluster();
+        cluster.sync();
+        const float *parts[SPLIT];
+#pragma unroll
+        for (int r = 0; r < SPLIT; ++r) parts[r] = cluster.map_shared_rank(cs, r);
+        const T *bias = static_cast<const T *>(p.bias);
+        T *y = static_cast<T *>(p.y);
+        constexpr int ROWS = BM / SPLIT;
+        const int lo = split_rank * ROWS;
+        for (int e = tid; e < ROWS * BN; e += NT) {
+            const int mi = lo + e % ROWS, nl = e / ROWS;
+            const int64_t m = m0 + mi;
+            const int k = n0 + nl;
+            if (m < p.M && k < p.K) {
+                float v = 0.f;
+#pragma unroll
+                for (int r = 0; r < SPLIT; ++r) v += parts[r][nl * CS + mi];
+                if (bias) v += to_f32<T>(bias[k]);
+                if (LAYOUT == CONV2D_NCHW) {
+                    const int n = (int)(m / PQ);
+                    const int pq = (int)(m - (int64_t)n * PQ);
+                    y[((int64_t)n * p.K + k) * PQ + pq] = from_f32<T>(v);
+                } else {
+                    y[m * p.K + k] = from_f32<T>(v);
+                }
+            }
+        }
+        cluster.sync();   // peers may still be reading this CTA's partial tile
+        return;
+    }
     const T *bias = static_cast<const T *>(p.bias);
     T *y = static_cast<T *>(p.y);
     if (LAYOUT == CONV2D_NCHW) {
@@ -295,23 +352,32 @@ cc_conv_kernel(const CcParams p) {
 
 struct TileEntry {
     int BM, BN, BK, TM, TN;
+    bool all_dtypes;   // instantiated for fp16 / bf16 too (otherwise fp32 only)
 };
 // Kept in sync with the dispatch switch below.
 constexpr TileEntry kTiles[] = {
-    {128, 64, 8, 8, 8},    // 0: 128 threads, 64 acc/thread
-    {128, 128, 8, 8, 8},   // 1: 256 threads
-    {64, 64, 16, 4, 4},    // 2: 256 threads, 16 acc/thread
-    {128, 32, 16, 8, 4},   // 3: 128 threads (narrow K, e.g. 32 output channels)
-    {64, 32, 16, 4, 4},    // 4: 128 threads
-    {32, 32, 16, 4, 4},    // 5: 64 threads (tiny layers)
+    {128, 64, 8, 8, 8, true},     // 0: 128 threads, 64 acc/thread
+    {128, 128, 8, 8, 8, false},   // 1: 256 threads
+    {64, 64, 16, 4, 4, true},     // 2: 256 threads, 16 acc/thread
+    {128, 32, 16, 8, 4, false},   // 3: 128 threads (narrow K, e.g. 32 output channels)
+    {64, 32, 16, 4, 4, false},    // 4: 128 threads
+    {32, 32, 16, 4, 4, true},     // 5: 64 threads (tiny layers)
+    {128, 128, 16, 8, 8, false},  // 6: 256 threads, deeper k-tile
+    {128, 64, 16, 8, 8, false},   // 7: 128 threads, deeper k-tile
 };
 constexpr int kNumTiles = sizeof(kTiles) / sizeof(kTiles[0]);
 
-template <typename T, int LAYOUT, int BM, int BN, int BK, int TM, int TN>
+// Split-K factors compiled for fp32 (tile ids 1, 6, 7, 2, 0).
+bool split_compiled(int id, int split) {
+    if (split == 1) return true;
+    return (split == 2 || split == 4) && (id == 0 || id == 1 || id == 2 || id == 6 || id == 7);
+}
+
+template <typename T, int LAYOUT, int BM, int BN, int BK, int TM, int TN, int SPLIT>
 conv2d_status_t launch_one(const Shape &s, const Tensors &t, int grid_m, int grid_n,
                            size_t smem, cudaStream_t st) {
     using Cfg = CcCfg<T, LAYOUT, BM, BN, BK, TM, TN>;
-    auto kern = cc_conv_kernel<T, LAYOUT, BM, BN, BK, TM, TN>;
+    auto kern = cc_conv_kernel<T, LAYOUT, BM, BN, BK, TM, TN, SPLIT>;
     // Opt in to >48 KB dynamic shared memory: raise the kernel's limit when a
     // launch needs more than was set before (per device).
     if (smem > 48 * 1024) {
@@ -333,25 +399,69 @@ conv2d_status_t launch_one(const Shape &s, const Tensors &t, int grid_m, int gri
     p.N = s.N; p.C = s.C; p.H = s.H; p.W = s.W; p.K = s.K; p.R = s.R; p.S = s.S;
     p.stride = s.stride; p.pad = s.pad; p.dil = s.dil; p.P = s.P; p.Q = s.Q;
     p.Kg = (int)s.Kg; p.M = s.M;
-    dim3 grid(grid_m, grid_n);
-    kern<<<grid, Cfg::NT, smem, st>>>(p);
+    if (SPLIT == 1) {
+        dim3 grid(grid_m, grid_n);
+        kern<<<grid, Cfg::NT, smem, st>>>(p);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid_m, grid_n, SPLIT);
+        cfg.blockDim = dim3(Cfg::NT);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = SPLIT;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return CONV2D_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
+template <typename T, int LAYOUT, int SPLIT>
+conv2d_status_t dispatch_tile_split(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    const CudaCoreTile &c = pl.cc;
+    const int gm = (int)((s.M + c.BM - 1) / c.BM);
+    const int gn = (s.K + c.BN - 1) / c.BN;
+    constexpr bool f32 = std::is_same<T, float>::value;
+    switch (c.id) {
+        case 0: return launch_one<T, LAYOUT, 128, 64, 8, 8, 8, SPLIT>(s, t, gm, gn, pl.smem_bytes, st);
+        case 2: return launch_one<T, LAYOUT, 64, 64, 16, 4, 4, SPLIT>(s, t, gm, gn, pl.smem_bytes, st);
+        case 5:
+            if constexpr (SPLIT == 1)
+                return launch_one<T, LAYOUT, 32, 32, 16, 4, 4, 1>(s, t, gm, gn, pl.smem_bytes, st);
+            break;
+        default: break;
+    }
+    if constexpr (f32) {
+        switch (c.id) {
+            case 1: return launch_one<T, LAYOUT, 128, 128, 8, 8, 8, SPLIT>(s, t, gm, gn, pl.smem_bytes, st);
+            case 6: return launch_one<T, LAYOUT, 128, 128, 16, 8, 8, SPLIT>(s, t, gm, gn, pl.smem_bytes, st);
+            case 7: return launch_one<T, LAYOUT, 128, 64, 16, 8, 8, SPLIT>(s, t, gm, gn, pl.smem_bytes, st);
+            case 3:
+                if constexpr (SPLIT == 1)
+                    return launch_one<T, LAYOUT, 128, 32, 16, 8, 4, 1>(s, t, gm, gn, pl.smem_bytes, st);
+                break;
+            case 4:
+                if constexpr (SPLIT == 1)
+                    return launch_one<T, LAYOUT, 64, 32, 16, 4, 4, 1>(s, t, gm, gn, pl.smem_bytes, st);
+                break;
+            default: break;
+        }
+    }
+    return CONV2D_ERR_INTERNAL;
 }
 
 template <typename T, int LAYOUT>
 conv2d_status_t dispatch_tile(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
-    const CudaCoreTile &c = pl.cc;
-    const int gm = (int)((s.M + c.BM - 1) / c.BM);
-    const int gn = (s.K + c.BN - 1) / c.BN;
-    switch (c.id) {
-        case 0: return launch_one<T, LAYOUT, 128, 64, 8, 8, 8>(s, t, gm, gn, pl.smem_bytes, st);
-        case 1: return launch_one<T, LAYOUT, 128, 128, 8, 8, 8>(s, t, gm, gn, pl.smem_bytes, st);
-        case 2: return launch_one<T, LAYOUT, 64, 64, 16, 4, 4>(s, t, gm, gn, pl.smem_bytes, st);
-        case 3: return launch_one<T, LAYOUT, 128, 32, 16, 8, 4>(s, t, gm, gn, pl.smem_bytes, st);
-        case 4: return launch_one<T, LAYOUT, 64, 32, 16, 4, 4>(s, t, gm, gn, pl.smem_bytes, st);
-        case 5: return launch_one<T, LAYOUT, 32, 32, 16, 4, 4>(s, t, gm, gn, pl.smem_bytes, st);
-        default: return CONV2D_ERR_INTERNAL;
+    if constexpr (std::is_same<T, float>::value) {
+        if (pl.cc.split == 2) return dispatch_tile_split<T, LAYOUT, 2>(s, pl, t, st);
+        if (pl.cc.split == 4) return dispatch_tile_split<T, LAYOUT, 4>(s, pl, t, st);
     }
+    if (pl.cc.split != 1) return CONV2D_ERR_INTERNAL;
+    return dispatch_tile_split<T, LAYOUT, 1>(s, pl, t, st);
 }
 
 template <int LAYOUT>
@@ -368,12 +478,19 @@ conv2d_status_t dispatch_dtype(const Shape &s, const Plan &pl, const Tensors &t,
 
 int cc_num_tiles() { return kNumTiles; }
 
+bool cc_tile_available(int id, conv2d_dtype_t dtype, int split) {
+    if (id < 0 || id >= kNumTiles) return false;
+    if (dtype != CONV2D_F32) return kTiles[id].all_dtypes && split == 1;
+    return split_compiled(id, split);
+}
+
 CudaCoreTile cc_tile(int id) {
     const TileEntry &e = kTiles[id];
     CudaCoreTile t;
     t.id = id;
     t.BM = e.BM; t.BN = e.BN; t.BK = e.BK; t.TM = e.TM; t.TN = e.TN;
     t.threads = (e.BM / e.TM) * (e.BN / e.TN);
+    t.split = 1;
     return t;
 }
 

@@ -30,6 +30,7 @@ struct CudaCoreTile {
     int id;          // index into the kernel table
     int BM, BN, BK, TM, TN;
     int threads;
+    int split;       // CTAs (one cluster) sharing one output tile's reduction
 };
 
 // Tile configurations of the tensor-core kernel.
@@ -65,6 +66,7 @@ struct Tensors {
 // CUDA-core path (any dtype / layout).  Returns CONV2D_OK or an error code.
 int cc_num_tiles();
 CudaCoreTile cc_tile(int id);
+bool cc_tile_available(int id, conv2d_dtype_t dtype, int split);
 bool cc_shape_ok(const Shape &s);
 size_t cc_smem_bytes(const Shape &s, const CudaCoreTile &t);
 conv2d_status_t cc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);

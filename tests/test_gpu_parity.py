@@ -231,3 +231,33 @@ def test_misaligned_device_pointer_rejected():
 
 def test_device_status_clean():
     assert conv2d.get_device_status() == 0
+
+
+SPLIT_SHAPES = [
+    wl.ConvSpec("split_a", 2, 64, 15, 15, 128, 2, 2, 2, 1),
+    wl.ConvSpec("split_b", 3, 128, 8, 8, 256, 2, 2, 2, 0),
+    wl.ConvSpec("split_c", 1, 37, 11, 13, 70, 3, 3, 1, 1),       # ragged everything
+    wl.ConvSpec("split_d", 2, 600, 5, 5, 40, 3, 3, 1, 1),        # long reduction: tap-table rebuild
+    wl.ConvSpec("split_e", 4, 96, 7, 9, 64, 3, 1, 2, 1, bias=False),
+]
+
+
+@pytest.mark.parametrize("layout", ["NCHW", "NHWC"])
+@pytest.mark.parametrize("tile,split", [(0, 2), (1, 4), (2, 2), (6, 2), (6, 4), (7, 4)])
+def test_cuda_core_split_k_clusters(tile, split, layout):
+    """fp32 split-K: a cluster of `split` CTAs shares each output tile's
+    reduction and sums the partial tiles through distributed shared memory."""
+    import os
+    os.environ["CONV2D_CC_TILE"] = str(tile)
+    os.environ["CONV2D_CC_SPLIT"] = str(split)
+    try:
+        for base in SPLIT_SHAPES:
+            spec = base.replace(layout=layout)
+            x, w, b = wl.random_inputs(spec, seed=31)
+            y, d = run_gpu(spec, x, w, b, "cuda_core")
+            assert f"split={split}" in d.plan(), d.plan()
+            err = full_parity(spec, x, w, b, "cuda_core")
+            assert err <= TOL["f32"], f"{spec.name} tile {tile} split {split}: {err}"
+    finally:
+        os.environ.pop("CONV2D_CC_TILE", None)
+        os.environ.pop("CONV2D_CC_SPLIT", None)
