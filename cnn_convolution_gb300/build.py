@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(PKG, "_build", platform.machine())
 LIB_NAME = "libconv2d_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
-SOURCES = ["api.cpp", "status.cu", "cuda_core_conv.cu", "tc_conv_sm103a.cu"]
+SOURCES = ["api.cpp", "status.cu", "cuda_core_conv.cu", "tc_conv_sm103a.cu", "tf32x3_conv_sm103a.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -51,7 +51,7 @@ def _newer(target: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = nvcc_path()
-    headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith(".h")]
+    headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "conv2d.h"))
     objs, jobs = [], []
     for src in SOURCES:

@@ -118,11 +118,14 @@ double cc_cost(const Shape &s, const CudaCoreTile &t, int split, int sms) {
     const Rate r = kRates[t.id];
     const int64_t tiles = ((s.M + t.BM - 1) / t.BM) * ((s.K + t.BN - 1) / t.BN);
     const int64_t kt = (s.Kg + t.BK - 1) / t.BK;
-    if (kt < 4 * split) return 1e300;                      // too little reduction to split
+    if (split > 1 && kt < 8 * split) return 1e300;         // too little reduction to split
     const double work = (double)tiles * t.BM * t.BN * kt * t.BK;   // FMAs incl. padding
     const double per_sm = (double)tiles * split / sms;
     const double fill = std::min(1.0, per_sm / r.full_ctas);
-    const double reduce = split > 1 ? 1.0 + 0.06 * split : 1.0;
+    // Each cluster rank pays the tap-table build, two cluster barriers and
+    // the partial-tile exchange: about as much as 6 k-tiles of its own loop
+    // (measured on the MSCRED encoder layers).
+    const double reduce = split > 1 ? 1.0 + 6.0 * split / kt : 1.0;
     return work * reduce / (r.tflops * fill);
 }
 
@@ -256,6 +259,48 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     return CONV2D_OK;
 }
 
+// fp32 split-precision tensor-core plan (3xTF32).  Per 32-element stage of
+// a 128 x BN tile the tensor cores spend 3 x 128 x BN x 32 / 2048 = 6 BN SM
+// cycles; the producer warps spend about (1408 + 5 BN) warp instructions on
+// the gather, the split and the shared-memory stores (A: 11 per element,
+// B: 5), issued at about 2 (4 producer warps) or 3 (8 warps) per cycle.  A
+// stage takes the larger of the two; a CTA runs ceil(tiles / SMs) tiles.
+// The result is in nanoseconds (at 1.9 GHz) plus a fixed 2 us for launch and
+// pipeline fill.
+double tf_cost_ns(const Shape &s, const TfTile &t, int sms) {
+    const int64_t tiles = ((s.M + 127) / 128) * ((s.K + t.BN - 1) / t.BN);
+    const int64_t rounds = (tiles + sms - 1) / sms;
+    const int64_t kt = (s.Kg + 31) / 32;
+    const double mma = 6.0 * t.BN;
+    const double prod = (1408.0 + 5.0 * t.BN) / (t.nprod >= 8 ? 3.0 : 2.0);
+    return 2000.0 + (double)rounds * kt * std::max(mma, prod) / 1.9;
+}
+
+conv2d_status_t choose_tf(const Shape &s, const DevInfo &d, Plan *p, double *cost_ns) {
+    if (!(d.cc_major == 10 && d.cc_minor == 3) || !tf_shape_ok(s)) return CONV2D_ERR_UNSUPPORTED;
+    const int forced = env_int("CONV2D_TF_VAR");
+    double best = 1e300;
+    int best_id = -1;
+    for (int id = 0; id < tf_num_variants(); ++id) {
+        if (forced >= 0 && id != forced) continue;
+        const TfTile t = tf_variant(id);
+        if (tf_smem_bytes(s, t) > d.smem_optin) continue;
+        // a tile much wider than K wastes tensor-core work
+        if (forced < 0 && t.BN > 32 && s.K <= t.BN / 2) continue;
+        const double c = tf_cost_ns(s, t, d.sm_count);
+        if (c < best) { best = c; best_id = id; }
+    }
+    if (best_id < 0) return CONV2D_ERR_UNSUPPORTED;
+    p->algo = Algo::Tf32x3;
+    p->tf = tf_variant(best_id);
+    p->smem_bytes = tf_smem_bytes(s, p->tf);
+    const int64_t tiles = ((s.M + 127) / 128) * ((s.K + p->tf.BN - 1) / p->tf.BN);
+    p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
+    p->sm_count = d.sm_count;
+    if (cost_ns) *cost_ns = best;
+    return CONV2D_OK;
+}
+
 bool aligned16(const Tensors &t) {
     auto a = [](const void *p) { return ((uintptr_t)p & 15) == 0; };
     return a(t.x) && a(t.w) && a(t.y) && (t.bias == nullptr || ((uintptr_t)t.bias & 1) == 0);
@@ -265,7 +310,7 @@ bool aligned16(const Tensors &t) {
 // tile overrides).  CONV2D_CC_TILE / CONV2D_TC_BN force a tile (tests and
 // A/B measurements); they are read on every call so they can change.
 using PlanKey = std::tuple<int, int, int, int, int, int, int, int, int, int, int, int, int, int, int,
-                           int, int>;
+                           int, int, int>;
 
 
 std::mutex g_plan_mu;
@@ -282,7 +327,8 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
                       env_int("CONV2D_CC_TILE") * 8 + env_int("CONV2D_CC_SPLIT"),
                       (((env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 +
                         env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW")) * 4 +
-                          env_int("CONV2D_TC_ROTATE") + 64 * env_int("CONV2D_TC_WINVAR")};
+                          env_int("CONV2D_TC_ROTATE") + 64 * env_int("CONV2D_TC_WINVAR"),
+                      env_int("CONV2D_TF_VAR") * 4 + env_int("CONV2D_FP32_TC")};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);
@@ -290,7 +336,25 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
     }
     Plan p{};
     const bool tc_ok = tc_shape_ok(s, t);
-    if (algo == CONV2D_ALGO_TENSOR_CORE) {
+    if (s.dtype == CONV2D_F32) {
+        // fp32: FFMA on CUDA cores, or 3xTF32 on tensor cores, whichever the
+        // cost models expect to be faster (CONV2D_FP32_TC=0 keeps FFMA).
+        if (algo == CONV2D_ALGO_TENSOR_CORE) {
+            st = choose_tf(s, d, &p, nullptr);
+        } else if (algo == CONV2D_ALGO_CUDA_CORE) {
+            st = choose_cc(s, d, &p);
+        } else {
+            Plan ptf{};
+            double tf_ns = 1e300;
+            const bool tf_on = env_int("CONV2D_FP32_TC") != 0 &&
+                               choose_tf(s, d, &ptf, &tf_ns) == CONV2D_OK;
+            st = choose_cc(s, d, &p);
+            if (tf_on && (st != CONV2D_OK || tf_ns < cc_cost(s, p.cc, p.cc.split, d.sm_count) * 2e-3)) {
+                p = ptf;
+                st = CONV2D_OK;
+            }
+        }
+    } else if (algo == CONV2D_ALGO_TENSOR_CORE) {
         if (!tc_ok) return CONV2D_ERR_UNSUPPORTED;
         st = choose_tc(s, d, &p);
     } else if (algo == CONV2D_ALGO_CUDA_CORE) {
@@ -304,6 +368,9 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
         if (p.algo == Algo::TensorCore)
             std::fprintf(stderr, "[conv2d] tensor-core BM=128 BN=%d ksub=%d stages=%d grid=%d smem=%zu\n",
                          p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes);
+        else if (p.algo == Algo::Tf32x3)
+            std::fprintf(stderr, "[conv2d] tensor-core 3xtf32 BM=128 BN=%d stages=%d producers=%d grid=%d smem=%zu\n",
+                         p.tf.BN, p.tf.stages, p.tf.nprod, p.grid, p.smem_bytes);
         else
             std::fprintf(stderr, "[conv2d] cuda-core tile=%d (%dx%dx%d, %dx%d/thread) split=%d grid=%d smem=%zu\n",
                          p.cc.id, p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.split, p.grid, p.smem_bytes);
@@ -376,6 +443,7 @@ conv2d_status_t run(const Shape &s, conv2d_algo_t algo, const Tensors &t, cudaSt
     st = get_plan(s, algo, &t, &p);
     if (st != CONV2D_OK) return st;
     if (p.algo == Algo::TensorCore) return tc_launch(s, p, t, stream);
+    if (p.algo == Algo::Tf32x3) return tf_launch(s, p, t, stream);
     return cc_launch(s, p, t, stream);
 }
 
@@ -419,7 +487,7 @@ conv2d_status_t conv2d_desc_set_algo(conv2d_desc_t desc, conv2d_algo_t algo) {
     if (!desc) return CONV2D_ERR_INVALID_ARG;
     if (algo != CONV2D_ALGO_AUTO && algo != CONV2D_ALGO_CUDA_CORE && algo != CONV2D_ALGO_TENSOR_CORE)
         return CONV2D_ERR_INVALID_ARG;
-    if (algo == CONV2D_ALGO_TENSOR_CORE && !tc_shape_ok(desc->s, nullptr))
+    if (algo == CONV2D_ALGO_TENSOR_CORE && !tc_shape_ok(desc->s, nullptr) && !tf_shape_ok(desc->s))
         return CONV2D_ERR_UNSUPPORTED;
     if (algo == CONV2D_ALGO_CUDA_CORE && !cc_shape_ok(desc->s)) return CONV2D_ERR_UNSUPPORTED;
     desc->algo = algo;
@@ -438,6 +506,9 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
                       p.tc.window ? "window"
                       : (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
                          !p.tc.force_im2col) ? "tile" : "im2col");
+    else if (p.algo == Algo::Tf32x3)
+        std::snprintf(buf, len, "tensor_core tcgen05 3xtf32 BM=128 BN=%d BK=32 stages=%d producers=%d grid=%d smem=%zu",
+                      p.tf.BN, p.tf.stages, p.tf.nprod * 32, p.grid, p.smem_bytes);
     else
         std::snprintf(buf, len, "cuda_core ffma BM=%d BN=%d BK=%d TM=%d TN=%d threads=%d split=%d grid=%d smem=%zu",
                       p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.threads, p.cc.split, p.grid,

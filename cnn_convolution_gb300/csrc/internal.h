@@ -45,12 +45,21 @@ struct TcTile {
     bool rotate = true;          // CTA-dependent start of the k-loop
 };
 
-enum class Algo { CudaCore, TensorCore };
+// Variants of the fp32 split-precision (3xTF32) tensor-core kernel.
+struct TfTile {
+    int BN;          // output channels per tile
+    int stages;      // smem pipeline depth (32 reduction elements per stage)
+    int nprod;       // producer (gather + split) warps
+    int id;          // index into the variant table
+};
+
+enum class Algo { CudaCore, TensorCore, Tf32x3 };
 
 struct Plan {
     Algo algo;
     CudaCoreTile cc;
     TcTile tc;
+    TfTile tf;
     int grid;        // CTAs launched
     int sm_count;
     size_t smem_bytes;
@@ -86,6 +95,13 @@ int tc_window_variants();
 TcWinVariant tc_window_variant(int id);
 bool tc_window_variant_ok(const Shape &s, int id);
 conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
+
+// fp32 tensor-core path (3xTF32 split precision, NCHW or NHWC).
+bool tf_shape_ok(const Shape &s);
+int tf_num_variants();
+TfTile tf_variant(int id);
+size_t tf_smem_bytes(const Shape &s, const TfTile &t);
+conv2d_status_t tf_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
 
 // Device status word (bounded-wait failures).
 conv2d_status_t status_read_and_clear();

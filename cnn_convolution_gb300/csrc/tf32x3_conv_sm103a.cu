@@ -1,0 +1,590 @@
+// Split-precision tensor-core convolution for fp32 tensors on sm_103a (3xTF32).
+//
+// The fp32 path of "Enabling Memory-efficient Im2win Convolution with
+// Multi-precision Support on GPU CUDA and Tensor Cores" (abstract: the same
+// convolution across precisions) moved from CUDA cores to tensor cores while
+// keeping fp32 accuracy.  Blackwell has no full-rate fp32 MMA, but it has
+// TF32 (fp32 range, 11 significant bits).  Every fp32 operand a is split, as
+// it is staged into shared memory, into
+//     a_hi = tf32_rn(a),   a_lo = tf32_rn(a - a_hi)       (a - a_hi is exact)
+// and each product is formed as x_hi*w_hi + x_hi*w_lo + x_lo*w_hi: three
+// kind::tf32 MMAs into one fp32 accumulator in tensor memory.  What is left
+// out per product -- x_lo*w_lo and the two split residues |a - a_hi - a_lo|
+// <= 2^-22 |a| -- is at most about 3 * 2^-22 |x||w|, i.e. below 7.2e-7 of
+// sum |x||w| over a whole output even if every term erred the same way.
+//
+// GEMM view as in "GPU-Accelerating MSCRED with CUDA, im2col, GEMM, and a
+// Custom PyTorch Extension" (section "Transforming Conv2D into im2col and
+// GEMM"), without materialising the im2col matrix: D[m, k] = sum_g
+// A[m, g] * W[k, g] with m = (n, p, q) and g the reduction index in the
+// weight tensor's own order -- (c, r, s) for KCRS weights (NCHW), (r, s, c)
+// for KRSC weights (NHWC) -- so every weight row is contiguous.  A[m, g] is
+// gathered from x through a per-CTA table g -> (offset, r*dil, s*dil), zero
+// outside the image, exactly like the CUDA-core kernel's tap table.
+//
+// Warp roles: warps 0..3 epilogue (warp w owns accumulator lanes 32w..32w+31),
+// warps 4..3+NPROD gather + split + store the A and B tiles of each stage in
+// the 128-byte-swizzled K-major layout the MMA descriptors expect, the last
+// warp allocates tensor memory and issues the MMAs.  A stage covers 32
+// reduction elements (one 128-byte row of fp32); tiles are 128 output pixels
+// x BN output channels; the accumulator is double-buffered in tensor memory
+// so the epilogue of one tile overlaps the main loop of the next; CTAs are
+// persistent.  Every mbarrier wait is bounded (see ptx_sm103a.cuh).
+
+#include <cuda.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx_sm103a.cuh"
+
+namespace conv2d {
+namespace {
+
+using namespace sm103a;
+
+constexpr int kTfBM = 128;                    // output pixels per tile (MMA M, TMEM lanes)
+constexpr int kTfBK = 32;                     // reduction elements per stage (128 B of fp32)
+constexpr int kTfATile = kTfBM * kTfBK * 4;   // one A operand tile: 16 KB
+
+// D(tmem) (+)= A(smem) * B(smem)^T, M=128, N from idesc, K=8 (TF32).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor, kind::tf32: fp32 accumulate, A and B TF32, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc_tf32(int n) {
+    return (1u << 4)                                   // D format: f32
+           | (2u << 7)                                 // A format: TF32
+           | (2u << 10)                                // B format: TF32
+           | ((uint32_t)(n >> 3) << 17)                // N / 8
+           | ((uint32_t)(kTfBM >> 4) << 24);           // M / 16
+}
+
+// fp32 -> nearest TF32 value as an fp32 bit pattern; the 13 low mantissa
+// bits are cleared explicitly so the value is exactly the TF32 number.
+__device__ __forceinline__ uint32_t tf32_rn(float a) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(a));
+    return r & 0xFFFFE000u;
+}
+
+// Split four values into their TF32 high and low parts.
+__device__ __forceinline__ void split4(const float (&v)[4], uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        hi[e] = tf32_rn(v[e]);
+        lo[e] = tf32_rn(v[e] - __uint_as_float(hi[e]));
+    }
+}
+
+struct TfParams {
+    const float *x;
+    const float *w;
+    const float *bias;
+    float *y;
+    unsigned int *status;
+    int64_t M;          // N*P*Q
+    int64_t img;        // elements of x per image (C*H*W)
+    int K, Kg, KT;      // output channels, reduction length, stages per tile
+    int C, H, W, S, RS;
+    int Q, PQ;
+    int stride, pad, dil;
+    int n_tiles_n, total_tiles;
+    int nhwc;
+    int w_vec;          // Kg % 4 == 0 and w 16-byte aligned: weight rows load as float4
+    int y_vec;          // NHWC, K % 4 == 0 and y 16-byte aligned: outputs store as float4
+};
+
+// Tensor memory: columns [0, 2 BN) hold the correction accumulators (x_hi*w_lo
+// + x_lo*w_hi) of two tiles in flight; NSLOT slots of BN columns after them
+// receive the x_hi*w_hi partial sum of one 32-element stage each.
+template <int BN>
+struct TfTmem {
+    static constexpr int kSlots = BN >= 128 ? 2 : 6;
+    static constexpr int kUsed = 2 * BN + kSlots * BN;
+    static constexpr uint32_t kCols = kUsed <= 32 ? 32 : kUsed <= 64 ? 64 : kUsed <= 128 ? 128
+                                      : kUsed <= 256 ? 256 : 512;
+    static_assert(kUsed <= 512, "tensor memory");
+};
+
+// Shared memory: STAGES x (A_hi, A_lo, B_hi, B_lo), barriers, then the tap table.
+template <int BN, int STAGES>
+struct TfSmem {
+    static constexpr int kBTile = BN * kTfBK * 4;
+    static constexpr int kStage = 2 * kTfATile + 2 * kBTile;
+    static constexpr int kSlots = TfTmem<BN>::kSlots;
+    static constexpr size_t kBarOffset = (size_t)STAGES * kStage;
+    // full[S], empty[S], slot_full[NS], slot_empty[NS], corr_full[2], corr_empty[2], drain;
+    // then the tensor-memory address and the abort flag
+    static constexpr size_t kBarBytes = (2 * STAGES + 2 * kSlots + 5) * 8;
+    static constexpr size_t kTapOffset = (kBarOffset + kBarBytes + 16 + 15) / 16 * 16;
+    static constexpr size_t bytes(int kt) { return kTapOffset + (size_t)kt * kTfBK * 8 + 1024; }
+};
+
+template <int BN> constexpr int tf_epi_warps() { return BN >= 128 ? 8 : 4; }
+template <int BN, int NPROD> constexpr int tf_threads() { return 32 * (tf_epi_warps<BN>() + NPROD + 1); }
+
+// Accuracy: the tensor cores add each MMA's products into the fp32
+// accumulator with their own (not round-to-nearest) alignment and rounding,
+// so one long accumulation chain loses bits in proportion to its length.
+// Hence the x_hi*w_hi term -- the only one of full magnitude -- is summed in
+// tensor memory over one stage only (4 MMAs of K=8) and the stage sums are
+// added in fp32 registers by the epilogue warps; the correction terms, 2^-11
+// smaller, stay in one accumulator per tile.
+template <int BN, int STAGES, int NPROD>
+__global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel(const TfParams p) {
+    using L = TfSmem<BN, STAGES>;
+    using TM = TfTmem<BN>;
+    constexpr uint32_t kIdesc = make_idesc_tf32(BN);
+    constexpr int kSlots = TM::kSlots;
+    constexpr int kEpiWarps = tf_epi_warps<BN>();
+    constexpr int kEpiThreads = 32 * kEpiWarps;
+    constexpr int kCpt = BN * 4 / kEpiWarps;                     // accumulator columns per epilogue thread
+    constexpr int kProd = 32 * NPROD;                            // producer threads
+    constexpr int kMmaWarp = kEpiWarps + NPROD;
+    constexpr int kChunks = 8 * kTfBM / kProd;                   // A chunks (4 values) per thread per stage
+    constexpr int kBIter = BN * 8 / kProd;                       // B chunks per thread per stage
+    static_assert(kChunks >= 1 && kChunks * kProd == 8 * kTfBM, "producer split (A)");
+    static_assert(kBIter >= 1 && kBIter * kProd == 8 * BN, "producer split (B)");
+    static_assert(kCpt % 32 == 0, "epilogue columns");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t bar_base = smem_base + (uint32_t)L::kBarOffset;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto slotf_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
+    auto slote_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + kSlots + s); };
+    auto corrf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * kSlots + a); };
+    auto corre_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * kSlots + 2 + a); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * kSlots + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
+    int2 *taps = reinterpret_cast<int2 *>(smem + L::kTapOffset);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    // Tap table: reduction index g -> (offset of x[g] from the output pixel's
+    // input origin, (r*dil) << 16 | s*dil).  Entries past Kg carry a row
+    // offset of -32768, which no pixel of the image reaches: they read as 0.
+    for (int g = threadIdx.x; g < p.KT * kTfBK; g += blockDim.x) {
+        int2 t;
+        if (g < p.Kg) {
+            int c, rs;
+            if (p.nhwc) {
+                rs = g / p.C;
+                c = g - rs * p.C;
+            } else {
+                c = g / p.RS;
+                rs = g - c * p.RS;
+            }
+            const int r = rs / p.S, s = rs - r * p.S;
+            const int dh = r * p.dil, dw = s * p.dil;
+            t.x = p.nhwc ? (dh * p.W + dw) * p.C + c : (c * p.H + dh) * p.W + dw;
+            t.y = (dh << 16) | dw;
+        } else {
+            t.x = 0;
+            t.y = (int)0x80000000u;
+        }
+        taps[g] = t;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), kProd);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(slotf_bar(s), 1);
+            mbar_init(slote_bar(s), kEpiThreads);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(corrf_bar(a), 1);
+            mbar_init(corre_bar(a), kEpiThreads);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_holder), TM::kCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    auto a_hi = [&](int s) { return smem_base + (uint32_t)(s * L::kStage); };
+    auto a_lo = [&](int s) { return smem_base + (uint32_t)(s * L::kStage + kTfATile); };
+    auto b_hi = [&](int s) { return smem_base + (uint32_t)(s * L::kStage + 2 * kTfATile); };
+    auto b_lo = [&](int s) { return smem_base + (uint32_t)(s * L::kStage + 2 * kTfATile + L::kBTile); };
+
+    if (warp >= kEpiWarps && warp < kMmaWarp) {
+        // ---------------------------------------------------------- producers
+        // Thread pt owns A row (pt % 128) and kChunks of its 8 16-byte chunks;
+        // B rows are shared out 8 chunks per row across all producer threads.
+        // All global loads of a stage are issued before the first shared
+        // store, so their latencies overlap.  Stores follow the 128-byte
+        // swizzle: chunk j of row r sits at position j ^ (r % 8) of the row.
+        const int pt = threadIdx.x - kEpiThreads;
+        const int row = pt & (kTfBM - 1);
+        const int chunk0 = (pt / kTfBM) * kChunks;
+        const uint32_t a_row_off = (uint32_t)row * 128u;
+        const uint32_t row_sw = (uint32_t)(row & 7);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            const int tm = tile / p.n_tiles_n;
+            const int tn = tile - tm * p.n_tiles_n;
+            const int64_t m = (int64_t)tm * kTfBM + row;
+            int h0 = -65536, w0 = 0;
+            int64_t base = 0;
+            if (m < p.M) {
+                const int n = (int)(m / p.PQ);
+                const int pq = (int)(m - (int64_t)n * p.PQ);
+                const int pp = pq / p.Q, q = pq - pp * p.Q;
+                h0 = pp * p.stride - p.pad;
+                w0 = q * p.stride - p.pad;
+                base = (int64_t)n * p.img +
+                       (p.nhwc ? ((int64_t)h0 * p.W + w0) * p.C : (int64_t)h0 * p.W + w0);
+            }
+            const int k0 = tn * BN;
+            for (int ks = 0; ks < p.KT; ++ks) {
+                // every lane observes the MMAs' release of the stage itself
+                // before overwriting it
+                if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                const int2 *tp = taps + ks * kTfBK;
+                float va[kChunks][4];
+#pragma unroll
+                for (int j = 0; j < kChunks; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int2 t = tp[(chunk0 + j) * 4 + e];
+                        const int dh = t.y >> 16, dw = (int)(short)(t.y & 0xFFFF);
+                        const bool in = (unsigned)(h0 + dh) < (unsigned)p.H &&
+                                        (unsigned)(w0 + dw) < (unsigned)p.W;
+                        va[j][e] = in ? __ldg(p.x + base + t.x) : 0.f;
+                    }
+                }
+                float vb[kBIter][4];
+#pragma unroll
+                for (int it = 0; it < kBIter; ++it) {
+                    const int i = pt + it * kProd;
+                    const int k = k0 + (i >> 3);
+                    const int g = ks * kTfBK + (i & 7) * 4;
+                    vb[it][0] = vb[it][1] = vb[it][2] = vb[it][3] = 0.f;
+                    if (k < p.K) {
+                        const float *wr = p.w + (int64_t)k * p.Kg + g;
+                        if (p.w_vec) {
+                            if (g < p.Kg) {
+                                const float4 f = __ldg(reinterpret_cast<const float4 *>(wr));
+                                vb[it][0] = f.x; vb[it][1] = f.y; vb[it][2] = f.z; vb[it][3] = f.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (g + e < p.Kg) vb[it][e] = __ldg(wr + e);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kChunks; ++j) {
+                    uint32_t hi[4], lo[4];
+                    split4(va[j], hi, lo);
+                    const uint32_t off = a_row_off + ((((uint32_t)(chunk0 + j)) ^ row_sw) << 4);
+                    st_shared_v4(a_hi(stage) + off, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(a_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
+                }
+#pragma unroll
+                for (int it = 0; it < kBIter; ++it) {
+                    const int i = pt + it * kProd;
+                    const int kr = i >> 3, cj = i & 7;
+                    uint32_t hi[4], lo[4];
+                    split4(vb[it], hi, lo);
+                    const uint32_t off = (uint32_t)kr * 128u + ((((uint32_t)cj) ^ (uint32_t)(kr & 7)) << 4);
+                    st_shared_v4(b_hi(stage) + off, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(b_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
+                }
+                // make this thread's generic-proxy stores visible to the tensor cores
+                fence_proxy_async_smem();
+                mbar_arrive(full_bar(stage));
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == kMmaWarp && lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        int stage = 0, slot = 0, acc = 0;
+        uint32_t phase = 0, slot_phase = 0, acc_phase = 0;
+        bool ok = true, any = false;
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            if (!mbar_wait(corre_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_corr = tmem_base + (uint32_t)(acc * BN);
+            for (int ks = 0; ks < p.KT; ++ks) {
+                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status) ||
+                    !mbar_wait(slote_bar(slot), slot_phase ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_main = tmem_base + (uint32_t)(2 * BN + slot * BN);
+                const uint64_t ah = smem_desc_sw128(a_hi(stage)), al = smem_desc_sw128(a_lo(stage));
+                const uint64_t bh = smem_desc_sw128(b_hi(stage)), bl = smem_desc_sw128(b_lo(stage));
+                // advance 8 elements (32 bytes) along K inside the swizzled rows
+#pragma unroll
+                for (int kk = 0; kk < kTfBK / 8; ++kk)
+                    mma_tf32(d_main, ah + (uint64_t)(kk * 2), bh + (uint64_t)(kk * 2), kIdesc, kk != 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kTfBK / 8; ++kk) {
+                    const uint64_t o = (uint64_t)(kk * 2);
+                    mma_tf32(d_corr, ah + o, bl + o, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+                    mma_tf32(d_corr, al + o, bh + o, kIdesc, 1u);
+                }
+                any = true;
+                mma_commit(empty_bar(stage));
+                mma_commit(slotf_bar(slot));
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++slot == kSlots) { slot = 0; slot_phase ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit(corrf_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (any) {
+            // every MMA must retire before tensor memory is released
+            mma_commit(drain_bar);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(drain_bar, 0) && cycles_left(t0)) {
+            }
+        }
+    } else if (warp < kEpiWarps) {
+        // ---------------------------------------------------------- epilogue
+        // Thread = one output pixel (accumulator lane) x kCpt channels.  Per
+        // stage: tcgen05.ld of the stage's x_hi*w_hi slot, fp32 adds into
+        // registers; per tile: + the correction accumulator, + bias, store.
+        // NCHW: a warp's 32 pixels are consecutive in y for each channel, so
+        // every store instruction writes whole lines.
+        const int quarter = warp & 3;
+        const int col0 = (warp >> 2) * kCpt;
+        const int row = quarter * 32 + lane;
+        const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+        int slot = 0, acc = 0;
+        uint32_t slot_phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            float a[kCpt];
+#pragma unroll
+            for (int j = 0; j < kCpt; ++j) a[j] = 0.f;
+            for (int ks = 0; ks < p.KT; ++ks) {
+                int okw = 1;
+                if (lane == 0) okw = mbar_wait(slotf_bar(slot), slot_phase, abort_flag, p.status) ? 1 : 0;
+                okw = __shfl_sync(0xffffffffu, okw, 0);
+                if (!okw) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < kCpt; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32cols(t_lane + (uint32_t)(2 * BN + slot * BN + col0 + c), v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) a[c + j] += __uint_as_float(v[j]);
+                }
+                tc_fence_before();
+                mbar_arrive(slote_bar(slot));
+                if (++slot == kSlots) { slot = 0; slot_phase ^= 1u; }
+            }
+            if (!ok) break;
+            int okw = 1;
+            if (lane == 0) okw = mbar_wait(corrf_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            if (!okw) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < kCpt; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32cols(t_lane + (uint32_t)(acc * BN + col0 + c), v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a[c + j] += __uint_as_float(v[j]);
+            }
+            tc_fence_before();
+            mbar_arrive(corre_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+
+            const int tm = tile / p.n_tiles_n;
+            const int tn = tile - tm * p.n_tiles_n;
+            const int64_t m = (int64_t)tm * kTfBM + row;
+            if (m >= p.M) continue;
+            const int kb = tn * BN + col0;
+            if (p.nhwc) {
+                float *yr = p.y + m * p.K;
+                if (p.y_vec) {
+#pragma unroll
+                    for (int j = 0; j < kCpt; j += 4) {
+                        const int k = kb + j;
+                        if (k < p.K) {
+                            float4 o;
+                            o.x = a[j] + (p.bias ? __ldg(p.bias + k) : 0.f);
+                            o.y = a[j + 1] + (p.bias ? __ldg(p.bias + k + 1) : 0.f);
+                            o.z = a[j + 2] + (p.bias ? __ldg(p.bias + k + 2) : 0.f);
+                            o.w = a[j + 3] + (p.bias ? __ldg(p.bias + k + 3) : 0.f);
+                            *reinterpret_cast<float4 *>(yr + k) = o;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kCpt; ++j) {
+                        const int k = kb + j;
+                        if (k < p.K) yr[k] = a[j] + (p.bias ? __ldg(p.bias + k) : 0.f);
+                    }
+                }
+            } else {
+                const int64_t n = m / p.PQ;
+                float *yr = p.y + n * p.K * p.PQ + (m - n * p.PQ);
+#pragma unroll
+                for (int j = 0; j < kCpt; ++j) {
+                    const int k = kb + j;
+                    if (k < p.K) yr[(int64_t)k * p.PQ] = a[j] + (p.bias ? __ldg(p.bias + k) : 0.f);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TM::kCols);
+    }
+}
+
+bool ensure_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &done_mask) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const uint64_t bit = (uint64_t)1 << (dev & 63);
+    if (done_mask.load(std::memory_order_acquire) & bit) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return false;
+    done_mask.fetch_or(bit, std::memory_order_release);
+    return true;
+}
+
+template <int BN, int STAGES, int NPROD>
+conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    using L = TfSmem<BN, STAGES>;
+    TfParams p;
+    p.x = static_cast<const float *>(t.x);
+    p.w = static_cast<const float *>(t.w);
+    p.bias = static_cast<const float *>(t.bias);
+    p.y = static_cast<float *>(t.y);
+    p.status = status_word_ptr();
+    p.M = s.M;
+    p.img = (int64_t)s.C * s.H * s.W;
+    p.K = s.K;
+    p.Kg = (int)s.Kg;
+    p.KT = (int)((s.Kg + kTfBK - 1) / kTfBK);
+    p.C = s.C;
+    p.H = s.H;
+    p.W = s.W;
+    p.S = s.S;
+    p.RS = s.R * s.S;
+    p.Q = s.Q;
+    p.PQ = s.P * s.Q;
+    p.stride = s.stride;
+    p.pad = s.pad;
+    p.dil = s.dil;
+    p.n_tiles_n = (s.K + BN - 1) / BN;
+    const int64_t tiles = ((s.M + kTfBM - 1) / kTfBM) * (int64_t)p.n_tiles_n;
+    if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
+    p.total_tiles = (int)tiles;
+    p.nhwc = s.layout == CONV2D_NHWC ? 1 : 0;
+    p.w_vec = (s.Kg % 4 == 0 && ((uintptr_t)t.w & 15) == 0) ? 1 : 0;
+    p.y_vec = (p.nhwc && s.K % 4 == 0 && ((uintptr_t)t.y & 15) == 0) ? 1 : 0;
+    const size_t bytes = L::bytes(p.KT);
+    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD>;
+    static std::atomic<uint64_t> attr_done{0};   // this instantiation's per-device flags
+    // the attribute is set for the largest table this variant accepts
+    if (!ensure_attr(reinterpret_cast<const void *>(kern), 227 * 1024, attr_done)) return CONV2D_ERR_CUDA;
+    if (bytes > 227 * 1024) return CONV2D_ERR_UNSUPPORTED;
+    const int grid = pl.grid > 0 ? pl.grid : 1;
+    kern<<<grid, tf_threads<BN, NPROD>(), bytes, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
+// (BN, STAGES, producer warps) of every compiled variant.
+#define CONV2D_TF_VARIANTS(X) \
+    X(32, 5, 4)               \
+    X(64, 4, 4)               \
+    X(128, 3, 4)              \
+    X(32, 5, 8)               \
+    X(64, 4, 8)               \
+    X(128, 3, 8)
+
+}  // namespace
+
+int tf_num_variants() {
+    int n = 0;
+#define X(vbn, vst, vnp) ++n;
+    CONV2D_TF_VARIANTS(X)
+#undef X
+    return n;
+}
+
+TfTile tf_variant(int id) {
+    int i = 0;
+    TfTile t{0, 0, 0, -1};
+#define X(vbn, vst, vnp)              \
+    if (i == id) t = TfTile{vbn, vst, vnp, id}; \
+    ++i;
+    CONV2D_TF_VARIANTS(X)
+#undef X
+    return t;
+}
+
+size_t tf_smem_bytes(const Shape &s, const TfTile &t) {
+    const size_t kt = (size_t)((s.Kg + kTfBK - 1) / kTfBK);
+    const size_t stage = 2 * (size_t)kTfATile + 2 * (size_t)t.BN * kTfBK * 4;
+    const size_t slots = t.BN >= 128 ? 2 : 6;
+    const size_t bars = (2 * (size_t)t.stages + 2 * slots + 5) * 8;
+    return ((size_t)t.stages * stage + bars + 16 + 15) / 16 * 16 + kt * kTfBK * 8 + 1024;
+}
+
+bool tf_shape_ok(const Shape &s) {
+    if (s.dtype != CONV2D_F32) return false;
+    if (s.H > 32767 || s.W > 32767) return false;
+    if ((int64_t)s.dil * (s.R - 1) > 32767 || (int64_t)s.dil * (s.S - 1) > 32767) return false;
+    if (s.Kg > ((int64_t)1 << 20)) return false;
+    // 32-bit tap offsets within one image
+    const int64_t span_h = (int64_t)s.dil * (s.R - 1) + 1, span_w = (int64_t)s.dil * (s.S - 1) + 1;
+    const int64_t lim = (int64_t)1 << 31;
+    if ((int64_t)s.C * s.H * s.W >= lim) return false;
+    if ((span_h * s.W + span_w) * s.C >= lim) return false;
+    if ((int64_t)s.C * s.H * s.W + span_h * s.W + span_w >= lim) return false;
+    if ((int64_t)s.P * s.Q >= lim) return false;
+    return true;
+}
+
+conv2d_status_t tf_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+#define X(vbn, vst, vnp) \
+    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp) return launch_tf<vbn, vst, vnp>(s, pl, t, st);
+    CONV2D_TF_VARIANTS(X)
+#undef X
+    return CONV2D_ERR_INTERNAL;
+}
+
+}  // namespace conv2d

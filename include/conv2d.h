@@ -73,7 +73,8 @@ typedef enum { CONV2D_NCHW = 0, CONV2D_NHWC = 1 } conv2d_layout_t;
 typedef enum {
     CONV2D_ALGO_AUTO = 0,
     CONV2D_ALGO_CUDA_CORE = 1,    /* shared-memory implicit GEMM on FFMA, any dtype/layout */
-    CONV2D_ALGO_TENSOR_CORE = 2   /* tcgen05 + TMA im2col implicit GEMM, f16/bf16 NHWC */
+    CONV2D_ALGO_TENSOR_CORE = 2   /* tcgen05 implicit GEMM: f16/bf16 NHWC (TMA im2col / windows),
+                                     or fp32 either layout as split-precision 3xTF32 */
 } conv2d_algo_t;
 
 typedef struct conv2d_desc *conv2d_desc_t;

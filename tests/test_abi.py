@@ -139,7 +139,12 @@ def test_set_algo_validation(lib):
     assert rc == 0
     assert lib.conv2d_desc_set_algo(h, 1) == 0
     assert lib.conv2d_desc_set_algo(h, 9) == 1
-    # fp32 NCHW has no tensor-core kernel
+    # fp32 (either layout) has the split-precision tensor-core kernel
+    assert lib.conv2d_desc_set_algo(h, 2) == 0
+    lib.conv2d_desc_destroy(h)
+    # fp16 NCHW has no tensor-core kernel
+    rc, h = _desc(lib, 2, 8, 8, 8, 8, 3, 3, 1, 1, 1, 1, 0)
+    assert rc == 0
     assert lib.conv2d_desc_set_algo(h, 2) == 2
     lib.conv2d_desc_destroy(h)
 
