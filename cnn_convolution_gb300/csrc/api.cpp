@@ -259,21 +259,16 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     return CONV2D_OK;
 }
 
-// fp32 split-precision tensor-core plan (3xTF32).  Per 32-element stage of
-// a 128 x BN tile the tensor cores spend 3 x 128 x BN x 32 / 2048 = 6 BN SM
-// cycles; the producer warps spend about (1408 + 5 BN) warp instructions on
-// the gather, the split and the shared-memory stores (A: 11 per element,
-// B: 5), issued at about 2 (4 producer warps) or 3 (8 warps) per cycle.  A
-// stage takes the larger of the two; a CTA runs ceil(tiles / SMs) tiles.
-// The result is in nanoseconds (at 1.9 GHz) plus a fixed 2 us for launch and
-// pipeline fill.
+// fp32 split-precision tensor-core plan (3xTF32).  Each variant carries its
+// measured time per 32-element stage of one 128 x BN tile; a tile also pays
+// about 2 us of pipeline fill and epilogue, a launch about 2 us.  Persistent
+// CTAs run ceil(tiles / SMs) tiles each.  Result in nanoseconds, comparable
+// with cc_cost() * 2e-3.
 double tf_cost_ns(const Shape &s, const TfTile &t, int sms) {
     const int64_t tiles = ((s.M + 127) / 128) * ((s.K + t.BN - 1) / t.BN);
     const int64_t rounds = (tiles + sms - 1) / sms;
     const int64_t kt = (s.Kg + 31) / 32;
-    const double mma = 6.0 * t.BN;
-    const double prod = (1408.0 + 5.0 * t.BN) / (t.nprod >= 8 ? 3.0 : 2.0);
-    return 2000.0 + (double)rounds * kt * std::max(mma, prod) / 1.9;
+    return 2000.0 + (double)rounds * ((double)kt * t.stage_ns + 2000.0);
 }
 
 conv2d_status_t choose_tf(const Shape &s, const DevInfo &d, Plan *p, double *cost_ns) {

@@ -51,6 +51,7 @@ struct TfTile {
     int stages;      // smem pipeline depth (32 reduction elements per stage)
     int nprod;       // producer (gather + split) warps
     int id;          // index into the variant table
+    int stage_ns;    // measured time of one 32-element stage of one tile (GB300)
 };
 
 enum class Algo { CudaCore, TensorCore, Tf32x3 };

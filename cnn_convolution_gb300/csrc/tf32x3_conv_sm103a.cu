@@ -68,12 +68,36 @@ __host__ __device__ constexpr uint32_t make_idesc_tf32(int n) {
            | ((uint32_t)(kTfBM >> 4) << 24);           // M / 16
 }
 
-// fp32 -> nearest TF32 value as an fp32 bit pattern; the 13 low mantissa
-// bits are cleared explicitly so the value is exactly the TF32 number.
+// fp32 -> nearest TF32 value (ties away from zero), on the bit pattern:
+// adding half a TF32 unit (bit 12) to the sign-magnitude encoding and
+// clearing the 13 low mantissa bits rounds the magnitude; a carry moves into
+// the exponent as it should.  Integer ALU work at full rate, unlike a
+// conversion instruction.
 __device__ __forceinline__ uint32_t tf32_rn(float a) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(a));
-    return r & 0xFFFFE000u;
+    return (__float_as_uint(a) + 0x1000u) & 0xFFFFE000u;
+}
+
+// Predicated read-only loads that leave 0 where the predicate is false.  The
+// register is zeroed and then conditionally loaded inside one asm statement,
+// so nothing consumes the loaded value before it is used: a C++ `p ? ld : 0`
+// becomes a select right after the load and stalls on every load in turn.
+__device__ __forceinline__ float ldg_or_zero(const float *ptr, bool pred) {
+    float v;
+    asm("{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %2, 0;\n\t"
+        "mov.b32 %0, 0;\n\t"
+        "@p ld.global.nc.f32 %0, [%1];\n\t}"
+        : "=f"(v)
+        : "l"(ptr), "r"((int)pred));
+    return v;
+}
+__device__ __forceinline__ void ldg4_or_zero(const float *ptr, bool pred, float (&v)[4]) {
+    asm("{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "@p ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+        : "l"(ptr), "r"((int)pred));
 }
 
 // Split four values into their TF32 high and low parts.
@@ -84,6 +108,28 @@ __device__ __forceinline__ void split4(const float (&v)[4], uint32_t (&hi)[4], u
         lo[e] = tf32_rn(v[e] - __uint_as_float(hi[e]));
     }
 }
+
+// Optional timeline trace of CTA 0 (compile with -DCONV2D_TC_TRACE; off in
+// the library build), read back with conv2d_tf_trace_dump().
+#ifdef CONV2D_TC_TRACE
+__device__ unsigned long long g_tf_trace[4][8192];
+__device__ unsigned int g_tf_trace_n[4];
+// one tracing thread per role keeps its own event count in a register
+#define TF_TRACE(role, tag)                                                                  \
+    do {                                                                                     \
+        if (blockIdx.x == 0) {                                                               \
+            if (tr_n < 8192u)                                                                \
+                g_tf_trace[role][tr_n] =                                                     \
+                    ((unsigned long long)(tag) << 48) | ((unsigned long long)clock64() & 0xFFFFFFFFFFFFull); \
+            ++tr_n;                                                                          \
+            g_tf_trace_n[role] = tr_n;                                                       \
+        }                                                                                    \
+    } while (0)
+#else
+#define TF_TRACE(role, tag) \
+    do {                    \
+    } while (0)
+#endif
 
 struct TfParams {
     const float *x;
@@ -99,6 +145,8 @@ struct TfParams {
     int stride, pad, dil;
     int n_tiles_n, total_tiles;
     int nhwc;
+    int rs_mask;        // R*S <= 63: taps carry their (r, s) index, tested against a per-tile mask
+    int R;
     int w_vec;          // Kg % 4 == 0 and w 16-byte aligned: weight rows load as float4
     int y_vec;          // NHWC, K % 4 == 0 and y 16-byte aligned: outputs store as float4
 };
@@ -129,7 +177,7 @@ struct TfSmem {
     static constexpr size_t bytes(int kt) { return kTapOffset + (size_t)kt * kTfBK * 8 + 1024; }
 };
 
-template <int BN> constexpr int tf_epi_warps() { return BN >= 128 ? 8 : 4; }
+template <int BN> constexpr int tf_epi_warps() { return BN >= 64 ? 8 : 4; }
 template <int BN, int NPROD> constexpr int tf_threads() { return 32 * (tf_epi_warps<BN>() + NPROD + 1); }
 
 // Accuracy: the tensor cores add each MMA's products into the fp32
@@ -147,6 +195,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     constexpr int kSlots = TM::kSlots;
     constexpr int kEpiWarps = tf_epi_warps<BN>();
     constexpr int kEpiThreads = 32 * kEpiWarps;
+    static_assert(NPROD <= 32 && kEpiWarps <= 32, "arrival counts");
     constexpr int kCpt = BN * 4 / kEpiWarps;                     // accumulator columns per epilogue thread
     constexpr int kProd = 32 * NPROD;                            // producer threads
     constexpr int kMmaWarp = kEpiWarps + NPROD;
@@ -154,11 +203,12 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     constexpr int kBIter = BN * 8 / kProd;                       // B chunks per thread per stage
     static_assert(kChunks >= 1 && kChunks * kProd == 8 * kTfBM, "producer split (A)");
     static_assert(kBIter >= 1 && kBIter * kProd == 8 * BN, "producer split (B)");
-    static_assert(kCpt % 32 == 0, "epilogue columns");
+    static_assert(kCpt % 16 == 0, "epilogue columns");
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned base, derived from the shared array itself so that
+    // the compiler keeps the shared address space (plain shared loads)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t bar_base = smem_base + (uint32_t)L::kBarOffset;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
@@ -174,10 +224,15 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+#ifdef CONV2D_TC_TRACE
+    unsigned tr_n = 0;
+#endif
 
     // Tap table: reduction index g -> (offset of x[g] from the output pixel's
-    // input origin, (r*dil) << 16 | s*dil).  Entries past Kg carry a row
-    // offset of -32768, which no pixel of the image reaches: they read as 0.
+    // input origin, tap id).  With R*S <= 63 the tap id is r*S + s, looked up
+    // in a per-tile bitmask of the taps that fall inside the image; entries
+    // past Kg use id 63, never set.  Otherwise it is (r*dil) << 16 | s*dil and
+    // entries past Kg carry a row offset of -32768, which no pixel reaches.
     for (int g = threadIdx.x; g < p.KT * kTfBK; g += blockDim.x) {
         int2 t;
         if (g < p.Kg) {
@@ -192,25 +247,25 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             const int r = rs / p.S, s = rs - r * p.S;
             const int dh = r * p.dil, dw = s * p.dil;
             t.x = p.nhwc ? (dh * p.W + dw) * p.C + c : (c * p.H + dh) * p.W + dw;
-            t.y = (dh << 16) | dw;
+            t.y = p.rs_mask ? rs : (dh << 16) | dw;
         } else {
             t.x = 0;
-            t.y = (int)0x80000000u;
+            t.y = p.rs_mask ? 63 : (int)0x80000000u;
         }
         taps[g] = t;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), kProd);
+            mbar_init(full_bar(s), NPROD);          // one arrival per producer warp
             mbar_init(empty_bar(s), 1);
         }
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(slotf_bar(s), 1);
-            mbar_init(slote_bar(s), kEpiThreads);
+            mbar_init(slote_bar(s), kEpiWarps);     // one arrival per epilogue warp
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(corrf_bar(a), 1);
-            mbar_init(corre_bar(a), kEpiThreads);
+            mbar_init(corre_bar(a), kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -234,96 +289,151 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
         // ---------------------------------------------------------- producers
         // Thread pt owns A row (pt % 128) and kChunks of its 8 16-byte chunks;
         // B rows are shared out 8 chunks per row across all producer threads.
-        // All global loads of a stage are issued before the first shared
-        // store, so their latencies overlap.  Stores follow the 128-byte
-        // swizzle: chunk j of row r sits at position j ^ (r % 8) of the row.
+        // The CTA's (tile, stage) pairs are numbered f = 0, 1, ...; the loads
+        // of stage f+1 are issued before stage f is split and stored, so one
+        // stage of global loads is always in flight per thread.  Stores
+        // follow the 128-byte swizzle: chunk j of row r sits at position
+        // j ^ (r % 8) of the row.
         const int pt = threadIdx.x - kEpiThreads;
         const int row = pt & (kTfBM - 1);
         const int chunk0 = (pt / kTfBM) * kChunks;
         const uint32_t a_row_off = (uint32_t)row * 128u;
         const uint32_t row_sw = (uint32_t)(row & 7);
-        int stage = 0;
-        uint32_t phase = 0;
+        const int my_tiles = (p.total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+        const int nf = my_tiles * p.KT;
+        // loader position (tile, stage) and the row state of that tile
+        int l_tile = (int)blockIdx.x, l_ks = 0, cur_tile = -1;
+        int h0 = -65536, w0 = 0, base = 0, k0 = 0;
+        uint64_t vmask = 0;          // bit r*S+s: tap (r, s) of this row's pixel lies inside the image
+        const float *ximg = p.x;
+        const int4 *taps4 = reinterpret_cast<const int4 *>(taps);   // two taps per 16 bytes
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
-            const int tm = tile / p.n_tiles_n;
-            const int tn = tile - tm * p.n_tiles_n;
-            const int64_t m = (int64_t)tm * kTfBM + row;
-            int h0 = -65536, w0 = 0;
-            int64_t base = 0;
-            if (m < p.M) {
-                const int n = (int)(m / p.PQ);
-                const int pq = (int)(m - (int64_t)n * p.PQ);
-                const int pp = pq / p.Q, q = pq - pp * p.Q;
-                h0 = pp * p.stride - p.pad;
-                w0 = q * p.stride - p.pad;
-                base = (int64_t)n * p.img +
-                       (p.nhwc ? ((int64_t)h0 * p.W + w0) * p.C : (int64_t)h0 * p.W + w0);
-            }
-            const int k0 = tn * BN;
-            for (int ks = 0; ks < p.KT; ++ks) {
-                // every lane observes the MMAs' release of the stage itself
-                // before overwriting it
-                if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status))) {
-                    ok = false;
-                    break;
+
+        auto load = [&](float (&va)[kChunks][4], float (&vb)[kBIter][4]) {
+            if (pt == 0) TF_TRACE(0, 1);
+            const int ks = l_ks;
+            if (l_tile != cur_tile) {
+                cur_tile = l_tile;
+                const int tm = l_tile / p.n_tiles_n;
+                k0 = (l_tile - tm * p.n_tiles_n) * BN;
+                const int64_t m = (int64_t)tm * kTfBM + row;
+                h0 = -65536;
+                w0 = 0;
+                base = 0;
+                ximg = p.x;
+                if (m < p.M) {
+                    const int n = (int)(m / p.PQ);
+                    const int pq = (int)(m - (int64_t)n * p.PQ);
+                    const int pp = pq / p.Q, q = pq - pp * p.Q;
+                    h0 = pp * p.stride - p.pad;
+                    w0 = q * p.stride - p.pad;
+                    ximg = p.x + (int64_t)n * p.img;
+                    base = p.nhwc ? (h0 * p.W + w0) * p.C : h0 * p.W + w0;
                 }
-                const int2 *tp = taps + ks * kTfBK;
-                float va[kChunks][4];
+                if (p.rs_mask) {
+                    vmask = 0;
+                    if (m < p.M) {
+                        uint32_t wbits = 0;
+                        for (int s = 0; s < p.S; ++s)
+                            wbits |= ((unsigned)(w0 + s * p.dil) < (unsigned)p.W ? 1u : 0u) << s;
+                        for (int r = 0; r < p.R; ++r)
+                            if ((unsigned)(h0 + r * p.dil) < (unsigned)p.H)
+                                vmask |= (uint64_t)wbits << (r * p.S);
+                    }
+                }
+            }
+            if (++l_ks == p.KT) { l_ks = 0; l_tile += (int)gridDim.x; }
+            // all taps of this thread's chunks first (shared broadcast reads),
+            // then all the global loads
+            int4 tv[kChunks * 2];
+#pragma unroll
+            for (int q = 0; q < kChunks * 2; ++q) tv[q] = taps4[(ks * kTfBK + chunk0 * 4) / 2 + q];
+            const float *xrow = ximg + base;   // the pixel's input origin (may lie in the padding)
+            if (p.rs_mask) {
 #pragma unroll
                 for (int j = 0; j < kChunks; ++j) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int2 t = tp[(chunk0 + j) * 4 + e];
-                        const int dh = t.y >> 16, dw = (int)(short)(t.y & 0xFFFF);
-                        const bool in = (unsigned)(h0 + dh) < (unsigned)p.H &&
-                                        (unsigned)(w0 + dw) < (unsigned)p.W;
-                        va[j][e] = in ? __ldg(p.x + base + t.x) : 0.f;
+                        const int4 t2 = tv[j * 2 + (e >> 1)];
+                        const int off = (e & 1) ? t2.z : t2.x;
+                        const int rs = (e & 1) ? t2.w : t2.y;
+                        va[j][e] = ldg_or_zero(xrow + off, (vmask >> rs) & 1u);
                     }
                 }
-                float vb[kBIter][4];
-#pragma unroll
-                for (int it = 0; it < kBIter; ++it) {
-                    const int i = pt + it * kProd;
-                    const int k = k0 + (i >> 3);
-                    const int g = ks * kTfBK + (i & 7) * 4;
-                    vb[it][0] = vb[it][1] = vb[it][2] = vb[it][3] = 0.f;
-                    if (k < p.K) {
-                        const float *wr = p.w + (int64_t)k * p.Kg + g;
-                        if (p.w_vec) {
-                            if (g < p.Kg) {
-                                const float4 f = __ldg(reinterpret_cast<const float4 *>(wr));
-                                vb[it][0] = f.x; vb[it][1] = f.y; vb[it][2] = f.z; vb[it][3] = f.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (g + e < p.Kg) vb[it][e] = __ldg(wr + e);
-                        }
-                    }
-                }
+            } else {
 #pragma unroll
                 for (int j = 0; j < kChunks; ++j) {
-                    uint32_t hi[4], lo[4];
-                    split4(va[j], hi, lo);
-                    const uint32_t off = a_row_off + ((((uint32_t)(chunk0 + j)) ^ row_sw) << 4);
-                    st_shared_v4(a_hi(stage) + off, hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_v4(a_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
-                }
 #pragma unroll
-                for (int it = 0; it < kBIter; ++it) {
-                    const int i = pt + it * kProd;
-                    const int kr = i >> 3, cj = i & 7;
-                    uint32_t hi[4], lo[4];
-                    split4(vb[it], hi, lo);
-                    const uint32_t off = (uint32_t)kr * 128u + ((((uint32_t)cj) ^ (uint32_t)(kr & 7)) << 4);
-                    st_shared_v4(b_hi(stage) + off, hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_v4(b_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const int4 t2 = tv[j * 2 + (e >> 1)];
+                        const int off = (e & 1) ? t2.z : t2.x;
+                        const int hw = (e & 1) ? t2.w : t2.y;
+                        const int dh = hw >> 16, dw = (int)(short)(hw & 0xFFFF);
+                        const bool in = (unsigned)(h0 + dh) < (unsigned)p.H &&
+                                        (unsigned)(w0 + dw) < (unsigned)p.W;
+                        va[j][e] = ldg_or_zero(xrow + off, in);
+                    }
                 }
-                // make this thread's generic-proxy stores visible to the tensor cores
-                fence_proxy_async_smem();
-                mbar_arrive(full_bar(stage));
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+#pragma unroll
+            for (int it = 0; it < kBIter; ++it) {
+                const int i = pt + it * kProd;
+                const int k = k0 + (i >> 3);
+                const int g = ks * kTfBK + (i & 7) * 4;
+                const float *wr = p.w + (int64_t)k * p.Kg + g;
+                if (p.w_vec) {
+                    ldg4_or_zero(wr, k < p.K && g < p.Kg, vb[it]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) vb[it][e] = ldg_or_zero(wr + e, k < p.K && g + e < p.Kg);
+                }
+            }
+        };
+        auto store = [&](int f, const float (&va)[kChunks][4], const float (&vb)[kBIter][4]) -> bool {
+            if (pt == 0) TF_TRACE(0, 6);
+            const int stage = f % STAGES;
+            const uint32_t phase = (uint32_t)(f / STAGES) & 1u;
+            // every lane observes the MMAs' release of the stage itself before overwriting it
+            if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)))
+                return false;
+            if (pt == 0) TF_TRACE(0, 2);
+#pragma unroll
+            for (int j = 0; j < kChunks; ++j) {
+                uint32_t hi[4], lo[4];
+                split4(va[j], hi, lo);
+                const uint32_t off = a_row_off + ((((uint32_t)(chunk0 + j)) ^ row_sw) << 4);
+                st_shared_v4(a_hi(stage) + off, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(a_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
+            }
+#pragma unroll
+            for (int it = 0; it < kBIter; ++it) {
+                const int i = pt + it * kProd;
+                const int kr = i >> 3, cj = i & 7;
+                uint32_t hi[4], lo[4];
+                split4(vb[it], hi, lo);
+                const uint32_t off = (uint32_t)kr * 128u + ((((uint32_t)cj) ^ (uint32_t)(kr & 7)) << 4);
+                st_shared_v4(b_hi(stage) + off, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(b_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
+            }
+            // make this thread's generic-proxy stores visible to the tensor cores
+            if (pt == 0) TF_TRACE(0, 5);
+            // each thread makes its generic-proxy stores visible to the tensor
+            // cores; then one lane per warp arrives for the whole warp
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(stage));
+            if (pt == 0) TF_TRACE(0, 3);
+            return true;
+        };
+
+        float va0[kChunks][4], vb0[kBIter][4], va1[kChunks][4], vb1[kBIter][4];
+        if (nf > 0) load(va0, vb0);
+        for (int f = 0; f < nf && ok; f += 2) {
+            if (f + 1 < nf) load(va1, vb1);
+            if (!store(f, va0, vb0)) { ok = false; break; }
+            if (f + 1 < nf) {
+                if (f + 2 < nf) load(va0, vb0);
+                if (!store(f + 1, va1, vb1)) { ok = false; break; }
             }
         }
     } else if (warp == kMmaWarp && lane == 0) {
@@ -336,11 +446,10 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             tc_fence_after();
             const uint32_t d_corr = tmem_base + (uint32_t)(acc * BN);
             for (int ks = 0; ks < p.KT; ++ks) {
-                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status) ||
-                    !mbar_wait(slote_bar(slot), slot_phase ^ 1u, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                TF_TRACE(1, 9);
+                if (!mbar_wait(slote_bar(slot), slot_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                TF_TRACE(1, 4);
                 tc_fence_after();
                 const uint32_t d_main = tmem_base + (uint32_t)(2 * BN + slot * BN);
                 const uint64_t ah = smem_desc_sw128(a_hi(stage)), al = smem_desc_sw128(a_lo(stage));
@@ -395,16 +504,19 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 if (lane == 0) okw = mbar_wait(slotf_bar(slot), slot_phase, abort_flag, p.status) ? 1 : 0;
                 okw = __shfl_sync(0xffffffffu, okw, 0);
                 if (!okw) { ok = false; break; }
+                if (threadIdx.x == 0) TF_TRACE(2, 7);
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < kCpt; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32cols(t_lane + (uint32_t)(2 * BN + slot * BN + col0 + c), v);
+                for (int c = 0; c < kCpt; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld_16cols(t_lane + (uint32_t)(2 * BN + slot * BN + col0 + c), v);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) a[c + j] += __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j) a[c + j] += __uint_as_float(v[j]);
                 }
                 tc_fence_before();
-                mbar_arrive(slote_bar(slot));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(slote_bar(slot));
+                if (threadIdx.x == 0) TF_TRACE(2, 8);
                 if (++slot == kSlots) { slot = 0; slot_phase ^= 1u; }
             }
             if (!ok) break;
@@ -414,14 +526,15 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             if (!okw) break;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < kCpt; c += 32) {
-                uint32_t v[32];
-                tmem_ld_32cols(t_lane + (uint32_t)(acc * BN + col0 + c), v);
+            for (int c = 0; c < kCpt; c += 16) {
+                uint32_t v[16];
+                tmem_ld_16cols(t_lane + (uint32_t)(acc * BN + col0 + c), v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) a[c + j] += __uint_as_float(v[j]);
+                for (int j = 0; j < 16; ++j) a[c + j] += __uint_as_float(v[j]);
             }
             tc_fence_before();
-            mbar_arrive(corre_bar(acc));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(corre_bar(acc));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
 
             const int tm = tile / p.n_tiles_n;
@@ -513,6 +626,8 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cuda
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     p.total_tiles = (int)tiles;
     p.nhwc = s.layout == CONV2D_NHWC ? 1 : 0;
+    p.R = s.R;
+    p.rs_mask = s.R * s.S <= 63 ? 1 : 0;
     p.w_vec = (s.Kg % 4 == 0 && ((uintptr_t)t.w & 15) == 0) ? 1 : 0;
     p.y_vec = (p.nhwc && s.K % 4 == 0 && ((uintptr_t)t.y & 15) == 0) ? 1 : 0;
     const size_t bytes = L::bytes(p.KT);
@@ -526,20 +641,24 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cuda
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 
-// (BN, STAGES, producer warps) of every compiled variant.
+// (BN, STAGES, producer warps, measured ns per stage of one tile) of every
+// compiled variant.  The stage times were measured on GB300 on the MSCRED
+// encoder layers (fp32 NCHW, 3x3 / 2x2 filters); the producers' gather is
+// latency-bound, so more producer warps per SM run a stage faster.
 #define CONV2D_TF_VARIANTS(X) \
-    X(32, 5, 4)               \
-    X(64, 4, 4)               \
-    X(128, 3, 4)              \
-    X(32, 5, 8)               \
-    X(64, 4, 8)               \
-    X(128, 3, 8)
+    X(32, 5, 4, 1240)         \
+    X(64, 4, 4, 3850)         \
+    X(128, 3, 4, 5000)        \
+    X(32, 5, 8, 920)          \
+    X(64, 4, 8, 1370)         \
+    X(128, 3, 8, 3100)        \
+    X(64, 4, 16, 1030)
 
 }  // namespace
 
 int tf_num_variants() {
     int n = 0;
-#define X(vbn, vst, vnp) ++n;
+#define X(vbn, vst, vnp, vns) ++n;
     CONV2D_TF_VARIANTS(X)
 #undef X
     return n;
@@ -547,9 +666,9 @@ int tf_num_variants() {
 
 TfTile tf_variant(int id) {
     int i = 0;
-    TfTile t{0, 0, 0, -1};
-#define X(vbn, vst, vnp)              \
-    if (i == id) t = TfTile{vbn, vst, vnp, id}; \
+    TfTile t{0, 0, 0, -1, 0};
+#define X(vbn, vst, vnp, vns)                        \
+    if (i == id) t = TfTile{vbn, vst, vnp, id, vns}; \
     ++i;
     CONV2D_TF_VARIANTS(X)
 #undef X
@@ -579,8 +698,18 @@ bool tf_shape_ok(const Shape &s) {
     return true;
 }
 
+#ifdef CONV2D_TC_TRACE
+extern "C" int conv2d_tf_trace_dump(unsigned long long *out, unsigned int *counts) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(counts, g_tf_trace_n, sizeof(unsigned int) * 4) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(out, g_tf_trace, sizeof(unsigned long long) * 4 * 8192) != cudaSuccess) return -1;
+    const unsigned int zero[4] = {0, 0, 0, 0};
+    return cudaMemcpyToSymbol(g_tf_trace_n, zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
+}
+#endif
+
 conv2d_status_t tf_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
-#define X(vbn, vst, vnp) \
+#define X(vbn, vst, vnp, vns) \
     if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp) return launch_tf<vbn, vst, vnp>(s, pl, t, st);
     CONV2D_TF_VARIANTS(X)
 #undef X
