@@ -67,6 +67,26 @@ def fp32_alu_peak_tflops():
     return SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
 
 
+# nominal dense TF32 / BF16 tensor rates of GB300 (1.1 and 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def fp32_3xtf32_peak_tflops(peaks):
+    """fp32 convolution on tensor cores as three TF32 products per multiply-add:
+    measured bf16 peak x nominal TF32/BF16 ratio / 3."""
+    return peaks["bf16_tflops"] * TF32_PER_BF16 / 3.0
+
+
+def layer_peak(plan, peaks):
+    """(bound, peak TFLOP/s, source) for the kernel a plan string names."""
+    if plan.startswith("tensor_core tcgen05 3xtf32"):
+        return ("tensor", fp32_3xtf32_peak_tflops(peaks),
+                f"measured bf16 {peaks['bf16_tflops']} TFLOP/s x nominal TF32/BF16 (1.1/2.25) "
+                "/ 3 TF32 products per fp32 multiply-add")
+    return ("alu", fp32_alu_peak_tflops(),
+            "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz")
+
+
 # ------------------------------------------------------------------ distributed
 
 def dist_setup(n_gpus):
@@ -331,16 +351,18 @@ def bench_main(args):
         t = statistics.mean(layer_ms[i])
         tf = flops[i] / (t * 1e-3) / 1e12
         gbs = layer_bytes(spec, P, Q) / (t * 1e-3) / 1e9
+        bound, cpeak, _ = layer_peak(d.plan(), peaks)
         layers.append({"layer": spec.name, "plan": d.plan(), "ms": round(t, 5),
-                       "tflops": round(tf, 3), "alu_frac": round(tf / alu_peak, 4),
+                       "tflops": round(tf, 3), "bound": bound, "compute_frac": round(tf / cpeak, 4),
+                       "alu_frac": round(tf / alu_peak, 4),
                        "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)})
     dom = max(range(n_layers), key=lambda i: statistics.mean(layer_ms[i]))
     dom_t = statistics.mean(layer_ms[dom])
     achieved = flops[dom] / (dom_t * 1e-3) / 1e12
-    roofline = {"kernel": specs[dom].name, "bound": "alu", "achieved": round(achieved, 3),
-                "peak": round(alu_peak, 2), "unit": "TFLOP/s", "frac": round(achieved / alu_peak, 4),
-                "traffic": None,
-                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz"}
+    dom_bound, dom_peak, dom_src = layer_peak(descs[dom].plan(), peaks)
+    roofline = {"kernel": specs[dom].name, "plan": descs[dom].plan(), "bound": dom_bound,
+                "achieved": round(achieved, 3), "peak": round(dom_peak, 2), "unit": "TFLOP/s",
+                "frac": round(achieved / dom_peak, 4), "traffic": None, "peak_source": dom_src}
 
     # end to end through the C ABI: pinned host x -> device, 4 layers, y -> pinned host
     x_pin = x_host.pin_memory()
@@ -393,7 +415,8 @@ def bench_main(args):
             "gpu_launches": n_layers * args.steps,
             "clocks": clocks,
             "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
-                      "bf16_tflops": peaks["bf16_tflops"], "fp32_alu_tflops": round(alu_peak, 2)},
+                      "bf16_tflops": peaks["bf16_tflops"], "fp32_alu_tflops": round(alu_peak, 2),
+                      "fp32_3xtf32_tflops": round(fp32_3xtf32_peak_tflops(peaks), 2)},
             "wall_s_timed_region": round(t_wall, 4),
             "tensor_core_layers": extra,
             "cpu_baseline": cpu,

@@ -143,7 +143,8 @@ conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
             const CudaCoreTile t = cc_tile(id);
             const size_t smem = cc_smem_bytes(s, t);
             if (smem > d.smem_optin) continue;
-            const double c = cc_cost(s, t, split, d.sm_count);
+            double c = cc_cost(s, t, split, d.sm_count);
+            if (c >= 1e300 && forced_split > 0) c = 1e299;   // a forced split skips the gate
             if (c < best) { best = c; best_id = id; best_split = split; }
         }
     }
