@@ -129,7 +129,42 @@ double cc_cost(const Shape &s, const CudaCoreTile &t, int split, int sms) {
     return work * reduce / (r.tflops * fill);
 }
 
+// Direct kernel (short reductions): FFMAs of whole 16 x 32 pixel blocks x
+// 32-channel blocks at about 20 TFLOP/s (measured on GB300 on the MSCRED
+// layer-1 shape), plus about 3 us of launch and staging.  In the units of
+// cc_cost().
+double dc_cost(const Shape &s) {
+    const double blocks = (double)s.N * ((s.P + 15) / 16) * ((s.Q + 31) / 32);
+    const double fma = blocks * 512.0 * (double)((s.K + 31) / 32 * 32) * (double)s.Kg;
+    return (2.0 * fma / 20e3 + 3000.0) / 2e-3;
+}
+
 conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
+    const int force_direct = env_int("CONV2D_DIRECT");
+    if (force_direct != 0 && dc_shape_ok(s) && dc_smem_bytes(s) <= d.smem_optin &&
+        env_int("CONV2D_CC_TILE") < 0 && env_int("CONV2D_CC_SPLIT") < 0) {
+        // take the direct kernel when forced, or when it beats every tile
+        bool take = force_direct == 1;
+        if (!take) {
+            take = true;
+            const double dc = dc_cost(s);
+            for (int id = 0; id < cc_num_tiles() && take; ++id) {
+                if (!cc_tile_available(id, s.dtype, 1)) continue;
+                const CudaCoreTile t = cc_tile(id);
+                if (cc_smem_bytes(s, t) > d.smem_optin) continue;
+                if (cc_cost(s, t, 1, d.sm_count) < dc) take = false;
+            }
+        }
+        if (take) {
+            p->algo = Algo::Direct;
+            p->cc = cc_tile(0);
+            p->cc.split = 1;
+            p->smem_bytes = dc_smem_bytes(s);
+            p->grid = dc_grid(s);
+            p->sm_count = d.sm_count;
+            return CONV2D_OK;
+        }
+    }
     if (!cc_shape_ok(s)) return CONV2D_ERR_UNSUPPORTED;
     const int forced = env_int("CONV2D_CC_TILE");
     const int forced_split = env_int("CONV2D_CC_SPLIT");
@@ -324,7 +359,7 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
                       (((env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 +
                         env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW")) * 4 +
                           env_int("CONV2D_TC_ROTATE") + 64 * env_int("CONV2D_TC_WINVAR"),
-                      env_int("CONV2D_TF_VAR") * 4 + env_int("CONV2D_FP32_TC")};
+                      (env_int("CONV2D_TF_VAR") * 4 + env_int("CONV2D_FP32_TC")) * 4 + env_int("CONV2D_DIRECT")};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);
@@ -345,7 +380,10 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
             const bool tf_on = env_int("CONV2D_FP32_TC") != 0 &&
                                choose_tf(s, d, &ptf, &tf_ns) == CONV2D_OK;
             st = choose_cc(s, d, &p);
-            if (tf_on && (st != CONV2D_OK || tf_ns < cc_cost(s, p.cc, p.cc.split, d.sm_count) * 2e-3)) {
+            const double cc_ns = st != CONV2D_OK ? 1e300
+                                 : p.algo == Algo::Direct ? dc_cost(s) * 2e-3
+                                 : cc_cost(s, p.cc, p.cc.split, d.sm_count) * 2e-3;
+            if (tf_on && (st != CONV2D_OK || tf_ns < cc_ns)) {
                 p = ptf;
                 st = CONV2D_OK;
             }
@@ -440,6 +478,7 @@ conv2d_status_t run(const Shape &s, conv2d_algo_t algo, const Tensors &t, cudaSt
     if (st != CONV2D_OK) return st;
     if (p.algo == Algo::TensorCore) return tc_launch(s, p, t, stream);
     if (p.algo == Algo::Tf32x3) return tf_launch(s, p, t, stream);
+    if (p.algo == Algo::Direct) return dc_launch(s, p, t, stream);
     return cc_launch(s, p, t, stream);
 }
 
@@ -485,7 +524,8 @@ conv2d_status_t conv2d_desc_set_algo(conv2d_desc_t desc, conv2d_algo_t algo) {
         return CONV2D_ERR_INVALID_ARG;
     if (algo == CONV2D_ALGO_TENSOR_CORE && !tc_shape_ok(desc->s, nullptr) && !tf_shape_ok(desc->s))
         return CONV2D_ERR_UNSUPPORTED;
-    if (algo == CONV2D_ALGO_CUDA_CORE && !cc_shape_ok(desc->s)) return CONV2D_ERR_UNSUPPORTED;
+    if (algo == CONV2D_ALGO_CUDA_CORE && !cc_shape_ok(desc->s) && !dc_shape_ok(desc->s))
+        return CONV2D_ERR_UNSUPPORTED;
     desc->algo = algo;
     return CONV2D_OK;
 }
@@ -502,6 +542,9 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
                       p.tc.window ? "window"
                       : (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
                          !p.tc.force_im2col) ? "tile" : "im2col");
+    else if (p.algo == Algo::Direct)
+        std::snprintf(buf, len, "cuda_core direct ffma block=16x32px kc=32 threads=256 grid=%d smem=%zu",
+                      p.grid, p.smem_bytes);
     else if (p.algo == Algo::Tf32x3)
         std::snprintf(buf, len, "tensor_core tcgen05 3xtf32 BM=128 BN=%d BK=32 stages=%d producers=%d grid=%d smem=%zu",
                       p.tf.BN, p.tf.stages, p.tf.nprod * 32, p.grid, p.smem_bytes);

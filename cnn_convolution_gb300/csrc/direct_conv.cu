@@ -1,0 +1,259 @@
+// Direct fp32 convolution for layers with a short reduction (C*R*S <= 64),
+// such as the first MSCRED encoder layer (3 signature-matrix channels, 3x3).
+//
+// The plain definition of the forward convolution as "GPU-Accelerating
+// MSCRED with CUDA, im2col, GEMM, and a Custom PyTorch Extension" states it
+// (section "Understanding the Convolution Operation": every output is the
+// bias plus the sum over input channels and filter taps of input x weight),
+// computed without any lowering: with only C*R*S <= 64 products per output
+// the im2col / GEMM machinery costs more than the arithmetic.
+//
+// A CTA of 256 threads owns a 16 x 32 block of output pixels of one image
+// and every output channel.  It stages the zero-padded input patch that
+// block reads ([C][IH][IW]) and the weights transposed to [C*R*S][K] in
+// shared memory, then each thread accumulates 2 pixels (rows 2w, 2w+1 of the
+// block, column = lane) x 32 channels in registers: per filter tap, 2 patch
+// reads and 8 broadcast 16-byte weight reads feed 64 FFMAs.  Channel blocks
+// of 32 repeat over the same staged patch.  (A 16-channel block with 4 CTAs
+// per SM measured slower on GB300: the register cap forces spills.)  Zero padding lives in the patch,
+// so the inner loop has no bounds tests.  NCHW stores are coalesced across
+// the lanes of a warp (consecutive q); NHWC stores are 16-byte vectors.
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx_sm103a.cuh"
+
+namespace conv2d {
+namespace {
+
+constexpr int kDcThreads = 256;
+constexpr int kDcRows = 16;      // output rows per CTA (2 per warp)
+constexpr int kDcCols = 32;      // output columns per CTA (1 per lane)
+constexpr int kDcKc = 32;        // output channels per register block
+constexpr int kDcBatch = 8;      // staging loads each thread has in flight at once
+
+struct DcParams {
+    const float *x, *w, *bias;
+    float *y;
+    int N, C, H, W, K, R, S, P, Q;
+    int stride, pad, dil;
+    int IH, IW;           // staged patch rows / columns
+    int Kp;               // K rounded up to kDcKc (row length of the transposed weights)
+    int tiles_p, tiles_q;
+    int nhwc;
+};
+
+// RT, ST: compile-time filter size (0 = read from the parameters).
+template <int RT, int ST>
+__global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcParams p) {
+    extern __shared__ float4 dc_smem4[];
+    const int R = RT > 0 ? RT : p.R;
+    const int S = ST > 0 ? ST : p.S;
+    float *xs = reinterpret_cast<float *>(dc_smem4);           // [C][IH][IW]
+    const int plane = p.IH * p.IW;
+    const int patch = p.C * plane;
+    const int RS = R * S;
+    const int Kg = p.C * RS;
+    float *wt = xs + ((patch + 3) & ~3);                       // [Kg][Kp], 16-byte aligned rows
+
+    int t = blockIdx.x;
+    const int tq = t % p.tiles_q;
+    t /= p.tiles_q;
+    const int tp = t % p.tiles_p;
+    const int n = t / p.tiles_p;
+    const int p0 = tp * kDcRows, q0 = tq * kDcCols;
+    const int h0 = p0 * p.stride - p.pad, w0 = q0 * p.stride - p.pad;
+
+    // Stage the input patch (zero outside the image) and the weights as
+    // [g = (c, r, s)][k] (zero for k >= K).  Each thread issues kDcBatch
+    // predicated loads before it stores any of them, so their latencies
+    // overlap instead of adding up.
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int i0 = 0; i0 < patch; i0 += kDcThreads * kDcBatch) {
+        float v[kDcBatch];
+#pragma unroll
+        for (int j = 0; j < kDcBatch; ++j) {
+            const int i = i0 + j * kDcThreads + (int)threadIdx.x;
+            const int iw = i % p.IW;
+            const int r2 = i / p.IW;
+            const int ih = r2 % p.IH;
+            const int c = r2 / p.IH;
+            const int h = h0 + ih, wc = w0 + iw;
+            const bool in = i < patch && (unsigned)h < (unsigned)p.H && (unsigned)wc < (unsigned)p.W;
+            const int64_t off = p.nhwc ? (((int64_t)n * p.H + h) * p.W + wc) * p.C + c
+                                       : (((int64_t)n * p.C + c) * p.H + h) * p.W + wc;
+            v[j] = sm103a::ldg_or_zero(p.x + (in ? off : 0), in);
+        }
+#pragma unroll
+        for (int j = 0; j < kDcBatch; ++j) {
+            const int i = i0 + j * kDcThreads + (int)threadIdx.x;
+            if (i < patch) xs[i] = v[j];
+        }
+    }
+    const int wn = Kg * p.Kp;
+    for (int i0 = 0; i0 < wn; i0 += kDcThreads * kDcBatch) {
+        float v[kDcBatch];
+#pragma unroll
+        for (int j = 0; j < kDcBatch; ++j) {
+            const int i = i0 + j * kDcThreads + (int)threadIdx.x;
+            const int k = i % p.Kp, g = i / p.Kp;
+            int woff = g;                       // offset of w[k = 0][g]
+            if (p.nhwc) {
+                const int c = g / RS, rs = g - c * RS;
+                woff = rs * p.C + c;
+            }
+            const bool in = i < wn && k < p.K;
+            v[j] = sm103a::ldg_or_zero(p.w + (in ? (int64_t)k * Kg + woff : 0), in);
+        }
+#pragma unroll
+        for (int j = 0; j < kDcBatch; ++j) {
+            const int i = i0 + j * kDcThreads + (int)threadIdx.x;
+            if (i < wn) wt[i] = v[j];
+        }
+    }
+    __syncthreads();
+
+    const int pr0 = 2 * warp;                      // this thread's first row in the block
+    const int pa = p0 + pr0, pb = pa + 1, q = q0 + lane;
+    const bool va = pa < p.P && q < p.Q, vb = pb < p.P && q < p.Q;
+    const int xa = (pr0 * p.stride) * p.IW + lane * p.stride;
+    const int xb = xa + p.stride * p.IW;
+    const int64_t PQ = (int64_t)p.P * p.Q;
+
+    for (int kc = 0; kc < p.K; kc += kDcKc) {
+        float acc_a[kDcKc], acc_b[kDcKc];
+#pragma unroll
+        for (int j = 0; j < kDcKc; ++j) acc_a[j] = acc_b[j] = 0.f;
+        const float *wrow = wt + kc;
+        for (int c = 0; c < p.C; ++c) {
+            const float *xc = xs + c * plane;
+#pragma unroll
+            for (int r = 0; r < (RT > 0 ? RT : 1); ++r) {
+                for (int rr = (RT > 0 ? r : 0); rr < (RT > 0 ? r + 1 : R); ++rr) {
+                    const float *xr = xc + rr * p.dil * p.IW;
+#pragma unroll
+                    for (int s0 = 0; s0 < (ST > 0 ? ST : 1); ++s0) {
+                        for (int ss = (ST > 0 ? s0 : 0); ss < (ST > 0 ? s0 + 1 : S); ++ss) {
+                            const float a = xr[xa + ss * p.dil];
+                            const float b = xr[xb + ss * p.dil];
+                            const float4 *w4 = reinterpret_cast<const float4 *>(wrow);
+#pragma unroll
+                            for (int j = 0; j < kDcKc / 4; ++j) {
+                                const float4 wv = w4[j];
+                                acc_a[4 * j] = fmaf(a, wv.x, acc_a[4 * j]);
+                                acc_a[4 * j + 1] = fmaf(a, wv.y, acc_a[4 * j + 1]);
+                                acc_a[4 * j + 2] = fmaf(a, wv.z, acc_a[4 * j + 2]);
+                                acc_a[4 * j + 3] = fmaf(a, wv.w, acc_a[4 * j + 3]);
+                                acc_b[4 * j] = fmaf(b, wv.x, acc_b[4 * j]);
+                                acc_b[4 * j + 1] = fmaf(b, wv.y, acc_b[4 * j + 1]);
+                                acc_b[4 * j + 2] = fmaf(b, wv.z, acc_b[4 * j + 2]);
+                                acc_b[4 * j + 3] = fmaf(b, wv.w, acc_b[4 * j + 3]);
+                            }
+                            wrow += p.Kp;
+                        }
+                    }
+                }
+            }
+        }
+        // + bias, store
+        const int kn = min(kDcKc, p.K - kc);
+        if (p.nhwc) {
+            float *ya = p.y + (((int64_t)n * p.P + pa) * p.Q + q) * p.K + kc;
+            float *yb = ya + (int64_t)p.Q * p.K;
+            const bool vec = (p.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.y) & 15) == 0);
+#pragma unroll
+            for (int j = 0; j < kDcKc; j += 4) {
+                if (j >= kn) break;
+                float bj[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    bj[e] = (p.bias && j + e < kn) ? __ldg(p.bias + kc + j + e) : 0.f;
+                if (vec) {
+                    if (va) *reinterpret_cast<float4 *>(ya + j) =
+                        make_float4(acc_a[j] + bj[0], acc_a[j + 1] + bj[1], acc_a[j + 2] + bj[2], acc_a[j + 3] + bj[3]);
+                    if (vb) *reinterpret_cast<float4 *>(yb + j) =
+                        make_float4(acc_b[j] + bj[0], acc_b[j + 1] + bj[1], acc_b[j + 2] + bj[2], acc_b[j + 3] + bj[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (j + e < kn) {
+                            if (va) ya[j + e] = acc_a[j + e] + bj[e];
+                            if (vb) yb[j + e] = acc_b[j + e] + bj[e];
+                        }
+                    }
+                }
+            }
+        } else {
+            float *ya = p.y + ((int64_t)n * p.K + kc) * PQ + (int64_t)pa * p.Q + q;
+            float *yb = ya + p.Q;
+#pragma unroll
+            for (int j = 0; j < kDcKc; ++j) {
+                if (j < kn) {
+                    const float bj = p.bias ? __ldg(p.bias + kc + j) : 0.f;
+                    if (va) ya[(int64_t)j * PQ] = acc_a[j] + bj;
+                    if (vb) yb[(int64_t)j * PQ] = acc_b[j] + bj;
+                }
+            }
+        }
+    }
+}
+
+void patch_dims(const Shape &s, int *ih, int *iw) {
+    *ih = (kDcRows - 1) * s.stride + (s.R - 1) * s.dil + 1;
+    *iw = (kDcCols - 1) * s.stride + (s.S - 1) * s.dil + 1;
+}
+
+}  // namespace
+
+size_t dc_smem_bytes(const Shape &s) {
+    int ih, iw;
+    patch_dims(s, &ih, &iw);
+    const size_t patch = ((size_t)s.C * ih * iw + 3) & ~(size_t)3;
+    const size_t kp = ((size_t)s.K + kDcKc - 1) / kDcKc * kDcKc;
+    return (patch + (size_t)s.Kg * kp) * sizeof(float);
+}
+
+bool dc_shape_ok(const Shape &s) {
+    if (s.dtype != CONV2D_F32) return false;
+    if (s.Kg > 64 || s.stride > 4 || (int64_t)s.dil * (s.R - 1) > 64 || (int64_t)s.dil * (s.S - 1) > 64)
+        return false;
+    if ((int64_t)s.N * ((s.P + kDcRows - 1) / kDcRows) * ((s.Q + kDcCols - 1) / kDcCols) > INT32_MAX)
+        return false;
+    return dc_smem_bytes(s) <= 96 * 1024;
+}
+
+int dc_grid(const Shape &s) {
+    return (int)((int64_t)s.N * ((s.P + kDcRows - 1) / kDcRows) * ((s.Q + kDcCols - 1) / kDcCols));
+}
+
+conv2d_status_t dc_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    (void)pl;
+    DcParams p;
+    p.x = static_cast<const float *>(t.x);
+    p.w = static_cast<const float *>(t.w);
+    p.bias = static_cast<const float *>(t.bias);
+    p.y = static_cast<float *>(t.y);
+    p.N = s.N; p.C = s.C; p.H = s.H; p.W = s.W; p.K = s.K; p.R = s.R; p.S = s.S;
+    p.P = s.P; p.Q = s.Q;
+    p.stride = s.stride; p.pad = s.pad; p.dil = s.dil;
+    patch_dims(s, &p.IH, &p.IW);
+    p.Kp = (s.K + kDcKc - 1) / kDcKc * kDcKc;
+    p.tiles_p = (s.P + kDcRows - 1) / kDcRows;
+    p.tiles_q = (s.Q + kDcCols - 1) / kDcCols;
+    p.nhwc = s.layout == CONV2D_NHWC ? 1 : 0;
+    const size_t bytes = dc_smem_bytes(s);
+    void (*kern)(DcParams);
+    if (s.R == 3 && s.S == 3) kern = direct_conv_kernel<3, 3>;
+    else if (s.R == 2 && s.S == 2) kern = direct_conv_kernel<2, 2>;
+    else if (s.R == 1 && s.S == 1) kern = direct_conv_kernel<1, 1>;
+    else if (s.R == 5 && s.S == 5) kern = direct_conv_kernel<5, 5>;
+    else kern = direct_conv_kernel<0, 0>;
+    if (bytes > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024) != cudaSuccess)
+        return CONV2D_ERR_CUDA;
+    kern<<<dc_grid(s), kDcThreads, bytes, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
+}  // namespace conv2d

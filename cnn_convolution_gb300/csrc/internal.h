@@ -54,7 +54,7 @@ struct TfTile {
     int stage_ns;    // measured time of one 32-element stage of one tile (GB300)
 };
 
-enum class Algo { CudaCore, TensorCore, Tf32x3 };
+enum class Algo { CudaCore, TensorCore, Tf32x3, Direct };
 
 struct Plan {
     Algo algo;
@@ -96,6 +96,12 @@ int tc_window_variants();
 TcWinVariant tc_window_variant(int id);
 bool tc_window_variant_ok(const Shape &s, int id);
 conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
+
+// Direct fp32 kernel for short reductions (C*R*S <= 64), either layout.
+bool dc_shape_ok(const Shape &s);
+size_t dc_smem_bytes(const Shape &s);
+int dc_grid(const Shape &s);
+conv2d_status_t dc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
 
 // fp32 tensor-core path (3xTF32 split precision, NCHW or NHWC).
 bool tf_shape_ok(const Shape &s);

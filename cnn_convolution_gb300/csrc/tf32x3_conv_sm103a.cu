@@ -77,29 +77,6 @@ __device__ __forceinline__ uint32_t tf32_rn(float a) {
     return (__float_as_uint(a) + 0x1000u) & 0xFFFFE000u;
 }
 
-// Predicated read-only loads that leave 0 where the predicate is false.  The
-// register is zeroed and then conditionally loaded inside one asm statement,
-// so nothing consumes the loaded value before it is used: a C++ `p ? ld : 0`
-// becomes a select right after the load and stalls on every load in turn.
-__device__ __forceinline__ float ldg_or_zero(const float *ptr, bool pred) {
-    float v;
-    asm("{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %2, 0;\n\t"
-        "mov.b32 %0, 0;\n\t"
-        "@p ld.global.nc.f32 %0, [%1];\n\t}"
-        : "=f"(v)
-        : "l"(ptr), "r"((int)pred));
-    return v;
-}
-__device__ __forceinline__ void ldg4_or_zero(const float *ptr, bool pred, float (&v)[4]) {
-    asm("{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
-        "@p ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}"
-        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
-        : "l"(ptr), "r"((int)pred));
-}
-
 // Split four values into their TF32 high and low parts.
 __device__ __forceinline__ void split4(const float (&v)[4], uint32_t (&hi)[4], uint32_t (&lo)[4]) {
 #pragma unroll
