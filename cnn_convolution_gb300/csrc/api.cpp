@@ -130,13 +130,14 @@ double cc_cost(const Shape &s, const CudaCoreTile &t, int split, int sms) {
 }
 
 // Direct kernel (short reductions): FFMAs of whole 16 x 32 pixel blocks x
-// 32-channel blocks at about 20 TFLOP/s (measured on GB300 on the MSCRED
-// layer-1 shape), plus about 3 us of launch and staging.  In the units of
-// cc_cost().
+// 32-channel blocks at an effective 30 TFLOP/s, plus about 3 us of launch
+// and staging.  In the units of cc_cost(), whose tile rates overestimate
+// short reductions by a similar factor: on the MSCRED layer-1 shape on GB300
+// the direct kernel measures 26 us against 32 us for the best tile.
 double dc_cost(const Shape &s) {
     const double blocks = (double)s.N * ((s.P + 15) / 16) * ((s.Q + 31) / 32);
     const double fma = blocks * 512.0 * (double)((s.K + 31) / 32 * 32) * (double)s.Kg;
-    return (2.0 * fma / 20e3 + 3000.0) / 2e-3;
+    return (2.0 * fma / 30e3 + 3000.0) / 2e-3;
 }
 
 conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
