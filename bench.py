@@ -14,7 +14,8 @@ launches, with the L2 flush (a 256 MiB write) and the two timing events
 captured inside the same graph, so the events bracket only the 4 kernels:
 neither host-side validation nor the graph launch latency sits inside them.
 The JSON line also reports the eager (non-graph) step time, the host time of
-one C-ABI call, and an end-to-end time with host<->device copies.  Barrier + synchronize on both sides of the timed region;
+one C-ABI call, an end-to-end time with host<->device copies, and the step
+with the fp32 tensor-core (3xTF32) path switched off (CUDA-core FFMA only).  Barrier + synchronize on both sides of the timed region;
 the slowest rank's time is reported.  With --gpus N > 1 (torchrun) every rank
 runs an independent replica of the workload (the layer needs no exchange),
 so the total work grows with N ("weak" scaling).
@@ -387,6 +388,22 @@ def bench_main(args):
            "h2d_bytes_per_step": x_pin.numel() * 4, "d2h_bytes_per_step": y_pin.numel() * 4,
            "launch": "eager C-ABI calls from Python (host overhead included)"}
 
+    # the same step with the fp32 tensor-core (3xTF32) path switched off:
+    # every layer on CUDA-core FFMA kernels (direct / implicit GEMM)
+    os.environ["CONV2D_FP32_TC"] = "0"
+    try:
+        for _ in range(2):
+            run_encoder(descs, x_dev, ws, bs, outs)
+        torch.cuda.synchronize()
+        cc_graph = TimedGraph(lambda: run_encoder(descs, x_dev, ws, bs, outs), flush)
+        cc_plans = [d.plan() for d in descs]
+        cc_ms = [cc_graph.replay_ms() for _ in range(max(5, args.steps // 4))]
+    finally:
+        os.environ.pop("CONV2D_FP32_TC", None)
+    cc_t = max_over_ranks(statistics.mean(cc_ms), world)
+    fp32_cuda_core_only = {"value": round(step_flops * world / (cc_t * 1e-3) / 1e12, 4),
+                           "unit": "TFLOPS", "ms_per_step": round(cc_t, 5), "plans": cc_plans}
+
     extra = []
     if not args.no_tensor_core and rank == 0:
         extra = tensor_core_layers(device, peaks, flush, iters=max(5, args.steps // 4))
@@ -412,6 +429,7 @@ def bench_main(args):
             "eager_ms_per_step": round(statistics.mean(eager), 5),
             "host_us_per_call": round(host_us, 2),
             "e2e": e2e,
+            "fp32_cuda_core_only": fp32_cuda_core_only,
             "gpu_launches": n_layers * args.steps,
             "clocks": clocks,
             "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
