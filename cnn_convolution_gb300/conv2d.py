@@ -82,6 +82,9 @@ def _declare(lib):
     lib.conv2d_get_device_status.argtypes = []
     lib.conv2d_version.restype = c_int
     lib.conv2d_version.argtypes = []
+    lib.conv2d_signature_matrices.restype = c_int
+    lib.conv2d_signature_matrices.argtypes = [vp, i32, i32, ctypes.POINTER(i32), i32, i32, i32,
+                                              vp, vp]
 
 
 def _check(code: int, what: str):
@@ -198,6 +201,34 @@ def forward(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = Non
                               N, C, H, W, K, R, S, stride, pad, dil,
                               _DTYPE_CODE[x.dtype], _LAYOUT_CODE[layout], st), "conv2d_forward")
     return y
+
+
+def signature_matrices(series: torch.Tensor, windows, t_first: int, n_steps: int,
+                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """MSCRED signature matrices through conv2d_signature_matrices.
+
+    series: CUDA fp32 [n_signals, T]; returns fp32 [n_steps, len(windows),
+    n_signals, n_signals] with out[b, c] = the Gram matrix of the last
+    windows[c] samples before time t_first + b, divided by windows[c] (the
+    NCHW input of the encoder's first convolution).
+    """
+    lib = load()
+    if not isinstance(series, torch.Tensor) or not series.is_cuda or series.dtype != torch.float32:
+        raise ValueError("series must be a CUDA float32 tensor")
+    if series.dim() != 2 or not series.is_contiguous():
+        raise ValueError("series must be a contiguous [n_signals, T] tensor")
+    n, T = series.shape
+    wins = [int(w) for w in windows]
+    shape = (n_steps, len(wins), n, n)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=series.device)
+    elif tuple(out.shape) != shape or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous float32 tensor of shape {shape}")
+    warr = (ctypes.c_int * max(1, len(wins)))(*wins)
+    _check(lib.conv2d_signature_matrices(series.data_ptr(), n, T, warr, len(wins), t_first, n_steps,
+                                         out.data_ptr(), _stream_handle(stream, series.device)),
+           "conv2d_signature_matrices")
+    return out
 
 
 def get_device_status() -> int:

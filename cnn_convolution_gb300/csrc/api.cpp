@@ -572,6 +572,28 @@ conv2d_status_t conv2d_forward(const void *x, const void *w, const void *bias, v
     return run(s, CONV2D_ALGO_AUTO, Tensors{x, w, bias, y}, stream);
 }
 
+conv2d_status_t conv2d_signature_matrices(const float *series, int n_signals, int T,
+                                          const int *windows, int n_windows, int t_first,
+                                          int n_steps, float *out, cudaStream_t stream) {
+    if (!series || !out || !windows) return CONV2D_ERR_INVALID_ARG;
+    if (n_signals < 1 || n_signals > 128 || T < 1 || n_windows < 1 || n_windows > 8 || n_steps < 1)
+        return CONV2D_ERR_INVALID_ARG;
+    int wmax = 0;
+    for (int c = 0; c < n_windows; ++c) {
+        if (windows[c] < 1) return CONV2D_ERR_INVALID_ARG;
+        wmax = std::max(wmax, windows[c]);
+    }
+    if (wmax > t_first || (int64_t)t_first + n_steps - 1 > T) return CONV2D_ERR_INVALID_ARG;
+    if (((uintptr_t)series & 3) || ((uintptr_t)out & 3)) return CONV2D_ERR_MISALIGNED;
+    const size_t sb = (size_t)n_signals * T * sizeof(float);
+    const size_t ob = (size_t)n_steps * n_windows * n_signals * n_signals * sizeof(float);
+    if (overlaps(out, ob, series, sb)) return CONV2D_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (!is_device_ptr(series, dev) || !is_device_ptr(out, dev)) return CONV2D_ERR_INVALID_ARG;
+    return sig_launch(series, n_signals, T, windows, n_windows, t_first, n_steps, out, stream);
+}
+
 const char *conv2d_status_string(conv2d_status_t status) {
     switch (status) {
         case CONV2D_OK: return "ok";

@@ -110,6 +110,10 @@ TfTile tf_variant(int id);
 size_t tf_smem_bytes(const Shape &s, const TfTile &t);
 conv2d_status_t tf_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
 
+// MSCRED signature matrices (arguments validated by the caller).
+conv2d_status_t sig_launch(const float *series, int n, int T, const int *windows, int n_windows,
+                           int t_first, int n_steps, float *out, cudaStream_t st);
+
 // Device status word (bounded-wait failures).
 conv2d_status_t status_read_and_clear();
 unsigned int *status_word_ptr();   // device address, per current device

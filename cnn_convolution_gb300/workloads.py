@@ -86,6 +86,17 @@ def _finish(a: np.ndarray, spec: ConvSpec, kind: str) -> torch.Tensor:
     return t.contiguous()
 
 
+def random_walk_series(n_signals: int, length: int, seed: int) -> np.ndarray:
+    """Seeded random walks s_i(t) = cumulative sum of N(0,1) steps, fp64 [n_signals, length]."""
+    rng = np.random.default_rng(seed)
+    return np.cumsum(rng.standard_normal(size=(n_signals, length)), axis=1)
+
+
+def mscred_encoder_series(n: int = 256) -> torch.Tensor:
+    """The raw signals behind ``mscred_encoder_input(n)``: fp32 [30, 60 + n - 1]."""
+    return torch.from_numpy(random_walk_series(MSCRED_SIGNALS, 60 + n - 1, 1000).astype(np.float32))
+
+
 def signature_matrices(n_signals: int, length: int, windows: Tuple[int, ...],
                        end_times: List[int], seed: int) -> np.ndarray:
     """MSCRED-style signature matrices, fp64, shape [len(end_times), len(windows), n, n].
@@ -94,8 +105,7 @@ def signature_matrices(n_signals: int, length: int, windows: Tuple[int, ...],
     t = 0..length-1.  For an end time e and window w the matrix is
     M_ij = sum_{t=e-w}^{e-1} s_i(t) s_j(t) / w.
     """
-    rng = np.random.default_rng(seed)
-    sig = np.cumsum(rng.standard_normal(size=(n_signals, length)), axis=1)
+    sig = random_walk_series(n_signals, length, seed)
     out = np.empty((len(end_times), len(windows), n_signals, n_signals), dtype=np.float64)
     for b, e in enumerate(end_times):
         for c, win in enumerate(windows):

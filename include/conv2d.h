@@ -129,6 +129,32 @@ conv2d_status_t conv2d_forward(const void *x, const void *w, const void *bias, v
                                conv2d_dtype_t dtype, conv2d_layout_t layout,
                                cudaStream_t stream);
 
+/*
+ * MSCRED signature matrices, the input of the encoder's first convolution
+ * ("GPU-Accelerating MSCRED with CUDA, im2col, GEMM, and a Custom PyTorch
+ * Extension", section "Why Signature Matrices Are Useful": pairwise
+ * relationships of the signals over a time interval, at several interval
+ * lengths; the definition is the one of the MSCRED paper the page cites):
+ *
+ *   out[b][c][i][j] = sum_{t = e-w}^{e-1} series[i][t] * series[j][t] / w,
+ *   e = t_first + b, w = windows[c],
+ *
+ * for b < n_steps, c < n_windows, i, j < n_signals.  series: device fp32
+ * [n_signals][T] row-major; out: device fp32 [n_steps][n_windows][n_signals]
+ * [n_signals] (NCHW with C = n_windows), caller-owned, must not overlap
+ * series; windows: HOST array of n_windows lengths (any order, repeats
+ * allowed).  fp32 products accumulated with FMA, newest sample first, one
+ * division by w.  Asynchronous on stream; allocates nothing.
+ * CONV2D_ERR_INVALID_ARG unless 1 <= n_signals <= 128, T >= 1,
+ * 1 <= n_windows <= 8, every window >= 1, max window <= t_first,
+ * t_first + n_steps - 1 <= T, n_steps >= 1 and both pointers are device
+ * memory of the current device; CONV2D_ERR_MISALIGNED for pointers that are
+ * not 4-byte aligned; CONV2D_ERR_CUDA if the launch fails.
+ */
+conv2d_status_t conv2d_signature_matrices(const float *series, int n_signals, int T,
+                                          const int *windows, int n_windows, int t_first,
+                                          int n_steps, float *out, cudaStream_t stream);
+
 /* Static text for a status code. */
 const char *conv2d_status_string(conv2d_status_t status);
 
