@@ -68,6 +68,13 @@ def fp32_alu_peak_tflops():
     return SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
 
 
+# DRAM bytes (read + write) per launch of a layer's kernel, from one ncu
+# capture of the current kernel (profiles/ holds the summary and command);
+# keyed by (layer, kernel family as the plan string starts).
+DRAM_TRAFFIC = {
+    ("mscred_enc_l2_n256_c32_30x30_k64_3x3s2p1", "tensor_core tcgen05 3xtf32"): 29634048 + 256,
+}
+
 # nominal dense TF32 / BF16 tensor rates of GB300 (1.1 and 2.25 PFLOP/s)
 TF32_PER_BF16 = 1.1 / 2.25
 
@@ -361,9 +368,10 @@ def bench_main(args):
     dom_t = statistics.mean(layer_ms[dom])
     achieved = flops[dom] / (dom_t * 1e-3) / 1e12
     dom_bound, dom_peak, dom_src = layer_peak(descs[dom].plan(), peaks)
+    traffic = DRAM_TRAFFIC.get((specs[dom].name, descs[dom].plan().split(" BM=")[0]))
     roofline = {"kernel": specs[dom].name, "plan": descs[dom].plan(), "bound": dom_bound,
                 "achieved": round(achieved, 3), "peak": round(dom_peak, 2), "unit": "TFLOP/s",
-                "frac": round(achieved / dom_peak, 4), "traffic": None, "peak_source": dom_src}
+                "frac": round(achieved / dom_peak, 4), "traffic": traffic, "peak_source": dom_src}
 
     # end to end through the C ABI: pinned host x -> device, 4 layers, y -> pinned host
     x_pin = x_host.pin_memory()
@@ -404,6 +412,12 @@ def bench_main(args):
     fp32_cuda_core_only = {"value": round(step_flops * world / (cc_t * 1e-3) / 1e12, 4),
                            "unit": "TFLOPS", "ms_per_step": round(cc_t, 5), "plans": cc_plans}
 
+    # signature matrices on the GPU: the kernel alone (its roofline is the
+    # HBM traffic of series slice + output), and the encoder end to end from
+    # the raw signals (pinned host series -> signature kernel -> 4 layers ->
+    # pinned host y), which moves 38 KB to the device instead of 2.8 MB
+    sig = signature_stage(device, flush, descs, ws, bs, outs, peaks, args, world)
+
     extra = []
     if not args.no_tensor_core and rank == 0:
         extra = tensor_core_layers(device, peaks, flush, iters=max(5, args.steps // 4))
@@ -430,6 +444,7 @@ def bench_main(args):
             "host_us_per_call": round(host_us, 2),
             "e2e": e2e,
             "fp32_cuda_core_only": fp32_cuda_core_only,
+            "signature_matrices": sig,
             "gpu_launches": n_layers * args.steps,
             "clocks": clocks,
             "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
@@ -444,6 +459,57 @@ def bench_main(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def signature_stage(device, flush, descs, ws, bs, outs, peaks, args, world):
+    from cnn_convolution_gb300 import conv2d, workloads as wl
+    n = 256
+    windows = list(wl.MSCRED_WINDOWS)
+    series_host = wl.mscred_encoder_series(n)
+    series = series_host.to(device)
+    x_sig = torch.empty((n, len(windows), 30, 30), dtype=torch.float32, device=device)
+    for _ in range(3):
+        conv2d.signature_matrices(series, windows, 60, n, out=x_sig)
+    torch.cuda.synchronize()
+    tg = TimedGraph(lambda: conv2d.signature_matrices(series, windows, 60, n, out=x_sig), flush)
+    ts = [tg.replay_ms() for _ in range(max(10, args.steps // 4))]
+    t = statistics.median(ts)
+    # algorithmic bytes: the series samples the end times read, once, and the output
+    read = series_host.shape[0] * (60 + n - 1) * 4
+    written = x_sig.numel() * 4
+    gbs = (read + written) / (t * 1e-3) / 1e9
+    # end to end from the raw signals, through the C ABI
+    s_pin = series_host.pin_memory()
+    y_pin = torch.empty(outs[-1].shape, dtype=torch.float32).pin_memory()
+    s_buf = torch.empty_like(series)
+    e2e = []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        s_buf.copy_(s_pin, non_blocking=True)
+        conv2d.signature_matrices(s_buf, windows, 60, n, out=x_sig)
+        run_encoder(descs, x_sig, ws, bs, outs)
+        y_pin.copy_(outs[-1], non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if it >= args.warmup:
+            e2e.append(e0.elapsed_time(e1))
+    e2e_t = max_over_ranks(statistics.mean(e2e), world)
+    enc_flops = 0.0
+    for d in descs:
+        N, C, H, W, K, R, S, st, pad, dil = d.sizes
+        P, Q = d.output_dims()
+        enc_flops += 2.0 * N * K * P * Q * C * R * S
+    return {"us": round(t * 1e3, 3), "shape": [n, len(windows), 30, 30], "windows": windows,
+            "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+            "bound": "hbm", "algorithmic_bytes": read + written,
+            "e2e_from_series": {"value": round(enc_flops * world / (e2e_t * 1e-3) / 1e12, 4),
+                                "unit": "TFLOPS", "ms_per_step": round(e2e_t, 5),
+                                "h2d_bytes_per_step": s_pin.numel() * 4,
+                                "d2h_bytes_per_step": y_pin.numel() * 4,
+                                "note": "signature kernel + 4 layers, eager C-ABI calls"}}
 
 
 def time_layer(d, x, w, b, y, flush, iters, warm=3):
