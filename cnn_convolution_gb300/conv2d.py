@@ -82,6 +82,8 @@ def _declare(lib):
     lib.conv2d_get_device_status.argtypes = []
     lib.conv2d_version.restype = c_int
     lib.conv2d_version.argtypes = []
+    lib.conv2d_convlstm_cell.restype = c_int
+    lib.conv2d_convlstm_cell.argtypes = [vp] * 6 + [i32] * 9 + [ctypes.c_longlong, vp]
     lib.conv2d_signature_matrices.restype = c_int
     lib.conv2d_signature_matrices.argtypes = [vp, i32, i32, ctypes.POINTER(i32), i32, i32, i32,
                                               vp, vp]
@@ -229,6 +231,40 @@ def signature_matrices(series: torch.Tensor, windows, t_first: int, n_steps: int
                                          out.data_ptr(), _stream_handle(stream, series.device)),
            "conv2d_signature_matrices")
     return out
+
+
+def convlstm_cell(xh: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                  c_prev: torch.Tensor, pad: int, dil: int = 1,
+                  c_next: Optional[torch.Tensor] = None, h_next: Optional[torch.Tensor] = None,
+                  h_img_stride: Optional[int] = None, stream=None):
+    """One ConvLSTM cell step through conv2d_convlstm_cell (fp32, NCHW).
+
+    xh [N, Cx+Ch, H, W] = [x_t, h_{t-1}]; w [4Ch, Cx+Ch, R, S] with gates
+    (i, f, o, g); c_prev [N, Ch, H, W].  Returns (c_next, h_next).  h_next may
+    be a view into another buffer: pass its first element's tensor and
+    h_img_stride, the element distance between its images.
+    """
+    lib = load()
+    N, C, H, W = xh.shape
+    K, C2, R, S = w.shape
+    Ch = K // 4
+    if C2 != C or K % 4 or tuple(c_prev.shape) != (N, Ch, H, W):
+        raise ValueError("shapes of xh, w and c_prev disagree")
+    for name, t in (("xh", xh), ("w", w), ("c_prev", c_prev)) + ((("bias", bias),) if bias is not None else ()):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor")
+    if c_next is None:
+        c_next = torch.empty_like(c_prev)
+    if h_next is None:
+        h_next = torch.empty_like(c_prev)
+    if h_img_stride is None:
+        h_img_stride = Ch * H * W
+    _check(lib.conv2d_convlstm_cell(xh.data_ptr(), w.data_ptr(),
+                                    None if bias is None else bias.data_ptr(), c_prev.data_ptr(),
+                                    c_next.data_ptr(), h_next.data_ptr(), N, C - Ch, Ch, H, W, R, S,
+                                    pad, dil, int(h_img_stride), _stream_handle(stream, xh.device)),
+           "conv2d_convlstm_cell")
+    return c_next, h_next
 
 
 def get_device_status() -> int:

@@ -308,7 +308,8 @@ double tf_cost_ns(const Shape &s, const TfTile &t, int sms) {
     return 2000.0 + (double)rounds * ((double)kt * t.stage_ns + 2000.0);
 }
 
-conv2d_status_t choose_tf(const Shape &s, const DevInfo &d, Plan *p, double *cost_ns) {
+conv2d_status_t choose_tf(const Shape &s, const DevInfo &d, Plan *p, double *cost_ns,
+                          bool lstm = false) {
     if (!(d.cc_major == 10 && d.cc_minor == 3) || !tf_shape_ok(s)) return CONV2D_ERR_UNSUPPORTED;
     const int forced = env_int("CONV2D_TF_VAR");
     double best = 1e300;
@@ -316,6 +317,7 @@ conv2d_status_t choose_tf(const Shape &s, const DevInfo &d, Plan *p, double *cos
     for (int id = 0; id < tf_num_variants(); ++id) {
         if (forced >= 0 && id != forced) continue;
         const TfTile t = tf_variant(id);
+        if (lstm && !tf_lstm_variant(id)) continue;
         if (tf_smem_bytes(s, t) > d.smem_optin) continue;
         // a tile much wider than K wastes tensor-core work
         if (forced < 0 && t.BN > 32 && s.K <= t.BN / 2) continue;
@@ -592,6 +594,45 @@ conv2d_status_t conv2d_signature_matrices(const float *series, int n_signals, in
     if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
     if (!is_device_ptr(series, dev) || !is_device_ptr(out, dev)) return CONV2D_ERR_INVALID_ARG;
     return sig_launch(series, n_signals, T, windows, n_windows, t_first, n_steps, out, stream);
+}
+
+conv2d_status_t conv2d_convlstm_cell(const float *xh, const float *w, const float *bias,
+                                     const float *c_prev, float *c_next, float *h_next,
+                                     int N, int Cx, int Ch, int H, int W, int R, int S, int pad,
+                                     int dil, long long h_img_stride, cudaStream_t stream) {
+    if (Cx < 0 || Ch < 1) return CONV2D_ERR_INVALID_ARG;
+    Shape s;
+    conv2d_status_t st = make_shape(&s, N, Cx + Ch, H, W, 4 * Ch, R, S, 1, pad, dil, CONV2D_F32,
+                                    CONV2D_NCHW);
+    if (st != CONV2D_OK) return st;
+    if (s.P != H || s.Q != W) return CONV2D_ERR_INVALID_ARG;            // the state keeps H x W
+    const int64_t plane = (int64_t)Ch * H * W;
+    if (h_img_stride < plane) return CONV2D_ERR_INVALID_ARG;
+    if (!xh || !w || !c_prev || !c_next || !h_next) return CONV2D_ERR_INVALID_ARG;
+    const uintptr_t m4 = 3;
+    if (((uintptr_t)xh & m4) || ((uintptr_t)w & m4) || ((uintptr_t)c_prev & m4) ||
+        ((uintptr_t)c_next & m4) || ((uintptr_t)h_next & m4) || (bias && ((uintptr_t)bias & m4)))
+        return CONV2D_ERR_MISALIGNED;
+    // outputs must not overlap the inputs they are computed from
+    const size_t xb = (size_t)s.x_elems() * 4, wb = (size_t)s.w_elems() * 4, cb = (size_t)N * plane * 4;
+    const size_t hb = ((size_t)(N - 1) * (size_t)h_img_stride + (size_t)plane) * 4;
+    if (overlaps(c_next, cb, xh, xb) || overlaps(c_next, cb, w, wb) || overlaps(c_next, cb, c_prev, cb) ||
+        overlaps(h_next, hb, xh, xb) || overlaps(h_next, hb, w, wb) || overlaps(h_next, hb, c_prev, cb) ||
+        overlaps(h_next, hb, c_next, cb) ||
+        (bias && (overlaps(c_next, cb, bias, (size_t)s.K * 4) || overlaps(h_next, hb, bias, (size_t)s.K * 4))))
+        return CONV2D_ERR_INVALID_ARG;
+    int dev = 0;
+    DevInfo d;
+    st = device_info(&dev, &d);
+    if (st != CONV2D_OK) return st;
+    if (!is_device_ptr(xh, dev) || !is_device_ptr(w, dev) || !is_device_ptr(c_prev, dev) ||
+        !is_device_ptr(c_next, dev) || !is_device_ptr(h_next, dev) || (bias && !is_device_ptr(bias, dev)))
+        return CONV2D_ERR_INVALID_ARG;
+    Plan p{};
+    st = choose_tf(s, d, &p, nullptr, true);
+    if (st != CONV2D_OK) return st;
+    const TfLstm lstm{c_prev, c_next, h_next, (int64_t)h_img_stride};
+    return tf_launch(s, p, Tensors{xh, w, bias, nullptr}, stream, &lstm);
 }
 
 const char *conv2d_status_string(conv2d_status_t status) {

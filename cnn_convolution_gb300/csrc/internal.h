@@ -108,7 +108,16 @@ bool tf_shape_ok(const Shape &s);
 int tf_num_variants();
 TfTile tf_variant(int id);
 size_t tf_smem_bytes(const Shape &s, const TfTile &t);
-conv2d_status_t tf_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
+// ConvLSTM-cell epilogue arguments of the 3xTF32 kernel (fp32, NCHW).
+struct TfLstm {
+    const float *c_prev;
+    float *c_next;
+    float *h_next;
+    int64_t h_img;      // elements between images of h_next
+};
+bool tf_lstm_variant(int id);
+conv2d_status_t tf_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st,
+                          const TfLstm *lstm = nullptr);
 
 // MSCRED signature matrices (arguments validated by the caller).
 conv2d_status_t sig_launch(const float *series, int n, int T, const int *windows, int n_windows,

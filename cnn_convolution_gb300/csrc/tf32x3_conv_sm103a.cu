@@ -126,7 +126,18 @@ struct TfParams {
     int R;
     int w_vec;          // Kg % 4 == 0 and w 16-byte aligned: weight rows load as float4
     int y_vec;          // NHWC, K % 4 == 0 and y 16-byte aligned: outputs store as float4
+    // ConvLSTM cell epilogue (LSTM instantiations only): K = 4*Ch gate columns,
+    // read from gate-major weight rows in interleaved order (column 4u+gate is
+    // weight row gate*Ch + u), so that each group of 4 columns holds the
+    // i, f, o, g pre-activations of hidden unit u
+    int lstm_ch;
+    const float *c_prev;   // [N][Ch][P][Q]
+    float *c_next;         // [N][Ch][P][Q]
+    float *h_next;         // image n at h_next + n * h_img, [Ch][P][Q] inside
+    int64_t h_img;
 };
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
 
 // Tensor memory: columns [0, 2 BN) hold the correction accumulators (x_hi*w_lo
 // + x_lo*w_hi) of two tiles in flight; NSLOT slots of BN columns after them
@@ -164,7 +175,7 @@ template <int BN, int NPROD> constexpr int tf_threads() { return 32 * (tf_epi_wa
 // tensor memory over one stage only (4 MMAs of K=8) and the stage sums are
 // added in fp32 registers by the epilogue warps; the correction terms, 2^-11
 // smaller, stay in one accumulator per tile.
-template <int BN, int STAGES, int NPROD>
+template <int BN, int STAGES, int NPROD, bool LSTM>
 __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel(const TfParams p) {
     using L = TfSmem<BN, STAGES>;
     using TM = TfTmem<BN>;
@@ -357,7 +368,8 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 const int i = pt + it * kProd;
                 const int k = k0 + (i >> 3);
                 const int g = ks * kTfBK + (i & 7) * 4;
-                const float *wr = p.w + (int64_t)k * p.Kg + g;
+                const int wrow = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
+                const float *wr = p.w + (int64_t)wrow * p.Kg + g;
                 if (p.w_vec) {
                     ldg4_or_zero(wr, k < p.K && g < p.Kg, vb[it]);
                 } else {
@@ -519,7 +531,27 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             const int64_t m = (int64_t)tm * kTfBM + row;
             if (m >= p.M) continue;
             const int kb = tn * BN + col0;
-            if (p.nhwc) {
+            if (LSTM) {
+                // gates -> state update: c = f*c_prev + i*g, h = o*tanh(c)
+                const int64_t n = m / p.PQ;
+                const int64_t pq = m - n * p.PQ;
+                const int Ch = p.lstm_ch;
+#pragma unroll
+                for (int j = 0; j < kCpt; j += 4) {
+                    const int u = (kb + j) >> 2;
+                    if (u >= Ch) break;
+                    float z[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        z[e] = a[j + e] + (p.bias ? __ldg(p.bias + e * Ch + u) : 0.f);
+                    const float ig = sigmoidf_(z[0]), fg = sigmoidf_(z[1]), og = sigmoidf_(z[2]);
+                    const float gg = tanhf(z[3]);
+                    const int64_t ci = (n * Ch + u) * p.PQ + pq;
+                    const float c = fg * __ldg(p.c_prev + ci) + ig * gg;
+                    p.c_next[ci] = c;
+                    p.h_next[n * p.h_img + (int64_t)u * p.PQ + pq] = og * tanhf(c);
+                }
+            } else if (p.nhwc) {
                 float *yr = p.y + m * p.K;
                 if (p.y_vec) {
 #pragma unroll
@@ -574,8 +606,9 @@ bool ensure_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &done_mas
     return true;
 }
 
-template <int BN, int STAGES, int NPROD>
-conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+template <int BN, int STAGES, int NPROD, bool LSTM>
+conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
+                          cudaStream_t st) {
     using L = TfSmem<BN, STAGES>;
     TfParams p;
     p.x = static_cast<const float *>(t.x);
@@ -605,10 +638,23 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.nhwc = s.layout == CONV2D_NHWC ? 1 : 0;
     p.R = s.R;
     p.rs_mask = s.R * s.S <= 63 ? 1 : 0;
+    p.lstm_ch = 0;
+    p.c_prev = nullptr;
+    p.c_next = nullptr;
+    p.h_next = nullptr;
+    p.h_img = 0;
+    if (LSTM) {
+        if (!lstm || s.layout != CONV2D_NCHW || s.K % 4) return CONV2D_ERR_INTERNAL;
+        p.lstm_ch = s.K / 4;
+        p.c_prev = lstm->c_prev;
+        p.c_next = lstm->c_next;
+        p.h_next = lstm->h_next;
+        p.h_img = lstm->h_img;
+    }
     p.w_vec = (s.Kg % 4 == 0 && ((uintptr_t)t.w & 15) == 0) ? 1 : 0;
     p.y_vec = (p.nhwc && s.K % 4 == 0 && ((uintptr_t)t.y & 15) == 0) ? 1 : 0;
     const size_t bytes = L::bytes(p.KT);
-    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD>;
+    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD, LSTM>;
     static std::atomic<uint64_t> attr_done{0};   // this instantiation's per-device flags
     // the attribute is set for the largest table this variant accepts
     if (!ensure_attr(reinterpret_cast<const void *>(kern), 227 * 1024, attr_done)) return CONV2D_ERR_CUDA;
@@ -616,6 +662,14 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cuda
     const int grid = pl.grid > 0 ? pl.grid : 1;
     kern<<<grid, tf_threads<BN, NPROD>(), bytes, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
+// Only variants with 8 or more producer warps carry the ConvLSTM epilogue.
+template <int BN, int STAGES, int NPROD>
+conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
+                               cudaStream_t st) {
+    if constexpr (NPROD >= 8) return launch_tf<BN, STAGES, NPROD, true>(s, pl, t, lstm, st);
+    return CONV2D_ERR_UNSUPPORTED;
 }
 
 // (BN, STAGES, producer warps, measured ns per stage of one tile) of every
@@ -632,6 +686,9 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cuda
     X(64, 4, 16, 1030)
 
 }  // namespace
+
+// Variants compiled with the ConvLSTM-cell epilogue: 8 and 16 producer warps.
+bool tf_lstm_variant(int id) { return tf_variant(id).nprod >= 8; }
 
 int tf_num_variants() {
     int n = 0;
@@ -685,9 +742,18 @@ extern "C" int conv2d_tf_trace_dump(unsigned long long *out, unsigned int *count
 }
 #endif
 
-conv2d_status_t tf_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+conv2d_status_t tf_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st,
+                          const TfLstm *lstm) {
+    if (lstm) {
+#define X(vbn, vst, vnp, vns)                                            \
+    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp)     \
+        return launch_tf_lstm<vbn, vst, vnp>(s, pl, t, lstm, st);
+        CONV2D_TF_VARIANTS(X)
+#undef X
+        return CONV2D_ERR_INTERNAL;
+    }
 #define X(vbn, vst, vnp, vns) \
-    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp) return launch_tf<vbn, vst, vnp>(s, pl, t, st);
+    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp) return launch_tf<vbn, vst, vnp, false>(s, pl, t, nullptr, st);
     CONV2D_TF_VARIANTS(X)
 #undef X
     return CONV2D_ERR_INTERNAL;

@@ -155,6 +155,33 @@ conv2d_status_t conv2d_signature_matrices(const float *series, int n_signals, in
                                           const int *windows, int n_windows, int t_first,
                                           int n_steps, float *out, cudaStream_t stream);
 
+/*
+ * One ConvLSTM cell step with the gate non-linearities and the state update
+ * fused into the gate convolution's epilogue (ConvLSTM as "GPU-Accelerating
+ * MSCRED with CUDA, im2col, GEMM, and a Custom PyTorch Extension" uses it,
+ * section "Understanding MSCRED", the cell of the ConvLSTM paper its
+ * References cite, without peephole terms):
+ *
+ *   z = conv2d(xh, w) + bias          stride 1, padding pad, dilation dil
+ *   i, f, o = sigmoid(z[0:Ch]), sigmoid(z[Ch:2Ch]), sigmoid(z[2Ch:3Ch]); g = tanh(z[3Ch:4Ch])
+ *   c_next = f * c_prev + i * g;      h_next = o * tanh(c_next)
+ *
+ * fp32, NCHW.  xh: [N][Cx+Ch][H][W], the step input x_t (channels 0..Cx-1)
+ * followed by h_{t-1}; w: [4*Ch][Cx+Ch][R][S], gate-major (i, f, o, g);
+ * bias: [4*Ch] or NULL; c_prev, c_next: [N][Ch][H][W]; h_next: image n starts
+ * at h_next + n*h_img_stride and holds [Ch][H][W] (h_img_stride =
+ * (Cx+Ch)*H*W with h_next = the h slice of the next step's xh buffer writes
+ * h_t where the next step reads it).  The padding must keep H x W.  Runs on
+ * the 3xTF32 tensor-core kernel (the gate convolution meets the fp32 bound);
+ * the gates never reach memory.  All pointers device memory of the current
+ * device, 4-byte aligned; outputs must not overlap the inputs.  Errors as
+ * for conv2d_forward; CONV2D_ERR_UNSUPPORTED if no kernel variant fits.
+ */
+conv2d_status_t conv2d_convlstm_cell(const float *xh, const float *w, const float *bias,
+                                     const float *c_prev, float *c_next, float *h_next,
+                                     int N, int Cx, int Ch, int H, int W, int R, int S, int pad,
+                                     int dil, long long h_img_stride, cudaStream_t stream);
+
 /* Static text for a status code. */
 const char *conv2d_status_string(conv2d_status_t status);
 
