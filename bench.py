@@ -418,6 +418,8 @@ def bench_main(args):
     # pinned host y), which moves 38 KB to the device instead of 2.8 MB
     sig = signature_stage(device, flush, descs, ws, bs, outs, peaks, args, world)
 
+    cells = convlstm_cells(device, flush, peaks, iters=max(5, args.steps // 4)) if rank == 0 else []
+
     extra = []
     if not args.no_tensor_core and rank == 0:
         extra = tensor_core_layers(device, peaks, flush, iters=max(5, args.steps // 4))
@@ -445,6 +447,7 @@ def bench_main(args):
             "e2e": e2e,
             "fp32_cuda_core_only": fp32_cuda_core_only,
             "signature_matrices": sig,
+            "convlstm_cells": cells,
             "gpu_launches": n_layers * args.steps,
             "clocks": clocks,
             "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
@@ -510,6 +513,32 @@ def signature_stage(device, flush, descs, ws, bs, outs, peaks, args, world):
                                 "h2d_bytes_per_step": s_pin.numel() * 4,
                                 "d2h_bytes_per_step": y_pin.numel() * 4,
                                 "note": "signature kernel + 4 layers, eager C-ABI calls"}}
+
+
+def convlstm_cells(device, flush, peaks, iters, n=64):
+    """One fused ConvLSTM cell step per MSCRED scale (Cx = Ch = the encoder
+    layer's channels, 3x3 gates, batch n), timed alone after an L2 flush.
+    FLOPs = those of the gate convolution (2*N*4Ch*H*W*(Cx+Ch)*9)."""
+    from cnn_convolution_gb300 import conv2d, workloads as wl
+    out = []
+    peak = fp32_3xtf32_peak_tflops(peaks)
+    for ch, hw in ((32, 30), (64, 15), (128, 8), (256, 4)):
+        spec = wl.ConvSpec(f"convlstm_cell_n{n}_c{ch}_{hw}x{hw}_3x3", n, 2 * ch, hw, hw, 4 * ch, 3, 3, 1, 1)
+        xh, w, b = wl.random_inputs(spec, seed=ch)
+        xh, w, b = xh.to(device), w.to(device), b.to(device)
+        c0 = torch.zeros(n, ch, hw, hw, device=device)
+        c1, h1 = torch.empty_like(c0), torch.empty_like(c0)
+        for _ in range(3):
+            conv2d.convlstm_cell(xh, w, b, c0, 1, c_next=c1, h_next=h1)
+        torch.cuda.synchronize()
+        tg = TimedGraph(lambda: conv2d.convlstm_cell(xh, w, b, c0, 1, c_next=c1, h_next=h1), flush)
+        ts = [tg.replay_ms() for _ in range(iters)]
+        t = statistics.median(ts)
+        fl = 2.0 * n * 4 * ch * hw * hw * 2 * ch * 9
+        tf = fl / (t * 1e-3) / 1e12
+        out.append({"cell": spec.name, "us": round(t * 1e3, 2), "tflops": round(tf, 2),
+                    "bound": "tensor", "peak": round(peak, 1), "frac": round(tf / peak, 4)})
+    return out
 
 
 def time_layer(d, x, w, b, y, flush, iters, warm=3):
