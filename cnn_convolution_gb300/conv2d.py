@@ -82,6 +82,10 @@ def _declare(lib):
     lib.conv2d_get_device_status.argtypes = []
     lib.conv2d_version.restype = c_int
     lib.conv2d_version.argtypes = []
+    lib.conv2d_deconv_output_dims.restype = c_int
+    lib.conv2d_deconv_output_dims.argtypes = [i32] * 8 + [ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.conv2d_deconv_forward.restype = c_int
+    lib.conv2d_deconv_forward.argtypes = [vp] * 4 + [i32] * 11 + [c_int, c_int, vp]
     lib.conv2d_convlstm_cell.restype = c_int
     lib.conv2d_convlstm_cell.argtypes = [vp] * 6 + [i32] * 9 + [ctypes.c_longlong, vp]
     lib.conv2d_signature_matrices.restype = c_int
@@ -265,6 +269,37 @@ def convlstm_cell(xh: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor
                                     pad, dil, int(h_img_stride), _stream_handle(stream, xh.device)),
            "conv2d_convlstm_cell")
     return c_next, h_next
+
+
+def deconv_output_dims(P, Q, R, S, stride=1, pad=0, dil=1, out_pad=0) -> Tuple[int, int]:
+    lib = load()
+    H, W = ctypes.c_int(), ctypes.c_int()
+    _check(lib.conv2d_deconv_output_dims(P, Q, R, S, stride, pad, dil, out_pad,
+                                         ctypes.byref(H), ctypes.byref(W)), "conv2d_deconv_output_dims")
+    return H.value, W.value
+
+
+def deconv_forward(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                   stride: int = 1, pad: int = 0, dil: int = 1, out_pad: int = 0,
+                   y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Transposed convolution through conv2d_deconv_forward (fp32 NCHW).
+
+    x [N, K, P, Q], w [K, C, R, S] -> y [N, C, H, W]."""
+    lib = load()
+    N, K, P, Q = x.shape
+    K2, C, R, S = w.shape
+    if K2 != K:
+        raise ValueError("x and w disagree on K")
+    H, W = deconv_output_dims(P, Q, R, S, stride, pad, dil, out_pad)
+    if y is None:
+        y = torch.empty((N, C, H, W), dtype=x.dtype, device=x.device)
+    _validate(x, w, bias, y, x.dtype)
+    _check(lib.conv2d_deconv_forward(x.data_ptr(), w.data_ptr(),
+                                     None if bias is None else bias.data_ptr(), y.data_ptr(),
+                                     N, K, P, Q, C, R, S, stride, pad, dil, out_pad,
+                                     _DTYPE_CODE[x.dtype], _LAYOUT_CODE["NCHW"],
+                                     _stream_handle(stream, x.device)), "conv2d_deconv_forward")
+    return y
 
 
 def get_device_status() -> int:

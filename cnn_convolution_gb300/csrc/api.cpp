@@ -574,6 +574,48 @@ conv2d_status_t conv2d_forward(const void *x, const void *w, const void *bias, v
     return run(s, CONV2D_ALGO_AUTO, Tensors{x, w, bias, y}, stream);
 }
 
+conv2d_status_t conv2d_deconv_output_dims(int P, int Q, int R, int S, int stride, int pad, int dil,
+                                          int out_pad, int *H, int *W) {
+    if (!H || !W || P < 1 || Q < 1 || R < 1 || S < 1 || stride < 1 || dil < 1 || pad < 0 ||
+        out_pad < 0 || out_pad >= std::max(stride, dil))
+        return CONV2D_ERR_INVALID_ARG;
+    const int64_t h = (int64_t)(P - 1) * stride - 2 * (int64_t)pad + (int64_t)dil * (R - 1) + 1 + out_pad;
+    const int64_t w = (int64_t)(Q - 1) * stride - 2 * (int64_t)pad + (int64_t)dil * (S - 1) + 1 + out_pad;
+    if (h < 1 || w < 1 || h > INT32_MAX || w > INT32_MAX) return CONV2D_ERR_INVALID_ARG;
+    *H = (int)h;
+    *W = (int)w;
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_deconv_forward(const void *x, const void *w, const void *bias, void *y,
+                                      int N, int K, int P, int Q, int C, int R, int S, int stride,
+                                      int pad, int dil, int out_pad, conv2d_dtype_t dtype,
+                                      conv2d_layout_t layout, cudaStream_t stream) {
+    int H = 0, W = 0;
+    if (N < 1 || K < 1 || C < 1) return CONV2D_ERR_INVALID_ARG;
+    conv2d_status_t st = conv2d_deconv_output_dims(P, Q, R, S, stride, pad, dil, out_pad, &H, &W);
+    if (st != CONV2D_OK) return st;
+    if (dtype != CONV2D_F32 && dtype != CONV2D_F16 && dtype != CONV2D_BF16) return CONV2D_ERR_INVALID_ARG;
+    if (layout != CONV2D_NCHW && layout != CONV2D_NHWC) return CONV2D_ERR_INVALID_ARG;
+    if (dtype != CONV2D_F32 || layout != CONV2D_NCHW) return CONV2D_ERR_UNSUPPORTED;
+    const int64_t xe = (int64_t)N * K * P * Q, we = (int64_t)K * C * R * S, ye = (int64_t)N * C * H * W;
+    if (xe >= kMaxElems || we >= kMaxElems || ye >= kMaxElems) return CONV2D_ERR_INVALID_ARG;
+    if (!x || !w || !y) return CONV2D_ERR_INVALID_ARG;
+    if (((uintptr_t)x & 3) || ((uintptr_t)w & 3) || ((uintptr_t)y & 3) || (bias && ((uintptr_t)bias & 3)))
+        return CONV2D_ERR_MISALIGNED;
+    if (overlaps(y, (size_t)ye * 4, x, (size_t)xe * 4) || overlaps(y, (size_t)ye * 4, w, (size_t)we * 4) ||
+        (bias && overlaps(y, (size_t)ye * 4, bias, (size_t)C * 4)))
+        return CONV2D_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (!is_device_ptr(x, dev) || !is_device_ptr(w, dev) || !is_device_ptr(y, dev) ||
+        (bias && !is_device_ptr(bias, dev)))
+        return CONV2D_ERR_INVALID_ARG;
+    return dv_launch(static_cast<const float *>(x), static_cast<const float *>(w),
+                     static_cast<const float *>(bias), static_cast<float *>(y), N, K, P, Q, C, R, S,
+                     H, W, stride, pad, dil, stream);
+}
+
 conv2d_status_t conv2d_signature_matrices(const float *series, int n_signals, int T,
                                           const int *windows, int n_windows, int t_first,
                                           int n_steps, float *out, cudaStream_t stream) {

@@ -119,6 +119,12 @@ bool tf_lstm_variant(int id);
 conv2d_status_t tf_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st,
                           const TfLstm *lstm = nullptr);
 
+// Transposed convolution, fp32 NCHW (arguments validated by the caller).
+size_t dv_smem_bytes(int stride, int dil, int R, int S);
+conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, float *y, int N, int K,
+                          int P, int Q, int C, int R, int S, int H, int W, int stride, int pad,
+                          int dil, cudaStream_t st);
+
 // MSCRED signature matrices (arguments validated by the caller).
 conv2d_status_t sig_launch(const float *series, int n, int T, const int *windows, int n_windows,
                            int t_first, int n_steps, float *out, cudaStream_t st);

@@ -182,6 +182,35 @@ conv2d_status_t conv2d_convlstm_cell(const float *xh, const float *w, const floa
                                      int N, int Cx, int Ch, int H, int W, int R, int S, int pad,
                                      int dil, long long h_img_stride, cudaStream_t stream);
 
+/*
+ * Output size of the transposed convolution: H = (P-1)*stride - 2*pad +
+ * dil*(R-1) + 1 + out_pad, W likewise from Q and S.  out_pad in
+ * [0, max(stride, dil)) picks among the sizes whose forward convolution gives
+ * P x Q.  CONV2D_ERR_INVALID_ARG if anything is out of range or H, W < 1.
+ */
+conv2d_status_t conv2d_deconv_output_dims(int P, int Q, int R, int S, int stride, int pad, int dil,
+                                          int out_pad, int *H, int *W);
+
+/*
+ * Transposed convolution forward ("deconvolution"), the MSCRED decoder's
+ * up-sampling layer ("GPU-Accelerating MSCRED with CUDA, im2col, GEMM, and a
+ * Custom PyTorch Extension", section "Understanding MSCRED": the decoder
+ * reconstructs the signature matrices): the adjoint of conv2d_forward in its
+ * input,
+ *   y[n,c,h,w] = bias[c] + sum_{k,p,q,r,s : h = p*stride-pad+r*dil,
+ *                w = q*stride-pad+s*dil} x[n,k,p,q] * w[k,c,r,s].
+ * x: [N][K][P][Q]; w: [K][C][R][S] (the forward convolution's weights);
+ * bias: [C] or NULL; y: [N][C][H][W] (conv2d_deconv_output_dims).  fp32 NCHW
+ * (CONV2D_ERR_UNSUPPORTED for other dtypes / layouts), R, S <= 8.  A gather,
+ * deterministic, no atomics, no workspace.  Pointers: device memory of the
+ * current device, 4-byte aligned; y must not overlap x, w or bias.
+ * Asynchronous on stream.  Errors as for conv2d_forward.
+ */
+conv2d_status_t conv2d_deconv_forward(const void *x, const void *w, const void *bias, void *y,
+                                      int N, int K, int P, int Q, int C, int R, int S, int stride,
+                                      int pad, int dil, int out_pad, conv2d_dtype_t dtype,
+                                      conv2d_layout_t layout, cudaStream_t stream);
+
 /* Static text for a status code. */
 const char *conv2d_status_string(conv2d_status_t status);
 
