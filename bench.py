@@ -419,6 +419,7 @@ def bench_main(args):
     sig = signature_stage(device, flush, descs, ws, bs, outs, peaks, args, world)
 
     cells = convlstm_cells(device, flush, peaks, iters=max(5, args.steps // 4)) if rank == 0 else []
+    decoder = decoder_layers(device, flush, iters=max(5, args.steps // 4)) if rank == 0 else []
 
     extra = []
     if not args.no_tensor_core and rank == 0:
@@ -448,6 +449,7 @@ def bench_main(args):
             "fp32_cuda_core_only": fp32_cuda_core_only,
             "signature_matrices": sig,
             "convlstm_cells": cells,
+            "decoder_deconv_layers": decoder,
             "gpu_launches": n_layers * args.steps,
             "clocks": clocks,
             "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
@@ -538,6 +540,39 @@ def convlstm_cells(device, flush, peaks, iters, n=64):
         tf = fl / (t * 1e-3) / 1e12
         out.append({"cell": spec.name, "us": round(t * 1e3, 2), "tflops": round(tf, 2),
                     "bound": "tensor", "peak": round(peak, 1), "frac": round(tf / peak, 4)})
+    return out
+
+
+def decoder_layers(device, flush, iters, n=256):
+    """The MSCRED decoder's transposed convolutions (fp32 NCHW, batch n), each
+    timed alone after an L2 flush.  FLOPs count the products that land inside
+    the output: 2 * N * K * C * (valid (p, r) pairs) * (valid (q, s) pairs)."""
+    from cnn_convolution_gb300 import conv2d
+    shapes = [("deconv4_256to128_4to8_2x2s2", 256, 4, 128, 2, 2, 0, 0),
+              ("deconv3_256to64_8to15_3x3s2", 256, 8, 64, 3, 2, 1, 0),
+              ("deconv2_128to32_15to30_3x3s2", 128, 15, 32, 3, 2, 1, 1),
+              ("deconv1_64to3_30to30_3x3s1", 64, 30, 3, 3, 1, 1, 0)]
+    out = []
+    alu = fp32_alu_peak_tflops()
+    g = torch.Generator().manual_seed(7)
+    for name, K, P, C, R, st, pad, op in shapes:
+        x = torch.randn((n, K, P, P), generator=g).to(device)
+        w = (torch.randn((K, C, R, R), generator=g) / math.sqrt(K * R * R)).to(device)
+        b = torch.zeros(C).to(device)
+        H, W = conv2d.deconv_output_dims(P, P, R, R, st, pad, 1, op)
+        y = torch.empty((n, C, H, W), device=device)
+        for _ in range(3):
+            conv2d.deconv_forward(x, w, b, st, pad, 1, op, y=y)
+        torch.cuda.synchronize()
+        tg = TimedGraph(lambda: conv2d.deconv_forward(x, w, b, st, pad, 1, op, y=y), flush)
+        t = statistics.median([tg.replay_ms() for _ in range(iters)])
+        valid = sum(1 for p in range(P) for r in range(R) if 0 <= p * st - pad + r < H)
+        fl = 2.0 * n * K * C * valid * valid
+        by = 4.0 * (x.numel() + w.numel() + C + y.numel())
+        tf = fl / (t * 1e-3) / 1e12
+        gbs = by / (t * 1e-3) / 1e9
+        out.append({"layer": name, "us": round(t * 1e3, 2), "tflops": round(tf, 2),
+                    "alu_frac": round(tf / alu, 4), "hbm_gbs": round(gbs, 1)})
     return out
 
 
