@@ -14,14 +14,16 @@
 // pixel takes tap r exactly when (h + pad - r*dil) is a multiple of the
 // stride and p = (h + pad - r*dil) / stride lies in [0, P).
 //
-// A CTA of 256 threads owns an 8 x 32 block of output pixels of one image
-// (warp = row, lane = column) and 32 output channels (registers).  For each
-// chunk of 8 input channels it stages the input footprint of the block
-// (zero outside x) and the chunk's weights as [k][r][s][32 channels] in
-// shared memory.  A warp's row decides its valid filter rows uniformly; each
-// lane keeps a bitmask of its valid filter columns.  Per valid tap: one
-// input read, 8 broadcast 16-byte weight reads, 32 FFMAs.
+// A CTA of 256 threads owns 256 output pixels -- whole images when an image
+// has at most 256 outputs, else 256 consecutive pixels of one image -- and
+// 32 output channels (registers); thread = pixel.  For each chunk of 16 input
+// channels it stages the input rows those pixels read (whole rows, zero
+// outside x) and the chunk's weights as [k][r][s][32 channels] in shared
+// memory, every staging load issued before the stores.  Each thread keeps
+// bitmasks of its valid filter rows and columns; per valid tap: one input
+// read, 8 broadcast 16-byte weight reads, 32 FFMAs.
 
+#include <algorithm>
 #include <cstdint>
 
 #include "internal.h"
@@ -30,103 +32,132 @@
 namespace conv2d {
 namespace {
 
-constexpr int kDvThreads = 256;
-constexpr int kDvRows = 8, kDvCols = 32;
+constexpr int kDvThreads = 256;      // = output pixels per CTA (one per thread)
 constexpr int kDvC = 32;             // output channels per CTA
-constexpr int kDvK = 8;              // input channels per staged chunk
+constexpr int kDvK = 16;             // input channels per staged chunk
 constexpr int kDvMaxTap = 8;         // R, S <= 8
+constexpr int kDvBatch = 8;          // staging loads in flight per thread
 
 struct DvParams {
     const float *x, *w, *bias;
     float *y;
     int N, K, P, Q, C, R, S, H, W;
     int stride, pad, dil;
-    int tiles_h, tiles_w, c_blocks;
-    int IP, IQ;                      // staged footprint rows / columns (upper bounds)
+    int imgs;              // > 0: a CTA owns `imgs` whole images (H*W <= 256)
+    int tiles_per_img;     // imgs == 0: a CTA owns 256 consecutive pixels of one image
+    int tiles, c_blocks;
+    int IP, IQ;            // staged input rows per image / columns (= Q)
 };
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p) {
     extern __shared__ float4 dv_smem4[];
-    float *xs = reinterpret_cast<float *>(dv_smem4);                   // [kDvK][IP][IQ]
-    const int xs_sz = (kDvK * p.IP * p.IQ + 3) & ~3;
+    const int nimg = p.imgs > 0 ? p.imgs : 1;
+    float *xs = reinterpret_cast<float *>(dv_smem4);                   // [img][kDvK][IP][IQ]
+    const int xs_sz = (nimg * kDvK * p.IP * p.IQ + 3) & ~3;
     float *ws = xs + xs_sz;                                             // [kDvK][R][S][kDvC]
 
-    int t = blockIdx.x;
-    const int cb = t % p.c_blocks;
-    t /= p.c_blocks;
-    const int tw = t % p.tiles_w;
-    t /= p.tiles_w;
-    const int th = t % p.tiles_h;
-    const int n = t / p.tiles_h;
-    const int h0 = th * kDvRows, w0 = tw * kDvCols, c0 = cb * kDvC;
-    // first input row / column the block can read
-    const int p_lo = floor_div(h0 + p.pad - (p.R - 1) * p.dil + p.stride - 1, p.stride);
-    const int q_lo = floor_div(w0 + p.pad - (p.S - 1) * p.dil + p.stride - 1, p.stride);
+    const int cb = blockIdx.x % p.c_blocks;
+    const int tile = blockIdx.x / p.c_blocks;
+    const int c0 = cb * kDvC;
+    const int HW = p.H * p.W;
+    // this CTA's images and pixels
+    int n0, pix0, p_lo;
+    if (p.imgs > 0) {
+        n0 = tile * p.imgs;
+        pix0 = 0;
+        p_lo = 0;
+    } else {
+        n0 = tile / p.tiles_per_img;
+        pix0 = (tile - n0 * p.tiles_per_img) * kDvThreads;
+        const int h_first = pix0 / p.W;
+        p_lo = floor_div(h_first + p.pad - (p.R - 1) * p.dil + p.stride - 1, p.stride);
+    }
+    const int t = threadIdx.x;
+    const int img = p.imgs > 0 ? t / HW : 0;
+    const int pix = p.imgs > 0 ? t - img * HW : pix0 + t;
+    const int n = n0 + img;
+    const bool active = n < p.N && pix < HW && (p.imgs == 0 || img < p.imgs);
+    const int h = active ? pix / p.W : 0, wcol = active ? pix - h * p.W : 0;
 
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int h = h0 + warp, wcol = w0 + lane;
-    // valid taps: rows (uniform in the warp), columns (per lane)
+    // valid taps of this pixel, with staged row / column indices
     unsigned rmask = 0, smask = 0;
     int pl[kDvMaxTap], ql[kDvMaxTap];
 #pragma unroll
     for (int r = 0; r < kDvMaxTap; ++r) {
         pl[r] = 0;
-        if (r < p.R) {
-            const int hp = h + p.pad - r * p.dil;
-            if (hp >= 0 && hp % p.stride == 0 && hp / p.stride < p.P) {
-                rmask |= 1u << r;
-                pl[r] = hp / p.stride - p_lo;
-            }
+        const int hp = h + p.pad - r * p.dil;
+        if (active && r < p.R && hp >= 0 && hp % p.stride == 0 && hp / p.stride < p.P) {
+            rmask |= 1u << r;
+            pl[r] = hp / p.stride - p_lo;
         }
     }
 #pragma unroll
     for (int s = 0; s < kDvMaxTap; ++s) {
         ql[s] = 0;
-        if (s < p.S) {
-            const int wp = wcol + p.pad - s * p.dil;
-            if (wp >= 0 && wp % p.stride == 0 && wp / p.stride < p.Q) {
-                smask |= 1u << s;
-                ql[s] = wp / p.stride - q_lo;
-            }
+        const int wp = wcol + p.pad - s * p.dil;
+        if (active && s < p.S && wp >= 0 && wp % p.stride == 0 && wp / p.stride < p.Q) {
+            smask |= 1u << s;
+            ql[s] = wp / p.stride;
         }
     }
-    if (h >= p.H) rmask = 0;
-    if (wcol >= p.W) smask = 0;
 
     float acc[kDvC];
 #pragma unroll
     for (int j = 0; j < kDvC; ++j) acc[j] = 0.f;
     const int RS = p.R * p.S;
-    const int xn = kDvK * p.IP * p.IQ, wn = kDvK * RS * kDvC;
+    const int plane = p.IP * p.IQ;
+    const int xn = nimg * kDvK * plane, wn = kDvK * RS * kDvC;
 
     for (int k0 = 0; k0 < p.K; k0 += kDvK) {
         __syncthreads();
-        for (int i = threadIdx.x; i < xn; i += kDvThreads) {
-            const int iq = i % p.IQ;
-            const int r2 = i / p.IQ;
-            const int ip = r2 % p.IP;
-            const int kk = r2 / p.IP;
-            const int k = k0 + kk, pp = p_lo + ip, qq = q_lo + iq;
-            const bool in = k < p.K && (unsigned)pp < (unsigned)p.P && (unsigned)qq < (unsigned)p.Q;
-            const int64_t off = (((int64_t)n * p.K + k) * p.P + pp) * p.Q + qq;
-            xs[i] = sm103a::ldg_or_zero(p.x + (in ? off : 0), in);
-        }
-        for (int i = threadIdx.x; i < wn; i += kDvThreads) {
-            const int j = i % kDvC;
-            const int r2 = i / kDvC;
-            const int rs = r2 % RS;
-            const int kk = r2 / RS;
-            const int k = k0 + kk, c = c0 + j;
-            const bool in = k < p.K && c < p.C;
-            const int64_t off = ((int64_t)k * p.C + c) * RS + rs;
-            ws[i] = sm103a::ldg_or_zero(p.w + (in ? off : 0), in);
+        // stage x rows (zero outside x) and the chunk's weights; each thread
+        // issues kDvBatch loads before it stores any of them
+        for (int i0 = 0; i0 < xn + wn; i0 += kDvThreads * kDvBatch) {
+            float v[kDvBatch];
+#pragma unroll
+            for (int u = 0; u < kDvBatch; ++u) {
+                const int i = i0 + u * kDvThreads + t;
+                int64_t off = 0;
+                bool in = false;
+                if (i < xn) {
+                    const int iq = i % p.IQ;
+                    const int r2 = i / p.IQ;
+                    const int ip = r2 % p.IP;
+                    const int r3 = r2 / p.IP;
+                    const int kk = r3 % kDvK;
+                    const int im = r3 / kDvK;
+                    const int k = k0 + kk, pp = p_lo + ip, nn = n0 + im;
+                    in = nn < p.N && k < p.K && (unsigned)pp < (unsigned)p.P;
+                    off = (((int64_t)nn * p.K + k) * p.P + pp) * p.Q + iq;
+                    v[u] = sm103a::ldg_or_zero(p.x + (in ? off : 0), in);
+                } else if (i < xn + wn) {
+                    const int iw = i - xn;
+                    const int j = iw % kDvC;
+                    const int r2 = iw / kDvC;
+                    const int rs = r2 % RS;
+                    const int kk = r2 / RS;
+                    const int k = k0 + kk, c = c0 + j;
+                    in = k < p.K && c < p.C;
+                    off = ((int64_t)k * p.C + c) * RS + rs;
+                    v[u] = sm103a::ldg_or_zero(p.w + (in ? off : 0), in);
+                } else {
+                    v[u] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kDvBatch; ++u) {
+                const int i = i0 + u * kDvThreads + t;
+                if (i < xn) xs[i] = v[u];
+                else if (i < xn + wn) ws[i - xn] = v[u];
+            }
         }
         __syncthreads();
         const int kn = min(kDvK, p.K - k0);
+        const float *xi = xs + img * kDvK * plane;
         for (int kk = 0; kk < kn; ++kk) {
-            const float *xk = xs + kk * p.IP * p.IQ;
+            const float *xk = xi + kk * plane;
             const float *wk = ws + kk * RS * kDvC;
 #pragma unroll
             for (int r = 0; r < kDvMaxTap; ++r) {
@@ -149,27 +180,29 @@ __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p)
             }
         }
     }
-    if (h >= p.H || wcol >= p.W) return;
-    const int64_t HW = (int64_t)p.H * p.W;
-    float *yp = p.y + ((int64_t)n * p.C + c0) * HW + (int64_t)h * p.W + wcol;
+    if (!active) return;
+    float *yp = p.y + ((int64_t)n * p.C + c0) * HW + pix;
 #pragma unroll
     for (int j = 0; j < kDvC; ++j) {
         if (c0 + j < p.C) yp[(int64_t)j * HW] = acc[j] + (p.bias ? __ldg(p.bias + c0 + j) : 0.f);
     }
 }
 
-void footprint(int stride, int dil, int R, int S, int *ip, int *iq) {
-    // rows of x a block of kDvRows output rows can read (an upper bound)
-    *ip = (kDvRows - 1 + (R - 1) * dil) / stride + 2;
-    *iq = (kDvCols - 1 + (S - 1) * dil) / stride + 2;
+// Staged input rows per image for a CTA's pixels (an upper bound).
+int stage_rows(int H, int W, int P, int R, int stride, int dil) {
+    if (H * W <= kDvThreads) return P;
+    // rows p_lo .. p_lo + IP - 1 are staged (zero outside [0, P)); p_lo may be
+    // negative, so the count is not clamped to P
+    const int rows_out = (kDvThreads + W - 1) / W + 1;            // output rows 256 pixels can touch
+    return (rows_out - 1 + (R - 1) * dil) / stride + 2;
 }
 
 }  // namespace
 
-size_t dv_smem_bytes(int stride, int dil, int R, int S) {
-    int ip, iq;
-    footprint(stride, dil, R, S, &ip, &iq);
-    const size_t xs = ((size_t)kDvK * ip * iq + 3) & ~(size_t)3;
+size_t dv_smem_bytes(int H, int W, int P, int Q, int R, int S, int stride, int dil) {
+    const int imgs = H * W <= kDvThreads ? std::max(1, kDvThreads / (H * W)) : 1;
+    const int ip = stage_rows(H, W, P, R, stride, dil);
+    const size_t xs = ((size_t)imgs * kDvK * ip * Q + 3) & ~(size_t)3;
     return (xs + (size_t)kDvK * R * S * kDvC) * sizeof(float);
 }
 
@@ -181,13 +214,24 @@ conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, flo
     p.x = x; p.w = w; p.bias = bias; p.y = y;
     p.N = N; p.K = K; p.P = P; p.Q = Q; p.C = C; p.R = R; p.S = S; p.H = H; p.W = W;
     p.stride = stride; p.pad = pad; p.dil = dil;
-    p.tiles_h = (H + kDvRows - 1) / kDvRows;
-    p.tiles_w = (W + kDvCols - 1) / kDvCols;
+    const int64_t HW = (int64_t)H * W;
+    if (HW <= kDvThreads) {
+        p.imgs = (int)std::max<int64_t>(1, kDvThreads / HW);
+        p.tiles_per_img = 0;
+        p.tiles = (int)((N + p.imgs - 1) / p.imgs);
+    } else {
+        p.imgs = 0;
+        p.tiles_per_img = (int)((HW + kDvThreads - 1) / kDvThreads);
+        const int64_t tiles = (int64_t)N * p.tiles_per_img;
+        if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
+        p.tiles = (int)tiles;
+    }
     p.c_blocks = (C + kDvC - 1) / kDvC;
-    footprint(stride, dil, R, S, &p.IP, &p.IQ);
-    const int64_t grid = (int64_t)N * p.tiles_h * p.tiles_w * p.c_blocks;
+    p.IP = stage_rows(H, W, P, R, stride, dil);
+    p.IQ = Q;
+    const int64_t grid = (int64_t)p.tiles * p.c_blocks;
     if (grid > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
-    const size_t bytes = dv_smem_bytes(stride, dil, R, S);
+    const size_t bytes = dv_smem_bytes(H, W, P, Q, R, S, stride, dil);
     if (bytes > 96 * 1024) return CONV2D_ERR_UNSUPPORTED;
     if (bytes > 48 * 1024 &&
         cudaFuncSetAttribute(deconv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024) !=

@@ -120,7 +120,7 @@ conv2d_status_t tf_launch(const Shape &s, const Plan &p, const Tensors &t, cudaS
                           const TfLstm *lstm = nullptr);
 
 // Transposed convolution, fp32 NCHW (arguments validated by the caller).
-size_t dv_smem_bytes(int stride, int dil, int R, int S);
+size_t dv_smem_bytes(int H, int W, int P, int Q, int R, int S, int stride, int dil);
 conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, float *y, int N, int K,
                           int P, int Q, int C, int R, int S, int H, int W, int stride, int pad,
                           int dil, cudaStream_t st);

@@ -13,7 +13,9 @@
 //
 // One CTA per end time (grid.y splits the n*n pairs when there are more than
 // one CTA's worth).  The samples are staged in shared memory in chunks of
-// 64 time steps, walked from the most recent backwards; because every window
+// 64 time steps (rows padded to an odd stride, so the lanes of a warp, which
+// read different signals at one time step, hit different banks), walked
+// from the most recent backwards; because every window
 // ends at e, the windows are nested, so one pass over the longest window
 // emits every window's matrix as soon as its sample count is reached (the
 // windows are visited in increasing length).  Each thread accumulates its
@@ -23,12 +25,14 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx_sm103a.cuh"
 
 namespace conv2d {
 namespace {
 
 constexpr int kSigThreads = 256;
 constexpr int kSigChunk = 64;      // time steps staged per pass
+constexpr int kSigStride = kSigChunk + 1;   // odd row stride: lanes reading different rows hit different banks
 constexpr int kSigPairs = 4;       // (i, j) pairs per thread
 constexpr int kSigMaxWindows = 8;
 
@@ -41,7 +45,7 @@ struct SigParams {
 };
 
 __global__ void __launch_bounds__(kSigThreads) signature_kernel(const SigParams p) {
-    extern __shared__ float ss[];              // [n][kSigChunk]
+    extern __shared__ float ss[];              // [n][kSigStride]
     const int b = blockIdx.x;
     const int e = p.t_first + b;
     const int nn = p.n * p.n;
@@ -63,15 +67,28 @@ __global__ void __launch_bounds__(kSigThreads) signature_kernel(const SigParams 
         const int len = min(kSigChunk, t_hi - (e - wmax));
         const int t_lo = t_hi - len;
         __syncthreads();                       // the previous chunk is no longer read
-        for (int k = threadIdx.x; k < p.n * len; k += kSigThreads) {
-            const int i = k / len, tt = k - i * len;
-            ss[i * kSigChunk + tt] = __ldg(p.series + (int64_t)i * p.T + t_lo + tt);
+        // every load of the chunk is issued before any of them is stored
+        for (int k0 = 0; k0 < p.n * len; k0 += kSigThreads * 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int k = k0 + u * kSigThreads + (int)threadIdx.x;
+                const int i = k / len, tt = k - i * len;
+                const bool in = k < p.n * len;
+                v[u] = sm103a::ldg_or_zero(p.series + (in ? (int64_t)i * p.T + t_lo + tt : 0), in);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int k = k0 + u * kSigThreads + (int)threadIdx.x;
+                const int i = k / len, tt = k - i * len;
+                if (k < p.n * len) ss[i * kSigStride + tt] = v[u];
+            }
         }
         __syncthreads();
         for (int tt = len - 1; tt >= 0; --tt) {
 #pragma unroll
             for (int q = 0; q < kSigPairs; ++q)
-                acc[q] = fmaf(ss[pi[q] * kSigChunk + tt], ss[pj[q] * kSigChunk + tt], acc[q]);
+                acc[q] = fmaf(ss[pi[q] * kSigStride + tt], ss[pj[q] * kSigStride + tt], acc[q]);
             ++count;
             while (next < p.n_win && count == p.win[next]) {
                 const float w = (float)p.win[next];
@@ -109,7 +126,7 @@ conv2d_status_t sig_launch(const float *series, int n, int T, const int *windows
     }
     const int per_cta = kSigThreads * kSigPairs;
     const dim3 grid((unsigned)n_steps, (unsigned)((n * n + per_cta - 1) / per_cta));
-    const size_t smem = (size_t)n * kSigChunk * sizeof(float);
+    const size_t smem = (size_t)n * kSigStride * sizeof(float);
     signature_kernel<<<grid, kSigThreads, smem, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }

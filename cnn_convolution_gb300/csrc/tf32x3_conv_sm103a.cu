@@ -675,7 +675,9 @@ conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t,
 // (BN, STAGES, producer warps, measured ns per stage of one tile) of every
 // compiled variant.  The stage times were measured on GB300 on the MSCRED
 // encoder layers (fp32 NCHW, 3x3 / 2x2 filters); the producers' gather is
-// latency-bound, so more producer warps per SM run a stage faster.
+// latency-bound, so more producer warps per SM run a stage faster.  The
+// 3-stage variant leaves shared memory for the tap tables of long
+// reductions (C*R*S up to about 9,000); its stage time is an estimate.
 #define CONV2D_TF_VARIANTS(X) \
     X(32, 5, 4, 1240)         \
     X(64, 4, 4, 3850)         \
@@ -683,7 +685,8 @@ conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t,
     X(32, 5, 8, 920)          \
     X(64, 4, 8, 1370)         \
     X(128, 3, 8, 3100)        \
-    X(64, 4, 16, 1030)
+    X(64, 4, 16, 1030)        \
+    X(64, 3, 16, 1100)
 
 }  // namespace
 

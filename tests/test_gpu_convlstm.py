@@ -55,6 +55,7 @@ CASES = [
     (2, 32, 32, 30, 30, 3),       # MSCRED layer-1 scale
     (4, 64, 64, 15, 15, 3),       # layer-2 scale
     (8, 128, 128, 8, 8, 3),       # layer-3 scale (gate conv K = 512)
+    (4, 256, 256, 4, 4, 3),       # layer-4 scale: C*R*S = 4608, the 3-stage variant
 ]
 
 

@@ -20,7 +20,7 @@ from parity import TOL, full_parity, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-N_VARIANTS = 7   # (BN, stages, producer warps) table of the library
+N_VARIANTS = 8   # (BN, stages, producer warps) table of the library
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -187,6 +187,10 @@ RESIDENT_SHAPES = [
     (2, 32, 9, 20, 40, 3, 3, 1, 1, False),
     (2, 128, 8, 8, 64, 2, 2, 0, 1, True),
     (1, 64, 30, 40, 128, 2, 2, 1, 1, True),
+    # small enough for the 128-wide resident variant (64 channels x 4 taps or fewer)
+    (2, 64, 12, 12, 128, 2, 2, 0, 1, True),
+    (3, 32, 10, 10, 96, 1, 3, 0, 1, False),
+    (2, 64, 9, 9, 128, 2, 1, 0, 1, True),
 ]
 
 
