@@ -51,6 +51,8 @@ struct DvParams {
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
+// RT, ST: compile-time filter size bound of the tap loops (kDvMaxTap = any R, S <= 8).
+template <int RT, int ST>
 __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p) {
     extern __shared__ float4 dv_smem4[];
     const int nimg = p.imgs > 0 ? p.imgs : 1;
@@ -83,9 +85,9 @@ __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p)
 
     // valid taps of this pixel, with staged row / column indices
     unsigned rmask = 0, smask = 0;
-    int pl[kDvMaxTap], ql[kDvMaxTap];
+    int pl[RT], ql[ST];
 #pragma unroll
-    for (int r = 0; r < kDvMaxTap; ++r) {
+    for (int r = 0; r < RT; ++r) {
         pl[r] = 0;
         const int hp = h + p.pad - r * p.dil;
         if (active && r < p.R && hp >= 0 && hp % p.stride == 0 && hp / p.stride < p.P) {
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p)
         }
     }
 #pragma unroll
-    for (int s = 0; s < kDvMaxTap; ++s) {
+    for (int s = 0; s < ST; ++s) {
         ql[s] = 0;
         const int wp = wcol + p.pad - s * p.dil;
         if (active && s < p.S && wp >= 0 && wp % p.stride == 0 && wp / p.stride < p.Q) {
@@ -106,51 +108,96 @@ __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p)
     float acc[kDvC];
 #pragma unroll
     for (int j = 0; j < kDvC; ++j) acc[j] = 0.f;
-    const int RS = p.R * p.S;
+    // exact compile-time filter sizes make the staging index arithmetic cheap
+    const int RS = (RT < kDvMaxTap && RT * ST > 0) ? RT * ST : p.R * p.S;
     const int plane = p.IP * p.IQ;
-    const int xn = nimg * kDvK * plane, wn = kDvK * RS * kDvC;
+    const int warp = t / 32, lane = t % 32;
 
     for (int k0 = 0; k0 < p.K; k0 += kDvK) {
         __syncthreads();
-        // stage x rows (zero outside x) and the chunk's weights; each thread
-        // issues kDvBatch loads before it stores any of them
-        for (int i0 = 0; i0 < xn + wn; i0 += kDvThreads * kDvBatch) {
+        // stage x.  Whole images: the chunk of an image, x[n][k0 .. k0+15][..][..],
+        // is one contiguous run, copied flat.  Else one staged row (image,
+        // channel, input row) per warp pass, lanes along the row; 4 rows in
+        // flight per warp.
+        const int nrows = p.imgs > 0 ? 0 : nimg * kDvK * p.IP;
+        if (p.imgs > 0) {
+            const int per_img = kDvK * plane;              // plane = P*Q here
+            const int kn_img = min(kDvK, p.K - k0) * plane;
+            for (int i0 = 0; i0 < nimg * per_img; i0 += kDvThreads * kDvBatch) {
+                float v[kDvBatch];
+#pragma unroll
+                for (int u = 0; u < kDvBatch; ++u) {
+                    const int i = i0 + u * kDvThreads + t;
+                    const int im = i / per_img, f = i - im * per_img;
+                    const bool in = i < nimg * per_img && n0 + im < p.N && f < kn_img;
+                    v[u] = sm103a::ldg_or_zero(in ? p.x + ((int64_t)(n0 + im) * p.K + k0) * plane + f : p.x, in);
+                }
+#pragma unroll
+                for (int u = 0; u < kDvBatch; ++u) {
+                    const int i = i0 + u * kDvThreads + t;
+                    if (i < nimg * per_img) xs[i] = v[u];
+                }
+            }
+        }
+        for (int row0 = warp * 4; row0 < nrows; row0 += (kDvThreads / 32) * 4) {
+            float v[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int row = row0 + u;
+                const int ip = row % p.IP, r2 = row / p.IP;
+                const int kk = r2 % kDvK, im = r2 / kDvK;
+                const int k = k0 + kk, pp = p_lo + ip, nn = n0 + im;
+                const bool rin = row < nrows && nn < p.N && k < p.K && (unsigned)pp < (unsigned)p.P;
+                const float *src = p.x + (((int64_t)nn * p.K + k) * p.P + pp) * p.Q;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int iq = lane + 32 * e;
+                    const bool in = rin && iq < p.Q;
+                    v[u][e] = sm103a::ldg_or_zero(in ? src + iq : p.x, in);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int row = row0 + u;
+                if (row < nrows) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (lane + 32 * e < p.IQ) xs[row * p.IQ + lane + 32 * e] = v[u][e];
+                }
+            }
+            // rows longer than 64 columns (wide outputs): the rest, plainly
+            for (int u = 0; u < 4 && p.IQ > 64; ++u) {
+                const int row = row0 + u;
+                if (row >= nrows) break;
+                const int ip = row % p.IP, r2 = row / p.IP;
+                const int kk = r2 % kDvK, im = r2 / kDvK;
+                const int k = k0 + kk, pp = p_lo + ip, nn = n0 + im;
+                const bool rin = nn < p.N && k < p.K && (unsigned)pp < (unsigned)p.P;
+                for (int iq = 64 + lane; iq < p.IQ; iq += 32)
+                    xs[row * p.IQ + iq] = rin ? __ldg(p.x + (((int64_t)nn * p.K + k) * p.P + pp) * p.Q + iq) : 0.f;
+            }
+        }
+        // stage w: for each input channel the block's weights w[k][c0 .. c0+31][r][s]
+        // are contiguous; read them in that order, store as [k][r*S+s][c]
+        const int wrun = kDvC * RS;
+        for (int i0 = 0; i0 < kDvK * wrun; i0 += kDvThreads * kDvBatch) {
             float v[kDvBatch];
 #pragma unroll
             for (int u = 0; u < kDvBatch; ++u) {
                 const int i = i0 + u * kDvThreads + t;
-                int64_t off = 0;
-                bool in = false;
-                if (i < xn) {
-                    const int iq = i % p.IQ;
-                    const int r2 = i / p.IQ;
-                    const int ip = r2 % p.IP;
-                    const int r3 = r2 / p.IP;
-                    const int kk = r3 % kDvK;
-                    const int im = r3 / kDvK;
-                    const int k = k0 + kk, pp = p_lo + ip, nn = n0 + im;
-                    in = nn < p.N && k < p.K && (unsigned)pp < (unsigned)p.P;
-                    off = (((int64_t)nn * p.K + k) * p.P + pp) * p.Q + iq;
-                    v[u] = sm103a::ldg_or_zero(p.x + (in ? off : 0), in);
-                } else if (i < xn + wn) {
-                    const int iw = i - xn;
-                    const int j = iw % kDvC;
-                    const int r2 = iw / kDvC;
-                    const int rs = r2 % RS;
-                    const int kk = r2 / RS;
-                    const int k = k0 + kk, c = c0 + j;
-                    in = k < p.K && c < p.C;
-                    off = ((int64_t)k * p.C + c) * RS + rs;
-                    v[u] = sm103a::ldg_or_zero(p.w + (in ? off : 0), in);
-                } else {
-                    v[u] = 0.f;
-                }
+                const int kk = i / wrun, f = i - kk * wrun;
+                const int k = k0 + kk, c = c0 + f / RS;
+                const bool in = i < kDvK * wrun && k < p.K && c < p.C;
+                v[u] = sm103a::ldg_or_zero(in ? p.w + ((int64_t)k * p.C + c0) * RS + f : p.w, in);
             }
 #pragma unroll
             for (int u = 0; u < kDvBatch; ++u) {
                 const int i = i0 + u * kDvThreads + t;
-                if (i < xn) xs[i] = v[u];
-                else if (i < xn + wn) ws[i - xn] = v[u];
+                if (i < kDvK * wrun) {
+                    const int kk = i / wrun, f = i - kk * wrun;
+                    const int j = f / RS, rs = f - j * RS;
+                    ws[(kk * RS + rs) * kDvC + j] = v[u];
+                }
             }
         }
         __syncthreads();
@@ -160,14 +207,14 @@ __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p)
             const float *xk = xi + kk * plane;
             const float *wk = ws + kk * RS * kDvC;
 #pragma unroll
-            for (int r = 0; r < kDvMaxTap; ++r) {
+            for (int r = 0; r < RT; ++r) {
                 if (!((rmask >> r) & 1u)) continue;
                 const float *xr = xk + pl[r] * p.IQ;
 #pragma unroll
-                for (int s = 0; s < kDvMaxTap; ++s) {
+                for (int s = 0; s < ST; ++s) {
                     if (!((smask >> s) & 1u)) continue;
                     const float a = xr[ql[s]];
-                    const float4 *w4 = reinterpret_cast<const float4 *>(wk + (r * p.S + s) * kDvC);
+                    const float4 *w4 = reinterpret_cast<const float4 *>(wk + (r * (ST < kDvMaxTap ? ST : p.S) + s) * kDvC);
 #pragma unroll
                     for (int j = 0; j < kDvC / 4; ++j) {
                         const float4 v = w4[j];
@@ -233,11 +280,14 @@ conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, flo
     if (grid > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     const size_t bytes = dv_smem_bytes(H, W, P, Q, R, S, stride, dil);
     if (bytes > 96 * 1024) return CONV2D_ERR_UNSUPPORTED;
+    void (*kern)(DvParams);
+    if (R == 2 && S == 2) kern = deconv_kernel<2, 2>;
+    else if (R == 3 && S == 3) kern = deconv_kernel<3, 3>;
+    else kern = deconv_kernel<kDvMaxTap, kDvMaxTap>;
     if (bytes > 48 * 1024 &&
-        cudaFuncSetAttribute(deconv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024) !=
-            cudaSuccess)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024) != cudaSuccess)
         return CONV2D_ERR_CUDA;
-    deconv_kernel<<<(unsigned)grid, kDvThreads, bytes, st>>>(p);
+    kern<<<(unsigned)grid, kDvThreads, bytes, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 
