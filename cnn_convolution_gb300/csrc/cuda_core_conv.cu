@@ -40,6 +40,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "ptx_sm103a.cuh"
 
 namespace conv2d {
 namespace {
@@ -110,6 +111,9 @@ cc_conv_kernel(const CcParams p) {
     const T *__restrict__ x = static_cast<const T *>(p.x);
     const T *__restrict__ w = static_cast<const T *>(p.w);
     const int tid = threadIdx.x;
+    // no early trigger: a kernel of many short CTAs lets the next one launch
+    // at its exit, so the next grid is spread over idle SMs
+    sm103a::pdl_wait();                        // the previous kernel's writes are visible
     const int64_t m0 = (int64_t)blockIdx.x * BM;
     const int n0 = blockIdx.y * BN;
     const int Kg = p.Kg;
@@ -400,21 +404,25 @@ conv2d_status_t launch_one(const Shape &s, const Tensors &t, int grid_m, int gri
     p.stride = s.stride; p.pad = s.pad; p.dil = s.dil; p.P = s.P; p.Q = s.Q;
     p.Kg = (int)s.Kg; p.M = s.M;
     if (SPLIT == 1) {
-        dim3 grid(grid_m, grid_n);
-        kern<<<grid, Cfg::NT, smem, st>>>(p);
+        if (launch_pdl(kern, dim3(grid_m, grid_n), dim3(Cfg::NT), smem, st, p) != cudaSuccess) {
+            cudaGetLastError();
+            return CONV2D_ERR_CUDA;
+        }
     } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid_m, grid_n, SPLIT);
         cfg.blockDim = dim3(Cfg::NT);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 1;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = SPLIT;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return CONV2D_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;

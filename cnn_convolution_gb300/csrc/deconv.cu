@@ -60,6 +60,9 @@ __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p)
     const int xs_sz = (nimg * kDvK * p.IP * p.IQ + 3) & ~3;
     float *ws = xs + xs_sz;                                             // [kDvK][R][S][kDvC]
 
+    // no early trigger: a kernel of many short CTAs lets the next one launch
+    // at its exit, so the next grid is spread over idle SMs
+    sm103a::pdl_wait();                        // the previous kernel's writes are visible
     const int cb = blockIdx.x % p.c_blocks;
     const int tile = blockIdx.x / p.c_blocks;
     const int c0 = cb * kDvC;
@@ -287,8 +290,11 @@ conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, flo
     if (bytes > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024) != cudaSuccess)
         return CONV2D_ERR_CUDA;
-    kern<<<(unsigned)grid, kDvThreads, bytes, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+    if (launch_pdl(kern, dim3((unsigned)grid), dim3(kDvThreads), bytes, st, p) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV2D_ERR_CUDA;
+    }
+    return CONV2D_OK;
 }
 
 }  // namespace conv2d

@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcPara
     const int n = t / p.tiles_p;
     const int p0 = tp * kDcRows, q0 = tq * kDcCols;
     const int h0 = p0 * p.stride - p.pad, w0 = q0 * p.stride - p.pad;
+    sm103a::pdl_launch_dependents();
+    sm103a::pdl_wait();                        // the previous kernel's writes are visible
 
     // Stage the input patch (zero outside the image) and the weights as
     // [g = (c, r, s)][k] (zero for k >= K).  Each thread issues kDcBatch
@@ -252,8 +254,11 @@ conv2d_status_t dc_launch(const Shape &s, const Plan &pl, const Tensors &t, cuda
     if (bytes > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024) != cudaSuccess)
         return CONV2D_ERR_CUDA;
-    kern<<<dc_grid(s), kDcThreads, bytes, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+    if (launch_pdl(kern, dim3(dc_grid(s)), dim3(kDcThreads), bytes, st, p) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV2D_ERR_CUDA;
+    }
+    return CONV2D_OK;
 }
 
 }  // namespace conv2d

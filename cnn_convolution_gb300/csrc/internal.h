@@ -129,6 +129,25 @@ conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, flo
 conv2d_status_t sig_launch(const float *series, int n, int T, const int *windows, int n_windows,
                            int t_first, int n_steps, float *out, cudaStream_t st);
 
+// Launch with programmatic dependent launch (the kernel calls pdl_wait()
+// before touching global memory); falls back to nothing else -- an error
+// from the launch is returned as is.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Device status word (bounded-wait failures).
 conv2d_status_t status_read_and_clear();
 unsigned int *status_word_ptr();   // device address, per current device

@@ -239,5 +239,21 @@ __device__ __forceinline__ void ldg4_or_zero(const float *ptr, bool pred, float 
         : "l"(ptr), "r"((int)pred));
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel on the
+// stream is still running; pdl_wait() blocks until that kernel has finished
+// and its memory is visible (a no-op without the attribute).  Every kernel
+// here calls it before its first global-memory access, so only setup that
+// depends on parameters alone (barriers, tensor-memory allocation, tap
+// tables) overlaps the previous kernel.  pdl_launch_dependents() lets the
+// next kernel be launched once every CTA of this one has called it (or
+// exited).  Persistent kernels (one CTA per SM) call it on entry; kernels of
+// many short CTAs do not, because waiting CTAs of the next grid would be
+// placed onto whichever SMs free up first and unbalance it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace sm103a
 }  // namespace conv2d

@@ -46,6 +46,9 @@ struct SigParams {
 
 __global__ void __launch_bounds__(kSigThreads) signature_kernel(const SigParams p) {
     extern __shared__ float ss[];              // [n][kSigStride]
+    // no early trigger: a kernel of many short CTAs lets the next one launch
+    // at its exit, so the next grid is spread over idle SMs
+    sm103a::pdl_wait();                        // the previous kernel's writes are visible
     const int b = blockIdx.x;
     const int e = p.t_first + b;
     const int nn = p.n * p.n;
@@ -127,8 +130,11 @@ conv2d_status_t sig_launch(const float *series, int n, int T, const int *windows
     const int per_cta = kSigThreads * kSigPairs;
     const dim3 grid((unsigned)n_steps, (unsigned)((n * n + per_cta - 1) / per_cta));
     const size_t smem = (size_t)n * kSigStride * sizeof(float);
-    signature_kernel<<<grid, kSigThreads, smem, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+    if (launch_pdl(signature_kernel, grid, dim3(kSigThreads), smem, st, p) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV2D_ERR_CUDA;
+    }
+    return CONV2D_OK;
 }
 
 }  // namespace conv2d

@@ -216,6 +216,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    pdl_launch_dependents();
+    pdl_wait();                                // the previous kernel's writes are visible
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- TMA producer
@@ -526,6 +528,8 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    pdl_launch_dependents();
+    pdl_wait();                                // the previous kernel's writes are visible
     const uint32_t win_tx = (uint32_t)((p.TR + (p.R - 1) * p.dil) * p.Wp * 128);
 
     if (warp == 0 && lane == 0) {
@@ -976,8 +980,12 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
         return CONV2D_ERR_CUDA;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    kern<<<grid, kThreads, L::kBytes, st>>>(maps->a, maps->b, maps->y, p);
-    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, maps->y, p) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return CONV2D_ERR_CUDA;
+    }
+    return CONV2D_OK;
 }
 
 template <typename T, int BN, int KSUB, int STAGES, int WINKB, int NWIN, bool RES, int RESKB>
@@ -1016,8 +1024,12 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
         return CONV2D_ERR_CUDA;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    kern<<<grid, kThreads, L::kBytes, st>>>(maps->a, maps->b, maps->y, p);
-    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, maps->y, p) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return CONV2D_ERR_CUDA;
+    }
+    return CONV2D_OK;
 }
 
 // Variants: (BN, KSUB, STAGES) with about 192 KB of stages.

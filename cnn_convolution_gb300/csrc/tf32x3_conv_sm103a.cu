@@ -268,6 +268,10 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // everything above depends on parameters only; x, w, bias, c and y are
+    // touched after the previous kernel on the stream has finished
+    pdl_launch_dependents();
+    pdl_wait();
     auto a_hi = [&](int s) { return smem_base + (uint32_t)(s * L::kStage); };
     auto a_lo = [&](int s) { return smem_base + (uint32_t)(s * L::kStage + kTfATile); };
     auto b_hi = [&](int s) { return smem_base + (uint32_t)(s * L::kStage + 2 * kTfATile); };
@@ -660,8 +664,11 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
     if (!ensure_attr(reinterpret_cast<const void *>(kern), 227 * 1024, attr_done)) return CONV2D_ERR_CUDA;
     if (bytes > 227 * 1024) return CONV2D_ERR_UNSUPPORTED;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    kern<<<grid, tf_threads<BN, NPROD>(), bytes, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+    if (launch_pdl(kern, dim3(grid), dim3(tf_threads<BN, NPROD>()), bytes, st, p) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV2D_ERR_CUDA;
+    }
+    return CONV2D_OK;
 }
 
 // Only variants with 8 or more producer warps carry the ConvLSTM epilogue.
