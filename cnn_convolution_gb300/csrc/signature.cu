@@ -64,8 +64,16 @@ __global__ void __launch_bounds__(kSigThreads) signature_kernel(const SigParams 
 #pragma unroll
     for (int q = 0; q < kSigPairs; ++q) acc[q] = 0.f;
 
-    const int wmax = p.win[p.n_win - 1];
+    // the window table in shared memory; the next boundary stays in a register
+    __shared__ int s_win[kSigMaxWindows], s_chan[kSigMaxWindows];
+    if (threadIdx.x < kSigMaxWindows) {
+        s_win[threadIdx.x] = threadIdx.x < (unsigned)p.n_win ? p.win[threadIdx.x] : 0;
+        s_chan[threadIdx.x] = threadIdx.x < (unsigned)p.n_win ? p.chan[threadIdx.x] : 0;
+    }
+    __syncthreads();
+    const int wmax = s_win[p.n_win - 1];
     int count = 0, next = 0;                   // samples summed so far, next window to emit
+    int next_w = s_win[0];
     for (int t_hi = e; t_hi > e - wmax; t_hi -= kSigChunk) {
         const int len = min(kSigChunk, t_hi - (e - wmax));
         const int t_lo = t_hi - len;
@@ -93,15 +101,16 @@ __global__ void __launch_bounds__(kSigThreads) signature_kernel(const SigParams 
             for (int q = 0; q < kSigPairs; ++q)
                 acc[q] = fmaf(ss[pi[q] * kSigStride + tt], ss[pj[q] * kSigStride + tt], acc[q]);
             ++count;
-            while (next < p.n_win && count == p.win[next]) {
-                const float w = (float)p.win[next];
-                float *o = p.out + ((int64_t)b * p.n_win + p.chan[next]) * nn;
+            while (count == next_w) {
+                const float w = (float)next_w;
+                float *o = p.out + ((int64_t)b * p.n_win + s_chan[next]) * nn;
 #pragma unroll
                 for (int q = 0; q < kSigPairs; ++q) {
                     const int pid = pid0 + q * kSigThreads;
                     if (pid < nn) o[pid] = acc[q] / w;
                 }
                 ++next;
+                next_w = next < p.n_win ? s_win[next] : 0;
             }
         }
     }
