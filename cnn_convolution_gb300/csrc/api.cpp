@@ -302,8 +302,11 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
 // CTAs run ceil(tiles / SMs) tiles each.  Result in nanoseconds, comparable
 // with cc_cost() * 2e-3.
 double tf_cost_ns(const Shape &s, const TfTile &t, int sms) {
-    const int64_t tiles = ((s.M + 127) / 128) * ((s.K + t.BN - 1) / t.BN);
-    const int64_t rounds = (tiles + sms - 1) / sms;
+    const int64_t ntn = (s.K + t.BN - 1) / t.BN;
+    const int64_t tiles = ((s.M + 127) / 128) * ntn;
+    int64_t grid = std::min<int64_t>(tiles, sms);
+    if (t.resb) grid = std::max(ntn, grid / ntn * ntn);   // a CTA keeps one output-channel tile
+    const int64_t rounds = (tiles + grid - 1) / grid;
     const int64_t kt = (s.Kg + 31) / 32;
     return 2000.0 + (double)rounds * ((double)kt * t.stage_ns + 2000.0);
 }
@@ -549,8 +552,9 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
         std::snprintf(buf, len, "cuda_core direct ffma block=16x32px kc=32 threads=256 grid=%d smem=%zu",
                       p.grid, p.smem_bytes);
     else if (p.algo == Algo::Tf32x3)
-        std::snprintf(buf, len, "tensor_core tcgen05 3xtf32 BM=128 BN=%d BK=32 stages=%d producers=%d grid=%d smem=%zu",
-                      p.tf.BN, p.tf.stages, p.tf.nprod * 32, p.grid, p.smem_bytes);
+        std::snprintf(buf, len, "tensor_core tcgen05 3xtf32 BM=128 BN=%d BK=32 stages=%d producers=%d%s grid=%d smem=%zu",
+                      p.tf.BN, p.tf.stages, p.tf.nprod * 32, p.tf.resb ? " resident-w" : "", p.grid,
+                      p.smem_bytes);
     else
         std::snprintf(buf, len, "cuda_core ffma BM=%d BN=%d BK=%d TM=%d TN=%d threads=%d split=%d grid=%d smem=%zu",
                       p.cc.BM, p.cc.BN, p.cc.BK, p.cc.TM, p.cc.TN, p.cc.threads, p.cc.split, p.grid,

@@ -52,6 +52,7 @@ struct TfTile {
     int nprod;       // producer (gather + split) warps
     int id;          // index into the variant table
     int stage_ns;    // measured time of one 32-element stage of one tile (GB300)
+    bool resb;       // the split weights of the CTA's output-channel tile stay resident
 };
 
 enum class Algo { CudaCore, TensorCore, Tf32x3, Direct };

@@ -33,6 +33,7 @@
 
 #include <cuda.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 
@@ -151,18 +152,23 @@ struct TfTmem {
     static_assert(kUsed <= 512, "tensor memory");
 };
 
-// Shared memory: STAGES x (A_hi, A_lo, B_hi, B_lo), barriers, then the tap table.
-template <int BN, int STAGES>
+// Shared memory: STAGES x (A_hi, A_lo[, B_hi, B_lo]), barriers, then -- with
+// resident weights (RESB) -- the split weights of every stage of the CTA's
+// output-channel tile (KT x (B_hi, B_lo)), then the tap table.
+template <int BN, int STAGES, bool RESB = false>
 struct TfSmem {
     static constexpr int kBTile = BN * kTfBK * 4;
-    static constexpr int kStage = 2 * kTfATile + 2 * kBTile;
+    static constexpr int kStage = 2 * kTfATile + (RESB ? 0 : 2 * kBTile);
     static constexpr int kSlots = TfTmem<BN>::kSlots;
     static constexpr size_t kBarOffset = (size_t)STAGES * kStage;
-    // full[S], empty[S], slot_full[NS], slot_empty[NS], corr_full[2], corr_empty[2], drain;
-    // then the tensor-memory address and the abort flag
-    static constexpr size_t kBarBytes = (2 * STAGES + 2 * kSlots + 5) * 8;
-    static constexpr size_t kTapOffset = (kBarOffset + kBarBytes + 16 + 15) / 16 * 16;
-    static constexpr size_t bytes(int kt) { return kTapOffset + (size_t)kt * kTfBK * 8 + 1024; }
+    // full[S], empty[S], slot_full[NS], slot_empty[NS], corr_full[2], corr_empty[2], drain,
+    // weights-ready; then the tensor-memory address and the abort flag
+    static constexpr size_t kBarBytes = (2 * STAGES + 2 * kSlots + 6) * 8;
+    static constexpr size_t kResBOffset = (kBarOffset + kBarBytes + 16 + 1023) / 1024 * 1024;
+    static constexpr size_t tap_offset(int kt) {
+        return RESB ? kResBOffset + (size_t)kt * 2 * kBTile : (kBarOffset + kBarBytes + 16 + 15) / 16 * 16;
+    }
+    static constexpr size_t bytes(int kt) { return tap_offset(kt) + (size_t)kt * kTfBK * 8 + 1024; }
 };
 
 template <int BN> constexpr int tf_epi_warps() { return BN >= 64 ? 8 : 4; }
@@ -175,9 +181,9 @@ template <int BN, int NPROD> constexpr int tf_threads() { return 32 * (tf_epi_wa
 // tensor memory over one stage only (4 MMAs of K=8) and the stage sums are
 // added in fp32 registers by the epilogue warps; the correction terms, 2^-11
 // smaller, stay in one accumulator per tile.
-template <int BN, int STAGES, int NPROD, bool LSTM>
+template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB>
 __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel(const TfParams p) {
-    using L = TfSmem<BN, STAGES>;
+    using L = TfSmem<BN, STAGES, RESB>;
     using TM = TfTmem<BN>;
     constexpr uint32_t kIdesc = make_idesc_tf32(BN);
     constexpr int kSlots = TM::kSlots;
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     constexpr int kChunks = 8 * kTfBM / kProd;                   // A chunks (4 values) per thread per stage
     constexpr int kBIter = BN * 8 / kProd;                       // B chunks per thread per stage
     static_assert(kChunks >= 1 && kChunks * kProd == 8 * kTfBM, "producer split (A)");
-    static_assert(kBIter >= 1 && kBIter * kProd == 8 * BN, "producer split (B)");
+    static_assert(RESB || (kBIter >= 1 && kBIter * kProd == 8 * BN), "producer split (B)");
     static_assert(kCpt % 16 == 0, "epilogue columns");
 
     extern __shared__ uint8_t smem_raw[];
@@ -206,9 +212,10 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     auto corrf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * kSlots + a); };
     auto corre_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * kSlots + 2 + a); };
     const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * kSlots + 4);
+    const uint32_t bres_bar = bar_base + 8u * (2 * STAGES + 2 * kSlots + 5);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
-    int2 *taps = reinterpret_cast<int2 *>(smem + L::kTapOffset);
+    int2 *taps = reinterpret_cast<int2 *>(smem + L::tap_offset(p.KT));
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -256,6 +263,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             mbar_init(corre_bar(a), kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(bres_bar, NPROD);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -274,8 +282,12 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     pdl_wait();
     auto a_hi = [&](int s) { return smem_base + (uint32_t)(s * L::kStage); };
     auto a_lo = [&](int s) { return smem_base + (uint32_t)(s * L::kStage + kTfATile); };
-    auto b_hi = [&](int s) { return smem_base + (uint32_t)(s * L::kStage + 2 * kTfATile); };
-    auto b_lo = [&](int s) { return smem_base + (uint32_t)(s * L::kStage + 2 * kTfATile + L::kBTile); };
+    // weight tiles of stage s (streamed) or of reduction stage ks (resident)
+    auto b_hi = [&](int s) {
+        return RESB ? smem_base + (uint32_t)(L::kResBOffset + (size_t)s * 2 * L::kBTile)
+                    : smem_base + (uint32_t)(s * L::kStage + 2 * kTfATile);
+    };
+    auto b_lo = [&](int s) { return b_hi(s) + (uint32_t)L::kBTile; };
 
     if (warp >= kEpiWarps && warp < kMmaWarp) {
         // ---------------------------------------------------------- producers
@@ -368,7 +380,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 }
             }
 #pragma unroll
-            for (int it = 0; it < kBIter; ++it) {
+            for (int it = 0; it < (RESB ? 0 : kBIter); ++it) {
                 const int i = pt + it * kProd;
                 const int k = k0 + (i >> 3);
                 const int g = ks * kTfBK + (i & 7) * 4;
@@ -399,7 +411,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 st_shared_v4(a_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
             }
 #pragma unroll
-            for (int it = 0; it < kBIter; ++it) {
+            for (int it = 0; it < (RESB ? 0 : kBIter); ++it) {
                 const int i = pt + it * kProd;
                 const int kr = i >> 3, cj = i & 7;
                 uint32_t hi[4], lo[4];
@@ -419,6 +431,48 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             return true;
         };
 
+        if (RESB && nf > 0) {
+            // Split every stage's weights of this CTA's output-channel tile
+            // once (the tile is the same for all the CTA's tiles: the launch
+            // keeps gridDim a multiple of the tile count along K).
+            const int tn = (int)blockIdx.x % p.n_tiles_n;
+            const int kw0 = tn * BN;
+            const int total = p.KT * BN * 8;
+            for (int i0 = pt; i0 < total; i0 += kProd * 4) {
+                float vw[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kProd;
+                    const int ks = i / (BN * 8), r8 = i - ks * (BN * 8);
+                    const int k = kw0 + (r8 >> 3);
+                    const int g = ks * kTfBK + (r8 & 7) * 4;
+                    const int wrow = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
+                    const bool rowin = i < total && k < p.K;
+                    const float *wr = p.w + (rowin ? (int64_t)wrow * p.Kg + g : 0);
+                    if (p.w_vec) {
+                        ldg4_or_zero(wr, rowin && g < p.Kg, vw[u]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) vw[u][e] = ldg_or_zero(wr + e, rowin && g + e < p.Kg);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kProd;
+                    if (i >= total) break;
+                    const int ks = i / (BN * 8), r8 = i - ks * (BN * 8);
+                    const int kr = r8 >> 3, cj = r8 & 7;
+                    uint32_t hi[4], lo[4];
+                    split4(vw[u], hi, lo);
+                    const uint32_t off = (uint32_t)kr * 128u + ((((uint32_t)cj) ^ (uint32_t)(kr & 7)) << 4);
+                    st_shared_v4(b_hi(ks) + off, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(b_lo(ks) + off, lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bres_bar);
+        }
         float va0[kChunks][4], vb0[kBIter][4], va1[kChunks][4], vb1[kBIter][4];
         if (nf > 0) load(va0, vb0);
         for (int f = 0; f < nf && ok; f += 2) {
@@ -434,6 +488,8 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
         int stage = 0, slot = 0, acc = 0;
         uint32_t phase = 0, slot_phase = 0, acc_phase = 0;
         bool ok = true, any = false;
+        if (RESB && (int)blockIdx.x < p.total_tiles)
+            ok = mbar_wait(bres_bar, 0, abort_flag, p.status);   // the resident weights are split
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(corre_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
@@ -446,7 +502,8 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 tc_fence_after();
                 const uint32_t d_main = tmem_base + (uint32_t)(2 * BN + slot * BN);
                 const uint64_t ah = smem_desc_sw128(a_hi(stage)), al = smem_desc_sw128(a_lo(stage));
-                const uint64_t bh = smem_desc_sw128(b_hi(stage)), bl = smem_desc_sw128(b_lo(stage));
+                const uint64_t bh = smem_desc_sw128(b_hi(RESB ? ks : stage));
+                const uint64_t bl = smem_desc_sw128(b_lo(RESB ? ks : stage));
                 // advance 8 elements (32 bytes) along K inside the swizzled rows
 #pragma unroll
                 for (int kk = 0; kk < kTfBK / 8; ++kk)
@@ -610,10 +667,10 @@ bool ensure_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &done_mas
     return true;
 }
 
-template <int BN, int STAGES, int NPROD, bool LSTM>
+template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB>
 conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
                           cudaStream_t st) {
-    using L = TfSmem<BN, STAGES>;
+    using L = TfSmem<BN, STAGES, RESB>;
     TfParams p;
     p.x = static_cast<const float *>(t.x);
     p.w = static_cast<const float *>(t.w);
@@ -658,12 +715,16 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
     p.w_vec = (s.Kg % 4 == 0 && ((uintptr_t)t.w & 15) == 0) ? 1 : 0;
     p.y_vec = (p.nhwc && s.K % 4 == 0 && ((uintptr_t)t.y & 15) == 0) ? 1 : 0;
     const size_t bytes = L::bytes(p.KT);
-    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD, LSTM>;
+    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD, LSTM, RESB>;
     static std::atomic<uint64_t> attr_done{0};   // this instantiation's per-device flags
     // the attribute is set for the largest table this variant accepts
     if (!ensure_attr(reinterpret_cast<const void *>(kern), 227 * 1024, attr_done)) return CONV2D_ERR_CUDA;
     if (bytes > 227 * 1024) return CONV2D_ERR_UNSUPPORTED;
-    const int grid = pl.grid > 0 ? pl.grid : 1;
+    int grid = pl.grid > 0 ? pl.grid : 1;
+    if (RESB) {
+        // every CTA must keep one output-channel tile: gridDim % n_tiles_n == 0
+        grid = std::max(p.n_tiles_n, grid / p.n_tiles_n * p.n_tiles_n);
+    }
     if (launch_pdl(kern, dim3(grid), dim3(tf_threads<BN, NPROD>()), bytes, st, p) != cudaSuccess) {
         cudaGetLastError();
         return CONV2D_ERR_CUDA;
@@ -672,10 +733,10 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
 }
 
 // Only variants with 8 or more producer warps carry the ConvLSTM epilogue.
-template <int BN, int STAGES, int NPROD>
+template <int BN, int STAGES, int NPROD, bool RESB>
 conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
                                cudaStream_t st) {
-    if constexpr (NPROD >= 8) return launch_tf<BN, STAGES, NPROD, true>(s, pl, t, lstm, st);
+    if constexpr (NPROD >= 8) return launch_tf<BN, STAGES, NPROD, true, RESB>(s, pl, t, lstm, st);
     return CONV2D_ERR_UNSUPPORTED;
 }
 
@@ -684,16 +745,20 @@ conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t,
 // encoder layers (fp32 NCHW, 3x3 / 2x2 filters); the producers' gather is
 // latency-bound, so more producer warps per SM run a stage faster.  The
 // 3-stage variant leaves shared memory for the tap tables of long
-// reductions (C*R*S up to about 9,000); its stage time is an estimate.
-#define CONV2D_TF_VARIANTS(X) \
-    X(32, 5, 4, 1240)         \
-    X(64, 4, 4, 3850)         \
-    X(128, 3, 4, 5000)        \
-    X(32, 5, 8, 920)          \
-    X(64, 4, 8, 1370)         \
-    X(128, 3, 8, 3100)        \
-    X(64, 4, 16, 1030)        \
-    X(64, 3, 16, 1100)
+// reductions (C*R*S up to about 9,000).  The resident-weight variants split
+// the weights once per CTA (C*R*S up to about 350 at BN = 64); measured,
+// that saves only ~4 %: the activation gather sets the pace.
+#define CONV2D_TF_VARIANTS(X)     \
+    X(32, 5, 4, 1240, false)      \
+    X(64, 4, 4, 3850, false)      \
+    X(128, 3, 4, 5000, false)     \
+    X(32, 5, 8, 920, false)       \
+    X(64, 4, 8, 1370, false)      \
+    X(128, 3, 8, 3100, false)     \
+    X(64, 4, 16, 1100, false)     \
+    X(64, 3, 16, 1060, false)     \
+    X(64, 2, 16, 1060, true)      \
+    X(64, 3, 16, 1060, true)
 
 }  // namespace
 
@@ -702,7 +767,7 @@ bool tf_lstm_variant(int id) { return tf_variant(id).nprod >= 8; }
 
 int tf_num_variants() {
     int n = 0;
-#define X(vbn, vst, vnp, vns) ++n;
+#define X(vbn, vst, vnp, vns, vrb) ++n;
     CONV2D_TF_VARIANTS(X)
 #undef X
     return n;
@@ -710,9 +775,9 @@ int tf_num_variants() {
 
 TfTile tf_variant(int id) {
     int i = 0;
-    TfTile t{0, 0, 0, -1, 0};
-#define X(vbn, vst, vnp, vns)                        \
-    if (i == id) t = TfTile{vbn, vst, vnp, id, vns}; \
+    TfTile t{0, 0, 0, -1, 0, false};
+#define X(vbn, vst, vnp, vns, vrb)                        \
+    if (i == id) t = TfTile{vbn, vst, vnp, id, vns, vrb}; \
     ++i;
     CONV2D_TF_VARIANTS(X)
 #undef X
@@ -721,10 +786,13 @@ TfTile tf_variant(int id) {
 
 size_t tf_smem_bytes(const Shape &s, const TfTile &t) {
     const size_t kt = (size_t)((s.Kg + kTfBK - 1) / kTfBK);
-    const size_t stage = 2 * (size_t)kTfATile + 2 * (size_t)t.BN * kTfBK * 4;
+    const size_t btile = (size_t)t.BN * kTfBK * 4;
+    const size_t stage = 2 * (size_t)kTfATile + (t.resb ? 0 : 2 * btile);
     const size_t slots = t.BN >= 128 ? 2 : 6;
-    const size_t bars = (2 * (size_t)t.stages + 2 * slots + 5) * 8;
-    return ((size_t)t.stages * stage + bars + 16 + 15) / 16 * 16 + kt * kTfBK * 8 + 1024;
+    const size_t bars = (2 * (size_t)t.stages + 2 * slots + 6) * 8;
+    const size_t end = (size_t)t.stages * stage + bars + 16;
+    const size_t taps = t.resb ? (end + 1023) / 1024 * 1024 + kt * 2 * btile : (end + 15) / 16 * 16;
+    return taps + kt * kTfBK * 8 + 1024;
 }
 
 bool tf_shape_ok(const Shape &s) {
@@ -755,15 +823,16 @@ extern "C" int conv2d_tf_trace_dump(unsigned long long *out, unsigned int *count
 conv2d_status_t tf_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st,
                           const TfLstm *lstm) {
     if (lstm) {
-#define X(vbn, vst, vnp, vns)                                            \
-    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp)     \
-        return launch_tf_lstm<vbn, vst, vnp>(s, pl, t, lstm, st);
+#define X(vbn, vst, vnp, vns, vrb)                                                               \
+    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp && pl.tf.resb == vrb)        \
+        return launch_tf_lstm<vbn, vst, vnp, vrb>(s, pl, t, lstm, st);
         CONV2D_TF_VARIANTS(X)
 #undef X
         return CONV2D_ERR_INTERNAL;
     }
-#define X(vbn, vst, vnp, vns) \
-    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp) return launch_tf<vbn, vst, vnp, false>(s, pl, t, nullptr, st);
+#define X(vbn, vst, vnp, vns, vrb)                                                               \
+    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp && pl.tf.resb == vrb)        \
+        return launch_tf<vbn, vst, vnp, false, vrb>(s, pl, t, nullptr, st);
     CONV2D_TF_VARIANTS(X)
 #undef X
     return CONV2D_ERR_INTERNAL;

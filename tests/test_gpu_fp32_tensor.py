@@ -20,7 +20,7 @@ from parity import TOL, full_parity, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-N_VARIANTS = 8   # (BN, stages, producer warps) table of the library
+N_VARIANTS = 10   # (BN, stages, producer warps) table of the library
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -64,13 +64,22 @@ SHAPES = [
 @pytest.mark.parametrize("variant", range(N_VARIANTS))
 def test_forced_variants(variant, layout, variant_env):
     variant_env(variant)
+    ran = 0
     for i, (N, C, H, W, K, R, S, st, pad, dil, bias) in enumerate(SHAPES):
         spec = wl.ConvSpec(f"tf{i}", N, C, H, W, K, R, S, st, pad, dil, layout=layout, bias=bias)
         x, w, b = wl.random_inputs(spec, seed=300 + i)
-        y, d = run_gpu(spec, x, w, b, "tensor_core")
+        try:
+            y, d = run_gpu(spec, x, w, b, "tensor_core")
+        except conv2d.Conv2dError as e:
+            # resident-weight variants need C*R*S small enough for every
+            # stage's split weights to fit in shared memory
+            assert e.code == 2, e
+            continue
         assert "3xtf32" in d.plan(), d.plan()
         err = full_parity(spec, x, w, b, algo="tensor_core")
         assert err <= TOL["f32"], f"{spec} variant {variant}: err={err}"
+        ran += 1
+    assert ran >= 6
 
 
 @pytest.mark.parametrize("layout", ["NCHW", "NHWC"])
