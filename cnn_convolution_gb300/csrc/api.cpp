@@ -615,6 +615,66 @@ conv2d_status_t conv2d_deconv_forward(const void *x, const void *w, const void *
     if (!is_device_ptr(x, dev) || !is_device_ptr(w, dev) || !is_device_ptr(y, dev) ||
         (bias && !is_device_ptr(bias, dev)))
         return CONV2D_ERR_INVALID_ARG;
+    // Tensor cores first: split the outputs into the stride^2 residue classes
+    // (h mod stride, w mod stride).  Within a class every output takes the
+    // same filter rows r (those with r*dil = h + pad mod stride) and columns,
+    // reading input row i + e_r for class row i: a stride-1 gather, run on
+    // the 3xTF32 kernel with its outputs written in place into y.  A class
+    // without taps (only bias) or a shape the kernel cannot hold uses the
+    // gather kernel for the whole layer.
+    DevInfo d;
+    int dev2 = 0;
+    if (env_int("CONV2D_DECONV_TC") != 0 && R <= 8 && S <= 8 && device_info(&dev2, &d) == CONV2D_OK &&
+        d.cc_major == 10 && d.cc_minor == 3) {
+        struct Cls { int a, b; TfDeconv dv; Shape s; Plan p; };
+        Cls cls[64];
+        int nc = 0;
+        bool ok = stride * stride <= 64;
+        for (int a = 0; ok && a < stride; ++a) {
+            for (int b = 0; ok && b < stride; ++b) {
+                const int Pc = a < H ? (H - a + stride - 1) / stride : 0;
+                const int Qc = b < W ? (W - b + stride - 1) / stride : 0;
+                if (Pc == 0 || Qc == 0) continue;
+                TfDeconv dv{};
+                dv.H = H; dv.W = W; dv.a = a; dv.b = b; dv.st = stride; dv.R = R; dv.S = S;
+                for (int r = 0; r < R; ++r) {
+                    const int t = a + pad - r * dil;
+                    if (((t % stride) + stride) % stride == 0) {
+                        dv.r[dv.J] = r;
+                        dv.e[dv.J] = t >= 0 ? t / stride : -((-t) / stride);
+                        ++dv.J;
+                    }
+                }
+                for (int q = 0; q < S; ++q) {
+                    const int t = b + pad - q * dil;
+                    if (((t % stride) + stride) % stride == 0) {
+                        dv.s[dv.L] = q;
+                        dv.f[dv.L] = t >= 0 ? t / stride : -((-t) / stride);
+                        ++dv.L;
+                    }
+                }
+                if (dv.J == 0 || dv.L == 0) { ok = false; break; }
+                Shape cs{};
+                cs.N = N; cs.C = K; cs.H = P; cs.W = Q; cs.K = C; cs.R = dv.J; cs.S = dv.L;
+                cs.stride = 1; cs.pad = 0; cs.dil = 1; cs.P = Pc; cs.Q = Qc;
+                cs.dtype = CONV2D_F32; cs.layout = CONV2D_NCHW;
+                cs.M = (int64_t)N * Pc * Qc;
+                cs.Kg = (int64_t)K * dv.J * dv.L;
+                cs.elt = 4;
+                Plan pl{};
+                if (choose_tf(cs, d, &pl, nullptr) != CONV2D_OK) { ok = false; break; }
+                cls[nc++] = Cls{a, b, dv, cs, pl};
+            }
+        }
+        if (ok && nc > 0) {
+            for (int i = 0; i < nc; ++i) {
+                const conv2d_status_t st2 = tf_launch(cls[i].s, cls[i].p, Tensors{x, w, bias, y}, stream,
+                                                      nullptr, &cls[i].dv);
+                if (st2 != CONV2D_OK) return st2;
+            }
+            return CONV2D_OK;
+        }
+    }
     return dv_launch(static_cast<const float *>(x), static_cast<const float *>(w),
                      static_cast<const float *>(bias), static_cast<float *>(y), N, K, P, Q, C, R, S,
                      H, W, stride, pad, dil, stream);

@@ -116,9 +116,16 @@ struct TfLstm {
     float *h_next;
     int64_t h_img;      // elements between images of h_next
 };
+// One residue class of a transposed convolution on the 3xTF32 kernel: the
+// outputs (a + st*i, b + st*j) of y [N][C][H][W] gather input pixels
+// (i + e[rj], j + f[sl]) with filter taps (r[rj], s[sl]), rj < J, sl < L.
+struct TfDeconv {
+    int H, W, a, b, st, J, L, R, S;
+    int e[8], f[8], r[8], s[8];
+};
 bool tf_lstm_variant(int id);
 conv2d_status_t tf_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st,
-                          const TfLstm *lstm = nullptr);
+                          const TfLstm *lstm = nullptr, const TfDeconv *dv = nullptr);
 
 // Transposed convolution, fp32 NCHW (arguments validated by the caller).
 size_t dv_smem_bytes(int H, int W, int P, int Q, int R, int S, int stride, int dil);

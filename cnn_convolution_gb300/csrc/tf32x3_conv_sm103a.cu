@@ -131,6 +131,12 @@ struct TfParams {
     // read from gate-major weight rows in interleaved order (column 4u+gate is
     // weight row gate*Ch + u), so that each group of 4 columns holds the
     // i, f, o, g pre-activations of hidden unit u
+    // transposed-convolution residue class (dv = 1): the GEMM pixels are the
+    // outputs (a + st*i, b + st*j) of y [N][K][dv_H][dv_W]; the reduction index
+    // g = (k_in, rj, sl) takes filter tap (dv_r[rj], dv_s[sl]) of w [K_in][K][R][S]
+    // and input pixel (i + dv_e[rj], j + dv_f[sl]) of x [N][K_in][H][W]
+    int dv, dv_H, dv_W, dv_a, dv_b, dv_st, dv_J, dv_L, dv_R, dv_S;
+    int dv_e[8], dv_f[8], dv_r[8], dv_s[8];
     int lstm_ch;
     const float *c_prev;   // [N][Ch][P][Q]
     float *c_next;         // [N][Ch][P][Q]
@@ -168,7 +174,9 @@ struct TfSmem {
     static constexpr size_t tap_offset(int kt) {
         return RESB ? kResBOffset + (size_t)kt * 2 * kBTile : (kBarOffset + kBarBytes + 16 + 15) / 16 * 16;
     }
-    static constexpr size_t bytes(int kt) { return tap_offset(kt) + (size_t)kt * kTfBK * 8 + 1024; }
+    // tap table (8 bytes per reduction index), then the weight-offset table of
+    // transposed convolutions (4 bytes per index)
+    static constexpr size_t bytes(int kt) { return tap_offset(kt) + (size_t)kt * kTfBK * 12 + 1024; }
 };
 
 template <int BN> constexpr int tf_epi_warps() { return BN >= 64 ? 8 : 4; }
@@ -216,6 +224,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
     int2 *taps = reinterpret_cast<int2 *>(smem + L::tap_offset(p.KT));
+    int *wtaps = reinterpret_cast<int *>(taps + p.KT * kTfBK);     // transposed convolution only
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -230,6 +239,24 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     // entries past Kg carry a row offset of -32768, which no pixel reaches.
     for (int g = threadIdx.x; g < p.KT * kTfBK; g += blockDim.x) {
         int2 t;
+        if (p.dv) {
+            // transposed convolution: g = (k_in, rj, sl); offsets may be negative
+            int wo = 0;
+            t.x = 0;
+            t.y = (int)0x80000000u;
+            if (g < p.Kg) {
+                const int JL = p.dv_J * p.dv_L;
+                const int k = g / JL, rs = g - k * JL;
+                const int rj = rs / p.dv_L, sl = rs - rj * p.dv_L;
+                const int dh = p.dv_e[rj], dw = p.dv_f[sl];
+                t.x = (k * p.H + dh) * p.W + dw;
+                t.y = (dh << 16) | (dw & 0xFFFF);
+                wo = (k * p.K * p.dv_R + p.dv_r[rj]) * p.dv_S + p.dv_s[sl];
+            }
+            taps[g] = t;
+            wtaps[g] = wo;
+            continue;
+        }
         if (g < p.Kg) {
             int c, rs;
             if (p.nhwc) {
@@ -386,7 +413,14 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 const int g = ks * kTfBK + (i & 7) * 4;
                 const int wrow = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
                 const float *wr = p.w + (int64_t)wrow * p.Kg + g;
-                if (p.w_vec) {
+                if (p.dv) {
+                    // w [K_in][K][R][S]: element (k, g) at wtaps[g] + k*R*S
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const bool in = k < p.K && g + e < p.Kg;
+                        vb[it][e] = ldg_or_zero(p.w + (in ? wtaps[g + e] + k * p.dv_R * p.dv_S : 0), in);
+                    }
+                } else if (p.w_vec) {
                     ldg4_or_zero(wr, k < p.K && g < p.Kg, vb[it]);
                 } else {
 #pragma unroll
@@ -449,7 +483,13 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                     const int wrow = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
                     const bool rowin = i < total && k < p.K;
                     const float *wr = p.w + (rowin ? (int64_t)wrow * p.Kg + g : 0);
-                    if (p.w_vec) {
+                    if (p.dv) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const bool in = rowin && g + e < p.Kg;
+                            vw[u][e] = ldg_or_zero(p.w + (in ? wtaps[g + e] + k * p.dv_R * p.dv_S : 0), in);
+                        }
+                    } else if (p.w_vec) {
                         ldg4_or_zero(wr, rowin && g < p.Kg, vw[u]);
                     } else {
 #pragma unroll
@@ -636,11 +676,22 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 }
             } else {
                 const int64_t n = m / p.PQ;
-                float *yr = p.y + n * p.K * p.PQ + (m - n * p.PQ);
+                float *yr;
+                int64_t kst;
+                if (p.dv) {
+                    // output (a + st*i, b + st*j) of the residue class
+                    const int rem = (int)(m - n * p.PQ);
+                    const int i = rem / p.Q, jj = rem - i * p.Q;
+                    kst = (int64_t)p.dv_H * p.dv_W;
+                    yr = p.y + n * p.K * kst + (int64_t)(p.dv_a + p.dv_st * i) * p.dv_W + p.dv_b + p.dv_st * jj;
+                } else {
+                    kst = p.PQ;
+                    yr = p.y + n * p.K * p.PQ + (m - n * p.PQ);
+                }
 #pragma unroll
                 for (int j = 0; j < kCpt; ++j) {
                     const int k = kb + j;
-                    if (k < p.K) yr[(int64_t)k * p.PQ] = a[j] + (p.bias ? __ldg(p.bias + k) : 0.f);
+                    if (k < p.K) yr[(int64_t)k * kst] = a[j] + (p.bias ? __ldg(p.bias + k) : 0.f);
                 }
             }
         }
@@ -669,7 +720,7 @@ bool ensure_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &done_mas
 
 template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB>
 conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
-                          cudaStream_t st) {
+                          cudaStream_t st, const TfDeconv *dv = nullptr) {
     using L = TfSmem<BN, STAGES, RESB>;
     TfParams p;
     p.x = static_cast<const float *>(t.x);
@@ -699,6 +750,17 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
     p.nhwc = s.layout == CONV2D_NHWC ? 1 : 0;
     p.R = s.R;
     p.rs_mask = s.R * s.S <= 63 ? 1 : 0;
+    p.dv = 0;
+    if (dv) {
+        p.dv = 1;
+        p.dv_H = dv->H; p.dv_W = dv->W; p.dv_a = dv->a; p.dv_b = dv->b; p.dv_st = dv->st;
+        p.dv_J = dv->J; p.dv_L = dv->L; p.dv_R = dv->R; p.dv_S = dv->S;
+        for (int i = 0; i < 8; ++i) {
+            p.dv_e[i] = dv->e[i]; p.dv_f[i] = dv->f[i]; p.dv_r[i] = dv->r[i]; p.dv_s[i] = dv->s[i];
+        }
+        p.rs_mask = 0;
+        p.w_vec = 0;
+    }
     p.lstm_ch = 0;
     p.c_prev = nullptr;
     p.c_next = nullptr;
@@ -736,7 +798,7 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
 template <int BN, int STAGES, int NPROD, bool RESB>
 conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
                                cudaStream_t st) {
-    if constexpr (NPROD >= 8) return launch_tf<BN, STAGES, NPROD, true, RESB>(s, pl, t, lstm, st);
+    if constexpr (NPROD >= 8) return launch_tf<BN, STAGES, NPROD, true, RESB>(s, pl, t, lstm, st, nullptr);
     return CONV2D_ERR_UNSUPPORTED;
 }
 
@@ -792,7 +854,7 @@ size_t tf_smem_bytes(const Shape &s, const TfTile &t) {
     const size_t bars = (2 * (size_t)t.stages + 2 * slots + 6) * 8;
     const size_t end = (size_t)t.stages * stage + bars + 16;
     const size_t taps = t.resb ? (end + 1023) / 1024 * 1024 + kt * 2 * btile : (end + 15) / 16 * 16;
-    return taps + kt * kTfBK * 8 + 1024;
+    return taps + kt * kTfBK * 12 + 1024;
 }
 
 bool tf_shape_ok(const Shape &s) {
@@ -821,7 +883,15 @@ extern "C" int conv2d_tf_trace_dump(unsigned long long *out, unsigned int *count
 #endif
 
 conv2d_status_t tf_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st,
-                          const TfLstm *lstm) {
+                          const TfLstm *lstm, const TfDeconv *dv) {
+    if (dv) {
+#define X(vbn, vst, vnp, vns, vrb)                                                               \
+    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp && pl.tf.resb == vrb)        \
+        return launch_tf<vbn, vst, vnp, false, vrb>(s, pl, t, nullptr, st, dv);
+        CONV2D_TF_VARIANTS(X)
+#undef X
+        return CONV2D_ERR_INTERNAL;
+    }
     if (lstm) {
 #define X(vbn, vst, vnp, vns, vrb)                                                               \
     if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp && pl.tf.resb == vrb)        \

@@ -55,13 +55,29 @@ CASES = [
 ]
 
 
+@pytest.fixture(params=["tensor_core", "gather"])
+def deconv_path(request):
+    """The default path (3xTF32 tensor-core kernel per output residue class)
+    and the gather kernel (CONV2D_DECONV_TC=0)."""
+    import os
+    if request.param == "gather":
+        os.environ["CONV2D_DECONV_TC"] = "0"
+    yield request.param
+    os.environ.pop("CONV2D_DECONV_TC", None)
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
-def test_deconv_parity(case):
+def test_deconv_parity(case, deconv_path):
     err = _run(*case, seed=sum(case))
-    assert err <= TOL["f32"], f"{case}: err={err}"
+    assert err <= TOL["f32"], f"{case} ({deconv_path}): err={err}"
 
 
-def test_deconv_without_bias_and_all_positive():
+def test_deconv_class_without_taps_uses_the_gather_kernel():
+    # stride 2 with a 1x1 filter: odd output rows receive no tap (bias only)
+    assert _run(2, 4, 5, 5, 3, 1, 1, 2, 0, 1, 1, seed=11) <= TOL["f32"]
+
+
+def test_deconv_without_bias_and_all_positive(deconv_path):
     assert _run(2, 16, 6, 6, 8, 3, 3, 2, 1, 1, 1, bias=False, seed=3) <= TOL["f32"]
     assert _run(2, 64, 8, 8, 16, 3, 3, 2, 1, 1, 0, seed=4, dist="positive") <= TOL["f32"]
 
