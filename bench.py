@@ -419,7 +419,7 @@ def bench_main(args):
     sig = signature_stage(device, flush, descs, ws, bs, outs, peaks, args, world)
 
     cells = convlstm_cells(device, flush, peaks, iters=max(5, args.steps // 4)) if rank == 0 else []
-    decoder = decoder_layers(device, flush, iters=max(5, args.steps // 4)) if rank == 0 else []
+    decoder = decoder_layers(device, flush, peaks, iters=max(5, args.steps // 4)) if rank == 0 else []
 
     extra = []
     if not args.no_tensor_core and rank == 0:
@@ -543,7 +543,7 @@ def convlstm_cells(device, flush, peaks, iters, n=64):
     return out
 
 
-def decoder_layers(device, flush, iters, n=256):
+def decoder_layers(device, flush, peaks, iters, n=256):
     """The MSCRED decoder's transposed convolutions (fp32 NCHW, batch n), each
     timed alone after an L2 flush.  FLOPs count the products that land inside
     the output: 2 * N * K * C * (valid (p, r) pairs) * (valid (q, s) pairs)."""
@@ -553,7 +553,6 @@ def decoder_layers(device, flush, iters, n=256):
               ("deconv2_128to32_15to30_3x3s2", 128, 15, 32, 3, 2, 1, 1),
               ("deconv1_64to3_30to30_3x3s1", 64, 30, 3, 3, 1, 1, 0)]
     out = []
-    alu = fp32_alu_peak_tflops()
     g = torch.Generator().manual_seed(7)
     for name, K, P, C, R, st, pad, op in shapes:
         x = torch.randn((n, K, P, P), generator=g).to(device)
@@ -572,7 +571,9 @@ def decoder_layers(device, flush, iters, n=256):
         tf = fl / (t * 1e-3) / 1e12
         gbs = by / (t * 1e-3) / 1e9
         out.append({"layer": name, "us": round(t * 1e3, 2), "tflops": round(tf, 2),
-                    "alu_frac": round(tf / alu, 4), "hbm_gbs": round(gbs, 1)})
+                    "path": "3xTF32 tensor cores, one launch per output residue class",
+                    "bound": "tensor", "frac": round(tf / fp32_3xtf32_peak_tflops(peaks), 4),
+                    "hbm_gbs": round(gbs, 1)})
     return out
 
 
