@@ -261,6 +261,16 @@ cc_conv_kernel(const CcParams p) {
     }
 
     // Epilogue: stage the tile in shared memory, then write coalesced rows.
+    // The tile's bias values go to shared memory first: a global load placed
+    // after a global store through a possibly aliasing pointer waits for it,
+    // so bias loads inside the store loops would each cost a full latency.
+    // (The barrier before the stores below publishes s_bias.)
+    __shared__ float s_bias[BN];
+    {
+        const T *bias_g = static_cast<const T *>(p.bias);
+        for (int j = tid; j < BN; j += NT)
+            s_bias[j] = (bias_g && n0 + j < p.K) ? to_f32<T>(bias_g[n0 + j]) : 0.f;
+    }
     float *cs = smem;
     if constexpr (SPLIT > 1) {
         // Partial tile -> own shared memory as cs[nl][ml]; cluster barrier;
@@ -279,7 +289,6 @@ cc_conv_kernel(const CcParams p) {
         const float *parts[SPLIT];
 #pragma unroll
         for (int r = 0; r < SPLIT; ++r) parts[r] = cluster.map_shared_rank(cs, r);
-        const T *bias = static_cast<const T *>(p.bias);
         T *y = static_cast<T *>(p.y);
         constexpr int ROWS = BM / SPLIT;
         const int lo = split_rank * ROWS;
@@ -291,7 +300,7 @@ cc_conv_kernel(const CcParams p) {
                 float v = 0.f;
 #pragma unroll
                 for (int r = 0; r < SPLIT; ++r) v += parts[r][nl * CS + mi];
-                if (bias) v += to_f32<T>(bias[k]);
+                v += s_bias[nl];
                 if (LAYOUT == CONV2D_NCHW) {
                     const int n = (int)(m / PQ);
                     const int pq = (int)(m - (int64_t)n * PQ);
@@ -304,7 +313,6 @@ cc_conv_kernel(const CcParams p) {
         cluster.sync();   // peers may still be reading this CTA's partial tile
         return;
     }
-    const T *bias = static_cast<const T *>(p.bias);
     T *y = static_cast<T *>(p.y);
     if (LAYOUT == CONV2D_NCHW) {
         // cs[nl][ml]: m contiguous, as in y[n][k][p][q].
@@ -322,8 +330,7 @@ cc_conv_kernel(const CcParams p) {
             for (int nl = kl0; nl < BN; nl += TPB) {
                 const int k = n0 + nl;
                 if (k >= p.K) break;
-                float v = cs[nl * CS + ml];
-                if (bias) v += to_f32<T>(bias[k]);
+                const float v = cs[nl * CS + ml] + s_bias[nl];
                 y[ybase + (int64_t)k * PQ] = from_f32<T>(v);
             }
         }
@@ -344,8 +351,7 @@ cc_conv_kernel(const CcParams p) {
             const int64_t m = m0 + mi;
             const int k = n0 + nl;
             if (m < p.M && k < p.K) {
-                float v = cs[mi * CS + nl];
-                if (bias) v += to_f32<T>(bias[k]);
+                const float v = cs[mi * CS + nl] + s_bias[nl];
                 y[m * p.K + k] = from_f32<T>(v);
             }
         }

@@ -231,10 +231,17 @@ __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p)
         }
     }
     if (!active) return;
+    if (p.bias) {                              // all bias loads before the first store
+        float bv[kDvC];
+#pragma unroll
+        for (int j = 0; j < kDvC; ++j) bv[j] = sm103a::ldg_or_zero(p.bias + (c0 + j < p.C ? c0 + j : 0), c0 + j < p.C);
+#pragma unroll
+        for (int j = 0; j < kDvC; ++j) acc[j] += bv[j];
+    }
     float *yp = p.y + ((int64_t)n * p.C + c0) * HW + pix;
 #pragma unroll
     for (int j = 0; j < kDvC; ++j) {
-        if (c0 + j < p.C) yp[(int64_t)j * HW] = acc[j] + (p.bias ? __ldg(p.bias + c0 + j) : 0.f);
+        if (c0 + j < p.C) yp[(int64_t)j * HW] = acc[j];
     }
 }
 

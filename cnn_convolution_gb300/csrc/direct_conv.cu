@@ -158,8 +158,18 @@ __global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcPara
                 }
             }
         }
-        // + bias, store
+        // + bias (all loads before the first store), store
         const int kn = min(kDcKc, p.K - kc);
+        if (p.bias) {
+            float bv[kDcKc];
+#pragma unroll
+            for (int j = 0; j < kDcKc; ++j) bv[j] = sm103a::ldg_or_zero(p.bias + (j < kn ? kc + j : 0), j < kn);
+#pragma unroll
+            for (int j = 0; j < kDcKc; ++j) {
+                acc_a[j] += bv[j];
+                acc_b[j] += bv[j];
+            }
+        }
         if (p.nhwc) {
             float *ya = p.y + (((int64_t)n * p.P + pa) * p.Q + q) * p.K + kc;
             float *yb = ya + (int64_t)p.Q * p.K;
@@ -167,21 +177,17 @@ __global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcPara
 #pragma unroll
             for (int j = 0; j < kDcKc; j += 4) {
                 if (j >= kn) break;
-                float bj[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    bj[e] = (p.bias && j + e < kn) ? __ldg(p.bias + kc + j + e) : 0.f;
                 if (vec) {
                     if (va) *reinterpret_cast<float4 *>(ya + j) =
-                        make_float4(acc_a[j] + bj[0], acc_a[j + 1] + bj[1], acc_a[j + 2] + bj[2], acc_a[j + 3] + bj[3]);
+                        make_float4(acc_a[j], acc_a[j + 1], acc_a[j + 2], acc_a[j + 3]);
                     if (vb) *reinterpret_cast<float4 *>(yb + j) =
-                        make_float4(acc_b[j] + bj[0], acc_b[j + 1] + bj[1], acc_b[j + 2] + bj[2], acc_b[j + 3] + bj[3]);
+                        make_float4(acc_b[j], acc_b[j + 1], acc_b[j + 2], acc_b[j + 3]);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         if (j + e < kn) {
-                            if (va) ya[j + e] = acc_a[j + e] + bj[e];
-                            if (vb) yb[j + e] = acc_b[j + e] + bj[e];
+                            if (va) ya[j + e] = acc_a[j + e];
+                            if (vb) yb[j + e] = acc_b[j + e];
                         }
                     }
                 }
@@ -192,9 +198,8 @@ __global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcPara
 #pragma unroll
             for (int j = 0; j < kDcKc; ++j) {
                 if (j < kn) {
-                    const float bj = p.bias ? __ldg(p.bias + kc + j) : 0.f;
-                    if (va) ya[(int64_t)j * PQ] = acc_a[j] + bj;
-                    if (vb) yb[(int64_t)j * PQ] = acc_b[j] + bj;
+                    if (va) ya[(int64_t)j * PQ] = acc_a[j];
+                    if (vb) yb[(int64_t)j * PQ] = acc_b[j];
                 }
             }
         }

@@ -614,6 +614,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             if (lane == 0) okw = mbar_wait(corrf_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
             okw = __shfl_sync(0xffffffffu, okw, 0);
             if (!okw) break;
+            if (threadIdx.x == 0) TF_TRACE(2, 10);
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < kCpt; c += 16) {
@@ -630,25 +631,43 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
             const int64_t m = (int64_t)tm * kTfBM + row;
-            if (m >= p.M) continue;
             const int kb = tn * BN + col0;
+            // Add the bias before the first store: loads that follow stores
+            // through possibly aliasing pointers cannot be moved ahead of
+            // them, so interleaved they would cost a load latency per column.
+            if (p.bias) {
+                float bv[kCpt];
+#pragma unroll
+                for (int j = 0; j < kCpt; ++j) {
+                    const int k = kb + j;
+                    const int bk = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
+                    bv[j] = ldg_or_zero(p.bias + (k < p.K ? bk : 0), k < p.K);
+                }
+#pragma unroll
+                for (int j = 0; j < kCpt; ++j) a[j] += bv[j];
+            }
+            if (m >= p.M) continue;
             if (LSTM) {
                 // gates -> state update: c = f*c_prev + i*g, h = o*tanh(c)
                 const int64_t n = m / p.PQ;
                 const int64_t pq = m - n * p.PQ;
                 const int Ch = p.lstm_ch;
+                // the previous cell state of this pixel's hidden units, all
+                // loaded before the first store
+                float cp[kCpt / 4];
+#pragma unroll
+                for (int j = 0; j < kCpt; j += 4) {
+                    const int u = (kb + j) >> 2;
+                    cp[j / 4] = ldg_or_zero(p.c_prev + (u < Ch ? (n * Ch + u) * p.PQ + pq : 0), u < Ch);
+                }
 #pragma unroll
                 for (int j = 0; j < kCpt; j += 4) {
                     const int u = (kb + j) >> 2;
                     if (u >= Ch) break;
-                    float z[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        z[e] = a[j + e] + (p.bias ? __ldg(p.bias + e * Ch + u) : 0.f);
-                    const float ig = sigmoidf_(z[0]), fg = sigmoidf_(z[1]), og = sigmoidf_(z[2]);
-                    const float gg = tanhf(z[3]);
+                    const float ig = sigmoidf_(a[j]), fg = sigmoidf_(a[j + 1]), og = sigmoidf_(a[j + 2]);
+                    const float gg = tanhf(a[j + 3]);
                     const int64_t ci = (n * Ch + u) * p.PQ + pq;
-                    const float c = fg * __ldg(p.c_prev + ci) + ig * gg;
+                    const float c = fg * cp[j / 4] + ig * gg;
                     p.c_next[ci] = c;
                     p.h_next[n * p.h_img + (int64_t)u * p.PQ + pq] = og * tanhf(c);
                 }
@@ -660,10 +679,10 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                         const int k = kb + j;
                         if (k < p.K) {
                             float4 o;
-                            o.x = a[j] + (p.bias ? __ldg(p.bias + k) : 0.f);
-                            o.y = a[j + 1] + (p.bias ? __ldg(p.bias + k + 1) : 0.f);
-                            o.z = a[j + 2] + (p.bias ? __ldg(p.bias + k + 2) : 0.f);
-                            o.w = a[j + 3] + (p.bias ? __ldg(p.bias + k + 3) : 0.f);
+                            o.x = a[j];
+                            o.y = a[j + 1];
+                            o.z = a[j + 2];
+                            o.w = a[j + 3];
                             *reinterpret_cast<float4 *>(yr + k) = o;
                         }
                     }
@@ -671,7 +690,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
 #pragma unroll
                     for (int j = 0; j < kCpt; ++j) {
                         const int k = kb + j;
-                        if (k < p.K) yr[k] = a[j] + (p.bias ? __ldg(p.bias + k) : 0.f);
+                        if (k < p.K) yr[k] = a[j];
                     }
                 }
             } else {
@@ -691,9 +710,10 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
 #pragma unroll
                 for (int j = 0; j < kCpt; ++j) {
                     const int k = kb + j;
-                    if (k < p.K) yr[(int64_t)k * kst] = a[j] + (p.bias ? __ldg(p.bias + k) : 0.f);
+                    if (k < p.K) yr[(int64_t)k * kst] = a[j];
                 }
             }
+            if (threadIdx.x == 0) TF_TRACE(2, 11);
         }
     }
 
