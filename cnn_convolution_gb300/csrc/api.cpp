@@ -552,8 +552,8 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
         std::snprintf(buf, len, "cuda_core direct ffma block=16x32px kc=32 threads=256 grid=%d smem=%zu",
                       p.grid, p.smem_bytes);
     else if (p.algo == Algo::Tf32x3)
-        std::snprintf(buf, len, "tensor_core tcgen05 3xtf32 BM=128 BN=%d BK=32 stages=%d producers=%d%s grid=%d smem=%zu",
-                      p.tf.BN, p.tf.stages, p.tf.nprod * 32, p.tf.resb ? " resident-w" : "", p.grid,
+        std::snprintf(buf, len, "tensor_core tcgen05 3xtf32 BM=128 BN=%d BK=32 stages=%d producers=%d groups=%d%s grid=%d smem=%zu",
+                      p.tf.BN, p.tf.stages, p.tf.nprod * 32, p.tf.ngrp, p.tf.resb ? " resident-w" : "", p.grid,
                       p.smem_bytes);
     else
         std::snprintf(buf, len, "cuda_core ffma BM=%d BN=%d BK=%d TM=%d TN=%d threads=%d split=%d grid=%d smem=%zu",

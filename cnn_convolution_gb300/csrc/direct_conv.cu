@@ -42,7 +42,18 @@ struct DcParams {
     int Kp;               // K rounded up to kDcKc (row length of the transposed weights)
     int tiles_p, tiles_q;
     int nhwc;
+    // reciprocals for the staging index arithmetic (see fdiv): IW, IH, Kp, R*S
+    uint32_t m_iw, m_ih, m_kp, m_rs;
 };
+
+// n / d for 0 <= n with n * d < 2^32, given m = floor(2^32 / d) + 1 (d >= 2)
+// or m = 0 (d = 1): floor(n * m / 2^32) = floor(n/d + n*e/(d * 2^32)) with
+// m*d = 2^32 + e, 0 < e <= d, and the second term stays below 1/d.  The
+// staged patch and weight table are bounded by the shared-memory limit, so
+// every index and divisor here meets the condition.
+__device__ __forceinline__ int fdiv(int n, uint32_t m) {
+    return m ? (int)__umulhi((unsigned)n, m) : n;
+}
 
 // RT, ST: compile-time filter size (0 = read from the parameters).
 template <int RT, int ST>
@@ -72,20 +83,21 @@ __global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcPara
     // predicated loads before it stores any of them, so their latencies
     // overlap instead of adding up.
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const float *ximg = p.x + (int64_t)n * p.C * p.H * p.W;   // this image (C*H*W < 2^31)
     for (int i0 = 0; i0 < patch; i0 += kDcThreads * kDcBatch) {
         float v[kDcBatch];
 #pragma unroll
         for (int j = 0; j < kDcBatch; ++j) {
-            const int i = i0 + j * kDcThreads + (int)threadIdx.x;
-            const int iw = i % p.IW;
-            const int r2 = i / p.IW;
-            const int ih = r2 % p.IH;
-            const int c = r2 / p.IH;
+            const int i = min(i0 + j * kDcThreads + (int)threadIdx.x, patch);
+            const int r2 = fdiv(i, p.m_iw);
+            const int iw = i - r2 * p.IW;
+            const int c = fdiv(r2, p.m_ih);
+            const int ih = r2 - c * p.IH;
             const int h = h0 + ih, wc = w0 + iw;
             const bool in = i < patch && (unsigned)h < (unsigned)p.H && (unsigned)wc < (unsigned)p.W;
-            const int64_t off = p.nhwc ? (((int64_t)n * p.H + h) * p.W + wc) * p.C + c
-                                       : (((int64_t)n * p.C + c) * p.H + h) * p.W + wc;
-            v[j] = sm103a::ldg_or_zero(p.x + (in ? off : 0), in);
+            const int hh = in ? h : 0, ww = in ? wc : 0, cc = in ? c : 0;   // in-image: no overflow
+            const int off = p.nhwc ? (hh * p.W + ww) * p.C + cc : (cc * p.H + hh) * p.W + ww;
+            v[j] = sm103a::ldg_or_zero(ximg + off, in);
         }
 #pragma unroll
         for (int j = 0; j < kDcBatch; ++j) {
@@ -98,11 +110,11 @@ __global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcPara
         float v[kDcBatch];
 #pragma unroll
         for (int j = 0; j < kDcBatch; ++j) {
-            const int i = i0 + j * kDcThreads + (int)threadIdx.x;
-            const int k = i % p.Kp, g = i / p.Kp;
+            const int i = min(i0 + j * kDcThreads + (int)threadIdx.x, wn);
+            const int g = fdiv(i, p.m_kp), k = i - g * p.Kp;
             int woff = g;                       // offset of w[k = 0][g]
             if (p.nhwc) {
-                const int c = g / RS, rs = g - c * RS;
+                const int c = fdiv(g, p.m_rs), rs = g - c * RS;
                 woff = rs * p.C + c;
             }
             const bool in = i < wn && k < p.K;
@@ -227,8 +239,13 @@ bool dc_shape_ok(const Shape &s) {
         return false;
     if ((int64_t)s.N * ((s.P + kDcRows - 1) / kDcRows) * ((s.Q + kDcCols - 1) / kDcCols) > INT32_MAX)
         return false;
+    if ((int64_t)s.C * s.H * s.W >= ((int64_t)1 << 31)) return false;   // 32-bit offsets within an image
     return dc_smem_bytes(s) <= 96 * 1024;
 }
+
+namespace {
+uint32_t recip(int d) { return d <= 1 ? 0u : (uint32_t)((((uint64_t)1) << 32) / (uint64_t)d + 1); }
+}  // namespace
 
 int dc_grid(const Shape &s) {
     return (int)((int64_t)s.N * ((s.P + kDcRows - 1) / kDcRows) * ((s.Q + kDcCols - 1) / kDcCols));
@@ -249,6 +266,10 @@ conv2d_status_t dc_launch(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.tiles_p = (s.P + kDcRows - 1) / kDcRows;
     p.tiles_q = (s.Q + kDcCols - 1) / kDcCols;
     p.nhwc = s.layout == CONV2D_NHWC ? 1 : 0;
+    p.m_iw = recip(p.IW);
+    p.m_ih = recip(p.IH);
+    p.m_kp = recip(p.Kp);
+    p.m_rs = recip(s.R * s.S);
     const size_t bytes = dc_smem_bytes(s);
     void (*kern)(DcParams);
     if (s.R == 3 && s.S == 3) kern = direct_conv_kernel<3, 3>;

@@ -53,6 +53,7 @@ struct TfTile {
     int id;          // index into the variant table
     int stage_ns;    // measured time of one 32-element stage of one tile (GB300)
     bool resb;       // the split weights of the CTA's output-channel tile stay resident
+    int ngrp;        // producer groups: stage f is filled by group f % ngrp
 };
 
 enum class Algo { CudaCore, TensorCore, Tf32x3, Direct };

@@ -189,7 +189,18 @@ template <int BN, int NPROD> constexpr int tf_threads() { return 32 * (tf_epi_wa
 // tensor memory over one stage only (4 MMAs of K=8) and the stage sums are
 // added in fp32 registers by the epilogue warps; the correction terms, 2^-11
 // smaller, stay in one accumulator per tile.
-template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB>
+//
+// Producer groups: the NPROD producer warps form NGRP groups, and stage f of
+// the CTA's sequence is filled by group f % NGRP alone.  A producer warp's
+// pass over a stage is a chain of latencies (tap reads feeding the load
+// addresses, the wait for the stage to be free, the stores, the proxy fence
+// and the arrival) that more warps on the same stage do not shorten; with
+// two groups, two stages are filled at once and each warp pays the chain
+// once per two stages for twice the elements.  With one group a warp issues
+// the loads of its next stage before storing the current one; with several,
+// it issues its loads and then waits for the stage to be free, so that wait
+// overlaps the loads' latency.
+template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB, int NGRP>
 __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel(const TfParams p) {
     using L = TfSmem<BN, STAGES, RESB>;
     using TM = TfTmem<BN>;
@@ -201,10 +212,13 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     constexpr int kCpt = BN * 4 / kEpiWarps;                     // accumulator columns per epilogue thread
     constexpr int kProd = 32 * NPROD;                            // producer threads
     constexpr int kMmaWarp = kEpiWarps + NPROD;
-    constexpr int kChunks = 8 * kTfBM / kProd;                   // A chunks (4 values) per thread per stage
-    constexpr int kBIter = BN * 8 / kProd;                       // B chunks per thread per stage
-    static_assert(kChunks >= 1 && kChunks * kProd == 8 * kTfBM, "producer split (A)");
-    static_assert(RESB || (kBIter >= 1 && kBIter * kProd == 8 * BN), "producer split (B)");
+    static_assert(NGRP >= 1 && NPROD % NGRP == 0, "producer groups");
+    constexpr int kGrpWarps = NPROD / NGRP;                      // producer warps per group
+    constexpr int kGrpThr = 32 * kGrpWarps;
+    constexpr int kChunks = 8 * kTfBM / kGrpThr;                 // A chunks (4 values) per thread per stage
+    constexpr int kBIter = BN * 8 / kGrpThr;                     // B chunks per thread per stage
+    static_assert(kChunks >= 1 && kChunks * kGrpThr == 8 * kTfBM, "producer split (A)");
+    static_assert(RESB || (kBIter >= 1 && kBIter * kGrpThr == 8 * BN), "producer split (B)");
     static_assert(kCpt % 16 == 0, "epilogue columns");
 
     extern __shared__ uint8_t smem_raw[];
@@ -278,7 +292,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), NPROD);          // one arrival per producer warp
+            mbar_init(full_bar(s), kGrpWarps);      // one arrival per warp of the filling group
             mbar_init(empty_bar(s), 1);
         }
         for (int s = 0; s < kSlots; ++s) {
@@ -318,22 +332,23 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
 
     if (warp >= kEpiWarps && warp < kMmaWarp) {
         // ---------------------------------------------------------- producers
-        // Thread pt owns A row (pt % 128) and kChunks of its 8 16-byte chunks;
-        // B rows are shared out 8 chunks per row across all producer threads.
-        // The CTA's (tile, stage) pairs are numbered f = 0, 1, ...; the loads
-        // of stage f+1 are issued before stage f is split and stored, so one
-        // stage of global loads is always in flight per thread.  Stores
-        // follow the 128-byte swizzle: chunk j of row r sits at position
-        // j ^ (r % 8) of the row.
+        // The CTA's (tile, stage) pairs are numbered f = 0, 1, ...; group grp
+        // fills f = grp, grp + NGRP, ...  Thread gpt of a group owns A row
+        // (gpt % 128) and kChunks of its 8 16-byte chunks; B rows are shared
+        // out 8 chunks per row across the group's threads.  Stores follow the
+        // 128-byte swizzle: chunk j of row r sits at position j ^ (r % 8).
         const int pt = threadIdx.x - kEpiThreads;
-        const int row = pt & (kTfBM - 1);
-        const int chunk0 = (pt / kTfBM) * kChunks;
+        const int grp = pt / kGrpThr;
+        const int gpt = pt - grp * kGrpThr;
+        const int row = gpt & (kTfBM - 1);
+        const int chunk0 = (gpt / kTfBM) * kChunks;
         const uint32_t a_row_off = (uint32_t)row * 128u;
         const uint32_t row_sw = (uint32_t)(row & 7);
         const int my_tiles = (p.total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
         const int nf = my_tiles * p.KT;
         // loader position (tile, stage) and the row state of that tile
-        int l_tile = (int)blockIdx.x, l_ks = 0, cur_tile = -1;
+        int l_tile = (int)blockIdx.x, l_ks = grp, cur_tile = -1;
+        while (l_ks >= p.KT) { l_ks -= p.KT; l_tile += (int)gridDim.x; }
         int h0 = -65536, w0 = 0, base = 0, k0 = 0;
         uint64_t vmask = 0;          // bit r*S+s: tap (r, s) of this row's pixel lies inside the image
         const float *ximg = p.x;
@@ -373,7 +388,8 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                     }
                 }
             }
-            if (++l_ks == p.KT) { l_ks = 0; l_tile += (int)gridDim.x; }
+            l_ks += NGRP;
+            while (l_ks >= p.KT) { l_ks -= p.KT; l_tile += (int)gridDim.x; }
             // all taps of this thread's chunks first (shared broadcast reads),
             // then all the global loads
             int4 tv[kChunks * 2];
@@ -408,7 +424,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             }
 #pragma unroll
             for (int it = 0; it < (RESB ? 0 : kBIter); ++it) {
-                const int i = pt + it * kProd;
+                const int i = gpt + it * kGrpThr;
                 const int k = k0 + (i >> 3);
                 const int g = ks * kTfBK + (i & 7) * 4;
                 const int wrow = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
@@ -446,7 +462,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             }
 #pragma unroll
             for (int it = 0; it < (RESB ? 0 : kBIter); ++it) {
-                const int i = pt + it * kProd;
+                const int i = gpt + it * kGrpThr;
                 const int kr = i >> 3, cj = i & 7;
                 uint32_t hi[4], lo[4];
                 split4(vb[it], hi, lo);
@@ -513,14 +529,22 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             __syncwarp();
             if (lane == 0) mbar_arrive(bres_bar);
         }
-        float va0[kChunks][4], vb0[kBIter][4], va1[kChunks][4], vb1[kBIter][4];
-        if (nf > 0) load(va0, vb0);
-        for (int f = 0; f < nf && ok; f += 2) {
-            if (f + 1 < nf) load(va1, vb1);
-            if (!store(f, va0, vb0)) { ok = false; break; }
-            if (f + 1 < nf) {
-                if (f + 2 < nf) load(va0, vb0);
-                if (!store(f + 1, va1, vb1)) { ok = false; break; }
+        if constexpr (NGRP == 1) {
+            float va0[kChunks][4], vb0[kBIter][4], va1[kChunks][4], vb1[kBIter][4];
+            if (nf > 0) load(va0, vb0);
+            for (int f = 0; f < nf && ok; f += 2) {
+                if (f + 1 < nf) load(va1, vb1);
+                if (!store(f, va0, vb0)) { ok = false; break; }
+                if (f + 1 < nf) {
+                    if (f + 2 < nf) load(va0, vb0);
+                    if (!store(f + 1, va1, vb1)) { ok = false; break; }
+                }
+            }
+        } else {
+            float va[kChunks][4], vb[kBIter][4];
+            for (int f = grp; f < nf; f += NGRP) {
+                load(va, vb);
+                if (!store(f, va, vb)) break;
             }
         }
     } else if (warp == kMmaWarp && lane == 0) {
@@ -738,7 +762,7 @@ bool ensure_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &done_mas
     return true;
 }
 
-template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB>
+template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB, int NGRP>
 conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
                           cudaStream_t st, const TfDeconv *dv = nullptr) {
     using L = TfSmem<BN, STAGES, RESB>;
@@ -797,7 +821,7 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
     p.w_vec = (s.Kg % 4 == 0 && ((uintptr_t)t.w & 15) == 0) ? 1 : 0;
     p.y_vec = (p.nhwc && s.K % 4 == 0 && ((uintptr_t)t.y & 15) == 0) ? 1 : 0;
     const size_t bytes = L::bytes(p.KT);
-    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD, LSTM, RESB>;
+    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD, LSTM, RESB, NGRP>;
     static std::atomic<uint64_t> attr_done{0};   // this instantiation's per-device flags
     // the attribute is set for the largest table this variant accepts
     if (!ensure_attr(reinterpret_cast<const void *>(kern), 227 * 1024, attr_done)) return CONV2D_ERR_CUDA;
@@ -815,10 +839,11 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
 }
 
 // Only variants with 8 or more producer warps carry the ConvLSTM epilogue.
-template <int BN, int STAGES, int NPROD, bool RESB>
+template <int BN, int STAGES, int NPROD, bool RESB, int NGRP>
 conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
                                cudaStream_t st) {
-    if constexpr (NPROD >= 8) return launch_tf<BN, STAGES, NPROD, true, RESB>(s, pl, t, lstm, st, nullptr);
+    if constexpr (NPROD >= 8)
+        return launch_tf<BN, STAGES, NPROD, true, RESB, NGRP>(s, pl, t, lstm, st, nullptr);
     return CONV2D_ERR_UNSUPPORTED;
 }
 
@@ -828,19 +853,23 @@ conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t,
 // latency-bound, so more producer warps per SM run a stage faster.  The
 // 3-stage variant leaves shared memory for the tap tables of long
 // reductions (C*R*S up to about 9,000).  The resident-weight variants split
-// the weights once per CTA (C*R*S up to about 350 at BN = 64); measured,
-// that saves only ~4 %: the activation gather sets the pace.
-#define CONV2D_TF_VARIANTS(X)     \
-    X(32, 5, 4, 1240, false)      \
-    X(64, 4, 4, 3850, false)      \
-    X(128, 3, 4, 5000, false)     \
-    X(32, 5, 8, 920, false)       \
-    X(64, 4, 8, 1370, false)      \
-    X(128, 3, 8, 3100, false)     \
-    X(64, 4, 16, 1100, false)     \
-    X(64, 3, 16, 1060, false)     \
-    X(64, 2, 16, 1060, true)      \
-    X(64, 3, 16, 1060, true)
+// the weights once per CTA (C*R*S up to about 350 at BN = 64).  Two producer
+// groups (last three rows) took the encoder layers 5-10 % below the best
+// one-group variant.
+#define CONV2D_TF_VARIANTS(X)        \
+    X(32, 5, 4, 1240, false, 1)      \
+    X(64, 4, 4, 3850, false, 1)      \
+    X(128, 3, 4, 5000, false, 1)     \
+    X(32, 5, 8, 920, false, 1)       \
+    X(64, 4, 8, 1370, false, 1)      \
+    X(128, 3, 8, 3100, false, 1)     \
+    X(64, 4, 16, 1100, false, 1)     \
+    X(64, 3, 16, 1060, false, 1)     \
+    X(64, 2, 16, 1060, true, 1)      \
+    X(64, 3, 16, 1060, true, 1)      \
+    X(64, 4, 16, 990, false, 2)       \
+    X(64, 2, 16, 940, true, 2)         \
+    X(128, 2, 16, 2400, false, 2)
 
 }  // namespace
 
@@ -849,7 +878,7 @@ bool tf_lstm_variant(int id) { return tf_variant(id).nprod >= 8; }
 
 int tf_num_variants() {
     int n = 0;
-#define X(vbn, vst, vnp, vns, vrb) ++n;
+#define X(vbn, vst, vnp, vns, vrb, vng) ++n;
     CONV2D_TF_VARIANTS(X)
 #undef X
     return n;
@@ -857,9 +886,9 @@ int tf_num_variants() {
 
 TfTile tf_variant(int id) {
     int i = 0;
-    TfTile t{0, 0, 0, -1, 0, false};
-#define X(vbn, vst, vnp, vns, vrb)                        \
-    if (i == id) t = TfTile{vbn, vst, vnp, id, vns, vrb}; \
+    TfTile t{0, 0, 0, -1, 0, false, 1};
+#define X(vbn, vst, vnp, vns, vrb, vng)                        \
+    if (i == id) t = TfTile{vbn, vst, vnp, id, vns, vrb, vng}; \
     ++i;
     CONV2D_TF_VARIANTS(X)
 #undef X
@@ -904,25 +933,14 @@ extern "C" int conv2d_tf_trace_dump(unsigned long long *out, unsigned int *count
 
 conv2d_status_t tf_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st,
                           const TfLstm *lstm, const TfDeconv *dv) {
-    if (dv) {
-#define X(vbn, vst, vnp, vns, vrb)                                                               \
-    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp && pl.tf.resb == vrb)        \
-        return launch_tf<vbn, vst, vnp, false, vrb>(s, pl, t, nullptr, st, dv);
-        CONV2D_TF_VARIANTS(X)
-#undef X
-        return CONV2D_ERR_INTERNAL;
-    }
-    if (lstm) {
-#define X(vbn, vst, vnp, vns, vrb)                                                               \
-    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp && pl.tf.resb == vrb)        \
-        return launch_tf_lstm<vbn, vst, vnp, vrb>(s, pl, t, lstm, st);
-        CONV2D_TF_VARIANTS(X)
-#undef X
-        return CONV2D_ERR_INTERNAL;
-    }
-#define X(vbn, vst, vnp, vns, vrb)                                                               \
-    if (pl.tf.BN == vbn && pl.tf.stages == vst && pl.tf.nprod == vnp && pl.tf.resb == vrb)        \
-        return launch_tf<vbn, vst, vnp, false, vrb>(s, pl, t, nullptr, st);
+    int i = 0;
+#define X(vbn, vst, vnp, vns, vrb, vng)                                                   \
+    if (pl.tf.id == i) {                                                                  \
+        if (dv) return launch_tf<vbn, vst, vnp, false, vrb, vng>(s, pl, t, nullptr, st, dv); \
+        if (lstm) return launch_tf_lstm<vbn, vst, vnp, vrb, vng>(s, pl, t, lstm, st);      \
+        return launch_tf<vbn, vst, vnp, false, vrb, vng>(s, pl, t, nullptr, st);            \
+    }                                                                                     \
+    ++i;
     CONV2D_TF_VARIANTS(X)
 #undef X
     return CONV2D_ERR_INTERNAL;
