@@ -570,10 +570,14 @@ def decoder_layers(device, flush, peaks, iters, n=256):
         by = 4.0 * (x.numel() + w.numel() + C + y.numel())
         tf = fl / (t * 1e-3) / 1e12
         gbs = by / (t * 1e-3) / 1e9
-        out.append({"layer": name, "us": round(t * 1e3, 2), "tflops": round(tf, 2),
-                    "path": "3xTF32 tensor cores, one launch per output residue class",
-                    "bound": "tensor", "frac": round(tf / fp32_3xtf32_peak_tflops(peaks), 4),
-                    "hbm_gbs": round(gbs, 1)})
+        if C > 8:   # the library's rule: tensor cores unless the layer has <= 8 output channels
+            path, bound, peak = ("3xTF32 tensor cores, one launch per output residue class", "tensor",
+                                 fp32_3xtf32_peak_tflops(peaks))
+        else:
+            path, bound, peak = ("gather kernel, FFMA, %d-channel block" % (4 if C <= 4 else 8), "alu",
+                                 fp32_alu_peak_tflops())
+        out.append({"layer": name, "us": round(t * 1e3, 2), "tflops": round(tf, 2), "path": path,
+                    "bound": bound, "frac": round(tf / peak, 4), "hbm_gbs": round(gbs, 1)})
     return out
 
 

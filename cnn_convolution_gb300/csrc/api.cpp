@@ -621,10 +621,16 @@ conv2d_status_t conv2d_deconv_forward(const void *x, const void *w, const void *
     // reading input row i + e_r for class row i: a stride-1 gather, run on
     // the 3xTF32 kernel with its outputs written in place into y.  A class
     // without taps (only bias) or a shape the kernel cannot hold uses the
-    // gather kernel for the whole layer.
+    // gather kernel for the whole layer.  So does a layer with at most 8
+    // outputs channels: the tensor-core tile is at least 32 channels wide
+    // and its gather of the inputs costs the same however few of them are
+    // used, while the gather kernel's work shrinks with its channel block.
+    // CONV2D_DECONV_TC=1 / 0 forces either path.
     DevInfo d;
     int dev2 = 0;
-    if (env_int("CONV2D_DECONV_TC") != 0 && R <= 8 && S <= 8 && device_info(&dev2, &d) == CONV2D_OK &&
+    const int force_tc = env_int("CONV2D_DECONV_TC");
+    const bool try_tc = force_tc == 1 || (force_tc < 0 && C > 8);
+    if (try_tc && R <= 8 && S <= 8 && device_info(&dev2, &d) == CONV2D_OK &&
         d.cc_major == 10 && d.cc_minor == 3) {
         struct Cls { int a, b; TfDeconv dv; Shape s; Plan p; };
         Cls cls[64];

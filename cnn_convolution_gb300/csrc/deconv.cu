@@ -15,16 +15,20 @@
 // stride and p = (h + pad - r*dil) / stride lies in [0, P).
 //
 // A CTA of 256 threads owns 256 output pixels -- whole images when an image
-// has at most 256 outputs, else 256 consecutive pixels of one image -- and
-// 32 output channels (registers); thread = pixel.  For each chunk of 16 input
-// channels it stages the input rows those pixels read (whole rows, zero
-// outside x) and the chunk's weights as [k][r][s][32 channels] in shared
-// memory, every staging load issued before the stores.  Each thread keeps
-// bitmasks of its valid filter rows and columns; per valid tap: one input
-// read, 8 broadcast 16-byte weight reads, 32 FFMAs.
+// has at most 256 outputs, else 256 consecutive pixels of one image -- and a
+// block of CB output channels (registers; CB = 32, or 8 / 4 for layers with
+// that few outputs, such as the decoder's last layer back to the signature
+// channels); thread = pixel.  For each chunk of 16 input channels it stages
+// the input rows those pixels read (whole rows, zero outside x) and the
+// chunk's weights as [k][r][s][CB channels] in shared memory with 4-byte
+// asynchronous copies (cp.async, zero-fill outside x), double-buffered: the
+// next chunk is in flight while the current one is summed.  Each thread
+// keeps bitmasks of its valid filter rows and columns; per valid tap: one input
+// read, CB/4 broadcast 16-byte weight reads, CB FFMAs.
 
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx_sm103a.cuh"
@@ -33,7 +37,6 @@ namespace conv2d {
 namespace {
 
 constexpr int kDvThreads = 256;      // = output pixels per CTA (one per thread)
-constexpr int kDvC = 32;             // output channels per CTA
 constexpr int kDvK = 16;             // input channels per staged chunk
 constexpr int kDvMaxTap = 8;         // R, S <= 8
 constexpr int kDvBatch = 8;          // staging loads in flight per thread
@@ -47,18 +50,21 @@ struct DvParams {
     int tiles_per_img;     // imgs == 0: a CTA owns 256 consecutive pixels of one image
     int tiles, c_blocks;
     int IP, IQ;            // staged input rows per image / columns (= Q)
+    uint32_t m_iq, m_ip, m_img;   // reciprocals (sm103a::fdiv) of IQ, IP and kDvK*IP*IQ
 };
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 // RT, ST: compile-time filter size bound of the tap loops (kDvMaxTap = any R, S <= 8).
-template <int RT, int ST>
-__global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p) {
+template <int RT, int ST, int CB>
+__global__ void __launch_bounds__(kDvThreads, CB <= 8 ? 3 : 2) deconv_kernel(const DvParams p) {
+    constexpr int kDvC = CB;
     extern __shared__ float4 dv_smem4[];
     const int nimg = p.imgs > 0 ? p.imgs : 1;
-    float *xs = reinterpret_cast<float *>(dv_smem4);                   // [img][kDvK][IP][IQ]
+    // two buffers, each [img][kDvK][IP][IQ] inputs then [kDvK][R][S][kDvC] weights
+    float *xs = reinterpret_cast<float *>(dv_smem4);
     const int xs_sz = (nimg * kDvK * p.IP * p.IQ + 3) & ~3;
-    float *ws = xs + xs_sz;                                             // [kDvK][R][S][kDvC]
+    const int buf_sz = xs_sz + kDvK * p.R * p.S * kDvC;
 
     // no early trigger: a kernel of many short CTAs lets the next one launch
     // at its exit, so the next grid is spread over idle SMs
@@ -114,98 +120,97 @@ __global__ void __launch_bounds__(kDvThreads, 2) deconv_kernel(const DvParams p)
     // exact compile-time filter sizes make the staging index arithmetic cheap
     const int RS = (RT < kDvMaxTap && RT * ST > 0) ? RT * ST : p.R * p.S;
     const int plane = p.IP * p.IQ;
-    const int warp = t / 32, lane = t % 32;
 
-    for (int k0 = 0; k0 < p.K; k0 += kDvK) {
-        __syncthreads();
-        // stage x.  Whole images: the chunk of an image, x[n][k0 .. k0+15][..][..],
-        // is one contiguous run, copied flat.  Else one staged row (image,
-        // channel, input row) per warp pass, lanes along the row; 4 rows in
-        // flight per warp.
-        const int nrows = p.imgs > 0 ? 0 : nimg * kDvK * p.IP;
+    // Stage input channels [k0, k0 + kDvK) into buffer bf and commit the
+    // copies as one group.  Whole images: the chunk of an image,
+    // x[n][k0 .. k0+15][..][..], is one contiguous run.  Else the staged rows
+    // (channel, input row p_lo + ip) of the CTA's image, zero outside x.
+    auto stage = [&](int k0, int bf) {
+        const uint32_t xs_u = sm103a::smem_u32(xs + bf * buf_sz);
+        const uint32_t ws_u = xs_u + 4u * (uint32_t)xs_sz;
         if (p.imgs > 0) {
             const int per_img = kDvK * plane;              // plane = P*Q here
             const int kn_img = min(kDvK, p.K - k0) * plane;
-            for (int i0 = 0; i0 < nimg * per_img; i0 += kDvThreads * kDvBatch) {
-                float v[kDvBatch];
-#pragma unroll
-                for (int u = 0; u < kDvBatch; ++u) {
-                    const int i = i0 + u * kDvThreads + t;
-                    const int im = i / per_img, f = i - im * per_img;
-                    const bool in = i < nimg * per_img && n0 + im < p.N && f < kn_img;
-                    v[u] = sm103a::ldg_or_zero(in ? p.x + ((int64_t)(n0 + im) * p.K + k0) * plane + f : p.x, in);
-                }
-#pragma unroll
-                for (int u = 0; u < kDvBatch; ++u) {
-                    const int i = i0 + u * kDvThreads + t;
-                    if (i < nimg * per_img) xs[i] = v[u];
-                }
+            for (int i = t; i < nimg * per_img; i += kDvThreads) {
+                const int im = sm103a::fdiv(i, p.m_img), f = i - im * per_img;
+                const bool in = n0 + im < p.N && f < kn_img;
+                sm103a::cp_async_f32(xs_u + 4u * (uint32_t)i,
+                                     in ? p.x + ((int64_t)(n0 + im) * p.K + k0) * plane + f : p.x, in);
+            }
+        } else {
+            const int tot = kDvK * plane;
+            for (int i = t; i < tot; i += kDvThreads) {
+                const int row = sm103a::fdiv(i, p.m_iq), iq = i - row * p.IQ;
+                const int kk = sm103a::fdiv(row, p.m_ip), ip = row - kk * p.IP;
+                const int k = k0 + kk, pp = p_lo + ip;
+                const bool in = k < p.K && (unsigned)pp < (unsigned)p.P;
+                sm103a::cp_async_f32(xs_u + 4u * (uint32_t)i,
+                                     in ? p.x + (((int64_t)n0 * p.K + k) * p.P + pp) * p.Q + iq : p.x, in);
             }
         }
-        for (int row0 = warp * 4; row0 < nrows; row0 += (kDvThreads / 32) * 4) {
-            float v[4][2];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int row = row0 + u;
-                const int ip = row % p.IP, r2 = row / p.IP;
-                const int kk = r2 % kDvK, im = r2 / kDvK;
-                const int k = k0 + kk, pp = p_lo + ip, nn = n0 + im;
-                const bool rin = row < nrows && nn < p.N && k < p.K && (unsigned)pp < (unsigned)p.P;
-                const float *src = p.x + (((int64_t)nn * p.K + k) * p.P + pp) * p.Q;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int iq = lane + 32 * e;
-                    const bool in = rin && iq < p.Q;
-                    v[u][e] = sm103a::ldg_or_zero(in ? src + iq : p.x, in);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int row = row0 + u;
-                if (row < nrows) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        if (lane + 32 * e < p.IQ) xs[row * p.IQ + lane + 32 * e] = v[u][e];
-                }
-            }
-            // rows longer than 64 columns (wide outputs): the rest, plainly
-            for (int u = 0; u < 4 && p.IQ > 64; ++u) {
-                const int row = row0 + u;
-                if (row >= nrows) break;
-                const int ip = row % p.IP, r2 = row / p.IP;
-                const int kk = r2 % kDvK, im = r2 / kDvK;
-                const int k = k0 + kk, pp = p_lo + ip, nn = n0 + im;
-                const bool rin = nn < p.N && k < p.K && (unsigned)pp < (unsigned)p.P;
-                for (int iq = 64 + lane; iq < p.IQ; iq += 32)
-                    xs[row * p.IQ + iq] = rin ? __ldg(p.x + (((int64_t)nn * p.K + k) * p.P + pp) * p.Q + iq) : 0.f;
-            }
-        }
-        // stage w: for each input channel the block's weights w[k][c0 .. c0+31][r][s]
-        // are contiguous; read them in that order, store as [k][r*S+s][c]
+        // weights: for each input channel the block's w[k][c0 .. c0+CB-1][r][s]
+        // are contiguous; read in that order, stored as [k][r*S+s][c]
         const int wrun = kDvC * RS;
-        for (int i0 = 0; i0 < kDvK * wrun; i0 += kDvThreads * kDvBatch) {
-            float v[kDvBatch];
-#pragma unroll
-            for (int u = 0; u < kDvBatch; ++u) {
-                const int i = i0 + u * kDvThreads + t;
-                const int kk = i / wrun, f = i - kk * wrun;
-                const int k = k0 + kk, c = c0 + f / RS;
-                const bool in = i < kDvK * wrun && k < p.K && c < p.C;
-                v[u] = sm103a::ldg_or_zero(in ? p.w + ((int64_t)k * p.C + c0) * RS + f : p.w, in);
-            }
-#pragma unroll
-            for (int u = 0; u < kDvBatch; ++u) {
-                const int i = i0 + u * kDvThreads + t;
-                if (i < kDvK * wrun) {
-                    const int kk = i / wrun, f = i - kk * wrun;
-                    const int j = f / RS, rs = f - j * RS;
-                    ws[(kk * RS + rs) * kDvC + j] = v[u];
-                }
-            }
+        for (int i = t; i < kDvK * wrun; i += kDvThreads) {
+            const int kk = i / wrun, f = i - kk * wrun;
+            const int j = f / RS, rs = f - j * RS;
+            const int k = k0 + kk;
+            const bool in = k < p.K && c0 + j < p.C;
+            sm103a::cp_async_f32(ws_u + 4u * (uint32_t)((kk * RS + rs) * kDvC + j),
+                                 in ? p.w + ((int64_t)k * p.C + c0) * RS + f : p.w, in);
+        }
+        sm103a::cp_async_commit();
+    };
+
+    stage(0, 0);
+    int bf = 0;
+    for (int k0 = 0; k0 < p.K; k0 += kDvK, bf ^= 1) {
+        // every thread is done with the previous chunk, i.e. with the buffer
+        // that is refilled here
+        __syncthreads();
+        if (k0 + kDvK < p.K) {
+            stage(k0 + kDvK, bf ^ 1);
+            sm103a::cp_async_wait<1>();
+        } else {
+            sm103a::cp_async_wait<0>();
         }
         __syncthreads();
+        const float *ws = xs + bf * buf_sz + xs_sz;
         const int kn = min(kDvK, p.K - k0);
-        const float *xi = xs + img * kDvK * plane;
+        const float *xi = xs + bf * buf_sz + img * kDvK * plane;
+        if constexpr (RT < kDvMaxTap && ST < kDvMaxTap) {
+            // Compile-time filter: one staged-input offset per tap and a tap
+            // mask, so the loop is branch-free (a warp's pixels can span two
+            // output rows with different valid taps): predicated shared read,
+            // broadcast weights, CB FFMAs.
+            int toff[RT * ST];
+            unsigned tmask = 0;
+#pragma unroll
+            for (int r = 0; r < RT; ++r)
+#pragma unroll
+                for (int s = 0; s < ST; ++s) {
+                    const bool v = ((rmask >> r) & (smask >> s) & 1u) != 0;
+                    toff[r * ST + s] = v ? pl[r] * p.IQ + ql[s] : 0;
+                    tmask |= (v ? 1u : 0u) << (r * ST + s);
+                }
+            for (int kk = 0; kk < kn; ++kk) {
+                const float *xk = xi + kk * plane;
+                const float4 *wk4 = reinterpret_cast<const float4 *>(ws + kk * RT * ST * kDvC);
+#pragma unroll
+                for (int tp = 0; tp < RT * ST; ++tp) {
+                    const float a = ((tmask >> tp) & 1u) ? xk[toff[tp]] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < kDvC / 4; ++j) {
+                        const float4 v = wk4[tp * (kDvC / 4) + j];
+                        acc[4 * j] = fmaf(a, v.x, acc[4 * j]);
+                        acc[4 * j + 1] = fmaf(a, v.y, acc[4 * j + 1]);
+                        acc[4 * j + 2] = fmaf(a, v.z, acc[4 * j + 2]);
+                        acc[4 * j + 3] = fmaf(a, v.w, acc[4 * j + 3]);
+                    }
+                }
+            }
+            continue;
+        }
         for (int kk = 0; kk < kn; ++kk) {
             const float *xk = xi + kk * plane;
             const float *wk = ws + kk * RS * kDvC;
@@ -256,11 +261,14 @@ int stage_rows(int H, int W, int P, int R, int stride, int dil) {
 
 }  // namespace
 
-size_t dv_smem_bytes(int H, int W, int P, int Q, int R, int S, int stride, int dil) {
+// output channels per CTA: the smallest block that holds C, at most 32
+int dv_cblock(int C) { return C <= 4 ? 4 : C <= 8 ? 8 : 32; }
+
+size_t dv_smem_bytes(int H, int W, int P, int Q, int C, int R, int S, int stride, int dil) {
     const int imgs = H * W <= kDvThreads ? std::max(1, kDvThreads / (H * W)) : 1;
     const int ip = stage_rows(H, W, P, R, stride, dil);
     const size_t xs = ((size_t)imgs * kDvK * ip * Q + 3) & ~(size_t)3;
-    return (xs + (size_t)kDvK * R * S * kDvC) * sizeof(float);
+    return 2 * (xs + (size_t)kDvK * R * S * dv_cblock(C)) * sizeof(float);   // two buffers
 }
 
 conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, float *y, int N, int K,
@@ -283,17 +291,27 @@ conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, flo
         if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
         p.tiles = (int)tiles;
     }
-    p.c_blocks = (C + kDvC - 1) / kDvC;
+    const int cbk = dv_cblock(C);
+    p.c_blocks = (C + cbk - 1) / cbk;
     p.IP = stage_rows(H, W, P, R, stride, dil);
     p.IQ = Q;
+    p.m_iq = recip_u32(p.IQ);
+    p.m_ip = recip_u32(p.IP);
+    p.m_img = recip_u32(kDvK * p.IP * p.IQ);
     const int64_t grid = (int64_t)p.tiles * p.c_blocks;
     if (grid > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
-    const size_t bytes = dv_smem_bytes(H, W, P, Q, R, S, stride, dil);
+    const size_t bytes = dv_smem_bytes(H, W, P, Q, C, R, S, stride, dil);
     if (bytes > 96 * 1024) return CONV2D_ERR_UNSUPPORTED;
     void (*kern)(DvParams);
-    if (R == 2 && S == 2) kern = deconv_kernel<2, 2>;
-    else if (R == 3 && S == 3) kern = deconv_kernel<3, 3>;
-    else kern = deconv_kernel<kDvMaxTap, kDvMaxTap>;
+    auto pick = [&](auto cb) {
+        constexpr int B = decltype(cb)::value;
+        if (R == 2 && S == 2) kern = deconv_kernel<2, 2, B>;
+        else if (R == 3 && S == 3) kern = deconv_kernel<3, 3, B>;
+        else kern = deconv_kernel<kDvMaxTap, kDvMaxTap, B>;
+    };
+    if (cbk == 4) pick(std::integral_constant<int, 4>{});
+    else if (cbk == 8) pick(std::integral_constant<int, 8>{});
+    else pick(std::integral_constant<int, 32>{});
     if (bytes > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024) != cudaSuccess)
         return CONV2D_ERR_CUDA;

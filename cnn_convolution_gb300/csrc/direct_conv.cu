@@ -42,18 +42,13 @@ struct DcParams {
     int Kp;               // K rounded up to kDcKc (row length of the transposed weights)
     int tiles_p, tiles_q;
     int nhwc;
-    // reciprocals for the staging index arithmetic (see fdiv): IW, IH, Kp, R*S
+    // reciprocals for the staging index arithmetic (sm103a::fdiv): IW, IH, Kp, R*S
     uint32_t m_iw, m_ih, m_kp, m_rs;
 };
 
-// n / d for 0 <= n with n * d < 2^32, given m = floor(2^32 / d) + 1 (d >= 2)
-// or m = 0 (d = 1): floor(n * m / 2^32) = floor(n/d + n*e/(d * 2^32)) with
-// m*d = 2^32 + e, 0 < e <= d, and the second term stays below 1/d.  The
-// staged patch and weight table are bounded by the shared-memory limit, so
-// every index and divisor here meets the condition.
-__device__ __forceinline__ int fdiv(int n, uint32_t m) {
-    return m ? (int)__umulhi((unsigned)n, m) : n;
-}
+// The staged patch and weight table are bounded by the shared-memory limit,
+// so every index and divisor given to sm103a::fdiv meets its n * d < 2^32.
+using sm103a::fdiv;
 
 // RT, ST: compile-time filter size (0 = read from the parameters).
 template <int RT, int ST>
@@ -243,9 +238,6 @@ bool dc_shape_ok(const Shape &s) {
     return dc_smem_bytes(s) <= 96 * 1024;
 }
 
-namespace {
-uint32_t recip(int d) { return d <= 1 ? 0u : (uint32_t)((((uint64_t)1) << 32) / (uint64_t)d + 1); }
-}  // namespace
 
 int dc_grid(const Shape &s) {
     return (int)((int64_t)s.N * ((s.P + kDcRows - 1) / kDcRows) * ((s.Q + kDcCols - 1) / kDcCols));
@@ -266,10 +258,10 @@ conv2d_status_t dc_launch(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.tiles_p = (s.P + kDcRows - 1) / kDcRows;
     p.tiles_q = (s.Q + kDcCols - 1) / kDcCols;
     p.nhwc = s.layout == CONV2D_NHWC ? 1 : 0;
-    p.m_iw = recip(p.IW);
-    p.m_ih = recip(p.IH);
-    p.m_kp = recip(p.Kp);
-    p.m_rs = recip(s.R * s.S);
+    p.m_iw = recip_u32(p.IW);
+    p.m_ih = recip_u32(p.IH);
+    p.m_kp = recip_u32(p.Kp);
+    p.m_rs = recip_u32(s.R * s.S);
     const size_t bytes = dc_smem_bytes(s);
     void (*kern)(DcParams);
     if (s.R == 3 && s.S == 3) kern = direct_conv_kernel<3, 3>;

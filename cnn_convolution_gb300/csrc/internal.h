@@ -129,7 +129,7 @@ conv2d_status_t tf_launch(const Shape &s, const Plan &p, const Tensors &t, cudaS
                           const TfLstm *lstm = nullptr, const TfDeconv *dv = nullptr);
 
 // Transposed convolution, fp32 NCHW (arguments validated by the caller).
-size_t dv_smem_bytes(int H, int W, int P, int Q, int R, int S, int stride, int dil);
+size_t dv_smem_bytes(int H, int W, int P, int Q, int C, int R, int S, int stride, int dil);
 conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, float *y, int N, int K,
                           int P, int Q, int C, int R, int S, int H, int W, int stride, int pad,
                           int dil, cudaStream_t st);
@@ -137,6 +137,11 @@ conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, flo
 // MSCRED signature matrices (arguments validated by the caller).
 conv2d_status_t sig_launch(const float *series, int n, int T, const int *windows, int n_windows,
                            int t_first, int n_steps, float *out, cudaStream_t st);
+
+// Reciprocal for sm103a::fdiv: floor(2^32 / d) + 1, or 0 for d <= 1.
+inline uint32_t recip_u32(int d) {
+    return d <= 1 ? 0u : (uint32_t)((((uint64_t)1) << 32) / (uint64_t)d + 1);
+}
 
 // Launch with programmatic dependent launch (the kernel calls pdl_wait()
 // before touching global memory); falls back to nothing else -- an error

@@ -255,5 +255,26 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (cp.async, not the bulk
+// engine); with `valid` false nothing is read and the destination is zeroed.
+__device__ __forceinline__ void cp_async_f32(uint32_t dst, const float *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's committed groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// n / d for 0 <= n with n * d < 2^32, given m = recip_u32(d):
+// m = floor(2^32 / d) + 1 (d >= 2), or 0 (d = 1).  floor(n * m / 2^32) =
+// floor(n/d + n*e/(d * 2^32)) with m*d = 2^32 + e, 0 < e <= d, and the
+// second term stays below 1/d when n * d < 2^32.
+__device__ __forceinline__ int fdiv(int n, uint32_t m) {
+    return m ? (int)__umulhi((unsigned)n, m) : n;
+}
+
 }  // namespace sm103a
 }  // namespace conv2d

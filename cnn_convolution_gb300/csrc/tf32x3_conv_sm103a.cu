@@ -610,9 +610,20 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
         uint32_t slot_phase = 0, acc_phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            // The sums start from the bias: its loads are issued together
+            // here, while the tile's first stage is still being filled, and
+            // none of them follows a store of this tile.  (The tile's
+            // coordinates are computed again after the main loop, so that
+            // only the sums stay live across it.)
             float a[kCpt];
+            const int kb0 = (tile % p.n_tiles_n) * BN + col0;
 #pragma unroll
-            for (int j = 0; j < kCpt; ++j) a[j] = 0.f;
+            for (int j = 0; j < kCpt; ++j) {
+                const int k = kb0 + j;
+                const int bk = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
+                const bool bin = p.bias != nullptr && k < p.K;
+                a[j] = ldg_or_zero(bin ? p.bias + bk : p.x, bin);
+            }
             for (int ks = 0; ks < p.KT; ++ks) {
                 int okw = 1;
                 if (lane == 0) okw = mbar_wait(slotf_bar(slot), slot_phase, abort_flag, p.status) ? 1 : 0;
@@ -656,20 +667,6 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             const int tn = tile - tm * p.n_tiles_n;
             const int64_t m = (int64_t)tm * kTfBM + row;
             const int kb = tn * BN + col0;
-            // Add the bias before the first store: loads that follow stores
-            // through possibly aliasing pointers cannot be moved ahead of
-            // them, so interleaved they would cost a load latency per column.
-            if (p.bias) {
-                float bv[kCpt];
-#pragma unroll
-                for (int j = 0; j < kCpt; ++j) {
-                    const int k = kb + j;
-                    const int bk = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
-                    bv[j] = ldg_or_zero(p.bias + (k < p.K ? bk : 0), k < p.K);
-                }
-#pragma unroll
-                for (int j = 0; j < kCpt; ++j) a[j] += bv[j];
-            }
             if (m >= p.M) continue;
             if (LSTM) {
                 // gates -> state update: c = f*c_prev + i*g, h = o*tanh(c)

@@ -57,11 +57,10 @@ CASES = [
 
 @pytest.fixture(params=["tensor_core", "gather"])
 def deconv_path(request):
-    """The default path (3xTF32 tensor-core kernel per output residue class)
-    and the gather kernel (CONV2D_DECONV_TC=0)."""
+    """The 3xTF32 tensor-core kernel per output residue class
+    (CONV2D_DECONV_TC=1) and the gather kernel (CONV2D_DECONV_TC=0)."""
     import os
-    if request.param == "gather":
-        os.environ["CONV2D_DECONV_TC"] = "0"
+    os.environ["CONV2D_DECONV_TC"] = "1" if request.param == "tensor_core" else "0"
     yield request.param
     os.environ.pop("CONV2D_DECONV_TC", None)
 
