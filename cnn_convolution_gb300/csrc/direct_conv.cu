@@ -31,7 +31,6 @@ constexpr int kDcThreads = 256;
 constexpr int kDcRows = 16;      // output rows per CTA (2 per warp)
 constexpr int kDcCols = 32;      // output columns per CTA (1 per lane)
 constexpr int kDcKc = 32;        // output channels per register block
-constexpr int kDcBatch = 8;      // staging loads each thread has in flight at once
 
 struct DcParams {
     const float *x, *w, *bias;
@@ -74,53 +73,36 @@ __global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcPara
     sm103a::pdl_wait();                        // the previous kernel's writes are visible
 
     // Stage the input patch (zero outside the image) and the weights as
-    // [g = (c, r, s)][k] (zero for k >= K).  Each thread issues kDcBatch
-    // predicated loads before it stores any of them, so their latencies
-    // overlap instead of adding up.
+    // [g = (c, r, s)][k] (zero for k >= K) with 4-byte asynchronous copies
+    // (cp.async; a copy outside the image writes zero): every copy of the
+    // CTA is in flight at once, and no register holds them.
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const float *ximg = p.x + (int64_t)n * p.C * p.H * p.W;   // this image (C*H*W < 2^31)
-    for (int i0 = 0; i0 < patch; i0 += kDcThreads * kDcBatch) {
-        float v[kDcBatch];
-#pragma unroll
-        for (int j = 0; j < kDcBatch; ++j) {
-            const int i = min(i0 + j * kDcThreads + (int)threadIdx.x, patch);
-            const int r2 = fdiv(i, p.m_iw);
-            const int iw = i - r2 * p.IW;
-            const int c = fdiv(r2, p.m_ih);
-            const int ih = r2 - c * p.IH;
-            const int h = h0 + ih, wc = w0 + iw;
-            const bool in = i < patch && (unsigned)h < (unsigned)p.H && (unsigned)wc < (unsigned)p.W;
-            const int hh = in ? h : 0, ww = in ? wc : 0, cc = in ? c : 0;   // in-image: no overflow
-            const int off = p.nhwc ? (hh * p.W + ww) * p.C + cc : (cc * p.H + hh) * p.W + ww;
-            v[j] = sm103a::ldg_or_zero(ximg + off, in);
-        }
-#pragma unroll
-        for (int j = 0; j < kDcBatch; ++j) {
-            const int i = i0 + j * kDcThreads + (int)threadIdx.x;
-            if (i < patch) xs[i] = v[j];
-        }
+    const uint32_t xs_u = sm103a::smem_u32(xs), wt_u = sm103a::smem_u32(wt);
+    for (int i = (int)threadIdx.x; i < patch; i += kDcThreads) {
+        const int r2 = fdiv(i, p.m_iw);
+        const int iw = i - r2 * p.IW;
+        const int c = fdiv(r2, p.m_ih);
+        const int ih = r2 - c * p.IH;
+        const int h = h0 + ih, wc = w0 + iw;
+        const bool in = (unsigned)h < (unsigned)p.H && (unsigned)wc < (unsigned)p.W;
+        const int hh = in ? h : 0, ww = in ? wc : 0, cc = in ? c : 0;   // in-image: no overflow
+        const int off = p.nhwc ? (hh * p.W + ww) * p.C + cc : (cc * p.H + hh) * p.W + ww;
+        sm103a::cp_async_f32(xs_u + 4u * (uint32_t)i, ximg + off, in);
     }
     const int wn = Kg * p.Kp;
-    for (int i0 = 0; i0 < wn; i0 += kDcThreads * kDcBatch) {
-        float v[kDcBatch];
-#pragma unroll
-        for (int j = 0; j < kDcBatch; ++j) {
-            const int i = min(i0 + j * kDcThreads + (int)threadIdx.x, wn);
-            const int g = fdiv(i, p.m_kp), k = i - g * p.Kp;
-            int woff = g;                       // offset of w[k = 0][g]
-            if (p.nhwc) {
-                const int c = fdiv(g, p.m_rs), rs = g - c * RS;
-                woff = rs * p.C + c;
-            }
-            const bool in = i < wn && k < p.K;
-            v[j] = sm103a::ldg_or_zero(p.w + (in ? (int64_t)k * Kg + woff : 0), in);
+    for (int i = (int)threadIdx.x; i < wn; i += kDcThreads) {
+        const int g = fdiv(i, p.m_kp), k = i - g * p.Kp;
+        int woff = g;                       // offset of w[k = 0][g]
+        if (p.nhwc) {
+            const int c = fdiv(g, p.m_rs), rs = g - c * RS;
+            woff = rs * p.C + c;
         }
-#pragma unroll
-        for (int j = 0; j < kDcBatch; ++j) {
-            const int i = i0 + j * kDcThreads + (int)threadIdx.x;
-            if (i < wn) wt[i] = v[j];
-        }
+        const bool in = k < p.K;
+        sm103a::cp_async_f32(wt_u + 4u * (uint32_t)i, p.w + (in ? (int64_t)k * Kg + woff : 0), in);
     }
+    sm103a::cp_async_commit();
+    sm103a::cp_async_wait<0>();
     __syncthreads();
 
     const int pr0 = 2 * warp;                      // this thread's first row in the block
