@@ -574,8 +574,9 @@ def decoder_layers(device, flush, peaks, iters, n=256):
             path, bound, peak = ("3xTF32 tensor cores, one launch per output residue class", "tensor",
                                  fp32_3xtf32_peak_tflops(peaks))
         else:
-            path, bound, peak = ("gather kernel, FFMA, %d-channel block" % (4 if C <= 4 else 8), "alu",
-                                 fp32_alu_peak_tflops())
+            path = ("FFMA, one image per CTA, 4 pixels x %d channels per thread" % (4 if C <= 4 else 8)
+                    if st == 1 else "gather kernel, FFMA, %d-channel block" % (4 if C <= 4 else 8))
+            bound, peak = "alu", fp32_alu_peak_tflops()
         out.append({"layer": name, "us": round(t * 1e3, 2), "tflops": round(tf, 2), "path": path,
                     "bound": bound, "frac": round(tf / peak, 4), "hbm_gbs": round(gbs, 1)})
     return out

@@ -250,6 +250,120 @@ __global__ void __launch_bounds__(kDvThreads, CB <= 8 ? 3 : 2) deconv_kernel(con
     }
 }
 
+// Stride-1, dilation-1 layers with few output channels on small images
+// (the decoder's last layer, back to the signature channels): a CTA owns one
+// whole image; thread = 4 consecutive output pixels of a row x CB channels.
+// The chunk of kDvS1K input channels of the image is one contiguous run of
+// x, staged flat with cp.async (double-buffered), weights as in the gather
+// kernel.  Output (h, w) takes input (h + pad - r, w + pad - s): per filter
+// row a thread reads the 4 + ST - 1 inputs its pixels share once, then runs
+// ST taps x 4 pixels x CB channels of FFMAs on registers.
+constexpr int kDvS1K = 8;     // input channels per staged chunk
+constexpr int kDvS1Px = 4;    // consecutive output pixels per thread
+
+template <int RT, int ST, int CB>
+__global__ void __launch_bounds__(kDvThreads, 3) deconv_s1_kernel(const DvParams p) {
+    extern __shared__ float4 dv_smem4[];
+    float *sm = reinterpret_cast<float *>(dv_smem4);
+    const int plane = p.P * p.Q;
+    const int xs_sz = (kDvS1K * plane + 3) & ~3;
+    const int buf_sz = xs_sz + kDvS1K * RT * ST * CB;
+    sm103a::pdl_wait();
+    const int n = blockIdx.x / p.c_blocks;
+    const int c0 = (blockIdx.x - n * p.c_blocks) * CB;
+    const int t = threadIdx.x;
+    const int segs = (p.W + kDvS1Px - 1) / kDvS1Px;
+    const int h = t / segs, w0 = (t - h * segs) * kDvS1Px;
+    const bool active = h < p.H;
+    const int base = w0 + p.pad - (ST - 1);   // input column of register m = base + m
+
+    auto stage = [&](int k0, int bf) {
+        const uint32_t xs_u = sm103a::smem_u32(sm + bf * buf_sz);
+        const uint32_t ws_u = xs_u + 4u * (uint32_t)xs_sz;
+        const int kn = min(kDvS1K, p.K - k0) * plane;
+        const float *src = p.x + ((int64_t)n * p.K + k0) * plane;
+        for (int i = t; i < kDvS1K * plane; i += kDvThreads)
+            sm103a::cp_async_f32(xs_u + 4u * (uint32_t)i, i < kn ? src + i : p.x, i < kn);
+        constexpr int wrun = CB * RT * ST;
+        for (int i = t; i < kDvS1K * wrun; i += kDvThreads) {
+            const int kk = i / wrun, f = i - kk * wrun;
+            const int j = f / (RT * ST), rs = f - j * (RT * ST);
+            const int k = k0 + kk;
+            const bool in = k < p.K && c0 + j < p.C;
+            sm103a::cp_async_f32(ws_u + 4u * (uint32_t)((kk * RT * ST + rs) * CB + j),
+                                 in ? p.w + ((int64_t)k * p.C + c0) * (RT * ST) + f : p.w, in);
+        }
+        sm103a::cp_async_commit();
+    };
+
+    float acc[kDvS1Px][CB];
+#pragma unroll
+    for (int j = 0; j < kDvS1Px; ++j)
+#pragma unroll
+        for (int c = 0; c < CB; ++c) acc[j][c] = 0.f;
+
+    stage(0, 0);
+    int bf = 0;
+    for (int k0 = 0; k0 < p.K; k0 += kDvS1K, bf ^= 1) {
+        __syncthreads();                       // every thread is done with the buffer refilled here
+        if (k0 + kDvS1K < p.K) {
+            stage(k0 + kDvS1K, bf ^ 1);
+            sm103a::cp_async_wait<1>();
+        } else {
+            sm103a::cp_async_wait<0>();
+        }
+        __syncthreads();
+        const float *xs = sm + bf * buf_sz;
+        const float4 *ws4 = reinterpret_cast<const float4 *>(xs + xs_sz);
+        const int kn = min(kDvS1K, p.K - k0);
+        for (int kk = 0; kk < kn; ++kk) {
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+                const int ih = h + p.pad - r;
+                const bool rv = active && (unsigned)ih < (unsigned)p.P;
+                const float *xr = xs + (kk * p.P + (rv ? ih : 0)) * p.Q;
+                float xv[kDvS1Px + ST - 1];
+#pragma unroll
+                for (int m = 0; m < kDvS1Px + ST - 1; ++m) {
+                    const int col = base + m;
+                    xv[m] = (rv && (unsigned)col < (unsigned)p.Q) ? xr[col] : 0.f;
+                }
+#pragma unroll
+                for (int s = 0; s < ST; ++s) {
+#pragma unroll
+                    for (int q = 0; q < CB / 4; ++q) {
+                        const float4 wv = ws4[(kk * RT * ST + r * ST + s) * (CB / 4) + q];
+#pragma unroll
+                        for (int j = 0; j < kDvS1Px; ++j) {
+                            const float a = xv[ST - 1 - s + j];
+                            acc[j][4 * q] = fmaf(a, wv.x, acc[j][4 * q]);
+                            acc[j][4 * q + 1] = fmaf(a, wv.y, acc[j][4 * q + 1]);
+                            acc[j][4 * q + 2] = fmaf(a, wv.z, acc[j][4 * q + 2]);
+                            acc[j][4 * q + 3] = fmaf(a, wv.w, acc[j][4 * q + 3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if (!active) return;
+    float bv[CB];                               // all bias loads before the first store
+#pragma unroll
+    for (int c = 0; c < CB; ++c) {
+        const bool in = p.bias != nullptr && c0 + c < p.C;
+        bv[c] = sm103a::ldg_or_zero(in ? p.bias + c0 + c : p.x, in);
+    }
+    const int64_t HW = (int64_t)p.H * p.W;
+    float *yp = p.y + ((int64_t)n * p.C + c0) * HW + (int64_t)h * p.W + w0;
+#pragma unroll
+    for (int c = 0; c < CB; ++c) {
+        if (c0 + c >= p.C) break;
+#pragma unroll
+        for (int j = 0; j < kDvS1Px; ++j)
+            if (w0 + j < p.W) yp[(int64_t)c * HW + j] = acc[j][c] + bv[c];
+    }
+}
+
 // Staged input rows per image for a CTA's pixels (an upper bound).
 int stage_rows(int H, int W, int P, int R, int stride, int dil) {
     if (H * W <= kDvThreads) return P;
@@ -293,6 +407,25 @@ conv2d_status_t dv_launch(const float *x, const float *w, const float *bias, flo
     }
     const int cbk = dv_cblock(C);
     p.c_blocks = (C + cbk - 1) / cbk;
+    // stride 1, dilation 1, 2x2 or 3x3, at most 8 output channels, one image
+    // per CTA: the register-blocked kernel
+    const int64_t s1_bytes = 2 * ((((int64_t)kDvS1K * P * Q + 3) & ~(int64_t)3) + (int64_t)kDvS1K * R * S * cbk) * 4;
+    if (stride == 1 && dil == 1 && ((R == 3 && S == 3) || (R == 2 && S == 2)) && C <= 8 &&
+        (int64_t)H * ((W + kDvS1Px - 1) / kDvS1Px) <= kDvThreads && s1_bytes <= 96 * 1024 &&
+        (int64_t)N * p.c_blocks <= INT32_MAX) {
+        void (*k1)(DvParams);
+        if (R == 3) k1 = cbk == 4 ? deconv_s1_kernel<3, 3, 4> : deconv_s1_kernel<3, 3, 8>;
+        else k1 = cbk == 4 ? deconv_s1_kernel<2, 2, 4> : deconv_s1_kernel<2, 2, 8>;
+        if (s1_bytes > 48 * 1024 &&
+            cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024) != cudaSuccess)
+            return CONV2D_ERR_CUDA;
+        if (launch_pdl(k1, dim3((unsigned)(N * p.c_blocks)), dim3(kDvThreads), (size_t)s1_bytes, st, p) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return CONV2D_ERR_CUDA;
+        }
+        return CONV2D_OK;
+    }
     p.IP = stage_rows(H, W, P, R, stride, dil);
     p.IQ = Q;
     p.m_iq = recip_u32(p.IQ);

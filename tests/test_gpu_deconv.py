@@ -47,6 +47,9 @@ CASES = [
     (2, 6, 7, 8, 33, 3, 3, 2, 1, 2, 1),      # dilation, 33 output channels: 2 channel blocks
     (1, 2, 1, 1, 3, 4, 4, 1, 0, 1, 0),       # one input pixel
     (2, 20, 11, 13, 9, 3, 3, 1, 0, 1, 0),    # output 13 x 15: ragged blocks
+    (3, 11, 6, 9, 7, 2, 2, 1, 0, 1, 0),      # stride 1, 2x2, 8-channel block (one image per CTA)
+    (2, 19, 4, 4, 8, 3, 3, 1, 2, 1, 0),      # stride 1, pad 2, ragged last input-channel chunk
+    (1, 4, 70, 40, 3, 3, 3, 1, 1, 1, 0),     # stride 1, image too tall for one CTA: gather kernel
     # MSCRED decoder shapes (batch 8): 256->128 4->8, 256->64 8->15, 128->32 15->30, 64->3 30->30
     (8, 256, 4, 4, 128, 2, 2, 2, 0, 1, 0),
     (8, 256, 8, 8, 64, 3, 3, 2, 1, 1, 0),
