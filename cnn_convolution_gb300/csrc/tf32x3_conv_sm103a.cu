@@ -125,6 +125,9 @@ struct TfParams {
     int nhwc;
     int rs_mask;        // R*S <= 63: taps carry their (r, s) index, tested against a per-tile mask
     int R;
+    // NCHW 2x2 filter: reduction index g = 4c + 2r + s, so a 4-element chunk is
+    // one input channel's four taps and offsets follow from g without the table
+    int tap4, HW, dilW;
     int w_vec;          // Kg % 4 == 0 and w 16-byte aligned: weight rows load as float4
     int y_vec;          // NHWC, K % 4 == 0 and y 16-byte aligned: outputs store as float4
     // ConvLSTM cell epilogue (LSTM instantiations only): K = 4*Ch gate columns,
@@ -390,13 +393,26 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             }
             l_ks += NGRP;
             while (l_ks >= p.KT) { l_ks -= p.KT; l_tile += (int)gridDim.x; }
-            // all taps of this thread's chunks first (shared broadcast reads),
-            // then all the global loads
-            int4 tv[kChunks * 2];
-#pragma unroll
-            for (int q = 0; q < kChunks * 2; ++q) tv[q] = taps4[(ks * kTfBK + chunk0 * 4) / 2 + q];
             const float *xrow = ximg + base;   // the pixel's input origin (may lie in the padding)
-            if (p.rs_mask) {
+            if (p.tap4) {
+                // chunk j is input channel ks*8 + chunk0 + j; element e is tap
+                // (e >> 1, e & 1), bit e of the tile's tap mask
+                const int cb = ks * (kTfBK / 4) + chunk0;
+#pragma unroll
+                for (int j = 0; j < kChunks; ++j) {
+                    const bool cin = cb + j < p.C;
+                    const int coff = cin ? (cb + j) * p.HW : 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        va[j][e] = ldg_or_zero(xrow + coff + (e >> 1) * p.dilW + (e & 1) * p.dil,
+                                               cin && ((vmask >> e) & 1u));
+                }
+            } else if (p.rs_mask) {
+                // all taps of this thread's chunks first (shared broadcast
+                // reads), then all the global loads
+                int4 tv[kChunks * 2];
+#pragma unroll
+                for (int q = 0; q < kChunks * 2; ++q) tv[q] = taps4[(ks * kTfBK + chunk0 * 4) / 2 + q];
 #pragma unroll
                 for (int j = 0; j < kChunks; ++j) {
 #pragma unroll
@@ -408,6 +424,9 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                     }
                 }
             } else {
+                int4 tv[kChunks * 2];
+#pragma unroll
+                for (int q = 0; q < kChunks * 2; ++q) tv[q] = taps4[(ks * kTfBK + chunk0 * 4) / 2 + q];
 #pragma unroll
                 for (int j = 0; j < kChunks; ++j) {
 #pragma unroll
@@ -791,6 +810,9 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
     p.nhwc = s.layout == CONV2D_NHWC ? 1 : 0;
     p.R = s.R;
     p.rs_mask = s.R * s.S <= 63 ? 1 : 0;
+    p.tap4 = (s.layout == CONV2D_NCHW && s.R == 2 && s.S == 2) ? 1 : 0;
+    p.HW = s.H * s.W;   // C*H*W < 2^31 (tf_shape_ok)
+    p.dilW = s.dil * s.W;
     p.dv = 0;
     if (dv) {
         p.dv = 1;
@@ -800,6 +822,7 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
             p.dv_e[i] = dv->e[i]; p.dv_f[i] = dv->f[i]; p.dv_r[i] = dv->r[i]; p.dv_s[i] = dv->s[i];
         }
         p.rs_mask = 0;
+        p.tap4 = 0;
         p.w_vec = 0;
     }
     p.lstm_ch = 0;

@@ -57,6 +57,8 @@ SHAPES = [
     (2, 33, 7, 7, 264, 1, 1, 1, 0, 1, True),       # 1x1, ragged K past 256
     (1, 8, 3, 3, 16, 3, 3, 1, 0, 1, True),         # one output pixel per image
     (5, 24, 12, 12, 48, 3, 3, 1, 1, 1, True),      # several tiles per CTA
+    (2, 5, 9, 11, 24, 2, 2, 1, 1, 2, True),        # 2x2 (table-free taps), dilation 2, C % 8 != 0
+    (2, 13, 10, 7, 40, 2, 2, 2, 1, 1, False),      # 2x2 stride 2, ragged second stage
 ]
 
 
