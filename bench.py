@@ -72,7 +72,7 @@ def fp32_alu_peak_tflops():
 # capture of the current kernel (profiles/ holds the summary and command);
 # keyed by (layer, kernel family as the plan string starts).
 DRAM_TRAFFIC = {
-    ("mscred_enc_l2_n256_c32_30x30_k64_3x3s2p1", "tensor_core tcgen05 3xtf32"): 29627648 + 1280,
+    ("mscred_enc_l2_n256_c32_30x30_k64_3x3s2p1", "tensor_core tcgen05 3xtf32"): 29628416 + 1280,
 }
 
 # nominal dense TF32 / BF16 tensor rates of GB300 (1.1 and 2.25 PFLOP/s)
