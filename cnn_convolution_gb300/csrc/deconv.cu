@@ -24,7 +24,8 @@
 // asynchronous copies (cp.async, zero-fill outside x), double-buffered: the
 // next chunk is in flight while the current one is summed.  Each thread
 // keeps bitmasks of its valid filter rows and columns; per valid tap: one input
-// read, CB/4 broadcast 16-byte weight reads, CB FFMAs.
+// read, CB/4 broadcast 16-byte weight reads, CB FFMAs.  (Stride-1 layers with
+// few output channels on small images take deconv_s1_kernel, below.)
 
 #include <algorithm>
 #include <cstdint>
@@ -39,7 +40,6 @@ namespace {
 constexpr int kDvThreads = 256;      // = output pixels per CTA (one per thread)
 constexpr int kDvK = 16;             // input channels per staged chunk
 constexpr int kDvMaxTap = 8;         // R, S <= 8
-constexpr int kDvBatch = 8;          // staging loads in flight per thread
 
 struct DvParams {
     const float *x, *w, *bias;
