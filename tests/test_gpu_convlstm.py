@@ -114,3 +114,31 @@ def test_cell_argument_errors():
         conv2d.convlstm_cell(xh, w, None, c0, pad=0)
     with pytest.raises(conv2d.Conv2dError):       # c_next aliasing c_prev
         conv2d.convlstm_cell(xh, w, None, c0, pad=1, c_next=c0)
+
+
+N_TF_VARIANTS = 13   # the 3xTF32 variant table of the library
+
+
+@pytest.mark.parametrize("variant", range(N_TF_VARIANTS))
+def test_cell_forced_variants(variant):
+    """Every 3xTF32 variant that carries the gate epilogue (8 or more
+    producer warps, one or two producer groups) gives the same cell; the
+    others are refused as unsupported."""
+    import os
+    os.environ["CONV2D_TF_VAR"] = str(variant)
+    try:
+        ran = 0
+        for i, (N, Cx, Ch, H, W, R) in enumerate([(2, 5, 7, 6, 13, 3), (2, 16, 16, 12, 12, 3)]):
+            xh, w, b, c0 = _inputs(N, Cx, Ch, H, W, R, seed=500 + 10 * variant + i)
+            try:
+                c, h = conv2d.convlstm_cell(xh.cuda(), w.cuda(), b.cuda(), c0.cuda(), pad=R // 2)
+            except conv2d.Conv2dError as e:
+                assert e.code == 2, e
+                continue
+            torch.cuda.synchronize()
+            _check(xh, w, b, c0, R // 2, c, h)
+            ran += 1
+    finally:
+        os.environ.pop("CONV2D_TF_VAR", None)
+    if variant >= 3:    # 8 or more producer warps
+        assert ran >= 1

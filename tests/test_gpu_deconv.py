@@ -106,3 +106,20 @@ def test_deconv_argument_errors():
     with pytest.raises(conv2d.Conv2dError):
         conv2d.deconv_forward(x.half(), w.half(), None, 1, 0)       # fp16: not supported
     assert conv2d.get_device_status() == 0
+
+
+@pytest.mark.parametrize("variant", range(13))
+def test_deconv_forced_variants(variant):
+    """Each 3xTF32 variant in residue-class mode (a variant that cannot hold a
+    class sends the layer to the gather kernel, which must agree too)."""
+    import os
+    os.environ["CONV2D_TF_VAR"] = str(variant)
+    os.environ["CONV2D_DECONV_TC"] = "1"
+    try:
+        for case in [(2, 8, 6, 6, 5, 3, 3, 2, 1, 1, 1), (2, 6, 7, 8, 33, 3, 3, 2, 1, 2, 1),
+                     (2, 20, 5, 5, 40, 2, 2, 2, 0, 1, 0)]:
+            err = _run(*case, seed=900 + variant)
+            assert err <= TOL["f32"], (case, variant, err)
+    finally:
+        os.environ.pop("CONV2D_TF_VAR", None)
+        os.environ.pop("CONV2D_DECONV_TC", None)
