@@ -129,14 +129,16 @@ double cc_cost(const Shape &s, const CudaCoreTile &t, int split, int sms) {
     return work * reduce / (r.tflops * fill);
 }
 
-// Direct kernel (short reductions): FFMAs of whole 16 x 32 pixel blocks x
+// Direct kernel (short reductions): FFMAs of whole pixel blocks (8 x 32) x
 // 32-channel blocks at an effective 30 TFLOP/s, plus about 3 us of launch
 // and staging.  In the units of cc_cost(), whose tile rates overestimate
 // short reductions by a similar factor: on the MSCRED layer-1 shape on GB300
-// the direct kernel measures 26 us against 32 us for the best tile.
+// the direct kernel measures 24.5 us against 32 us for the best tile.
 double dc_cost(const Shape &s) {
-    const double blocks = (double)s.N * ((s.P + 15) / 16) * ((s.Q + 31) / 32);
-    const double fma = blocks * 512.0 * (double)((s.K + 31) / 32 * 32) * (double)s.Kg;
+    int rows, cols, threads, kc;
+    dc_block(&rows, &cols, &threads, &kc);
+    const double blocks = (double)s.N * ((s.P + rows - 1) / rows) * ((s.Q + cols - 1) / cols);
+    const double fma = blocks * rows * cols * (double)((s.K + kc - 1) / kc * kc) * (double)s.Kg;
     return (2.0 * fma / 30e3 + 3000.0) / 2e-3;
 }
 
@@ -548,10 +550,12 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
                       p.tc.window ? "window"
                       : (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
                          !p.tc.force_im2col) ? "tile" : "im2col");
-    else if (p.algo == Algo::Direct)
-        std::snprintf(buf, len, "cuda_core direct ffma block=16x32px kc=32 threads=256 grid=%d smem=%zu",
-                      p.grid, p.smem_bytes);
-    else if (p.algo == Algo::Tf32x3)
+    else if (p.algo == Algo::Direct) {
+        int rows, cols, threads, kc;
+        dc_block(&rows, &cols, &threads, &kc);
+        std::snprintf(buf, len, "cuda_core direct ffma block=%dx%dpx kc=%d threads=%d grid=%d smem=%zu",
+                      rows, cols, kc, threads, p.grid, p.smem_bytes);
+    } else if (p.algo == Algo::Tf32x3)
         std::snprintf(buf, len, "tensor_core tcgen05 3xtf32 BM=128 BN=%d BK=32 stages=%d producers=%d groups=%d%s grid=%d smem=%zu",
                       p.tf.BN, p.tf.stages, p.tf.nprod * 32, p.tf.ngrp, p.tf.resb ? " resident-w" : "", p.grid,
                       p.smem_bytes);

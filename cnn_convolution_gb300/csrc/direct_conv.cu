@@ -8,15 +8,17 @@
 // computed without any lowering: with only C*R*S <= 64 products per output
 // the im2col / GEMM machinery costs more than the arithmetic.
 //
-// A CTA of 256 threads owns a 16 x 32 block of output pixels of one image
-// and every output channel.  It stages the zero-padded input patch that
+// A CTA of 128 threads owns an 8 x 32 block of output pixels of one image
+// and every output channel; four CTAs share an SM (small blocks keep the
+// most loaded SM close to the average when the blocks do not divide evenly
+// over the SMs).  It stages the zero-padded input patch that
 // block reads ([C][IH][IW]) and the weights transposed to [C*R*S][K] in
 // shared memory, then each thread accumulates 2 pixels (rows 2w, 2w+1 of the
 // block, column = lane) x 32 channels in registers: per filter tap, 2 patch
 // reads and 8 broadcast 16-byte weight reads feed 64 FFMAs.  Channel blocks
-// of 32 repeat over the same staged patch.  (A 16-channel block with 4 CTAs
-// per SM measured slower on GB300: the register cap forces spills.)  Zero padding lives in the patch,
-// so the inner loop has no bounds tests.  NCHW stores are coalesced across
+// of 32 repeat over the same staged patch.  (A 16-channel block at 64
+// registers per thread measured slower on GB300: the cap forces spills.)
+// Zero padding lives in the patch, so the inner loop has no bounds tests.  NCHW stores are coalesced across
 // the lanes of a warp (consecutive q); NHWC stores are 16-byte vectors.
 
 #include <cstdint>
@@ -27,8 +29,8 @@
 namespace conv2d {
 namespace {
 
-constexpr int kDcThreads = 256;
-constexpr int kDcRows = 16;      // output rows per CTA (2 per warp)
+constexpr int kDcThreads = 128;
+constexpr int kDcRows = 8;       // output rows per CTA (2 per warp)
 constexpr int kDcCols = 32;      // output columns per CTA (1 per lane)
 constexpr int kDcKc = 32;        // output channels per register block
 
@@ -51,7 +53,7 @@ using sm103a::fdiv;
 
 // RT, ST: compile-time filter size (0 = read from the parameters).
 template <int RT, int ST>
-__global__ void __launch_bounds__(kDcThreads, 2) direct_conv_kernel(const DcParams p) {
+__global__ void __launch_bounds__(kDcThreads, 4) direct_conv_kernel(const DcParams p) {
     extern __shared__ float4 dc_smem4[];
     const int R = RT > 0 ? RT : p.R;
     const int S = ST > 0 ? ST : p.S;
@@ -220,6 +222,13 @@ bool dc_shape_ok(const Shape &s) {
     return dc_smem_bytes(s) <= 96 * 1024;
 }
 
+
+void dc_block(int *rows, int *cols, int *threads, int *kc) {
+    *rows = kDcRows;
+    *cols = kDcCols;
+    *threads = kDcThreads;
+    *kc = kDcKc;
+}
 
 int dc_grid(const Shape &s) {
     return (int)((int64_t)s.N * ((s.P + kDcRows - 1) / kDcRows) * ((s.Q + kDcCols - 1) / kDcCols));

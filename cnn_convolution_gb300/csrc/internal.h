@@ -103,6 +103,7 @@ conv2d_status_t tc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaS
 bool dc_shape_ok(const Shape &s);
 size_t dc_smem_bytes(const Shape &s);
 int dc_grid(const Shape &s);
+void dc_block(int *rows, int *cols, int *threads, int *kc);   // the direct kernel's CTA block
 conv2d_status_t dc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaStream_t st);
 
 // fp32 tensor-core path (3xTF32 split precision, NCHW or NHWC).

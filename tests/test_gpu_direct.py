@@ -1,6 +1,6 @@
 """GPU parity of the direct fp32 kernel for short reductions (C*R*S <= 64).
 
-Forced on (CONV2D_DIRECT=1) over both layouts: output blocks of 16 x 32
+Forced on (CONV2D_DIRECT=1) over both layouts: output blocks of 8 x 32
 pixels with ragged edges in both directions, several 32-channel blocks and a
 channel count that is not a multiple of 4 (scalar NHWC stores), strides,
 padding wider than the filter, dilation, bias on and off, and the MSCRED
@@ -80,9 +80,9 @@ def test_mscred_layers_direct(direct_on):
 
 
 def test_direct_not_used_where_it_cannot_apply(direct_on):
-    # C*R*S = 72 > 64; and a 1x1 layer with 64 channels whose staged patch
-    # (64 x 16 x 32 floats) exceeds the shared-memory budget
-    for (C, R) in [(8, 3), (64, 1)]:
-        d = conv2d.Conv2dDesc(2, C, 10, 10, 16, R, R, 1, R // 2, 1, torch.float32, "NCHW")
+    # C*R*S = 72 > 64; and a stride-4 1x1 layer with 64 channels whose staged
+    # patch (64 x 29 x 125 floats) exceeds the shared-memory budget
+    for (C, R, st) in [(8, 3, 1), (64, 1, 4)]:
+        d = conv2d.Conv2dDesc(2, C, 10, 10, 16, R, R, st, R // 2, 1, torch.float32, "NCHW")
         d.set_algo("cuda_core")
         assert "direct" not in d.plan(), d.plan()
