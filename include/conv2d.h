@@ -202,7 +202,11 @@ conv2d_status_t conv2d_deconv_output_dims(int P, int Q, int R, int S, int stride
  * x: [N][K][P][Q]; w: [K][C][R][S] (the forward convolution's weights);
  * bias: [C] or NULL; y: [N][C][H][W] (conv2d_deconv_output_dims).  fp32 NCHW
  * (CONV2D_ERR_UNSUPPORTED for other dtypes / layouts), R, S <= 8.  A gather,
- * deterministic, no atomics, no workspace.  Pointers: device memory of the
+ * deterministic, no atomics, no workspace: layers with more than 8 output
+ * channels run on the 3xTF32 tensor-core kernel, one launch per output
+ * residue class (h mod stride, w mod stride); the others (and layers with a
+ * residue class without taps) on FFMA kernels.  Results meet the fp32 bound
+ * 1e-6 * (sum |x||w| + |bias|) either way.  Pointers: device memory of the
  * current device, 4-byte aligned; y must not overlap x, w or bias.
  * Asynchronous on stream.  Errors as for conv2d_forward.
  */
