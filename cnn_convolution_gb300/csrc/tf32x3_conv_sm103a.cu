@@ -874,8 +874,8 @@ conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t,
 // 3-stage variant leaves shared memory for the tap tables of long
 // reductions (C*R*S up to about 9,000).  The resident-weight variants split
 // the weights once per CTA (C*R*S up to about 350 at BN = 64).  Two producer
-// groups (last three rows) took the encoder layers 5-10 % below the best
-// one-group variant.
+// groups (last four rows) took the encoder layers 5-10 % and the decoder's
+// 32-channel-wide residue classes 7-14 % below the best one-group variant.
 #define CONV2D_TF_VARIANTS(X)        \
     X(32, 5, 4, 1240, false, 1)      \
     X(64, 4, 4, 3850, false, 1)      \
@@ -889,7 +889,8 @@ conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t,
     X(64, 3, 16, 1060, true, 1)      \
     X(64, 4, 16, 990, false, 2)       \
     X(64, 2, 16, 940, true, 2)         \
-    X(128, 2, 16, 2400, false, 2)
+    X(128, 2, 16, 2400, false, 2)    \
+    X(32, 5, 16, 820, false, 2)
 
 }  // namespace
 

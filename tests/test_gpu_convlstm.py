@@ -116,7 +116,7 @@ def test_cell_argument_errors():
         conv2d.convlstm_cell(xh, w, None, c0, pad=1, c_next=c0)
 
 
-N_TF_VARIANTS = 13   # the 3xTF32 variant table of the library
+N_TF_VARIANTS = 14   # the 3xTF32 variant table of the library
 
 
 @pytest.mark.parametrize("variant", range(N_TF_VARIANTS))

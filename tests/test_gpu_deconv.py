@@ -108,7 +108,7 @@ def test_deconv_argument_errors():
     assert conv2d.get_device_status() == 0
 
 
-@pytest.mark.parametrize("variant", range(13))
+@pytest.mark.parametrize("variant", range(14))
 def test_deconv_forced_variants(variant):
     """Each 3xTF32 variant in residue-class mode (a variant that cannot hold a
     class sends the layer to the gather kernel, which must agree too)."""

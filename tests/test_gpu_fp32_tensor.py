@@ -20,7 +20,7 @@ from parity import TOL, full_parity, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-N_VARIANTS = 13   # (BN, stages, producer warps, groups) table of the library
+N_VARIANTS = 14   # (BN, stages, producer warps, groups) table of the library
 
 
 @pytest.fixture(scope="module", autouse=True)
