@@ -13,15 +13,25 @@ launching stream; a step is one replay of a CUDA graph holding the 4 C-ABI
 launches, with the L2 flush (a 256 MiB write) and the two timing events
 captured inside the same graph, so the events bracket only the 4 kernels:
 neither host-side validation nor the graph launch latency sits inside them.
-The JSON line also reports the eager (non-graph) step time, the host time of
-one C-ABI call, an end-to-end time with host<->device copies, and the step
-with the fp32 tensor-core (3xTF32) path switched off (CUDA-core FFMA only).  Barrier + synchronize on both sides of the timed region;
-the slowest rank's time is reported.  With --gpus N > 1 (torchrun) every rank
-runs an independent replica of the workload (the layer needs no exchange),
-so the total work grows with N ("weak" scaling).
+Barrier + synchronize on both sides of the timed region; the slowest rank's
+time is reported.  With --gpus N > 1 (torchrun) every rank runs an
+independent replica of the workload (the layer needs no exchange), so the
+total work grows with N ("weak" scaling).
 
-The same JSON line also carries the tensor-core layers (fp16/bf16 NHWC),
-each timed alone, with their own roofline fractions.
+Beside the step the JSON line carries: every encoder layer and every
+fp16/bf16 layer timed alone (--layer-iters replays, 10 warm-ups, L2 flushed
+before each, median / mean / min), the single signature-matrix convolution
+and the 1x1 kernel-size-sweep layer also as a CUDA graph of 100 back-to-back
+launches (the per-call floor), the eager step and the host time of one C-ABI
+call, an end-to-end step with host<->device copies, the step with the fp32
+tensor-core (3xTF32) path off, the fp32 FFMA / TF32 / BF16 MMA peaks measured
+by the library's probe kernels (the fp32 roofline denominators), and the
+nvidia-smi clocks sampled across every GPU leg.
+
+The cpu_baseline leg times the fp64 oracle on the host cores (all cores, and
+one core for the single convolution and layer 1) and compares the bench's own
+GPU outputs (encoder layers, fp16/bf16 layers, single convolution) with it at
+random, border and per-tile sample points.
 
 --impl reference times the fp64 CPU oracle on the same workload (a bounded
 sample of it) on the host cores.
@@ -38,6 +48,7 @@ import sys
 import threading
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -63,36 +74,71 @@ def load_peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
-def fp32_alu_peak_tflops():
-    """FFMA peak from unit counts and the maximum SM clock: SMs x 128 lanes x 2 x f."""
+def fp32_alu_peak_tflops(peaks=None):
+    """FFMA peak: the probe kernel's measurement of this run when there is one,
+    else SMs x 128 lanes x 2 x the maximum SM clock."""
+    if peaks and peaks.get("ffma_tflops_probe"):
+        return peaks["ffma_tflops_probe"]
     return SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
 
 
 # DRAM bytes (read + write) per launch of a layer's kernel, from one ncu
-# capture of the current kernel (profiles/ holds the summary and command);
-# keyed by (layer, kernel family as the plan string starts).
-DRAM_TRAFFIC = {
-    ("mscred_enc_l2_n256_c32_30x30_k64_3x3s2p1", "tensor_core tcgen05 3xtf32"): 29628416 + 1280,
-}
+# capture of the kernel with the plan given here (profiles/ holds the summary
+# and command); a plan that differs gets null.
+DRAM_TRAFFIC = {}
 
-# nominal dense TF32 / BF16 tensor rates of GB300 (1.1 and 2.25 PFLOP/s)
+# nominal dense TF32 / BF16 tensor rates of GB300 (1.1 and 2.25 PFLOP/s), used
+# only when the probe measurement is missing
 TF32_PER_BF16 = 1.1 / 2.25
 
 
 def fp32_3xtf32_peak_tflops(peaks):
     """fp32 convolution on tensor cores as three TF32 products per multiply-add:
-    measured bf16 peak x nominal TF32/BF16 ratio / 3."""
+    the measured TF32 MMA rate / 3."""
+    if peaks.get("tf32_mma_tflops_probe"):
+        return peaks["tf32_mma_tflops_probe"] / 3.0
     return peaks["bf16_tflops"] * TF32_PER_BF16 / 3.0
 
 
 def layer_peak(plan, peaks):
     """(bound, peak TFLOP/s, source) for the kernel a plan string names."""
     if plan.startswith("tensor_core tcgen05 3xtf32"):
+        if peaks.get("tf32_mma_tflops_probe"):
+            return ("tensor", fp32_3xtf32_peak_tflops(peaks),
+                    f"measured TF32 MMA rate {peaks['tf32_mma_tflops_probe']:.1f} TFLOP/s "
+                    "(conv2d_peak_probe, this run) / 3 TF32 products per fp32 multiply-add")
         return ("tensor", fp32_3xtf32_peak_tflops(peaks),
-                f"measured bf16 {peaks['bf16_tflops']} TFLOP/s x nominal TF32/BF16 (1.1/2.25) "
-                "/ 3 TF32 products per fp32 multiply-add")
-    return ("alu", fp32_alu_peak_tflops(),
-            "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz")
+                f"measured bf16 {peaks['bf16_tflops']} TFLOP/s x nominal TF32/BF16 (1.1/2.25) / 3")
+    if peaks.get("ffma_tflops_probe"):
+        return ("alu", fp32_alu_peak_tflops(peaks),
+                "measured FFMA rate (conv2d_peak_probe, this run)")
+    return ("alu", fp32_alu_peak_tflops(), "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz")
+
+
+def measure_probe_peaks(reps=5):
+    """TFLOP/s of the library's FFMA, TF32-MMA and BF16-MMA probe kernels
+    (best of `reps` timings of three back-to-back launches of a few ms each,
+    CUDA events)."""
+    from cnn_convolution_gb300 import conv2d
+    out = {}
+    for kind, iters in (("ffma", 4000), ("tf32_mma", 12000), ("bf16_mma", 12000)):
+        conv2d.peak_probe(kind, max(1, iters // 8))
+        torch.cuda.synchronize()
+        best = 0.0
+        for _ in range(reps):
+            # three launches between the events: the host time of a call
+            # overlaps the previous launch instead of sitting in the interval
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(1_000_000)
+            e0.record()
+            fl = sum(conv2d.peak_probe(kind, iters) for _ in range(3))
+            e1.record()
+            e1.synchronize()
+            best = max(best, fl / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+        out[f"{kind}_tflops_probe"] = round(best, 2)
+    if conv2d.get_device_status() != 0:
+        raise RuntimeError("a probe kernel reported a barrier timeout")
+    return out
 
 
 # ------------------------------------------------------------------ distributed
@@ -129,7 +175,8 @@ def max_over_ranks(v, world):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    """nvidia-smi clocks / throttle reasons, sampled every 50 ms from start()
+    to stop(); summary() covers a time window (default: all samples)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -137,13 +184,13 @@ class ClockSampler:
     def __init__(self, device_index):
         self.idx = device_index
         self.proc = None
-        self.lines = []
+        self.samples = []          # (perf_counter time, line)
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "20"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -151,11 +198,16 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def wait_first(self, timeout=5.0):
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.samples and time.perf_counter() - t0 < timeout:
+            time.sleep(0.02)
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.perf_counter(), line.strip()))
 
-    def __exit__(self, *a):
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -163,17 +215,21 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.thread.join(timeout=2)
+            self.proc = None
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
+    def summary(self, t0=None, t1=None):
+        sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in list(self.samples):
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for name, val in zip(names, parts[5:9]):
@@ -181,8 +237,8 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(mx),
+                "power_w_max": max(power), "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ------------------------------------------------------------------ workload
@@ -277,6 +333,60 @@ class TimedGraph:
         return self.e0.elapsed_time(self.e1)
 
 
+def time_graph(tg, iters, warm=10):
+    """Replay a TimedGraph `warm` times, then `iters` times; (median, mean, min) ms."""
+    for _ in range(warm):
+        tg.replay_ms()
+    ts = [tg.replay_ms() for _ in range(iters)]
+    return statistics.median(ts), statistics.mean(ts), min(ts)
+
+
+def graph_floor_us(fn, n=100, reps=5):
+    """Per-call time of `fn` in a CUDA graph of n back-to-back calls (no L2
+    flush between them): the launch-and-tail floor of a small layer."""
+    g = capture(lambda: [fn() for _ in range(n)])
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e3 / n)
+    return best
+
+
+def single_conv_leg(device, flush, iters, peaks):
+    """The single signature-matrix convolution (1x3x30x30 -> 32, 3x3, fp32):
+    one launch after an L2 flush, and the per-call floor of 100 launches."""
+    from cnn_convolution_gb300 import conv2d, workloads as wl
+    spec = wl.MSCRED_SINGLE
+    x, w, b = wl.mscred_single_inputs()
+    d = conv2d.Conv2dDesc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride,
+                          spec.pad, spec.dil, torch.float32, "NCHW")
+    xd, wd, bd = x.to(device), w.to(device), b.to(device)
+    y = torch.empty(d.y_shape(), dtype=torch.float32, device=device)
+    for _ in range(3):
+        d.forward(xd, wd, bd, y=y)
+    torch.cuda.synchronize()
+    med, mean, mn = time_graph(TimedGraph(lambda: d.forward(xd, wd, bd, y=y), flush), iters)
+    floor = graph_floor_us(lambda: d.forward(xd, wd, bd, y=y))
+    P, Q = d.output_dims()
+    fl = 2.0 * spec.N * spec.K * P * Q * spec.C * spec.R * spec.S
+    d.forward(xd, wd, bd, y=y)
+    torch.cuda.synchronize()
+    res = {"layer": spec.name, "plan": d.plan(), "us_median": round(med * 1e3, 3),
+           "us_min": round(mn * 1e3, 3), "tflops": round(fl / (med * 1e-3) / 1e12, 4),
+           "graph_100_per_call_us": round(floor, 3),
+           "graph_100_tflops": round(fl / (floor * 1e-6) / 1e12, 4), "bound": "latency",
+           "workspace_bytes": d.workspace_bytes(), "iters": iters}
+    idx = np.stack([a.reshape(-1) for a in np.indices((spec.N, spec.K, P, Q))], axis=1)
+    return res, (spec, x, w, b, idx, wl.gather_points(y, idx, "NCHW").cpu())
+
+
 def bench_main(args):
     rank, world, local = dist_setup(args.gpus)
     if not torch.cuda.is_available():
@@ -284,9 +394,15 @@ def bench_main(args):
         return 1
     device = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(device)
-    from cnn_convolution_gb300 import conv2d
+    from cnn_convolution_gb300 import conv2d, workloads as wl
     conv2d.load()
     peaks, peak_src = load_peaks()
+    peaks = dict(peaks)
+
+    clk = ClockSampler(device.index).start()
+    clk.wait_first()
+    t_gpu0 = time.perf_counter()
+    peaks.update(measure_probe_peaks())
 
     specs, x_host, descs, ws, bs, outs, flops = encoder_setup(device)
     x_dev = x_host.to(device)
@@ -307,32 +423,28 @@ def bench_main(args):
             lambda i=i, src=src: descs[i].forward(src, ws[i], bs[i], y=outs[i]), flush))
     torch.cuda.synchronize()
 
-    step_ms, layer_ms = [], [[] for _ in range(n_layers)]
-    # the clock sampler runs from the warm-up through the end of the timed region
-    with ClockSampler(device.index) as clk:
-        for _ in range(args.warmup):
-            step_graph.replay_ms()
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        t_wall0 = time.perf_counter()
-        for _ in range(args.steps):
-            step_ms.append(step_graph.replay_ms())
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
-        barrier(world)
-        # per-layer launches, each alone after an L2 flush (not part of the step time)
-        for _ in range(max(3, args.steps // 4)):
-            for i in range(n_layers):
-                layer_ms[i].append(layer_graphs[i].replay_ms())
-        torch.cuda.synchronize()
+    step_ms = []
+    for _ in range(args.warmup):
+        step_graph.replay_ms()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        step_ms.append(step_graph.replay_ms())
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
+    barrier(world)
     local_ms = statistics.mean(step_ms)
     ms = max_over_ranks(local_ms, world)
     value = step_flops * world / (ms * 1e-3) / 1e12
 
+    # per-layer launches, each alone after an L2 flush (not part of the step time)
+    layer_t = [time_graph(layer_graphs[i], args.layer_iters) for i in range(n_layers)]
+
     # eager step (every call through the C ABI from Python, host overhead included)
     eager = []
-    for _ in range(max(3, args.steps // 4)):
+    for _ in range(max(10, args.steps // 4)):
         flush.zero_()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -352,26 +464,30 @@ def bench_main(args):
     torch.cuda.synchronize()
 
     # per-layer roofline; the dominant kernel is the layer with the largest time
-    alu_peak = fp32_alu_peak_tflops()
     layers = []
     for i, (spec, d) in enumerate(zip(specs, descs)):
         P, Q = d.output_dims()
-        t = statistics.mean(layer_ms[i])
-        tf = flops[i] / (t * 1e-3) / 1e12
-        gbs = layer_bytes(spec, P, Q) / (t * 1e-3) / 1e9
+        med, mean, mn = layer_t[i]
+        tf = flops[i] / (mean * 1e-3) / 1e12
+        gbs = layer_bytes(spec, P, Q) / (mean * 1e-3) / 1e9
         bound, cpeak, _ = layer_peak(d.plan(), peaks)
-        layers.append({"layer": spec.name, "plan": d.plan(), "ms": round(t, 5),
-                       "tflops": round(tf, 3), "bound": bound, "compute_frac": round(tf / cpeak, 4),
-                       "alu_frac": round(tf / alu_peak, 4),
-                       "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)})
-    dom = max(range(n_layers), key=lambda i: statistics.mean(layer_ms[i]))
-    dom_t = statistics.mean(layer_ms[dom])
+        layers.append({"layer": spec.name, "plan": d.plan(), "ms": round(mean, 5),
+                       "ms_median": round(med, 5), "ms_min": round(mn, 5),
+                       "tflops": round(tf, 3), "bound": bound, "peak": round(cpeak, 2),
+                       "compute_frac": round(tf / cpeak, 4),
+                       "alu_frac": round(tf / fp32_alu_peak_tflops(peaks), 4),
+                       "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                       "iters": args.layer_iters})
+    dom = max(range(n_layers), key=lambda i: layer_t[i][1])
+    dom_t = layer_t[dom][1]
     achieved = flops[dom] / (dom_t * 1e-3) / 1e12
     dom_bound, dom_peak, dom_src = layer_peak(descs[dom].plan(), peaks)
-    traffic = DRAM_TRAFFIC.get((specs[dom].name, descs[dom].plan().split(" BM=")[0]))
+    traffic = DRAM_TRAFFIC.get((specs[dom].name, descs[dom].plan()))
     roofline = {"kernel": specs[dom].name, "plan": descs[dom].plan(), "bound": dom_bound,
                 "achieved": round(achieved, 3), "peak": round(dom_peak, 2), "unit": "TFLOP/s",
-                "frac": round(achieved / dom_peak, 4), "traffic": traffic, "peak_source": dom_src}
+                "frac": round(achieved / dom_peak, 4), "traffic": traffic, "peak_source": dom_src,
+                "duration_us": round(dom_t * 1e3, 3),
+                "algorithmic_flops_per_launch": flops[dom]}
 
     # end to end through the C ABI: pinned host x -> device, 4 layers, y -> pinned host
     x_pin = x_host.pin_memory()
@@ -396,18 +512,27 @@ def bench_main(args):
            "h2d_bytes_per_step": x_pin.numel() * 4, "d2h_bytes_per_step": y_pin.numel() * 4,
            "launch": "eager C-ABI calls from Python (host overhead included)"}
 
+    # the step's outputs, for the oracle check of the cpu_baseline leg: each
+    # layer's sampled outputs and the input that layer received
+    run_encoder(descs, x_dev, ws, bs, outs)
+    torch.cuda.synchronize()
+    enc_check = []
+    for i, (spec, d) in enumerate(zip(specs, descs)):
+        P, Q = d.output_dims()
+        idx = wl.check_points(spec, P, Q, seed=i)
+        src = x_host if i == 0 else outs[i - 1].cpu()
+        enc_check.append((spec, src, ws[i].cpu(), bs[i].cpu(), idx,
+                          wl.gather_points(outs[i], idx, "NCHW").cpu()))
+
     # the same step with the fp32 tensor-core (3xTF32) path switched off:
     # every layer on CUDA-core FFMA kernels (direct / implicit GEMM)
-    os.environ["CONV2D_FP32_TC"] = "0"
-    try:
+    with conv2d.overrides(fp32_tc=0):
         for _ in range(2):
             run_encoder(descs, x_dev, ws, bs, outs)
         torch.cuda.synchronize()
         cc_graph = TimedGraph(lambda: run_encoder(descs, x_dev, ws, bs, outs), flush)
         cc_plans = [d.plan() for d in descs]
-        cc_ms = [cc_graph.replay_ms() for _ in range(max(5, args.steps // 4))]
-    finally:
-        os.environ.pop("CONV2D_FP32_TC", None)
+        cc_ms = [cc_graph.replay_ms() for _ in range(max(10, args.steps // 4))]
     cc_t = max_over_ranks(statistics.mean(cc_ms), world)
     fp32_cuda_core_only = {"value": round(step_flops * world / (cc_t * 1e-3) / 1e12, 4),
                            "unit": "TFLOPS", "ms_per_step": round(cc_t, 5), "plans": cc_plans}
@@ -418,18 +543,29 @@ def bench_main(args):
     # pinned host y), which moves 38 KB to the device instead of 2.8 MB
     sig = signature_stage(device, flush, descs, ws, bs, outs, peaks, args, world)
 
-    cells = convlstm_cells(device, flush, peaks, iters=max(5, args.steps // 4)) if rank == 0 else []
-    decoder = decoder_layers(device, flush, peaks, iters=max(5, args.steps // 4)) if rank == 0 else []
+    single, single_check = single_conv_leg(device, flush, args.layer_iters, peaks) \
+        if rank == 0 else (None, None)
+    cells = convlstm_cells(device, flush, peaks, iters=args.layer_iters) if rank == 0 else []
+    decoder = decoder_layers(device, flush, peaks, iters=args.layer_iters) if rank == 0 else []
 
-    extra = []
+    extra, tc_check = [], []
     if not args.no_tensor_core and rank == 0:
-        extra = tensor_core_layers(device, peaks, flush, iters=max(5, args.steps // 4))
+        extra, tc_check = tensor_core_layers(device, peaks, flush, iters=args.layer_iters,
+                                             keep_check=True)
+    torch.cuda.synchronize()
+    t_gpu1 = time.perf_counter()
+    clk.stop()
+    clocks = clk.summary(t_gpu0, t_gpu1)
+    clocks["window"] = "every GPU leg of this run (probe peaks through the fp16/bf16 layers)"
+    step_clk = clk.summary(t_wall0, t_wall1)
+    clocks["timed_region_samples"] = step_clk["samples"]
+    clocks["timed_region_sm_mhz"] = step_clk["sm_mhz"]
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(x_host, [(w.cpu(), b.cpu()) for w, b in zip(ws, bs)], specs, flops)
+        cpu = cpu_baseline(x_host, [(w.cpu(), b.cpu()) for w, b in zip(ws, bs)], specs, flops,
+                           checks=enc_check + tc_check + ([single_check] if single_check else []))
 
-    clocks = clk.summary()
     if rank == 0:
         out = {
             "metric": METRIC, "value": round(value, 4), "unit": "TFLOPS", "n_gpus": world,
@@ -447,15 +583,20 @@ def bench_main(args):
             "host_us_per_call": round(host_us, 2),
             "e2e": e2e,
             "fp32_cuda_core_only": fp32_cuda_core_only,
+            "single_signature_conv": single,
             "signature_matrices": sig,
             "convlstm_cells": cells,
             "decoder_deconv_layers": decoder,
             "gpu_launches": n_layers * args.steps,
             "clocks": clocks,
             "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
-                      "bf16_tflops": peaks["bf16_tflops"], "fp32_alu_tflops": round(alu_peak, 2),
-                      "fp32_3xtf32_tflops": round(fp32_3xtf32_peak_tflops(peaks), 2)},
-            "wall_s_timed_region": round(t_wall, 4),
+                      "bf16_tflops": peaks["bf16_tflops"],
+                      "ffma_tflops_probe": peaks.get("ffma_tflops_probe"),
+                      "tf32_mma_tflops_probe": peaks.get("tf32_mma_tflops_probe"),
+                      "bf16_mma_tflops_probe": peaks.get("bf16_mma_tflops_probe"),
+                      "fp32_3xtf32_tflops": round(fp32_3xtf32_peak_tflops(peaks), 2),
+                      "probe": "conv2d_peak_probe kernels, best of 5 launches, CUDA events"},
+            "wall_s_timed_region": round(t_wall1 - t_wall0, 4),
             "tensor_core_layers": extra,
             "cpu_baseline": cpu,
         }
@@ -576,28 +717,28 @@ def decoder_layers(device, flush, peaks, iters, n=256):
         else:
             path = ("FFMA, one image per CTA, 4 pixels x %d channels per thread" % (4 if C <= 4 else 8)
                     if st == 1 else "gather kernel, FFMA, %d-channel block" % (4 if C <= 4 else 8))
-            bound, peak = "alu", fp32_alu_peak_tflops()
+            bound, peak = "alu", fp32_alu_peak_tflops(peaks)
         out.append({"layer": name, "us": round(t * 1e3, 2), "tflops": round(tf, 2), "path": path,
                     "bound": bound, "frac": round(tf / peak, 4), "hbm_gbs": round(gbs, 1)})
     return out
 
 
-def time_layer(d, x, w, b, y, flush, iters, warm=3):
-    """Median / min kernel time of one layer (L2 flushed before each launch)."""
-    for _ in range(warm):
+def time_layer(d, x, w, b, y, flush, iters, warm=10):
+    """(median, mean, min) kernel time of one layer, L2 flushed before each launch."""
+    for _ in range(3):
         d.forward(x, w, b, y=y)
     torch.cuda.synchronize()
-    tg = TimedGraph(lambda: d.forward(x, w, b, y=y), flush)
-    ts = [tg.replay_ms() for _ in range(iters)]
-    return statistics.median(ts), min(ts)
+    return time_graph(TimedGraph(lambda: d.forward(x, w, b, y=y), flush), iters, warm)
 
 
-def tensor_core_layers(device, peaks, flush, iters=10, names=None):
+def tensor_core_layers(device, peaks, flush, iters=50, names=None, keep_check=False):
     """Time each fp16/bf16 NHWC layer alone (L2 flushed before each launch).
 
-    With `names`, time those layers instead (any named layer, fp32 included)."""
+    With `names`, time those layers instead (any named layer, fp32 included).
+    With keep_check, also return each layer's sampled outputs (and inputs) for
+    the oracle check of the cpu_baseline leg."""
     from cnn_convolution_gb300 import conv2d, workloads as wl
-    res = []
+    res, checks = [], []
     tc_peak = peaks["bf16_tflops"]
     specs = [wl.ALL_LAYERS[n] for n in names] if names else wl.TENSOR_CORE_WORKLOADS
     for spec in specs:
@@ -607,46 +748,94 @@ def tensor_core_layers(device, peaks, flush, iters=10, names=None):
         xd, wd = x.to(device), w.to(device)
         bd = None if b is None else b.to(device)
         y = torch.empty(d.y_shape(), dtype=spec.torch_dtype, device=device)
-        med, mn = time_layer(d, xd, wd, bd, y, flush, iters)
+        med, mean, mn = time_layer(d, xd, wd, bd, y, flush, iters)
         P, Q = d.output_dims()
         fl = 2.0 * spec.N * spec.K * P * Q * spec.C * spec.R * spec.S
         by = layer_bytes(spec, P, Q)
         tf = fl / (med * 1e-3) / 1e12
         gbs = by / (med * 1e-3) / 1e9
-        cpeak = tc_peak if spec.dtype != "f32" else fp32_alu_peak_tflops()
+        cpeak = tc_peak if spec.dtype != "f32" else fp32_alu_peak_tflops(peaks)
         roof_t = max(fl / (cpeak * 1e12), by / (peaks["hbm_gbs"] * 1e9)) * 1e3
         bound = ("tensor" if spec.dtype != "f32" else "alu") \
             if fl / (cpeak * 1e12) >= by / (peaks["hbm_gbs"] * 1e9) else "hbm"
-        res.append({"layer": spec.name, "plan": d.plan(), "ms_median": round(med, 5),
-                    "ms_min": round(mn, 5), "tflops": round(tf, 2), "hbm_gbs": round(gbs, 1),
-                    "bound": bound, "roofline_frac": round(roof_t / med, 4),
-                    "compute_frac": round(tf / cpeak, 4), "workspace_bytes": d.workspace_bytes()})
+        row = {"layer": spec.name, "plan": d.plan(), "ms_median": round(med, 5),
+               "ms_mean": round(mean, 5), "ms_min": round(mn, 5), "tflops": round(tf, 2),
+               "hbm_gbs": round(gbs, 1), "bound": bound, "roofline_frac": round(roof_t / med, 4),
+               "compute_frac": round(tf / cpeak, 4), "workspace_bytes": d.workspace_bytes(),
+               "iters": iters}
+        if spec.R == 1 and spec.S == 1 and names is None:
+            # launch-bound at 3.8 us of HBM time: also the per-call floor of
+            # 100 back-to-back launches (x stays in L2 between them)
+            row["graph_100_per_call_us"] = round(
+                graph_floor_us(lambda: d.forward(xd, wd, bd, y=y)), 3)
+        res.append(row)
+        if keep_check:
+            d.forward(xd, wd, bd, y=y)
+            idx = wl.check_points(spec, P, Q, seed=11)
+            checks.append((spec, x, w, b, idx, wl.gather_points(y, idx, spec.layout).cpu()))
         del xd, wd, bd, y
-    return res
+    return (res, checks) if keep_check else res
 
 
 # ------------------------------------------------------------------ CPU oracle
 
-def cpu_baseline(x, params, specs, flops, budget_s=10.0):
-    """The fp64 oracle on the host cores: whole encoder steps, repeated within a budget."""
+def cpu_baseline(x, params, specs, flops, budget_s=10.0, checks=()):
+    """The fp64 oracle on the host cores: whole encoder steps, repeated within a
+    budget, on all cores; one-core times of the single signature-matrix
+    convolution and of encoder layer 1 (a slice of its batch); and the oracle
+    at the sample points of the bench's own GPU outputs (error ratios)."""
     import oracle
+    from cnn_convolution_gb300 import workloads as wl
     threads = oracle.max_threads()
     t0 = time.perf_counter()
     reps = 0
     while True:
         cur = x
         for spec, (w, b) in zip(specs, params):
-            y, _ = oracle.conv2d(cur, w, b, spec.stride, spec.pad, spec.dil)
+            y, _ = oracle.conv2d(cur, w, b, spec.stride, spec.pad, spec.dil, threads=threads)
             cur = y
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 20:
             break
     per = el / reps
-    return {"value": round(sum(flops) / per / 1e12, 6), "unit": "TFLOPS", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{reps} full encoder steps (batch 256, 4 layers), fp64 direct loop, "
-                      f"{per:.3f} s per step"}
+    # one core: the single convolution, and layer 1 on 32 of its 256 images
+    sx, sw, sb = wl.mscred_single_inputs()
+    t0 = time.perf_counter()
+    oracle.conv2d(sx, sw, sb, 1, 1, 1, threads=1)
+    single_1t = time.perf_counter() - t0
+    l1 = specs[0]
+    w1, b1 = params[0]
+    t0 = time.perf_counter()
+    oracle.conv2d(x[:32], w1, b1, l1.stride, l1.pad, l1.dil, threads=1)
+    l1_1t = (time.perf_counter() - t0) * 256 / 32
+    oracle.conv2d(sx, sw, sb, 1, 1, 1, threads=threads)   # restore the thread count
+    single_fl = 2.0 * 32 * 30 * 30 * 27
+    res = {"value": round(sum(flops) / per / 1e12, 6), "unit": "TFLOPS", "cores": threads,
+           "kind": "oracle",
+           "sample": f"{reps} full encoder steps (batch 256, 4 layers), fp64 direct loop, "
+                     f"{per:.3f} s per step",
+           "one_core": {"single_signature_conv_s": round(single_1t, 6),
+                        "single_signature_conv_tflops": round(single_fl / single_1t / 1e12, 6),
+                        "encoder_layer1_s": round(l1_1t, 4),
+                        "encoder_layer1_tflops": round(flops[0] / l1_1t / 1e12, 6),
+                        "sample": "layer 1 timed on 32 of 256 images, scaled to 256"}}
+    if checks:
+        errs, ok, points = {}, True, 0
+        for spec, cx, cw, cb, idx, got in checks:
+            y_ref, den = oracle.conv2d_points(cx, cw, cb, idx, spec.stride, spec.pad, spec.dil,
+                                              layout=spec.layout, threads=threads)
+            err = oracle.error_ratio(got, y_ref, den)
+            tol = 1e-6 if spec.dtype == "f32" else 4e-3
+            errs[spec.name] = float(f"{err:.3e}")
+            ok = ok and err <= tol
+            points += len(idx)
+        res["output_check"] = {"error_ratio": errs, "within_tolerance": ok, "points": points,
+                               "tolerance": {"f32": 1e-6, "f16": 4e-3, "bf16": 4e-3},
+                               "points_are": "random, borders of the first and last image, first "
+                                             "and last row of every 128-row M tile and of every "
+                                             "output row, one channel per 32-channel group"}
+    return res
 
 
 def reference_main(args):
@@ -704,11 +893,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-tensor-core", action="store_true", help="skip the fp16/bf16 layers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layer-iters", type=int, default=50,
+                    help="timed replays per single-layer measurement (median reported)")
     ap.add_argument("--layer", default=None,
                     help="time one named layer only (for profiling) and print its line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.layer is None:
         ap.error("--warmup must be at least 3")
+    if args.layer_iters < 1:
+        ap.error("--layer-iters must be positive")
     if args.impl == "reference":
         return reference_main(args)
     if args.layer:

@@ -24,7 +24,7 @@ LIB_NAME = "libconv2d_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
 SOURCES = ["api.cpp", "status.cu", "cuda_core_conv.cu", "tc_conv_sm103a.cu", "tf32x3_conv_sm103a.cu",
-           "direct_conv.cu", "signature.cu", "deconv.cu"]
+           "direct_conv.cu", "signature.cu", "deconv.cu", "peaks.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

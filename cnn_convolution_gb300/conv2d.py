@@ -11,6 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
+from contextlib import contextmanager
 from typing import Optional, Tuple
 
 import torch
@@ -88,6 +89,14 @@ def _declare(lib):
     lib.conv2d_deconv_forward.argtypes = [vp] * 4 + [i32] * 11 + [c_int, c_int, vp]
     lib.conv2d_convlstm_cell.restype = c_int
     lib.conv2d_convlstm_cell.argtypes = [vp] * 6 + [i32] * 9 + [ctypes.c_longlong, vp]
+    lib.conv2d_set_override.restype = c_int
+    lib.conv2d_set_override.argtypes = [c_int, c_int]
+    lib.conv2d_get_override.restype = c_int
+    lib.conv2d_get_override.argtypes = [c_int, ctypes.POINTER(c_int)]
+    lib.conv2d_variant_count.restype = c_int
+    lib.conv2d_variant_count.argtypes = [c_int, ctypes.POINTER(c_int)]
+    lib.conv2d_peak_probe.restype = c_int
+    lib.conv2d_peak_probe.argtypes = [c_int, c_int, vp, ctypes.POINTER(ctypes.c_double)]
     lib.conv2d_signature_matrices.restype = c_int
     lib.conv2d_signature_matrices.argtypes = [vp, i32, i32, ctypes.POINTER(i32), i32, i32, i32,
                                               vp, vp]
@@ -300,6 +309,59 @@ def deconv_forward(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor
                                      _DTYPE_CODE[x.dtype], _LAYOUT_CODE["NCHW"],
                                      _stream_handle(stream, x.device)), "conv2d_deconv_forward")
     return y
+
+
+# Process-wide chooser overrides (conv2d_set_override), by the names of their
+# enum constants without the CONV2D_OVR_ prefix, lower case.
+OVERRIDES = {name: i for i, name in enumerate(
+    ["direct", "cc_tile", "cc_split", "tc_bn", "tc_ksub", "tc_im2col", "tc_window", "tc_winvar",
+     "tc_rotate", "tf_var", "fp32_tc", "deconv_tc", "grid_cap", "test_withhold",
+     "test_wait_kcycles"])}
+FAMILIES = {"cuda_core_tile": 0, "tensor_core": 1, "tensor_core_window": 2, "tf32x3": 3}
+
+
+def set_override(name: str, value: Optional[int]):
+    """Set (or, with None, clear) one chooser override for the whole process."""
+    _check(load().conv2d_set_override(OVERRIDES[name], -1 if value is None else int(value)),
+           f"conv2d_set_override({name})")
+
+
+def get_override(name: str) -> Optional[int]:
+    v = ctypes.c_int()
+    _check(load().conv2d_get_override(OVERRIDES[name], ctypes.byref(v)), "conv2d_get_override")
+    return None if v.value == -1 else v.value
+
+
+@contextmanager
+def overrides(**kw):
+    """Set overrides for the duration of a with-block, then restore the old values."""
+    old = {k: get_override(k) for k in kw}
+    try:
+        for k, v in kw.items():
+            set_override(k, v)
+        yield
+    finally:
+        for k, v in old.items():
+            set_override(k, v)
+
+
+def variant_count(family: str) -> int:
+    """Number of compiled variants of a kernel family."""
+    n = ctypes.c_int()
+    _check(load().conv2d_variant_count(FAMILIES[family], ctypes.byref(n)), "conv2d_variant_count")
+    return n.value
+
+
+PEAK_KINDS = {"ffma": 0, "tf32_mma": 1, "bf16_mma": 2}
+
+
+def peak_probe(kind: str, iters: int, stream=None) -> float:
+    """Launch one throughput-probe kernel on the current stream; returns its FLOPs."""
+    f = ctypes.c_double()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check(load().conv2d_peak_probe(PEAK_KINDS[kind], int(iters), _stream_handle(stream, dev),
+                                    ctypes.byref(f)), f"conv2d_peak_probe({kind})")
+    return f.value
 
 
 def get_device_status() -> int:

@@ -14,6 +14,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <new>
@@ -98,10 +99,43 @@ conv2d_status_t device_info(int *dev_out, DevInfo *info) {
 
 // ------------------------------------------------------------ chooser
 
-int env_int(const char *name) {
-    const char *e = std::getenv(name);
-    return e ? std::atoi(e) : -1;
+// ------------------------------------------------------------ overrides
+//
+// Switches for tests and A/B measurements (force a kernel, a tile, a grid
+// cap, the stall test hook).  They are process-wide, seeded once from the
+// environment (CONV2D_<NAME>, e.g. CONV2D_TC_BN=128) the first time the
+// library needs them, and changed only through conv2d_set_override.  The
+// per-call path reads them as relaxed atomic loads; the plan cache is keyed
+// on a generation number that every change bumps, so a plan made under other
+// overrides is never reused.
+
+const char *const kOverrideEnv[CONV2D_OVR_COUNT] = {
+    "CONV2D_DIRECT",   "CONV2D_CC_TILE",   "CONV2D_CC_SPLIT",  "CONV2D_TC_BN",
+    "CONV2D_TC_KSUB",  "CONV2D_TC_IM2COL", "CONV2D_TC_WINDOW", "CONV2D_TC_WINVAR",
+    "CONV2D_TC_ROTATE", "CONV2D_TF_VAR",   "CONV2D_FP32_TC",   "CONV2D_DECONV_TC",
+    "CONV2D_GRID_CAP", "CONV2D_TEST_WITHHOLD", "CONV2D_TEST_WAIT_KCYCLES"};
+
+std::atomic<int> g_ovr[CONV2D_OVR_COUNT];
+std::atomic<int> g_ovr_gen{0};
+std::once_flag g_ovr_once;
+
+void seed_overrides() {
+    std::call_once(g_ovr_once, [] {
+        for (int i = 0; i < CONV2D_OVR_COUNT; ++i) {
+            const char *e = std::getenv(kOverrideEnv[i]);
+            g_ovr[i].store(e ? std::atoi(e) : -1, std::memory_order_relaxed);
+        }
+    });
 }
+
+}  // namespace
+
+int conv2d::ovr(conv2d_override_t k) {
+    seed_overrides();
+    return g_ovr[k].load(std::memory_order_relaxed);
+}
+
+namespace {
 
 // Estimated time (arbitrary units) of a CUDA-core tile on this layer.
 // Each tile has a whole-GPU FFMA rate, measured on GB300 with enough CTAs
@@ -143,9 +177,9 @@ double dc_cost(const Shape &s) {
 }
 
 conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
-    const int force_direct = env_int("CONV2D_DIRECT");
+    const int force_direct = ovr(CONV2D_OVR_DIRECT);
     if (force_direct != 0 && dc_shape_ok(s) && dc_smem_bytes(s) <= d.smem_optin &&
-        env_int("CONV2D_CC_TILE") < 0 && env_int("CONV2D_CC_SPLIT") < 0) {
+        ovr(CONV2D_OVR_CC_TILE) < 0 && ovr(CONV2D_OVR_CC_SPLIT) < 0) {
         // take the direct kernel when forced, or when it beats every tile
         bool take = force_direct == 1;
         if (!take) {
@@ -169,8 +203,8 @@ conv2d_status_t choose_cc(const Shape &s, const DevInfo &d, Plan *p) {
         }
     }
     if (!cc_shape_ok(s)) return CONV2D_ERR_UNSUPPORTED;
-    const int forced = env_int("CONV2D_CC_TILE");
-    const int forced_split = env_int("CONV2D_CC_SPLIT");
+    const int forced = ovr(CONV2D_OVR_CC_TILE);
+    const int forced_split = ovr(CONV2D_OVR_CC_SPLIT);
     double best = 1e300;
     int best_id = -1, best_split = 1;
     for (int id = 0; id < cc_num_tiles(); ++id) {
@@ -214,9 +248,9 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     const int64_t cb = (s.C + 63) / 64;
     const int64_t rs = (int64_t)s.R * s.S;
     const int64_t kb = rs * cb;
-    const int force_bn = env_int("CONV2D_TC_BN"), force_ks = env_int("CONV2D_TC_KSUB");
-    const int force_win = env_int("CONV2D_TC_WINDOW");
-    const int force_wv = env_int("CONV2D_TC_WINVAR");
+    const int force_bn = ovr(CONV2D_OVR_TC_BN), force_ks = ovr(CONV2D_OVR_TC_KSUB);
+    const int force_win = ovr(CONV2D_OVR_TC_WINDOW);
+    const int force_wv = ovr(CONV2D_OVR_TC_WINVAR);
     const bool win_ok = tc_window_ok(s);
     const int wp = s.W + 2 * s.pad;
     const int tr = wp > 0 ? 128 / wp : 0;
@@ -285,8 +319,8 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     t.win_variant = best.win_variant;
     t.stages = t.window ? tc_window_variant(best.win_variant).stages : tc_stages(best.bn, best.ks);
     t.tma_store = true;
-    t.force_im2col = env_int("CONV2D_TC_IM2COL") == 1;
-    t.rotate = env_int("CONV2D_TC_ROTATE") != 0;
+    t.force_im2col = ovr(CONV2D_OVR_TC_IM2COL) == 1;
+    t.rotate = ovr(CONV2D_OVR_TC_ROTATE) != 0;
     p->algo = Algo::TensorCore;
     p->tc = t;
     p->smem_bytes = t.window ? tc_window_smem_bytes(t) : tc_smem_bytes(t);
@@ -294,6 +328,7 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     const int64_t m_tiles = t.window ? (int64_t)s.N * ((s.P + tr - 1) / tr) : (s.M + 127) / 128;
     const int64_t tiles = m_tiles * ((s.K + best.bn - 1) / best.bn);
     p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
+    if (ovr(CONV2D_OVR_GRID_CAP) > 0) p->grid = std::min(p->grid, ovr(CONV2D_OVR_GRID_CAP));
     p->sm_count = d.sm_count;
     return CONV2D_OK;
 }
@@ -316,7 +351,7 @@ double tf_cost_ns(const Shape &s, const TfTile &t, int sms) {
 conv2d_status_t choose_tf(const Shape &s, const DevInfo &d, Plan *p, double *cost_ns,
                           bool lstm = false) {
     if (!(d.cc_major == 10 && d.cc_minor == 3) || !tf_shape_ok(s)) return CONV2D_ERR_UNSUPPORTED;
-    const int forced = env_int("CONV2D_TF_VAR");
+    const int forced = ovr(CONV2D_OVR_TF_VAR);
     double best = 1e300;
     int best_id = -1;
     for (int id = 0; id < tf_num_variants(); ++id) {
@@ -335,6 +370,7 @@ conv2d_status_t choose_tf(const Shape &s, const DevInfo &d, Plan *p, double *cos
     p->smem_bytes = tf_smem_bytes(s, p->tf);
     const int64_t tiles = ((s.M + 127) / 128) * ((s.K + p->tf.BN - 1) / p->tf.BN);
     p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
+    if (ovr(CONV2D_OVR_GRID_CAP) > 0) p->grid = std::min(p->grid, ovr(CONV2D_OVR_GRID_CAP));
     p->sm_count = d.sm_count;
     if (cost_ns) *cost_ns = best;
     return CONV2D_OK;
@@ -345,12 +381,10 @@ bool aligned16(const Tensors &t) {
     return a(t.x) && a(t.w) && a(t.y) && (t.bias == nullptr || ((uintptr_t)t.bias & 1) == 0);
 }
 
-// Plans are cached per (device, shape, dtype, layout, algo, alignment class,
-// tile overrides).  CONV2D_CC_TILE / CONV2D_TC_BN force a tile (tests and
-// A/B measurements); they are read on every call so they can change.
+// Plans are cached per (device, shape, dtype, layout, algo, alignment class)
+// and the override generation (conv2d_set_override bumps it).
 using PlanKey = std::tuple<int, int, int, int, int, int, int, int, int, int, int, int, int, int, int,
-                           int, int, int>;
-
+                           int>;
 
 std::mutex g_plan_mu;
 std::map<PlanKey, Plan> g_plans;
@@ -361,13 +395,10 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
     conv2d_status_t st = device_info(&dev, &d);
     if (st != CONV2D_OK) return st;
     const bool al = t == nullptr || aligned16(*t);
+    seed_overrides();
     const PlanKey key{dev, s.N, s.C, s.H, s.W, s.K, s.R, s.S, s.stride, s.pad, s.dil,
                       (int)s.dtype, (int)s.layout, (int)algo, al ? 1 : 0,
-                      env_int("CONV2D_CC_TILE") * 8 + env_int("CONV2D_CC_SPLIT"),
-                      (((env_int("CONV2D_TC_BN") * 8 + env_int("CONV2D_TC_KSUB")) * 4 +
-                        env_int("CONV2D_TC_IM2COL")) * 4 + env_int("CONV2D_TC_WINDOW")) * 4 +
-                          env_int("CONV2D_TC_ROTATE") + 64 * env_int("CONV2D_TC_WINVAR"),
-                      (env_int("CONV2D_TF_VAR") * 4 + env_int("CONV2D_FP32_TC")) * 4 + env_int("CONV2D_DIRECT")};
+                      g_ovr_gen.load(std::memory_order_acquire)};
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         auto it = g_plans.find(key);
@@ -385,7 +416,7 @@ conv2d_status_t get_plan(const Shape &s, conv2d_algo_t algo, const Tensors *t, P
         } else {
             Plan ptf{};
             double tf_ns = 1e300;
-            const bool tf_on = env_int("CONV2D_FP32_TC") != 0 &&
+            const bool tf_on = ovr(CONV2D_OVR_FP32_TC) != 0 &&
                                choose_tf(s, d, &ptf, &tf_ns) == CONV2D_OK;
             st = choose_cc(s, d, &p);
             const double cc_ns = st != CONV2D_OK ? 1e300
@@ -632,7 +663,7 @@ conv2d_status_t conv2d_deconv_forward(const void *x, const void *w, const void *
     // CONV2D_DECONV_TC=1 / 0 forces either path.
     DevInfo d;
     int dev2 = 0;
-    const int force_tc = env_int("CONV2D_DECONV_TC");
+    const int force_tc = ovr(CONV2D_OVR_DECONV_TC);
     const bool try_tc = force_tc == 1 || (force_tc < 0 && C > 8);
     if (try_tc && R <= 8 && S <= 8 && device_info(&dev2, &d) == CONV2D_OK &&
         d.cc_major == 10 && d.cc_minor == 3) {
@@ -765,6 +796,34 @@ const char *conv2d_status_string(conv2d_status_t status) {
 }
 
 conv2d_status_t conv2d_get_device_status(void) { return status_read_and_clear(); }
+
+conv2d_status_t conv2d_set_override(conv2d_override_t key, int value) {
+    if ((int)key < 0 || (int)key >= CONV2D_OVR_COUNT) return CONV2D_ERR_INVALID_ARG;
+    if (value < -1) return CONV2D_ERR_INVALID_ARG;
+    seed_overrides();
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    g_ovr[key].store(value, std::memory_order_relaxed);
+    g_ovr_gen.fetch_add(1, std::memory_order_acq_rel);
+    g_plans.clear();   // plans made under the old value are never looked up again
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_get_override(conv2d_override_t key, int *value) {
+    if ((int)key < 0 || (int)key >= CONV2D_OVR_COUNT || !value) return CONV2D_ERR_INVALID_ARG;
+    *value = ovr(key);
+    return CONV2D_OK;
+}
+
+conv2d_status_t conv2d_variant_count(conv2d_family_t family, int *count) {
+    if (!count) return CONV2D_ERR_INVALID_ARG;
+    switch (family) {
+        case CONV2D_FAMILY_CUDA_CORE_TILE: *count = cc_num_tiles(); return CONV2D_OK;
+        case CONV2D_FAMILY_TENSOR_CORE: *count = tc_num_variants(); return CONV2D_OK;
+        case CONV2D_FAMILY_TENSOR_CORE_WINDOW: *count = tc_window_variants(); return CONV2D_OK;
+        case CONV2D_FAMILY_TF32X3: *count = tf_num_variants(); return CONV2D_OK;
+    }
+    return CONV2D_ERR_INVALID_ARG;
+}
 
 int conv2d_version(void) { return 100; }
 

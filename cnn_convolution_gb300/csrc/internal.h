@@ -87,6 +87,7 @@ conv2d_status_t cc_launch(const Shape &s, const Plan &p, const Tensors &t, cudaS
 bool tc_shape_ok(const Shape &s, const Tensors *t);
 size_t tc_smem_bytes(const TcTile &t);
 int tc_stages(int bn, int ksub);   // 0 if the (BN, KSUB) variant does not exist
+int tc_num_variants();             // compiled (BN, KSUB) variants of the plain / im2col kernel
 bool tc_window_ok(const Shape &s);
 size_t tc_window_smem_bytes(const TcTile &t);
 struct TcWinVariant {
@@ -162,6 +163,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
+
+// Current value of a process-wide override (-1 = not set; see conv2d_set_override).
+int ovr(conv2d_override_t key);
 
 // Device status word (bounded-wait failures).
 conv2d_status_t status_read_and_clear();

@@ -44,11 +44,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait on phase `parity` of an mbarrier.  Returns false (after setting
-// the abort flag and the status word) if it gave up, or if another thread of
-// the CTA already gave up.  The SM cycle counter is read only every 256 failed
-// polls: reading a timer on every poll would slow the pipeline down.
+// the abort flag and the status word) if it gave up after `limit` SM cycles,
+// or if another thread of the CTA already gave up.  The SM cycle counter is
+// read only every 256 failed polls: reading a timer on every poll would slow
+// the pipeline down.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int *status) {
+                                          unsigned int *status, long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     long long t0 = 0;
     for (uint32_t i = 1;; ++i) {
@@ -58,7 +59,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             const long long now = clock64();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitLimitCycles) {
+            } else if (now - t0 > limit) {
                 *abort_flag = 1;
                 if (status) atomicOr(status, 1u);
                 return false;
@@ -68,7 +69,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Unbounded-looking drain loops are bounded by the same cycle budget.
-__device__ __forceinline__ bool cycles_left(long long t0) { return clock64() - t0 < kWaitLimitCycles; }
+__device__ __forceinline__ bool cycles_left(long long t0, long long limit = kWaitLimitCycles) {
+    return clock64() - t0 < limit;
+}
 
 __device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                                    int c, int w, int h, int n, uint16_t off_w,
@@ -135,6 +138,22 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 __device__ __forceinline__ void epilogue_bar_sync() {
     asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps only
+}
+// Barrier of the four epilogue warps that also ANDs a flag over their 128
+// threads: every thread gets the same answer, so the warps can leave a loop
+// together (one warp leaving alone would strand the others at the next
+// barrier).
+__device__ __forceinline__ bool epilogue_bar_all(bool v) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)v)
+        : "memory");
+    return out != 0;
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

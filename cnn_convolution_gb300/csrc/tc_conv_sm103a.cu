@@ -20,10 +20,10 @@
 //   * One thread issues tcgen05.mma (kind::f16, M=128, N=BN, K=16) into a
 //     fp32 accumulator in tensor memory; tcgen05.commit frees each shared
 //     memory stage and signals a finished accumulator.
-//   * Persistent CTAs (one per SM) loop over output tiles; the accumulator is
-//     double-buffered in tensor memory so the epilogue of one tile (tcgen05.ld,
-//     + bias, one round-to-nearest-even cast, 16-byte stores) overlaps the
-//     main loop of the next.
+//   * Persistent CTAs (one per SM) loop over output tiles; up to four
+//     accumulators in tensor memory let the main loop run ahead while the
+//     epilogue of earlier tiles (tcgen05.ld, + bias, one round-to-nearest-even
+//     cast, 16-byte stores of each pixel's outputs straight into y) drains.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = tensor-memory
 // allocator and MMA issuer, warps 2..5 = epilogue (warp w reads accumulator
@@ -76,6 +76,22 @@ __host__ __device__ constexpr uint32_t make_idesc(bool bf16, int n) {
            | ((uint32_t)(kBM >> 4) << 24);             // M / 16
 }
 
+// Accumulators in tensor memory: as many BN-column buffers as fit in 512
+// columns, at most 4, so the MMAs can run up to 3 tiles ahead of the epilogue.
+template <int BN> constexpr int tc_num_acc() { return 512 / BN >= 4 ? 4 : 512 / BN; }
+template <int BN> constexpr uint32_t tc_tmem_cols() {
+    return (uint32_t)(tc_num_acc<BN>() * BN) <= 256 ? 256u : 512u;
+}
+// The bias is staged once per CTA as fp32 in shared memory when K <= kBiasMax
+// (16 KB with its 32-entry tail); larger layers read it from global memory.
+constexpr int kBiasMax = 4064;
+constexpr int kBiasBytes = (kBiasMax + 32) * 4;
+
+__device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
@@ -99,18 +115,25 @@ template <> __device__ __forceinline__ float load_bias<__nv_bfloat16>(const __nv
 #ifdef CONV2D_TC_TRACE
 __device__ unsigned long long g_tc_trace[4][8192];
 __device__ unsigned int g_tc_trace_n[4];
+// One tracing thread per role keeps its event count in a register and only
+// stores (no atomics, nothing the thread waits for).
 #define TC_TRACE(role, tag)                                                                  \
     do {                                                                                     \
         if (blockIdx.x == 0) {                                                               \
-            const unsigned i_ = atomicAdd(&g_tc_trace_n[role], 1u);                          \
-            if (i_ < 8192u)                                                                  \
-                g_tc_trace[role][i_] =                                                       \
+            if (tr_n[role] < 8192u)                                                          \
+                g_tc_trace[role][tr_n[role]] =                                               \
                     ((unsigned long long)(tag) << 48) | ((unsigned long long)clock64() & 0xFFFFFFFFFFFFull); \
+            ++tr_n[role];                                                                    \
+            g_tc_trace_n[role] = tr_n[role];                                                 \
         }                                                                                    \
     } while (0)
+#define TC_TRACE_DECL unsigned tr_n[4] = {0u, 0u, 0u, 0u}
 #else
 #define TC_TRACE(role, tag) \
     do {                    \
+    } while (0)
+#define TC_TRACE_DECL \
+    do {              \
     } while (0)
 #endif
 
@@ -136,11 +159,16 @@ struct TcParams {
     int Wp;               // padded row length W + 2*pad (rows of the window)
     int TR;               // output rows per tile (TR * Wp <= 128)
     int tiles_per_img;    // ceil(P / TR)
+    // bounded waits give up after this many SM cycles
+    long long wait_limit;
+    // test hook (plain kernel): CTA 0 never issues the loads of its first
+    // stage, so its MMA warp's wait on that stage runs out
+    int withhold;
 };
 
 // Shared-memory layout: STAGES stages, each holding KSUB k-blocks (the KSUB A
-// tiles, then the KSUB B tiles, every tile 1024-byte aligned), the epilogue
-// staging buffers, then the barriers.  A stage is the unit of producer /
+// tiles, then the KSUB B tiles, every tile 1024-byte aligned), the fp32 bias,
+// then the barriers.  A stage is the unit of producer /
 // consumer hand-off.  Measured on GB300, TMA cost is per instruction and per
 // stage rather than per byte, so a stage carries KSUB k-blocks and its B tiles
 // (and, for 1x1 layers, its A tiles) arrive in ONE 3-D box each.
@@ -148,12 +176,12 @@ template <int BN, int KSUB, int STAGES>
 struct TcSmem {
     static constexpr int kBTileBytes = BN * kBK * 2;
     static constexpr int kStageBytes = KSUB * (kATileBytes + kBTileBytes);
-    // epilogue staging: two buffers of 128 rows x 32 outputs (64 B), 64-byte swizzled
-    static constexpr int kEpiBufBytes = kBM * 32 * 2;
-    static constexpr size_t kEpiOffset = (size_t)STAGES * kStageBytes;
-    static constexpr size_t kBarOffset = kEpiOffset + 2 * kEpiBufBytes;
-    // full[S], empty[S], acc_full[2], acc_empty[2], drain[1]; then tmem addr, abort flag
-    static constexpr size_t kBarBytes = (2 * STAGES + 5) * 8;
+    static constexpr int kAcc = tc_num_acc<BN>();
+    // the layer's bias as fp32
+    static constexpr size_t kBiasOffset = (size_t)STAGES * kStageBytes;
+    static constexpr size_t kBarOffset = kBiasOffset + kBiasBytes;
+    // full[S], empty[S], acc_full[A], acc_empty[A], drain[1]; then tmem addr, abort flag
+    static constexpr size_t kBarBytes = (2 * STAGES + 2 * kAcc + 1) * 8;
     static constexpr size_t kBytes = kBarOffset + kBarBytes + 16 + 1024;   // +1024 for alignment
 };
 
@@ -163,11 +191,12 @@ struct TcSmem {
 template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmY, const TcParams p) {
+               const TcParams p) {
     using L = TcSmem<BN, KSUB, STAGES>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
-    constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
+    constexpr int kAcc = L::kAcc;
+    constexpr uint32_t kTmemCols = tc_tmem_cols<BN>();
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -177,8 +206,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
-    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
-    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
+    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + kAcc + a); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * kAcc);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
     auto a_tile = [&](int s, int j) {
@@ -190,13 +219,14 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    TC_TRACE_DECL;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAcc; ++a) {
             mbar_init(accf_bar(a), 1);
             mbar_init(acce_bar(a), 128);
         }
@@ -206,7 +236,6 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
-        prefetch_tensormap(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -232,6 +261,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t n_issued = 0;       // stages filled so far
         bool ok = true;
         const int dil = p.dil;
+        // test hook: CTA 0 leaves its first stage empty (nothing armed, nothing in flight)
+        const bool held0 = p.withhold != 0 && blockIdx.x == 0;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
@@ -255,25 +286,27 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int i0 = (sidx - o * per_o) * KSUB;
                 const int nsub = min(KSUB, p.n_inner - i0);
                 const int cx = p.chunked ? 0 : o * kBK;     // channel offset of this outer block
-                if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
                 TC_TRACE(3, 8);
                 const uint32_t fb = full_bar(stage);
                 const int a_tiles = (A_TILE && p.chunked) ? KSUB : nsub;
-                mbar_arrive_expect_tx(fb, (uint32_t)(a_tiles * kATileBytes + KSUB * L::kBTileBytes));
-                if (A_TILE) {
-                    if (p.chunked)
-                        tma_load_tile_3d(a_tile(stage, 0), &tmA, fb, 0, (int)m0, i0);
-                    else
-                        tma_load_tile_2d(a_tile(stage, 0), &tmA, fb, cx, (int)m0);
-                } else {
-                    int r = i0 / p.S, s = i0 - r * p.S;
-                    for (int jj = 0; jj < nsub; ++jj) {
-                        tma_load_im2col_4d(a_tile(stage, jj), &tmA, fb, cx, w0, h0, n_img,
-                                           (uint16_t)(s * dil), (uint16_t)(r * dil));
-                        if (++s == p.S) { s = 0; ++r; }
+                if (!(held0 && n_issued == 0)) {
+                    mbar_arrive_expect_tx(fb, (uint32_t)(a_tiles * kATileBytes + KSUB * L::kBTileBytes));
+                    if (A_TILE) {
+                        if (p.chunked)
+                            tma_load_tile_3d(a_tile(stage, 0), &tmA, fb, 0, (int)m0, i0);
+                        else
+                            tma_load_tile_2d(a_tile(stage, 0), &tmA, fb, cx, (int)m0);
+                    } else {
+                        int r = i0 / p.S, s = i0 - r * p.S;
+                        for (int jj = 0; jj < nsub; ++jj) {
+                            tma_load_im2col_4d(a_tile(stage, jj), &tmA, fb, cx, w0, h0, n_img,
+                                               (uint16_t)(s * dil), (uint16_t)(r * dil));
+                            if (++s == p.S) { s = 0; ++r; }
+                        }
                     }
+                    tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
                 }
-                tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
                 ++n_issued;
                 TC_TRACE(0, 1);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -285,7 +318,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // stage i % STAGES with phase (i / STAGES) & 1.
             const long long t0 = clock64();
             for (uint32_t i = n_issued > (uint32_t)STAGES ? n_issued - STAGES : 0; i < n_issued; ++i) {
-                while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) && cycles_left(t0)) {
+                if (held0 && i == 0) continue;   // never armed: nothing to land
+                while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) && cycles_left(t0, p.wait_limit)) {
                 }
             }
         }
@@ -302,7 +336,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         constexpr uint64_t kADesc = (uint64_t)(kATileBytes >> 4);
         constexpr uint64_t kBDesc = (uint64_t)(L::kBTileBytes >> 4);
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
-            if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
             TC_TRACE(1, 4);
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -314,7 +348,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (sidx >= n_st) sidx -= n_st;
                 const int o = sidx / per_o;
                 const int nsub = min(KSUB, p.n_inner - (sidx - o * per_o) * KSUB);
-                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
                 TC_TRACE(1, 2);
                 tc_fence_after();
                 for (int jj = 0; jj < nsub; ++jj) {
@@ -334,82 +368,90 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!ok) break;
             mma_commit(accf_bar(acc));
             TC_TRACE(1, 3);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
         }
         if (any) {
             // Make sure every MMA has retired before tensor memory is released.
             mma_commit(drain_bar);
             const long long t0 = clock64();
-            while (!mbar_try_wait(drain_bar, 0) && cycles_left(t0)) {
+            while (!mbar_try_wait(drain_bar, 0) && cycles_left(t0, p.wait_limit)) {
             }
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
-        // Per 32-output chunk: tcgen05.ld -> + bias -> one RN cast -> this
-        // thread's 64-byte row segment into a 64-byte-swizzled staging buffer
-        // -> one TMA store of the 128 x 32 box (clipped at M and K).  Two
-        // buffers alternate so a store drains while the next chunk is staged.
+        // Thread = one output pixel (accumulator lane).  Per 32-output chunk:
+        // tcgen05.ld -> + bias (fp32, staged once per CTA) -> one RN cast ->
+        // four 16-byte stores of the pixel's 64 contiguous bytes of y.  No
+        // staging buffer and no barrier between the epilogue warps per chunk.
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        const bool issuer = threadIdx.x == 64;      // warp 2, lane 0
-        const T *bias = static_cast<const T *>(p.bias);
-        const uint32_t epi_base = smem_base + (uint32_t)L::kEpiOffset;
-        const uint32_t row_off = (uint32_t)row * 64u;
-        const uint32_t swz = (uint32_t)((row >> 1) & 3);
+        float *bias_s = reinterpret_cast<float *>(smem + L::kBiasOffset);
+        const T *bias_g = static_cast<const T *>(p.bias);
+        const bool bias_in_smem = bias_g != nullptr && p.K <= kBiasMax;
+        if (bias_in_smem)
+            for (int k = (int)threadIdx.x - 64; k < p.K; k += 128) bias_s[k] = load_bias<T>(bias_g, k);
+        epilogue_bar_sync();                      // the staged bias is visible to the four warps
+        T *y = static_cast<T *>(p.y);
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t chunk = 0;
         for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-            // one lane waits, the whole warp follows (tcgen05.ld needs a converged warp)
+            // One lane per warp waits, the whole warp follows (tcgen05.ld needs
+            // a converged warp); then the four warps decide together, so that
+            // if one warp's wait gave up they all leave the loop.
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+            if (lane == 0) ok = mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status, p.wait_limit) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (issuer) TC_TRACE(2, 5);
+            if (!epilogue_bar_all(ok != 0)) break;
+            if (row == 0) TC_TRACE(2, 5);
             tc_fence_after();
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
-            const int m0 = tm * kBM;
+            const int64_t m = (int64_t)tm * kBM + row;
+            const bool valid = m < p.M;
             const int k0 = tn * BN;
+            T *yrow = y + (valid ? m : 0) * (int64_t)p.K;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32cols(t_row + (uint32_t)c0, v);
-                if (k0 + c0 >= p.K) continue;       // uniform across the epilogue warps
+                const int kc = k0 + c0;
+                if (kc >= p.K) continue;            // uniform across the epilogue warps
                 uint32_t o[16];
+                const float4 *b4 = reinterpret_cast<const float4 *>(bias_s + kc);   // 128-byte aligned
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
-                    const int k = k0 + c0 + j;
-                    if (bias != nullptr && k < p.K) {
-                        a += load_bias<T>(bias, k);
-                        b += load_bias<T>(bias, k + 1);
+                for (int j = 0; j < 32; j += 4) {
+                    float a0 = __uint_as_float(v[j]), a1 = __uint_as_float(v[j + 1]);
+                    float a2 = __uint_as_float(v[j + 2]), a3 = __uint_as_float(v[j + 3]);
+                    if (bias_in_smem) {
+                        const float4 bv = b4[j / 4];
+                        a0 += bv.x;
+                        a1 += bv.y;
+                        a2 += bv.z;
+                        a3 += bv.w;
+                    } else if (bias_g != nullptr && kc + j < p.K) {
+                        a0 += load_bias<T>(bias_g, kc + j);
+                        a1 += load_bias<T>(bias_g, kc + j + 1);
+                        a2 += load_bias<T>(bias_g, kc + j + 2);
+                        a3 += load_bias<T>(bias_g, kc + j + 3);
                     }
-                    o[j / 2] = pack2<T>(a, b);
+                    o[j / 2] = pack2<T>(a0, a1);
+                    o[j / 2 + 1] = pack2<T>(a2, a3);
                 }
-                const uint32_t buf = epi_base + (chunk & 1u) * (uint32_t)L::kEpiBufBytes;
-                if (issuer) bulk_wait_read_le1();   // the store that used this buffer has read it
-                epilogue_bar_sync();
+                if (valid) {
+                    // K % 8 == 0: each 8-output group lies wholly inside or outside y
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    st_shared_v4(buf + row_off + ((((uint32_t)g) ^ swz) << 4), o[4 * g], o[4 * g + 1],
-                                 o[4 * g + 2], o[4 * g + 3]);
-                fence_proxy_async_smem();
-                epilogue_bar_sync();
-                if (issuer) {
-                    tma_store_2d(&tmY, buf, k0 + c0, m0);
-                    bulk_commit_group();
+                    for (int g = 0; g < 4; ++g)
+                        if (kc + 8 * g < p.K)
+                            st_global_v4(yrow + kc + 8 * g, o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
                 }
-                ++chunk;
             }
             tc_fence_before();
             __syncwarp();
             mbar_arrive(acce_bar(acc));
-            if (issuer) TC_TRACE(2, 6);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (row == 0) TC_TRACE(2, 6);
+            if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
         }
-        if (issuer) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -438,8 +480,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // a 3x3 layer loads each input window once per channel block instead of
 // nine 128-pixel im2col tiles.
 //
-// Shared memory: NWIN window slots of WINKB KB, the weight region, the
-// epilogue staging buffers, barriers.  The weight region is either STAGES
+// Shared memory: NWIN window slots of WINKB KB, the weight region, the fp32
+// bias, barriers.  The weight region is either STAGES
 // stages of KSUB weight tiles streamed per (tap group, channel block), or --
 // RES, for layers whose whole weight tensor fits (one output-channel tile) --
 // every weight tile of the layer, loaded once per CTA and kept resident; the
@@ -452,23 +494,24 @@ struct TcWinSmem {
     static constexpr int kStageBytes = KSUB * kBTileBytes;
     static constexpr int kResBytes = RESKB * 1024;
     static constexpr size_t kStageOffset = (size_t)NWIN * kWinBytes;
-    static constexpr int kEpiBufBytes = kBM * 32 * 2;
-    static constexpr size_t kEpiOffset =
+    static constexpr int kAcc = tc_num_acc<BN>();
+    static constexpr size_t kBiasOffset =
         kStageOffset + (RES ? (size_t)kResBytes : (size_t)STAGES * kStageBytes);
-    static constexpr size_t kBarOffset = kEpiOffset + 2 * kEpiBufBytes;
-    // full[S], empty[S], win_full[NWIN], win_empty[NWIN], acc_full[2], acc_empty[2], drain, resident
-    static constexpr size_t kBarBytes = (2 * STAGES + 2 * NWIN + 6) * 8;
+    static constexpr size_t kBarOffset = kBiasOffset + kBiasBytes;
+    // full[S], empty[S], win_full[NWIN], win_empty[NWIN], acc_full[A], acc_empty[A], drain, resident
+    static constexpr size_t kBarBytes = (2 * STAGES + 2 * NWIN + 2 * kAcc + 2) * 8;
     static constexpr size_t kBytes = kBarOffset + kBarBytes + 16 + 1024;
 };
 
 template <typename T, int BN, int KSUB, int STAGES, int WINKB, int NWIN, bool RES, int RESKB>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmY, const TcParams p) {
+                      const TcParams p) {
     using L = TcWinSmem<BN, KSUB, STAGES, WINKB, NWIN, RES, RESKB>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
-    constexpr uint32_t kTmemCols = 2 * BN;
+    constexpr int kAcc = L::kAcc;
+    constexpr uint32_t kTmemCols = tc_tmem_cols<BN>();
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -480,9 +523,9 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     auto wfull_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + w); };
     auto wempty_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + NWIN + w); };
     auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * NWIN + a); };
-    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * NWIN + 2 + a); };
-    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * NWIN + 4);
-    const uint32_t res_bar = bar_base + 8u * (2 * STAGES + 2 * NWIN + 5);
+    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * NWIN + kAcc + a); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * NWIN + 2 * kAcc);
+    const uint32_t res_bar = bar_base + 8u * (2 * STAGES + 2 * NWIN + 2 * kAcc + 1);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
     auto win_slot = [&](int w) { return smem_base + (uint32_t)(w * L::kWinBytes); };
@@ -497,6 +540,7 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int RS = p.R * p.S;
+    TC_TRACE_DECL;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -507,7 +551,7 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             mbar_init(wfull_bar(w), 1);
             mbar_init(wempty_bar(w), 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAcc; ++a) {
             mbar_init(accf_bar(a), 1);
             mbar_init(acce_bar(a), 128);
         }
@@ -518,7 +562,6 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
-        prefetch_tensormap(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -553,15 +596,17 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             const int p0 = (tm - n_img * p.tiles_per_img) * p.TR;
             const int k0 = tn * BN;
             for (int cb = 0; cb < p.CB && ok; ++cb) {
-                if (!mbar_wait(wempty_bar(wslot), wphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(wempty_bar(wslot), wphase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
+                TC_TRACE(3, 8);
                 mbar_arrive_expect_tx(wfull_bar(wslot), win_tx);
                 tma_load_tile_4d(win_slot(wslot), &tmA, wfull_bar(wslot), cb * kBK, -p.pad, p0 - p.pad,
                                  n_img);
+                TC_TRACE(0, 9);
                 ++n_w;
                 if (++wslot == NWIN) { wslot = 0; wphase ^= 1u; }
                 if (RES) continue;
                 for (int t0 = 0; t0 < RS; t0 += KSUB) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, (uint32_t)(KSUB * L::kBTileBytes));
                     // one box: 64 channels x BN outputs x KSUB taps (taps past R*S read as zero)
@@ -576,13 +621,13 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             // Let the copies already in flight land before the CTA goes away.
             const long long t0 = clock64();
             for (uint32_t i = n_b > (uint32_t)STAGES ? n_b - STAGES : 0; i < n_b; ++i)
-                while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) && cycles_left(t0)) {
+                while (!mbar_try_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u) && cycles_left(t0, p.wait_limit)) {
                 }
             for (uint32_t i = n_w > (uint32_t)NWIN ? n_w - NWIN : 0; i < n_w; ++i)
-                while (!mbar_try_wait(wfull_bar((int)(i % NWIN)), (i / NWIN) & 1u) && cycles_left(t0)) {
+                while (!mbar_try_wait(wfull_bar((int)(i % NWIN)), (i / NWIN) & 1u) && cycles_left(t0, p.wait_limit)) {
                 }
             if (res_issued)
-                while (!mbar_try_wait(res_bar, 0) && cycles_left(t0)) {
+                while (!mbar_try_wait(res_bar, 0) && cycles_left(t0, p.wait_limit)) {
                 }
         }
     } else if (warp == 1 && lane == 0) {
@@ -593,13 +638,14 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
         constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);
         constexpr uint64_t kSubDesc = (uint64_t)(L::kBTileBytes >> 4);
-        if (RES && !mbar_wait(res_bar, 0, abort_flag, p.status)) ok = false;
+        if (RES && !mbar_wait(res_bar, 0, abort_flag, p.status, p.wait_limit)) ok = false;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
-            if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
+            TC_TRACE(1, 4);
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int cb = 0; cb < p.CB && ok; ++cb) {
-                if (!mbar_wait(wfull_bar(wslot), wphase, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(wfull_bar(wslot), wphase, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
                 TC_TRACE(1, 7);
                 tc_fence_after();
                 const uint32_t wbase = win_slot(wslot);
@@ -607,7 +653,7 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 for (int t0 = 0; t0 < RS; t0 += KSUB) {
                     const int nsub = min(KSUB, RS - t0);
                     if (!RES) {
-                        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
                         TC_TRACE(1, 2);
                         tc_fence_after();
                     }
@@ -638,83 +684,90 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
             if (!ok) break;
             mma_commit(accf_bar(acc));
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            TC_TRACE(1, 3);
+            if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
         }
         if (any) {
             mma_commit(drain_bar);
             const long long t0 = clock64();
-            while (!mbar_try_wait(drain_bar, 0) && cycles_left(t0)) {
+            while (!mbar_try_wait(drain_bar, 0) && cycles_left(t0, p.wait_limit)) {
             }
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
-        // Accumulator lane j is padded-grid pixel (j / Wp, j % Wp); valid lanes
-        // are compacted into the staging buffer as rows i*Q + q, which is the
-        // layout of a (32 outputs x Q x TR x 1) box of the 4-D y map.
+        // Accumulator lane j is padded-grid pixel (j / Wp, j % Wp) of the
+        // tile's TR rows; lanes with j % Wp >= Q (or rows past P) are padding
+        // columns and are dropped.  Each valid lane writes its pixel's outputs
+        // straight into y, as in the im2col kernel.
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const int ti = row / p.Wp, tq = row - ti * p.Wp;
-        const bool valid = ti < p.TR && tq < p.Q;
-        const int srow = ti * p.Q + tq;
-        const uint32_t row_off = (uint32_t)srow * 64u;
-        const uint32_t swz = (uint32_t)((srow >> 1) & 3);
-        const bool issuer = threadIdx.x == 64;
-        const T *bias = static_cast<const T *>(p.bias);
-        const uint32_t epi_base = smem_base + (uint32_t)L::kEpiOffset;
+        const bool lane_valid = ti < p.TR && tq < p.Q;
+        float *bias_s = reinterpret_cast<float *>(smem + L::kBiasOffset);
+        const T *bias_g = static_cast<const T *>(p.bias);
+        const bool bias_in_smem = bias_g != nullptr && p.K <= kBiasMax;
+        if (bias_in_smem)
+            for (int k = (int)threadIdx.x - 64; k < p.K; k += 128) bias_s[k] = load_bias<T>(bias_g, k);
+        epilogue_bar_sync();                      // the staged bias is visible to the four warps
+        T *y = static_cast<T *>(p.y);
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t chunk = 0;
         for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+            if (lane == 0) ok = mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status, p.wait_limit) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            if (!epilogue_bar_all(ok != 0)) break;
+            if (row == 0) TC_TRACE(2, 5);
             tc_fence_after();
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
             const int n_img = tm / p.tiles_per_img;
             const int p0 = (tm - n_img * p.tiles_per_img) * p.TR;
             const int k0 = tn * BN;
+            const bool valid = lane_valid && p0 + ti < p.P;
+            const int64_t pix = ((int64_t)n_img * p.P + (valid ? p0 + ti : 0)) * p.Q + (valid ? tq : 0);
+            T *yrow = y + pix * (int64_t)p.K;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32cols(t_row + (uint32_t)c0, v);
-                if (k0 + c0 >= p.K) continue;
+                const int kc = k0 + c0;
+                if (kc >= p.K) continue;
                 uint32_t o[16];
+                const float4 *b4 = reinterpret_cast<const float4 *>(bias_s + kc);   // 128-byte aligned
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
-                    const int k = k0 + c0 + j;
-                    if (bias != nullptr && k < p.K) {
-                        a += load_bias<T>(bias, k);
-                        b += load_bias<T>(bias, k + 1);
+                for (int j = 0; j < 32; j += 4) {
+                    float a0 = __uint_as_float(v[j]), a1 = __uint_as_float(v[j + 1]);
+                    float a2 = __uint_as_float(v[j + 2]), a3 = __uint_as_float(v[j + 3]);
+                    if (bias_in_smem) {
+                        const float4 bv = b4[j / 4];
+                        a0 += bv.x;
+                        a1 += bv.y;
+                        a2 += bv.z;
+                        a3 += bv.w;
+                    } else if (bias_g != nullptr && kc + j < p.K) {
+                        a0 += load_bias<T>(bias_g, kc + j);
+                        a1 += load_bias<T>(bias_g, kc + j + 1);
+                        a2 += load_bias<T>(bias_g, kc + j + 2);
+                        a3 += load_bias<T>(bias_g, kc + j + 3);
                     }
-                    o[j / 2] = pack2<T>(a, b);
+                    o[j / 2] = pack2<T>(a0, a1);
+                    o[j / 2 + 1] = pack2<T>(a2, a3);
                 }
-                const uint32_t buf = epi_base + (chunk & 1u) * (uint32_t)L::kEpiBufBytes;
-                if (issuer) bulk_wait_read_le1();
-                epilogue_bar_sync();
                 if (valid) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g)
-                        st_shared_v4(buf + row_off + ((((uint32_t)g) ^ swz) << 4), o[4 * g],
-                                     o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
+                        if (kc + 8 * g < p.K)
+                            st_global_v4(yrow + kc + 8 * g, o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
                 }
-                fence_proxy_async_smem();
-                epilogue_bar_sync();
-                if (issuer) {
-                    tma_store_4d(&tmY, buf, k0 + c0, 0, p0, n_img);
-                    bulk_commit_group();
-                }
-                ++chunk;
             }
             tc_fence_before();
             __syncwarp();
             mbar_arrive(acce_bar(acc));
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (row == 0) TC_TRACE(2, 6);
+            if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
         }
-        if (issuer) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -760,10 +813,10 @@ bool load_driver_fns() {
 }
 
 struct TcMaps {
-    alignas(64) CUtensorMap a, b, y;
+    alignas(64) CUtensorMap a, b;
 };
 
-// Encode the three tensor maps of a launch (x as im2col or plain matrix, w, y).
+// Encode the two tensor maps of a launch (x as im2col, plain matrix or window, w).
 // Window geometry of a stride-1 layer (see the window kernel).
 struct WinGeom {
     int Wp, TR, TRW, max_shift;
@@ -861,39 +914,16 @@ conv2d_status_t encode_maps(const Shape &s, int BN, int KSUB, int amode, const T
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return CONV2D_ERR_CUDA;
     }
-    if (amode == 2) {
-        // y as (K, Q, P, N); boxes of 32 outputs x Q columns x TR rows x 1 image
-        const WinGeom g = win_geom(s);
-        const cuuint64_t dims[4] = {(cuuint64_t)s.K, (cuuint64_t)s.Q, (cuuint64_t)s.P, (cuuint64_t)s.N};
-        const cuuint64_t strides[3] = {(cuuint64_t)s.K * 2, (cuuint64_t)s.Q * s.K * 2,
-                                       (cuuint64_t)s.P * s.Q * s.K * 2};
-        const cuuint32_t box[4] = {32, (cuuint32_t)s.Q, (cuuint32_t)g.TR, 1};
-        const cuuint32_t estr[4] = {1, 1, 1, 1};
-        if (g_encode_tiled(&m->y, dt, 4, t.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return CONV2D_ERR_CUDA;
-    } else {
-        // y as the [M, K] row-major matrix; boxes of 128 rows x 32 outputs
-        const cuuint64_t dims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
-        const cuuint64_t strides[1] = {(cuuint64_t)s.K * 2};
-        const cuuint32_t box[2] = {32, kBM};
-        const cuuint32_t estr[2] = {1, 1};
-        if (g_encode_tiled(&m->y, dt, 2, t.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return CONV2D_ERR_CUDA;
-    }
     return CONV2D_OK;
 }
 
-// Maps depend only on the layer, the tile width, the A mode and the three
+// Maps depend only on the layer, the tile width, the A mode and the x and w
 // pointers; repeated calls with the same tensors reuse them (host time).
 struct MapKey {
     int v[15];
-    const void *x, *w, *y;
+    const void *x, *w;
     bool operator==(const MapKey &o) const {
-        return std::memcmp(v, o.v, sizeof(v)) == 0 && x == o.x && w == o.w && y == o.y;
+        return std::memcmp(v, o.v, sizeof(v)) == 0 && x == o.x && w == o.w;
     }
 };
 
@@ -915,7 +945,6 @@ conv2d_status_t cached_maps(const Shape &s, int BN, int KSUB, int amode, const T
     std::memcpy(k.v, vals, sizeof(vals));
     k.x = t.x;
     k.w = t.w;
-    k.y = t.y;
     for (int i = 0; i < kSlots; ++i) {
         if (slots[i].used && slots[i].key == k) {
             *out = &slots[i].maps;
@@ -947,6 +976,13 @@ bool ensure_smem_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &don
     return true;
 }
 
+// Bounded-wait limit and the stall test hook of a launch, from the overrides.
+void set_wait_hooks(TcParams *p, bool plain_kernel) {
+    const int kc = ovr(CONV2D_OVR_TEST_WAIT_KCYCLES);
+    p->wait_limit = kc > 0 ? (long long)kc * 1000 : kWaitLimitCycles;
+    p->withhold = plain_kernel && ovr(CONV2D_OVR_TEST_WITHHOLD) == 1 ? 1 : 0;
+}
+
 template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
 conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
     using L = TcSmem<BN, KSUB, STAGES>;
@@ -957,6 +993,7 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.bias = t.bias;
     p.y = t.y;
     p.status = status_word_ptr();
+    set_wait_hooks(&p, true);
     p.M = s.M;
     p.K = s.K;
     p.PQ = s.P * s.Q;
@@ -980,7 +1017,7 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
         return CONV2D_ERR_CUDA;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, maps->y, p) !=
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, p) !=
         cudaSuccess) {
         cudaGetLastError();
         return CONV2D_ERR_CUDA;
@@ -1000,6 +1037,7 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     p.bias = t.bias;
     p.y = t.y;
     p.status = status_word_ptr();
+    set_wait_hooks(&p, false);
     p.M = s.M;
     p.K = s.K;
     p.PQ = s.P * s.Q;
@@ -1024,7 +1062,7 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
         return CONV2D_ERR_CUDA;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, maps->y, p) !=
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, p) !=
         cudaSuccess) {
         cudaGetLastError();
         return CONV2D_ERR_CUDA;
@@ -1157,6 +1195,14 @@ bool tc_window_ok(const Shape &s) {
     if (g.TRW > 256) return false;
     if (g.max_shift + kBM > 48 * 1024 / 128) return false;
     return true;
+}
+
+int tc_num_variants() {
+    int n = 0;
+#define CONV2D_TC_COUNT(vbn, vks, vst) ++n;
+    CONV2D_TC_VARIANTS(CONV2D_TC_COUNT)
+#undef CONV2D_TC_COUNT
+    return n;
 }
 
 int tc_stages(int bn, int ksub) {

@@ -823,7 +823,6 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
         }
         p.rs_mask = 0;
         p.tap4 = 0;
-        p.w_vec = 0;
     }
     p.lstm_ch = 0;
     p.c_prev = nullptr;
@@ -838,7 +837,9 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
         p.h_next = lstm->h_next;
         p.h_img = lstm->h_img;
     }
-    p.w_vec = (s.Kg % 4 == 0 && ((uintptr_t)t.w & 15) == 0) ? 1 : 0;
+    // float4 weight loads need contiguous weight rows: not the transposed
+    // convolution's [K_in][K][R][S] layout
+    p.w_vec = (!dv && s.Kg % 4 == 0 && ((uintptr_t)t.w & 15) == 0) ? 1 : 0;
     p.y_vec = (p.nhwc && s.K % 4 == 0 && ((uintptr_t)t.y & 15) == 0) ? 1 : 0;
     const size_t bytes = L::bytes(p.KT);
     auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD, LSTM, RESB, NGRP>;

@@ -273,3 +273,61 @@ def random_inputs(spec: ConvSpec, seed: int, dist: str = "normal"):
         bias = _uniform(seed + 2, (spec.K,), -0.5, 0.5)
     b = _finish(bias, spec, "b") if spec.bias else None
     return _finish(x, spec, "x"), _finish(w, spec, "w"), b
+
+
+# ------------------------------------------------------------ output sample points
+#
+# Where a whole output is too large to check against the oracle, these pick
+# the logical outputs (n, k, p, q) to check.  Index selection only.
+
+def sample_indices(spec: ConvSpec, P: int, Q: int, count: int, seed: int) -> np.ndarray:
+    """Random outputs plus every border pixel of the first and last image
+    (8 random channels)."""
+    rng = np.random.default_rng(seed)
+    idx = [np.stack([rng.integers(0, d, size=count) for d in (spec.N, spec.K, P, Q)], axis=1)]
+    ks = rng.integers(0, spec.K, size=min(spec.K, 8))
+    for n in sorted({0, spec.N - 1}):
+        for k in ks:
+            for p in range(P):
+                for q in range(Q):
+                    if p in (0, P - 1) or q in (0, Q - 1):
+                        idx.append(np.array([[n, k, p, q]]))
+    return np.concatenate(idx, axis=0)
+
+
+def stratified_indices(spec: ConvSpec, P: int, Q: int, seed: int, tile_m: int = 128,
+                       chunk_k: int = 32) -> np.ndarray:
+    """Outputs that put at least two checked points into every output tile.
+
+    The GEMM rows m = (n, p, q) are cut into blocks of tile_m (the kernels'
+    M tile); for each block its first and last row are checked.  Window-mode
+    tiles are whole output rows, so the first and last pixel of every output
+    row are checked too.  Each such pixel is paired with one random channel
+    of every chunk_k-channel group (the epilogue's store box), so every
+    (M tile, N tile) and every store of a tile has checked elements."""
+    rng = np.random.default_rng(seed)
+    M = spec.N * P * Q
+    firsts = np.arange(0, M, tile_m, dtype=np.int64)
+    lasts = np.minimum(firsts + tile_m, M) - 1
+    row_starts = np.arange(spec.N * P, dtype=np.int64) * Q
+    rows = np.unique(np.concatenate([firsts, lasts, row_starts, row_starts + Q - 1]))
+    n, rem = np.divmod(rows, P * Q)
+    p, q = np.divmod(rem, Q)
+    out = []
+    for k0 in range(0, spec.K, chunk_k):
+        k = rng.integers(k0, min(k0 + chunk_k, spec.K), size=rows.size)
+        out.append(np.stack([n, k, p, q], axis=1))
+    return np.concatenate(out, axis=0)
+
+
+def check_points(spec: ConvSpec, P: int, Q: int, seed: int = 0, count: int = 6000) -> np.ndarray:
+    """Random, border and stratified sample points of one layer's output."""
+    return np.concatenate([sample_indices(spec, P, Q, count, seed),
+                           stratified_indices(spec, P, Q, seed + 1)], axis=0)
+
+
+def gather_points(y: torch.Tensor, idx: np.ndarray, layout: str) -> torch.Tensor:
+    """y at logical outputs idx[i] = (n, k, p, q), on y's device."""
+    t = torch.as_tensor(idx, dtype=torch.long, device=y.device)
+    n, k, p, q = t.unbind(1)
+    return y[n, k, p, q] if layout == "NCHW" else y[n, p, q, k]

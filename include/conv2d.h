@@ -27,9 +27,16 @@
  *  - Tensors are dense, contiguous and caller-owned device memory (cudaMalloc,
  *    cudaMallocAsync or managed memory; torch tensors qualify).  Host pointers
  *    are rejected with CONV2D_ERR_INVALID_ARG before anything is launched.
- *  - dtype applies to x, w, bias and y alike.  CONV2D_F32 computes in fp32 on
- *    CUDA cores (FFMA, never TF32).  CONV2D_F16 / CONV2D_BF16 multiply in the
- *    input type and accumulate in fp32; y is rounded once, to nearest even.
+ *  - dtype applies to x, w, bias and y alike.  CONV2D_F32 results meet the
+ *    fp32 bound |y - y_exact| <= 1e-6 * (sum |x||w| + |bias|) on every
+ *    kernel.  By default (CONV2D_ALGO_AUTO) the chooser runs an fp32 layer
+ *    either on tensor cores as split-precision 3xTF32 (each operand split
+ *    into two TF32 parts, three tcgen05 kind::tf32 products per multiply-add,
+ *    the full-magnitude term summed per 32-element stage in fp32 registers)
+ *    or on CUDA cores (FFMA), whichever its cost model expects to be faster;
+ *    plain single-pass TF32 is never used.  CONV2D_ALGO_CUDA_CORE keeps a
+ *    layer on FFMA.  CONV2D_F16 / CONV2D_BF16 multiply in the input type and
+ *    accumulate in fp32; y is rounded once, to nearest even.
  *  - layout CONV2D_NCHW: x [N][C][H][W], w [K][C][R][S], y [N][K][P][Q].
  *    layout CONV2D_NHWC: x [N][H][W][C], w [K][R][S][C], y [N][P][Q][K].
  *    bias is [K] or NULL (read as zero).
@@ -214,6 +221,82 @@ conv2d_status_t conv2d_deconv_forward(const void *x, const void *w, const void *
                                       int N, int K, int P, int Q, int C, int R, int S, int stride,
                                       int pad, int dil, int out_pad, conv2d_dtype_t dtype,
                                       conv2d_layout_t layout, cudaStream_t stream);
+
+/*
+ * Process-wide overrides of the chooser, for tests and A/B measurements.
+ * Each is -1 (not set: the chooser decides) or a value; they apply to every
+ * later call in the process, on every thread.  At the first call that needs
+ * them they are seeded from the environment variables named in brackets;
+ * after that only conv2d_set_override changes them (the environment is not
+ * read again, so the per-call path reads no environment).  A forced value
+ * that does not fit a layer makes that layer's call return
+ * CONV2D_ERR_UNSUPPORTED.
+ */
+typedef enum {
+    CONV2D_OVR_DIRECT = 0,        /* [CONV2D_DIRECT] fp32 direct kernel: 1 force, 0 never */
+    CONV2D_OVR_CC_TILE,           /* [CONV2D_CC_TILE] FFMA implicit-GEMM tile id */
+    CONV2D_OVR_CC_SPLIT,          /* [CONV2D_CC_SPLIT] FFMA cluster split-K: 1, 2 or 4 */
+    CONV2D_OVR_TC_BN,             /* [CONV2D_TC_BN] f16/bf16 tensor-core tile width: 64, 128, 256 */
+    CONV2D_OVR_TC_KSUB,           /* [CONV2D_TC_KSUB] 64-channel k-blocks per pipeline stage */
+    CONV2D_OVR_TC_IM2COL,         /* [CONV2D_TC_IM2COL] 1: 1x1 layers read x through the im2col map */
+    CONV2D_OVR_TC_WINDOW,         /* [CONV2D_TC_WINDOW] 1: window (im2win) mode only, 0: never */
+    CONV2D_OVR_TC_WINVAR,         /* [CONV2D_TC_WINVAR] window-mode variant id */
+    CONV2D_OVR_TC_ROTATE,         /* [CONV2D_TC_ROTATE] 0: every CTA starts its k-loop at stage 0 */
+    CONV2D_OVR_TF_VAR,            /* [CONV2D_TF_VAR] 3xTF32 variant id */
+    CONV2D_OVR_FP32_TC,           /* [CONV2D_FP32_TC] 0: AUTO never runs fp32 on tensor cores */
+    CONV2D_OVR_DECONV_TC,         /* [CONV2D_DECONV_TC] transposed conv: 1 tensor cores, 0 FFMA */
+    CONV2D_OVR_GRID_CAP,          /* [CONV2D_GRID_CAP] persistent kernels launch at most this many
+                                     CTAs (so small layers run several tiles per CTA) */
+    CONV2D_OVR_TEST_WITHHOLD,     /* [CONV2D_TEST_WITHHOLD] test hook, 1: in the f16/bf16 im2col /
+                                     plain tensor-core kernel, CTA 0 never issues the loads of its
+                                     first pipeline stage, so a bounded wait runs out: that CTA writes
+                                     none of its tiles, the call's device status becomes
+                                     CONV2D_ERR_TIMEOUT, the kernel still returns and the context
+                                     stays usable */
+    CONV2D_OVR_TEST_WAIT_KCYCLES, /* [CONV2D_TEST_WAIT_KCYCLES] f16/bf16 tensor-core kernels: a bounded
+                                     wait gives up after this many thousand SM cycles (default
+                                     4,000,000, about 2 s) */
+    CONV2D_OVR_COUNT
+} conv2d_override_t;
+
+/* Set an override (value -1 clears it).  CONV2D_ERR_INVALID_ARG for an
+ * unknown key or a value below -1.  Plans made before the change are
+ * discarded. */
+conv2d_status_t conv2d_set_override(conv2d_override_t key, int value);
+
+/* Current value of an override (-1 if not set). */
+conv2d_status_t conv2d_get_override(conv2d_override_t key, int *value);
+
+/* Kernel families with compiled variants (tile shapes, pipeline depths). */
+typedef enum {
+    CONV2D_FAMILY_CUDA_CORE_TILE = 0,   /* FFMA implicit-GEMM tiles (CONV2D_OVR_CC_TILE ids) */
+    CONV2D_FAMILY_TENSOR_CORE = 1,      /* f16/bf16 im2col / plain kernel: (BN, KSUB) pairs */
+    CONV2D_FAMILY_TENSOR_CORE_WINDOW = 2, /* f16/bf16 window kernel (CONV2D_OVR_TC_WINVAR ids) */
+    CONV2D_FAMILY_TF32X3 = 3            /* fp32 3xTF32 kernel (CONV2D_OVR_TF_VAR ids) */
+} conv2d_family_t;
+
+/* Number of compiled variants of a family (tests cover every one). */
+conv2d_status_t conv2d_variant_count(conv2d_family_t family, int *count);
+
+/*
+ * Throughput probes (measurement only, not part of the convolution path):
+ * one launch on `stream` of a kernel that does nothing but
+ *   CONV2D_PEAK_FFMA      fp32 FMAs in registers (8 CTAs of 256 threads per SM),
+ *   CONV2D_PEAK_TF32_MMA  tcgen05.mma kind::tf32, M=128 N=256 K=8, one CTA per SM,
+ *   CONV2D_PEAK_BF16_MMA  tcgen05.mma kind::f16 (bf16), M=128 N=256 K=16,
+ * `iters` rounds of them (1 .. 2^24), operands on chip.  *flops receives the
+ * floating-point operations the launch performs (2 per multiply-add); the
+ * caller times the launch with CUDA events.  CONV2D_ERR_UNSUPPORTED for the
+ * MMA probes on a GPU other than sm_103; CONV2D_ERR_CUDA if the launch fails.
+ */
+typedef enum {
+    CONV2D_PEAK_FFMA = 0,
+    CONV2D_PEAK_TF32_MMA = 1,
+    CONV2D_PEAK_BF16_MMA = 2
+} conv2d_peak_kind_t;
+
+conv2d_status_t conv2d_peak_probe(conv2d_peak_kind_t kind, int iters, cudaStream_t stream,
+                                  double *flops);
 
 /* Static text for a status code. */
 const char *conv2d_status_string(conv2d_status_t status);

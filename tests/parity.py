@@ -10,7 +10,7 @@ import numpy as np
 import torch
 
 import oracle
-from cnn_convolution_gb300 import conv2d
+from cnn_convolution_gb300 import conv2d, workloads as wl
 
 TOL = {"f32": 1e-6, "f16": 4e-3, "bf16": 4e-3}
 
@@ -35,27 +35,18 @@ def full_parity(spec, x, w, b, algo="auto"):
     return oracle.error_ratio(y, y_ref, den)
 
 
-def sample_indices(spec, P, Q, count, seed):
-    """Random outputs plus every border pixel of the first and last image."""
-    rng = np.random.default_rng(seed)
-    idx = [np.stack([rng.integers(0, d, size=count) for d in (spec.N, spec.K, P, Q)], axis=1)]
-    ks = rng.integers(0, spec.K, size=min(spec.K, 8))
-    for n in {0, spec.N - 1}:
-        for k in ks:
-            for p in range(P):
-                for q in range(Q):
-                    if p in (0, P - 1) or q in (0, Q - 1):
-                        idx.append(np.array([[n, k, p, q]]))
-    return np.concatenate(idx, axis=0)
-
-
-def sampled_parity(spec, x, w, b, y, count=6000, seed=0):
-    """Compare y (CPU tensor in spec.layout) at sampled logical outputs."""
+def sampled_parity(spec, x, w, b, y, count=6000, seed=0, stratified=True):
+    """Compare y (CPU tensor in spec.layout) at sampled logical outputs:
+    random ones, the borders of the first and last image, and (stratified)
+    points in every output tile."""
     if spec.layout == "NCHW":
         P, Q = y.shape[2], y.shape[3]
     else:
         P, Q = y.shape[1], y.shape[2]
-    idx = sample_indices(spec, P, Q, count, seed)
+    if stratified:
+        idx = wl.check_points(spec, P, Q, seed, count)
+    else:
+        idx = wl.sample_indices(spec, P, Q, count, seed)
     y_ref, den = oracle.conv2d_points(x, w, b, idx, spec.stride, spec.pad, spec.dil,
                                       layout=spec.layout)
     n, k, p, q = idx.T

@@ -154,3 +154,50 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         conv2d.load(str(tmp_path / "missing.so"))
     conv2d._lib = None   # reload the real library for later tests
+
+
+def test_overrides_set_get_and_validation(lib):
+    from cnn_convolution_gb300 import conv2d
+    assert conv2d.get_override("tc_bn") is None
+    with conv2d.overrides(tc_bn=128, grid_cap=3):
+        assert conv2d.get_override("tc_bn") == 128
+        assert conv2d.get_override("grid_cap") == 3
+    assert conv2d.get_override("tc_bn") is None
+    assert conv2d.get_override("grid_cap") is None
+    v = ctypes.c_int()
+    assert lib.conv2d_set_override(99, 1) == 1            # unknown key
+    assert lib.conv2d_set_override(-1, 1) == 1
+    assert lib.conv2d_set_override(0, -2) == 1            # below -1
+    assert lib.conv2d_get_override(99, ctypes.byref(v)) == 1
+    assert lib.conv2d_get_override(0, None) == 1
+    assert len(conv2d.OVERRIDES) == 15                    # CONV2D_OVR_COUNT in the header
+    text = open(HEADER).read()
+    body = text[text.index("typedef enum {\n    CONV2D_OVR_DIRECT"):text.index("CONV2D_OVR_COUNT")]
+    names = re.findall(r"CONV2D_OVR_([A-Z0-9_]+)", body)
+    assert [n.lower() for n in names] == list(conv2d.OVERRIDES)
+
+
+def test_overrides_are_seeded_from_the_environment_once():
+    """The environment is read at the first use only; later changes of it have no effect."""
+    import subprocess
+    import sys
+    code = ("import os, sys; sys.path.insert(0, %r)\n"
+            "from cnn_convolution_gb300 import conv2d\n"
+            "a = conv2d.get_override('tc_bn')\n"
+            "os.environ['CONV2D_TC_BN'] = '64'\n"
+            "b = conv2d.get_override('tc_bn')\n"
+            "print(a, b, conv2d.get_override('tf_var'))\n") % ROOT
+    env = dict(os.environ, CONV2D_TC_BN="256")
+    env.pop("CONV2D_TF_VAR", None)
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True).stdout.split()
+    assert out == ["256", "256", "None"]
+
+
+def test_variant_counts(lib):
+    from cnn_convolution_gb300 import conv2d
+    counts = {f: conv2d.variant_count(f) for f in conv2d.FAMILIES}
+    assert counts == {"cuda_core_tile": 8, "tensor_core": 7, "tensor_core_window": 9, "tf32x3": 14}
+    n = ctypes.c_int()
+    assert lib.conv2d_variant_count(7, ctypes.byref(n)) == 1
+    assert lib.conv2d_variant_count(0, None) == 1

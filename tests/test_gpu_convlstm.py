@@ -124,8 +124,7 @@ def test_cell_forced_variants(variant):
     """Every 3xTF32 variant that carries the gate epilogue (8 or more
     producer warps, one or two producer groups) gives the same cell; the
     others are refused as unsupported."""
-    import os
-    os.environ["CONV2D_TF_VAR"] = str(variant)
+    conv2d.set_override("tf_var", variant)
     try:
         ran = 0
         for i, (N, Cx, Ch, H, W, R) in enumerate([(2, 5, 7, 6, 13, 3), (2, 16, 16, 12, 12, 3)]):
@@ -139,6 +138,6 @@ def test_cell_forced_variants(variant):
             _check(xh, w, b, c0, R // 2, c, h)
             ran += 1
     finally:
-        os.environ.pop("CONV2D_TF_VAR", None)
+        conv2d.set_override("tf_var", None)
     if variant >= 3:    # 8 or more producer warps
         assert ran >= 1

@@ -62,10 +62,8 @@ CASES = [
 def deconv_path(request):
     """The 3xTF32 tensor-core kernel per output residue class
     (CONV2D_DECONV_TC=1) and the gather kernel (CONV2D_DECONV_TC=0)."""
-    import os
-    os.environ["CONV2D_DECONV_TC"] = "1" if request.param == "tensor_core" else "0"
-    yield request.param
-    os.environ.pop("CONV2D_DECONV_TC", None)
+    with conv2d.overrides(deconv_tc=1 if request.param == "tensor_core" else 0):
+        yield request.param
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
@@ -112,14 +110,8 @@ def test_deconv_argument_errors():
 def test_deconv_forced_variants(variant):
     """Each 3xTF32 variant in residue-class mode (a variant that cannot hold a
     class sends the layer to the gather kernel, which must agree too)."""
-    import os
-    os.environ["CONV2D_TF_VAR"] = str(variant)
-    os.environ["CONV2D_DECONV_TC"] = "1"
-    try:
+    with conv2d.overrides(tf_var=variant, deconv_tc=1):
         for case in [(2, 8, 6, 6, 5, 3, 3, 2, 1, 1, 1), (2, 6, 7, 8, 33, 3, 3, 2, 1, 2, 1),
                      (2, 20, 5, 5, 40, 2, 2, 2, 0, 1, 0)]:
             err = _run(*case, seed=900 + variant)
             assert err <= TOL["f32"], (case, variant, err)
-    finally:
-        os.environ.pop("CONV2D_TF_VAR", None)
-        os.environ.pop("CONV2D_DECONV_TC", None)

@@ -30,9 +30,8 @@ def _lib():
 
 @pytest.fixture
 def direct_on():
-    os.environ["CONV2D_DIRECT"] = "1"
-    yield
-    os.environ.pop("CONV2D_DIRECT", None)
+    with conv2d.overrides(direct=1):
+        yield
 
 
 SHAPES = [

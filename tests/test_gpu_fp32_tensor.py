@@ -10,8 +10,6 @@ M and K tiles, strides, padding, dilation, bias on and off, all-positive
 inputs (every rounding error with the same sign) and the MSCRED encoder
 layers at full size.
 """
-import os
-
 import pytest
 import torch
 
@@ -20,7 +18,9 @@ from parity import TOL, full_parity, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-N_VARIANTS = 14   # (BN, stages, producer warps, groups) table of the library
+# (BN, stages, producer warps, groups) table of the library; the count the
+# library reports must match, so a variant added there is not left untested
+N_VARIANTS = 14
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -37,12 +37,13 @@ def _lib():
 @pytest.fixture
 def variant_env():
     def set_variant(v):
-        if v is None:
-            os.environ.pop("CONV2D_TF_VAR", None)
-        else:
-            os.environ["CONV2D_TF_VAR"] = str(v)
+        conv2d.set_override("tf_var", v)
     yield set_variant
-    os.environ.pop("CONV2D_TF_VAR", None)
+    conv2d.set_override("tf_var", None)
+
+
+def test_variant_count_matches_library():
+    assert conv2d.variant_count("tf32x3") == N_VARIANTS
 
 
 SHAPES = [

@@ -247,10 +247,7 @@ SPLIT_SHAPES = [
 def test_cuda_core_split_k_clusters(tile, split, layout):
     """fp32 split-K: a cluster of `split` CTAs shares each output tile's
     reduction and sums the partial tiles through distributed shared memory."""
-    import os
-    os.environ["CONV2D_CC_TILE"] = str(tile)
-    os.environ["CONV2D_CC_SPLIT"] = str(split)
-    try:
+    with conv2d.overrides(cc_tile=tile, cc_split=split):
         for base in SPLIT_SHAPES:
             spec = base.replace(layout=layout)
             x, w, b = wl.random_inputs(spec, seed=31)
@@ -258,6 +255,3 @@ def test_cuda_core_split_k_clusters(tile, split, layout):
             assert f"split={split}" in d.plan(), d.plan()
             err = full_parity(spec, x, w, b, "cuda_core")
             assert err <= TOL["f32"], f"{spec.name} tile {tile} split {split}: {err}"
-    finally:
-        os.environ.pop("CONV2D_CC_TILE", None)
-        os.environ.pop("CONV2D_CC_SPLIT", None)

@@ -6,8 +6,6 @@ leave a ragged tile, M not a multiple of 128 (tiles running past the last
 image), strides, padding, dilation, non-square filters, bias on and off, and
 several persistent rounds per CTA.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -32,14 +30,11 @@ def _lib():
 @pytest.fixture
 def force_bn():
     def set_bn(bn, ksub=None):
-        for name, v in (("CONV2D_TC_BN", bn), ("CONV2D_TC_KSUB", ksub)):
-            if v is None:
-                os.environ.pop(name, None)
-            else:
-                os.environ[name] = str(v)
+        conv2d.set_override("tc_bn", bn)
+        conv2d.set_override("tc_ksub", ksub)
     yield set_bn
-    os.environ.pop("CONV2D_TC_BN", None)
-    os.environ.pop("CONV2D_TC_KSUB", None)
+    conv2d.set_override("tc_bn", None)
+    conv2d.set_override("tc_ksub", None)
 
 
 SHAPES = [
@@ -78,6 +73,53 @@ def test_forced_tile_widths(dtype, bn, ksub, force_bn):
         assert err <= TOL[dtype], f"{spec} BN={bn} KSUB={ksub}: err={err}"
 
 
+def test_variant_counts_match_library():
+    assert conv2d.variant_count("tensor_core") == len(VARIANTS)
+    assert conv2d.variant_count("tensor_core_window") == len(WINDOW_VARIANTS)
+
+
+# Persistent rounds: a CTA runs tiles blockIdx, blockIdx + grid, ...; the
+# accumulator alternates between two tensor-memory buffers, the stage and
+# accumulator phases flip every round and the epilogue's two staging buffers
+# alternate.  A grid capped at a few CTAs makes each CTA run many rounds on a
+# shape the oracle checks in full.
+MULTI_ROUND_SHAPES = [
+    # N, C, H, W, K, R, S, stride, pad, dil, bias
+    (6, 64, 20, 20, 96, 3, 3, 1, 1, 1, True),      # 19 M tiles x 1-2 N tiles
+    (4, 72, 17, 19, 136, 3, 3, 2, 1, 1, False),    # stride 2, ragged C, K and M
+    (5, 128, 12, 12, 264, 1, 1, 1, 0, 1, True),    # 1x1 plain A, ragged K
+]
+
+
+@pytest.mark.parametrize("grid_cap", [1, 3])
+@pytest.mark.parametrize("bn,ksub", VARIANTS)
+def test_forced_variants_many_rounds_per_cta(bn, ksub, grid_cap, force_bn):
+    force_bn(bn, ksub)
+    with conv2d.overrides(grid_cap=grid_cap, tc_window=0):
+        for i, (N, C, H, W, K, R, S, st, pad, dil, bias) in enumerate(MULTI_ROUND_SHAPES):
+            spec = wl.ConvSpec(f"rounds{i}", N, C, H, W, K, R, S, st, pad, dil, dtype="bf16",
+                               layout="NHWC", bias=bias)
+            x, w, b = wl.random_inputs(spec, seed=700 + i)
+            y, d = run_gpu(spec, x, w, b, "tensor_core")
+            assert f"grid={grid_cap} " in d.plan(), d.plan()
+            err = full_parity(spec, x, w, b, algo="tensor_core")
+            assert err <= TOL["bf16"], f"{spec} BN={bn} KSUB={ksub} grid={grid_cap}: err={err}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("mode", ["im2col", "window"])
+def test_full_grid_several_rounds_full_output(mode, dtype):
+    """At least 3 x 152 tiles on the natural (one CTA per SM) grid, whole
+    output compared: every CTA runs three or more persistent rounds."""
+    spec = wl.ConvSpec("rounds_full", 96, 8, 28, 28, 64, 3, 3, 1, 1, dtype=dtype, layout="NHWC")
+    x, w, b = wl.random_inputs(spec, seed=77)
+    with conv2d.overrides(tc_window=1 if mode == "window" else 0):
+        y, d = run_gpu(spec, x, w, b, "tensor_core")
+        assert mode in d.plan(), d.plan()
+        err = full_parity(spec, x, w, b, algo="tensor_core")
+    assert err <= TOL[dtype], f"{d.plan()}: err={err}"
+
+
 def test_plan_reports_tensor_core():
     d = conv2d.Conv2dDesc(2, 64, 8, 8, 64, 3, 3, 1, 1, 1, torch.bfloat16, "NHWC")
     assert d.plan().startswith("tensor_core")
@@ -107,8 +149,7 @@ def test_repeated_launches_are_deterministic():
 def test_1x1_plain_and_im2col_maps(im2col, force_bn):
     """1x1 / stride 1 / pad 0 layers read x as a plain [N*H*W, C] matrix; the
     im2col map must give the same answer."""
-    os.environ["CONV2D_TC_IM2COL"] = im2col
-    try:
+    with conv2d.overrides(tc_im2col=int(im2col)):
         for i, (N, C, H, W, K) in enumerate([(3, 64, 7, 7, 264), (1, 72, 5, 9, 64),
                                              (4, 512, 7, 7, 256), (2, 8, 13, 11, 16)]):
             spec = wl.ConvSpec(f"p1x1_{i}", N, C, H, W, K, 1, 1, 1, 0, 1, dtype="bf16",
@@ -116,8 +157,6 @@ def test_1x1_plain_and_im2col_maps(im2col, force_bn):
             x, w, b = wl.random_inputs(spec, seed=40 + i)
             err = full_parity(spec, x, w, b, algo="tensor_core")
             assert err <= TOL["bf16"], f"{spec}: {err}"
-    finally:
-        os.environ.pop("CONV2D_TC_IM2COL", None)
 
 
 WINDOW_SHAPES = [
@@ -159,10 +198,8 @@ def _window_fits(shape, variant):
 def test_window_mode(dtype, variant):
     """Stride-1 layers with one padded input window per channel block, the
     filter taps taken as row shifts of it (streamed or resident weights)."""
-    os.environ["CONV2D_TC_WINDOW"] = "1"
-    os.environ["CONV2D_TC_WINVAR"] = str(variant)
     ran = 0
-    try:
+    with conv2d.overrides(tc_window=1, tc_winvar=variant):
         for i, sh in enumerate(WINDOW_SHAPES + RESIDENT_SHAPES):
             if not _window_fits(sh, variant):
                 continue
@@ -175,10 +212,31 @@ def test_window_mode(dtype, variant):
             err = full_parity(spec, x, w, b, algo="tensor_core")
             assert err <= TOL[dtype], f"{spec} variant {variant}: err={err}"
             ran += 1
-    finally:
-        os.environ.pop("CONV2D_TC_WINDOW", None)
-        os.environ.pop("CONV2D_TC_WINVAR", None)
     assert ran >= 3
+
+
+@pytest.mark.parametrize("variant", sorted(WINDOW_VARIANTS))
+def test_window_mode_many_rounds_per_cta(variant):
+    """Window variants with the grid capped at 2 CTAs: many persistent rounds
+    per CTA (window slots, weight stages and accumulators all wrap)."""
+    ran = 0
+    with conv2d.overrides(tc_window=1, tc_winvar=variant, grid_cap=2):
+        for i, sh in enumerate([(5, 64, 14, 14, 64, 3, 3, 1, 1, True),
+                                (4, 72, 11, 10, 120, 3, 3, 1, 1, False),
+                                (6, 32, 9, 20, 40, 3, 3, 1, 1, True),
+                                (4, 64, 12, 12, 128, 2, 2, 0, 1, True)]):   # fits the 128-wide resident variant
+            if not _window_fits(sh, variant):
+                continue
+            N, C, H, W, K, R, S, pad, dil, bias = sh
+            spec = wl.ConvSpec(f"winr{i}", N, C, H, W, K, R, S, 1, pad, dil, dtype="bf16",
+                               layout="NHWC", bias=bias)
+            x, w, b = wl.random_inputs(spec, seed=260 + i)
+            y, d = run_gpu(spec, x, w, b, "tensor_core")
+            assert "window" in d.plan() and "grid=2 " in d.plan(), d.plan()
+            err = full_parity(spec, x, w, b, algo="tensor_core")
+            assert err <= TOL["bf16"], f"{spec} variant {variant}: err={err}"
+            ran += 1
+    assert ran >= 1
 
 
 RESIDENT_SHAPES = [
