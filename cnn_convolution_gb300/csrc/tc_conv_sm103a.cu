@@ -83,8 +83,8 @@ template <int BN> constexpr uint32_t tc_tmem_cols() {
     return (uint32_t)(tc_num_acc<BN>() * BN) <= 256 ? 256u : 512u;
 }
 // The bias is staged once per CTA as fp32 in shared memory when K <= kBiasMax
-// (16 KB with its 32-entry tail); larger layers read it from global memory.
-constexpr int kBiasMax = 4064;
+// (8 KB with its 32-entry tail); larger layers read it from global memory.
+constexpr int kBiasMax = 2016;
 constexpr int kBiasBytes = (kBiasMax + 32) * 4;
 
 __device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -167,8 +167,8 @@ struct TcParams {
 };
 
 // Shared-memory layout: STAGES stages, each holding KSUB k-blocks (the KSUB A
-// tiles, then the KSUB B tiles, every tile 1024-byte aligned), the fp32 bias,
-// then the barriers.  A stage is the unit of producer /
+// tiles, then the KSUB B tiles, every tile 1024-byte aligned), the epilogue
+// warps' store buffers, the fp32 bias, then the barriers.  A stage is the unit of producer /
 // consumer hand-off.  Measured on GB300, TMA cost is per instruction and per
 // stage rather than per byte, so a stage carries KSUB k-blocks and its B tiles
 // (and, for 1x1 layers, its A tiles) arrive in ONE 3-D box each.
@@ -177,8 +177,12 @@ struct TcSmem {
     static constexpr int kBTileBytes = BN * kBK * 2;
     static constexpr int kStageBytes = KSUB * (kATileBytes + kBTileBytes);
     static constexpr int kAcc = tc_num_acc<BN>();
+    // epilogue staging: per epilogue warp two buffers of 32 rows x 32 outputs
+    // (64 B), 64-byte swizzled, for its own TMA stores
+    static constexpr int kEpiBufBytes = 32 * 32 * 2;
+    static constexpr size_t kEpiOffset = (size_t)STAGES * kStageBytes;
     // the layer's bias as fp32
-    static constexpr size_t kBiasOffset = (size_t)STAGES * kStageBytes;
+    static constexpr size_t kBiasOffset = kEpiOffset + 4 * 2 * kEpiBufBytes;
     static constexpr size_t kBarOffset = kBiasOffset + kBiasBytes;
     // full[S], empty[S], acc_full[A], acc_empty[A], drain[1]; then tmem addr, abort flag
     static constexpr size_t kBarBytes = (2 * STAGES + 2 * kAcc + 1) * 8;
@@ -191,7 +195,7 @@ struct TcSmem {
 template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const TcParams p) {
+               const __grid_constant__ CUtensorMap tmY, const TcParams p) {
     using L = TcSmem<BN, KSUB, STAGES>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
@@ -236,6 +240,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -279,6 +284,18 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int per_o = (p.n_inner + KSUB - 1) / KSUB;
             const int n_st = p.n_outer * per_o;
             const int rot = p.rotate ? (int)(blockIdx.x % (unsigned)n_st) : 0;
+            if (A_TILE) {
+                // 1x1 layers read x once: warm L2 with the A rows of this CTA's
+                // next tile while this one streams (its boxes then hit L2)
+                const int tf = tile + (int)gridDim.x;
+                if (tf < p.total_tiles) {
+                    const int mf = (tf / p.n_tiles_n) * kBM;
+                    if (p.chunked)
+                        for (int i0 = 0; i0 < p.n_inner; i0 += KSUB) tma_prefetch_tile_3d(&tmA, 0, mf, i0);
+                    else
+                        for (int o = 0; o < p.n_outer; ++o) tma_prefetch_tile_2d(&tmA, o * kBK, mf);
+                }
+            }
             for (int j = 0; j < n_st; ++j) {
                 int sidx = rot + j;
                 if (sidx >= n_st) sidx -= n_st;
@@ -343,6 +360,18 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int per_o = (p.n_inner + KSUB - 1) / KSUB;
             const int n_st = p.n_outer * per_o;
             const int rot = p.rotate ? (int)(blockIdx.x % (unsigned)n_st) : 0;
+            if (A_TILE) {
+                // 1x1 layers read x once: warm L2 with the A rows of this CTA's
+                // next tile while this one streams (its boxes then hit L2)
+                const int tf = tile + (int)gridDim.x;
+                if (tf < p.total_tiles) {
+                    const int mf = (tf / p.n_tiles_n) * kBM;
+                    if (p.chunked)
+                        for (int i0 = 0; i0 < p.n_inner; i0 += KSUB) tma_prefetch_tile_3d(&tmA, 0, mf, i0);
+                    else
+                        for (int o = 0; o < p.n_outer; ++o) tma_prefetch_tile_2d(&tmA, o * kBK, mf);
+                }
+            }
             for (int j = 0; j < n_st; ++j) {
                 int sidx = rot + j;
                 if (sidx >= n_st) sidx -= n_st;
@@ -381,8 +410,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ---------------------------------------------------------- epilogue
         // Thread = one output pixel (accumulator lane).  Per 32-output chunk:
         // tcgen05.ld -> + bias (fp32, staged once per CTA) -> one RN cast ->
-        // four 16-byte stores of the pixel's 64 contiguous bytes of y.  No
-        // staging buffer and no barrier between the epilogue warps per chunk.
+        // the row's 64 bytes into the warp's own 64-byte-swizzled staging
+        // buffer -> one TMA store of the warp's 32 x 32 box (clipped at M and
+        // K).  Each warp alternates two buffers and orders its stores by
+        // itself: no barrier between the epilogue warps per chunk.
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         float *bias_s = reinterpret_cast<float *>(smem + L::kBiasOffset);
@@ -391,7 +422,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (bias_in_smem)
             for (int k = (int)threadIdx.x - 64; k < p.K; k += 128) bias_s[k] = load_bias<T>(bias_g, k);
         epilogue_bar_sync();                      // the staged bias is visible to the four warps
-        T *y = static_cast<T *>(p.y);
+        const uint32_t wbuf = smem_base + (uint32_t)L::kEpiOffset + (uint32_t)(quarter * 2 * L::kEpiBufBytes);
+        const uint32_t row_off = (uint32_t)lane * 64u;
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);
+        uint32_t chunk = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
@@ -406,10 +440,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_after();
             const int tm = tile / p.n_tiles_n;
             const int tn = tile - tm * p.n_tiles_n;
-            const int64_t m = (int64_t)tm * kBM + row;
-            const bool valid = m < p.M;
+            const int m_warp = tm * kBM + quarter * 32;
             const int k0 = tn * BN;
-            T *yrow = y + (valid ? m : 0) * (int64_t)p.K;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -438,13 +470,20 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     o[j / 2] = pack2<T>(a0, a1);
                     o[j / 2 + 1] = pack2<T>(a2, a3);
                 }
-                if (valid) {
-                    // K % 8 == 0: each 8-output group lies wholly inside or outside y
+                const uint32_t buf = wbuf + (chunk & 1u) * (uint32_t)L::kEpiBufBytes;
+                if (lane == 0) bulk_wait_read_le1();     // this warp's store from this buffer has read it
+                __syncwarp();
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
-                        if (kc + 8 * g < p.K)
-                            st_global_v4(yrow + kc + 8 * g, o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
+                for (int g = 0; g < 4; ++g)
+                    st_shared_v4(buf + row_off + ((((uint32_t)g) ^ swz) << 4), o[4 * g], o[4 * g + 1],
+                                 o[4 * g + 2], o[4 * g + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmY, buf, kc, m_warp);
+                    bulk_commit_group();
                 }
+                ++chunk;
             }
             tc_fence_before();
             __syncwarp();
@@ -452,6 +491,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (row == 0) TC_TRACE(2, 6);
             if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
         }
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -602,6 +642,18 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 tma_load_tile_4d(win_slot(wslot), &tmA, wfull_bar(wslot), cb * kBK, -p.pad, p0 - p.pad,
                                  n_img);
                 TC_TRACE(0, 9);
+                // Warm L2 with the window this CTA loads NWIN tiles later: its
+                // smem load is issued only when a slot frees, and then reads
+                // L2 instead of waiting on HBM.
+                {
+                    const int tf = tile + NWIN * (int)gridDim.x;
+                    if (tf < p.total_tiles) {
+                        const int tmf = tf / p.n_tiles_n;
+                        const int nf = tmf / p.tiles_per_img;
+                        const int pf = (tmf - nf * p.tiles_per_img) * p.TR;
+                        tma_prefetch_tile_4d(&tmA, cb * kBK, -p.pad, pf - p.pad, nf);
+                    }
+                }
                 ++n_w;
                 if (++wslot == NWIN) { wslot = 0; wphase ^= 1u; }
                 if (RES) continue;
@@ -638,6 +690,9 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
         constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);
         constexpr uint64_t kSubDesc = (uint64_t)(L::kBTileBytes >> 4);
+        // window row shifts in descriptor units (16 bytes; a row is 128 bytes)
+        const uint64_t a_col_step = (uint64_t)(p.dil * 8);
+        const uint64_t a_row_step = (uint64_t)(p.dil * p.Wp * 8 - p.S * p.dil * 8);
         if (RES && !mbar_wait(res_bar, 0, abort_flag, p.status, p.wait_limit)) ok = false;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
@@ -648,8 +703,18 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 if (!mbar_wait(wfull_bar(wslot), wphase, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
                 TC_TRACE(1, 7);
                 tc_fence_after();
-                const uint32_t wbase = win_slot(wslot);
-                int r = 0, s = 0;
+                // Descriptors advance incrementally: tap (r, s) reads the
+                // window's rows shifted by r*dil*Wp + s*dil pixels (8 descriptor
+                // units of 16 bytes per 128-byte row), and the resident weight
+                // tiles of consecutive taps are consecutive.  The start row need
+                // not be a multiple of 8: the 128-byte swizzle follows absolute
+                // shared-memory address bits, so the base-offset field stays 0.
+                // The issuing thread's loop is on the critical path for N = 64
+                // tiles (an MMA every ~50 cycles), so it does no multiplications.
+                const uint64_t a_desc_w = smem_desc_sw128(win_slot(wslot));
+                uint64_t a_tap = 0;                              // row shift of the tap, descriptor units
+                int s = 0;
+                uint64_t bd_res = RES ? smem_desc_sw128(res_tile(cb, 0)) : 0;
                 for (int t0 = 0; t0 < RS; t0 += KSUB) {
                     const int nsub = min(KSUB, RS - t0);
                     if (!RES) {
@@ -657,20 +722,19 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                         TC_TRACE(1, 2);
                         tc_fence_after();
                     }
+                    const uint64_t bd_stage = b_desc0 + (uint64_t)stage * kStageDesc;
+#pragma unroll 3
                     for (int j = 0; j < nsub; ++j) {
-                        // tap (r, s): the window's rows shifted by r*dil*Wp + s*dil pixels.
-                        // The start row need not be a multiple of 8: the 128-byte
-                        // swizzle follows absolute shared-memory address bits, so
-                        // the descriptor's base-offset field stays 0.
-                        const uint32_t a_start = wbase + (uint32_t)((r * p.dil * p.Wp + s * p.dil) * 128);
-                        const uint64_t ad = smem_desc_sw128(a_start);
-                        const uint64_t bd = RES ? smem_desc_sw128(res_tile(cb, t0 + j))
-                                                : b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)j * kSubDesc;
+                        const uint64_t ad = a_desc_w + a_tap;
+                        const uint64_t bd = RES ? bd_res : bd_stage + (uint64_t)j * kSubDesc;
+                        const uint32_t first = (cb | (t0 + j)) == 0 ? 1u : 0u;
+                        mma_f16(d_tmem, ad, bd, kIdesc, first ^ 1u);
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)
-                            mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
-                                    (cb | (t0 + j) | k) != 0 ? 1u : 0u);
-                        if (++s == p.S) { s = 0; ++r; }
+                        for (int k = 1; k < kBK / 16; ++k)
+                            mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc, 1u);
+                        if (RES) bd_res += kSubDesc;
+                        a_tap += a_col_step;
+                        if (++s == p.S) { s = 0; a_tap += a_row_step; }
                     }
                     any = true;
                     if (!RES) {
@@ -813,10 +877,11 @@ bool load_driver_fns() {
 }
 
 struct TcMaps {
-    alignas(64) CUtensorMap a, b;
+    alignas(64) CUtensorMap a, b, y;   // y: the im2col / plain kernel's store map
 };
 
-// Encode the two tensor maps of a launch (x as im2col, plain matrix or window, w).
+// Encode the tensor maps of a launch: x (im2col, plain matrix or window), w,
+// and for the im2col / plain kernel y.
 // Window geometry of a stride-1 layer (see the window kernel).
 struct WinGeom {
     int Wp, TR, TRW, max_shift;
@@ -914,16 +979,27 @@ conv2d_status_t encode_maps(const Shape &s, int BN, int KSUB, int amode, const T
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return CONV2D_ERR_CUDA;
     }
+    if (amode != 2) {
+        // y as the [M, K] row-major matrix; boxes of 32 rows x 32 outputs (one epilogue warp's store)
+        const cuuint64_t dims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.K * 2};
+        const cuuint32_t box[2] = {32, 32};
+        const cuuint32_t estr[2] = {1, 1};
+        if (g_encode_tiled(&m->y, dt, 2, t.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    }
     return CONV2D_OK;
 }
 
-// Maps depend only on the layer, the tile width, the A mode and the x and w
+// Maps depend only on the layer, the tile width, the A mode and the three
 // pointers; repeated calls with the same tensors reuse them (host time).
 struct MapKey {
     int v[15];
-    const void *x, *w;
+    const void *x, *w, *y;
     bool operator==(const MapKey &o) const {
-        return std::memcmp(v, o.v, sizeof(v)) == 0 && x == o.x && w == o.w;
+        return std::memcmp(v, o.v, sizeof(v)) == 0 && x == o.x && w == o.w && y == o.y;
     }
 };
 
@@ -945,6 +1021,7 @@ conv2d_status_t cached_maps(const Shape &s, int BN, int KSUB, int amode, const T
     std::memcpy(k.v, vals, sizeof(vals));
     k.x = t.x;
     k.w = t.w;
+    k.y = t.y;
     for (int i = 0; i < kSlots; ++i) {
         if (slots[i].used && slots[i].key == k) {
             *out = &slots[i].maps;
@@ -1017,7 +1094,7 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
         return CONV2D_ERR_CUDA;
     const int grid = pl.grid > 0 ? pl.grid : 1;
-    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, p) !=
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, maps->y, p) !=
         cudaSuccess) {
         cudaGetLastError();
         return CONV2D_ERR_CUDA;
