@@ -197,9 +197,159 @@ __global__ void __launch_bounds__(kDcThreads, 4) direct_conv_kernel(const DcPara
     }
 }
 
+// ------------------------------------------------------------------ quad kernel
+//
+// Register-blocked variant for stride-1, dilation-1 layers with at most 32
+// output channels and 1x1, 3x3 or 5x5 filters (the MSCRED encoder's first
+// layer and the single signature-matrix convolution).  Same CTA block and
+// staging as above (8 x 32 output pixels, 128 threads), but a thread owns 4
+// consecutive output pixels of one row x 16 output channels.  Per (input
+// channel, filter row) it reads the 8 patch values its pixels' S taps share
+// with two 16-byte shared loads and runs S taps x 4 pixels x 16 channels of
+// FFMAs from registers, reading each tap's 16 weights as four 16-byte
+// broadcasts: 2 + 4S shared loads per 64S FFMAs (the kernel above issues 10
+// per 64).  Patch rows are padded to kQdIWP = 36 floats so the 16-byte loads
+// stay aligned.
+constexpr int kQdIWP = 36;
+
+template <int R, int S>
+__global__ void __launch_bounds__(kDcThreads, 4) direct_quad_kernel(const DcParams p) {
+    extern __shared__ float4 dc_smem4[];
+    constexpr int IH = kDcRows + R - 1;
+    constexpr int plane = IH * kQdIWP;
+    float *xs = reinterpret_cast<float *>(dc_smem4);           // [C][IH][kQdIWP]
+    const int patch = p.C * plane;                             // a multiple of 4
+    const int Kg = p.C * R * S;
+    float *wt = xs + patch;                                    // [Kg][32]
+
+    int t = blockIdx.x;
+    const int tq = t % p.tiles_q;
+    t /= p.tiles_q;
+    const int tp = t % p.tiles_p;
+    const int n = t / p.tiles_p;
+    const int p0 = tp * kDcRows, q0 = tq * kDcCols;
+    const int h0 = p0 - p.pad, w0 = q0 - p.pad;
+    sm103a::pdl_launch_dependents();
+    sm103a::pdl_wait();
+
+    const float *ximg = p.x + (int64_t)n * p.C * p.H * p.W;
+    const uint32_t xs_u = sm103a::smem_u32(xs), wt_u = sm103a::smem_u32(wt);
+    for (int i = (int)threadIdx.x; i < patch; i += kDcThreads) {
+        const int r2 = fdiv(i, p.m_iw);
+        const int iw = i - r2 * kQdIWP;
+        const int c = fdiv(r2, p.m_ih);
+        const int ih = r2 - c * IH;
+        const int h = h0 + ih, wc = w0 + iw;
+        const bool in = (unsigned)h < (unsigned)p.H && (unsigned)wc < (unsigned)p.W;
+        const int hh = in ? h : 0, ww = in ? wc : 0, cc = in ? c : 0;
+        const int off = p.nhwc ? (hh * p.W + ww) * p.C + cc : (cc * p.H + hh) * p.W + ww;
+        sm103a::cp_async_f32(xs_u + 4u * (uint32_t)i, ximg + off, in);
+    }
+    for (int i = (int)threadIdx.x; i < Kg * 32; i += kDcThreads) {
+        const int g = i >> 5, k = i & 31;
+        int woff = g;
+        if (p.nhwc) {
+            const int c = fdiv(g, p.m_rs), rs = g - c * (R * S);
+            woff = rs * p.C + c;
+        }
+        const bool in = k < p.K;
+        sm103a::cp_async_f32(wt_u + 4u * (uint32_t)i, p.w + (in ? (int64_t)k * Kg + woff : 0), in);
+    }
+    sm103a::cp_async_commit();
+    sm103a::cp_async_wait<0>();
+    __syncthreads();
+
+    // warps 0-1: channels 0-15, warps 2-3: 16-31; a warp = 8 quads x 4 rows
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int kb = warp >> 1;
+    const int rho = (warp & 1) * 4 + (lane >> 3);
+    const int j = lane & 7;
+    float acc[4][16];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[a][k] = 0.f;
+    const float *xt = xs + rho * kQdIWP + 4 * j;
+    const float *wk = wt + kb * 16;
+    for (int c = 0; c < p.C; ++c) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float4 v0 = *reinterpret_cast<const float4 *>(xt + (c * IH + r) * kQdIWP);
+            const float4 v1 = *reinterpret_cast<const float4 *>(xt + (c * IH + r) * kQdIWP + 4);
+            const float xv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int s2 = 0; s2 < S; ++s2) {
+                const float4 *w4 = reinterpret_cast<const float4 *>(wk + ((c * R + r) * S + s2) * 32);
+                float wv[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 t4 = w4[q];
+                    wv[4 * q] = t4.x;
+                    wv[4 * q + 1] = t4.y;
+                    wv[4 * q + 2] = t4.z;
+                    wv[4 * q + 3] = t4.w;
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float xa = xv[a + s2];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) acc[a][k] = fmaf(xa, wv[k], acc[a][k]);
+                }
+            }
+        }
+    }
+    // + bias, store
+    const int k0 = kb * 16;
+    if (p.bias) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float bv = sm103a::ldg_or_zero(p.bias + (k0 + k < p.K ? k0 + k : 0), k0 + k < p.K);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) acc[a][k] += bv;
+        }
+    }
+    const int pp = p0 + rho;
+    if (pp >= p.P) return;
+    const int q = q0 + 4 * j;
+    if (p.nhwc) {
+        const bool vec = (p.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.y) & 15) == 0);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            if (q + a >= p.Q) break;
+            float *yr = p.y + (((int64_t)n * p.P + pp) * p.Q + q + a) * p.K + k0;
+#pragma unroll
+            for (int k = 0; k < 16; k += 4) {
+                if (k0 + k >= p.K) break;
+                if (vec)
+                    *reinterpret_cast<float4 *>(yr + k) = make_float4(acc[a][k], acc[a][k + 1], acc[a][k + 2], acc[a][k + 3]);
+                else
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (k0 + k + e < p.K) yr[k + e] = acc[a][k + e];
+            }
+        }
+    } else {
+        const int64_t PQ = (int64_t)p.P * p.Q;
+        float *yr = p.y + ((int64_t)n * p.K + k0) * PQ + (int64_t)pp * p.Q + q;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (k0 + k >= p.K) break;
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                if (q + a < p.Q) yr[(int64_t)k * PQ + a] = acc[a][k];
+        }
+    }
+}
+
+// The quad kernel takes stride-1, dilation-1 layers with K <= 32 and a 1x1,
+// 3x3 or 5x5 filter (the patch row of 32 + S - 1 columns fits kQdIWP).
+bool quad_ok(const Shape &s) {
+    return s.stride == 1 && s.dil == 1 && s.K <= 32 && s.R == s.S && (s.R == 1 || s.R == 3 || s.R == 5);
+}
+
 void patch_dims(const Shape &s, int *ih, int *iw) {
     *ih = (kDcRows - 1) * s.stride + (s.R - 1) * s.dil + 1;
-    *iw = (kDcCols - 1) * s.stride + (s.S - 1) * s.dil + 1;
+    *iw = quad_ok(s) ? kQdIWP : (kDcCols - 1) * s.stride + (s.S - 1) * s.dil + 1;
 }
 
 }  // namespace
@@ -208,7 +358,7 @@ size_t dc_smem_bytes(const Shape &s) {
     int ih, iw;
     patch_dims(s, &ih, &iw);
     const size_t patch = ((size_t)s.C * ih * iw + 3) & ~(size_t)3;
-    const size_t kp = ((size_t)s.K + kDcKc - 1) / kDcKc * kDcKc;
+    const size_t kp = ((size_t)s.K + kDcKc - 1) / kDcKc * kDcKc;   // 32 for the quad kernel
     return (patch + (size_t)s.Kg * kp) * sizeof(float);
 }
 
@@ -255,7 +405,11 @@ conv2d_status_t dc_launch(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.m_rs = recip_u32(s.R * s.S);
     const size_t bytes = dc_smem_bytes(s);
     void (*kern)(DcParams);
-    if (s.R == 3 && s.S == 3) kern = direct_conv_kernel<3, 3>;
+    if (quad_ok(s)) {
+        if (s.R == 3) kern = direct_quad_kernel<3, 3>;
+        else if (s.R == 1) kern = direct_quad_kernel<1, 1>;
+        else kern = direct_quad_kernel<5, 5>;
+    } else if (s.R == 3 && s.S == 3) kern = direct_conv_kernel<3, 3>;
     else if (s.R == 2 && s.S == 2) kern = direct_conv_kernel<2, 2>;
     else if (s.R == 1 && s.S == 1) kern = direct_conv_kernel<1, 1>;
     else if (s.R == 5 && s.S == 5) kern = direct_conv_kernel<5, 5>;

@@ -54,6 +54,7 @@ struct TfTile {
     int stage_ns;    // measured time of one 32-element stage of one tile (GB300)
     bool resb;       // the split weights of the CTA's output-channel tile stay resident
     int ngrp;        // producer groups: stage f is filled by group f % ngrp
+    bool at;         // the A operand (split input) lives in tensor memory
 };
 
 enum class Algo { CudaCore, TensorCore, Tf32x3, Direct };

@@ -60,6 +60,18 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D(tmem) (+)= A(tmem) * B(smem)^T: A is 128 lanes x 8 columns of TF32 values
+// (lane = row, column = reduction element) starting at a_tmem.
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor, kind::tf32: fp32 accumulate, A and B TF32, both K-major.
 __host__ __device__ constexpr uint32_t make_idesc_tf32(int n) {
     return (1u << 4)                                   // D format: f32
@@ -151,24 +163,29 @@ __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf
 
 // Tensor memory: columns [0, 2 BN) hold the correction accumulators (x_hi*w_lo
 // + x_lo*w_hi) of two tiles in flight; NSLOT slots of BN columns after them
-// receive the x_hi*w_hi partial sum of one 32-element stage each.
-template <int BN>
+// receive the x_hi*w_hi partial sum of one 32-element stage each.  With the
+// A operand in tensor memory (AT), STAGES stages of 64 columns follow: the
+// stage's 32 A_hi columns, then its 32 A_lo columns (lane = output pixel).
+template <int BN, bool AT = false, int STAGES = 1>
 struct TfTmem {
-    static constexpr int kSlots = BN >= 128 ? 2 : 6;
-    static constexpr int kUsed = 2 * BN + kSlots * BN;
+    static constexpr int kACols = AT ? 64 * STAGES : 0;
+    static constexpr int kFree = (512 - 2 * BN - kACols) / BN;
+    static constexpr int kSlots = AT ? (kFree > 6 ? 6 : kFree) : (BN >= 128 ? 2 : 6);
+    static constexpr int kACol0 = 2 * BN + kSlots * BN;
+    static constexpr int kUsed = kACol0 + kACols;
     static constexpr uint32_t kCols = kUsed <= 32 ? 32 : kUsed <= 64 ? 64 : kUsed <= 128 ? 128
                                       : kUsed <= 256 ? 256 : 512;
-    static_assert(kUsed <= 512, "tensor memory");
+    static_assert(kSlots >= 2 && kUsed <= 512, "tensor memory");
 };
 
-// Shared memory: STAGES x (A_hi, A_lo[, B_hi, B_lo]), barriers, then -- with
+// Shared memory: STAGES x ([A_hi, A_lo unless AT][, B_hi, B_lo]), barriers, then -- with
 // resident weights (RESB) -- the split weights of every stage of the CTA's
 // output-channel tile (KT x (B_hi, B_lo)), then the tap table.
-template <int BN, int STAGES, bool RESB = false>
+template <int BN, int STAGES, bool RESB = false, bool AT = false>
 struct TfSmem {
     static constexpr int kBTile = BN * kTfBK * 4;
-    static constexpr int kStage = 2 * kTfATile + (RESB ? 0 : 2 * kBTile);
-    static constexpr int kSlots = TfTmem<BN>::kSlots;
+    static constexpr int kStage = (AT ? 0 : 2 * kTfATile) + (RESB ? 0 : 2 * kBTile);
+    static constexpr int kSlots = TfTmem<BN, AT, STAGES>::kSlots;
     static constexpr size_t kBarOffset = (size_t)STAGES * kStage;
     // full[S], empty[S], slot_full[NS], slot_empty[NS], corr_full[2], corr_empty[2], drain,
     // weights-ready; then the tensor-memory address and the abort flag
@@ -203,10 +220,14 @@ template <int BN, int NPROD> constexpr int tf_threads() { return 32 * (tf_epi_wa
 // the loads of its next stage before storing the current one; with several,
 // it issues its loads and then waits for the stage to be free, so that wait
 // overlaps the loads' latency.
-template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB, int NGRP>
+// AT: the A operand lives in tensor memory.  The producers write each stage's
+// A_hi / A_lo columns with tcgen05.st (lane = their output pixel) and the
+// MMAs read A from there, so shared memory carries only the weights: the
+// tensor cores' operand reads no longer compete with the producers' stores.
+template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB, int NGRP, bool AT>
 __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel(const TfParams p) {
-    using L = TfSmem<BN, STAGES, RESB>;
-    using TM = TfTmem<BN>;
+    using L = TfSmem<BN, STAGES, RESB, AT>;
+    using TM = TfTmem<BN, AT, STAGES>;
     constexpr uint32_t kIdesc = make_idesc_tf32(BN);
     constexpr int kSlots = TM::kSlots;
     constexpr int kEpiWarps = tf_epi_warps<BN>();
@@ -329,7 +350,7 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
     // weight tiles of stage s (streamed) or of reduction stage ks (resident)
     auto b_hi = [&](int s) {
         return RESB ? smem_base + (uint32_t)(L::kResBOffset + (size_t)s * 2 * L::kBTile)
-                    : smem_base + (uint32_t)(s * L::kStage + 2 * kTfATile);
+                    : smem_base + (uint32_t)(s * L::kStage + (AT ? 0 : 2 * kTfATile));
     };
     auto b_lo = [&](int s) { return b_hi(s) + (uint32_t)L::kBTile; };
 
@@ -467,17 +488,45 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             if (pt == 0) TF_TRACE(0, 6);
             const int stage = f % STAGES;
             const uint32_t phase = (uint32_t)(f / STAGES) & 1u;
-            // every lane observes the MMAs' release of the stage itself before overwriting it
-            if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)))
-                return false;
+            // lane 0 waits for the MMAs' release of the stage, the warp follows
+            // (one poller per warp instead of 32 keeps the barrier polling off
+            // the shared-memory bandwidth the tensor cores read operands with)
+            int okw = 1;
+            if (lane == 0) okw = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status) ? 1 : 0;
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            __syncwarp();
+            if (!okw) return false;
             if (pt == 0) TF_TRACE(0, 2);
+            if constexpr (AT) {
+                // this warp's 32 lanes are its pixels' accumulator rows; the
+                // thread writes its kChunks * 4 reduction elements of the
+                // stage into the A_hi and A_lo columns
+                tc_fence_after();
+                uint32_t hi[kChunks * 4], lo[kChunks * 4];
 #pragma unroll
-            for (int j = 0; j < kChunks; ++j) {
-                uint32_t hi[4], lo[4];
-                split4(va[j], hi, lo);
-                const uint32_t off = a_row_off + ((((uint32_t)(chunk0 + j)) ^ row_sw) << 4);
-                st_shared_v4(a_hi(stage) + off, hi[0], hi[1], hi[2], hi[3]);
-                st_shared_v4(a_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
+                for (int j = 0; j < kChunks; ++j) {
+                    uint32_t h4[4], l4[4];
+                    split4(va[j], h4, l4);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hi[4 * j + e] = h4[e];
+                        lo[4 * j + e] = l4[e];
+                    }
+                }
+                const uint32_t ta = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) +
+                                    (uint32_t)(TM::kACol0 + stage * 64 + chunk0 * 4);
+                tmem_st<kChunks * 4>(ta, hi);
+                tmem_st<kChunks * 4>(ta + 32u, lo);
+                tmem_st_wait();
+            } else {
+#pragma unroll
+                for (int j = 0; j < kChunks; ++j) {
+                    uint32_t hi[4], lo[4];
+                    split4(va[j], hi, lo);
+                    const uint32_t off = a_row_off + ((((uint32_t)(chunk0 + j)) ^ row_sw) << 4);
+                    st_shared_v4(a_hi(stage) + off, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(a_lo(stage) + off, lo[0], lo[1], lo[2], lo[3]);
+                }
             }
 #pragma unroll
             for (int it = 0; it < (RESB ? 0 : kBIter); ++it) {
@@ -491,9 +540,11 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             }
             // make this thread's generic-proxy stores visible to the tensor cores
             if (pt == 0) TF_TRACE(0, 5);
-            // each thread makes its generic-proxy stores visible to the tensor
-            // cores; then one lane per warp arrives for the whole warp
+            // each thread makes its generic-proxy stores (and, with AT, its
+            // completed tensor-memory stores) visible to the tensor cores;
+            // then one lane per warp arrives for the whole warp
             fence_proxy_async_smem();
+            if (AT) tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(full_bar(stage));
             if (pt == 0) TF_TRACE(0, 3);
@@ -584,20 +635,37 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 TF_TRACE(1, 4);
                 tc_fence_after();
                 const uint32_t d_main = tmem_base + (uint32_t)(2 * BN + slot * BN);
-                const uint64_t ah = smem_desc_sw128(a_hi(stage)), al = smem_desc_sw128(a_lo(stage));
                 const uint64_t bh = smem_desc_sw128(b_hi(RESB ? ks : stage));
                 const uint64_t bl = smem_desc_sw128(b_lo(RESB ? ks : stage));
-                // advance 8 elements (32 bytes) along K inside the swizzled rows
+                if constexpr (AT) {
+                    // A in tensor memory: 8 columns per K step
+                    const uint32_t ah = tmem_base + (uint32_t)(TM::kACol0 + stage * 64), al = ah + 32u;
 #pragma unroll
-                for (int kk = 0; kk < kTfBK / 8; ++kk)
-                    mma_tf32(d_main, ah + (uint64_t)(kk * 2), bh + (uint64_t)(kk * 2), kIdesc, kk != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kTfBK / 8; ++kk)
+                        mma_tf32_ts(d_main, ah + (uint32_t)(kk * 8), bh + (uint64_t)(kk * 2), kIdesc,
+                                    kk != 0 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < kTfBK / 8; ++kk) {
-                    const uint64_t o = (uint64_t)(kk * 2);
-                    mma_tf32(d_corr, ah + o, bl + o, kIdesc, (ks | kk) != 0 ? 1u : 0u);
-                    mma_tf32(d_corr, al + o, bh + o, kIdesc, 1u);
+                    for (int kk = 0; kk < kTfBK / 8; ++kk) {
+                        const uint64_t o = (uint64_t)(kk * 2);
+                        mma_tf32_ts(d_corr, ah + (uint32_t)(kk * 8), bl + o, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+                        mma_tf32_ts(d_corr, al + (uint32_t)(kk * 8), bh + o, kIdesc, 1u);
+                    }
+                } else {
+                    const uint64_t ah = smem_desc_sw128(a_hi(stage)), al = smem_desc_sw128(a_lo(stage));
+                    // advance 8 elements (32 bytes) along K inside the swizzled rows
+#pragma unroll
+                    for (int kk = 0; kk < kTfBK / 8; ++kk)
+                        mma_tf32(d_main, ah + (uint64_t)(kk * 2), bh + (uint64_t)(kk * 2), kIdesc,
+                                 kk != 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kTfBK / 8; ++kk) {
+                        const uint64_t o = (uint64_t)(kk * 2);
+                        mma_tf32(d_corr, ah + o, bl + o, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+                        mma_tf32(d_corr, al + o, bh + o, kIdesc, 1u);
+                    }
                 }
                 any = true;
+                TF_TRACE(1, 12);
                 mma_commit(empty_bar(stage));
                 mma_commit(slotf_bar(slot));
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -778,10 +846,10 @@ bool ensure_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &done_mas
     return true;
 }
 
-template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB, int NGRP>
+template <int BN, int STAGES, int NPROD, bool LSTM, bool RESB, int NGRP, bool AT>
 conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
                           cudaStream_t st, const TfDeconv *dv = nullptr) {
-    using L = TfSmem<BN, STAGES, RESB>;
+    using L = TfSmem<BN, STAGES, RESB, AT>;
     TfParams p;
     p.x = static_cast<const float *>(t.x);
     p.w = static_cast<const float *>(t.w);
@@ -842,7 +910,7 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
     p.w_vec = (!dv && s.Kg % 4 == 0 && ((uintptr_t)t.w & 15) == 0) ? 1 : 0;
     p.y_vec = (p.nhwc && s.K % 4 == 0 && ((uintptr_t)t.y & 15) == 0) ? 1 : 0;
     const size_t bytes = L::bytes(p.KT);
-    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD, LSTM, RESB, NGRP>;
+    auto kern = tf32x3_conv_kernel<BN, STAGES, NPROD, LSTM, RESB, NGRP, AT>;
     static std::atomic<uint64_t> attr_done{0};   // this instantiation's per-device flags
     // the attribute is set for the largest table this variant accepts
     if (!ensure_attr(reinterpret_cast<const void *>(kern), 227 * 1024, attr_done)) return CONV2D_ERR_CUDA;
@@ -860,38 +928,44 @@ conv2d_status_t launch_tf(const Shape &s, const Plan &pl, const Tensors &t, cons
 }
 
 // Only variants with 8 or more producer warps carry the ConvLSTM epilogue.
-template <int BN, int STAGES, int NPROD, bool RESB, int NGRP>
+template <int BN, int STAGES, int NPROD, bool RESB, int NGRP, bool AT>
 conv2d_status_t launch_tf_lstm(const Shape &s, const Plan &pl, const Tensors &t, const TfLstm *lstm,
                                cudaStream_t st) {
     if constexpr (NPROD >= 8)
-        return launch_tf<BN, STAGES, NPROD, true, RESB, NGRP>(s, pl, t, lstm, st, nullptr);
+        return launch_tf<BN, STAGES, NPROD, true, RESB, NGRP, AT>(s, pl, t, lstm, st, nullptr);
     return CONV2D_ERR_UNSUPPORTED;
 }
 
-// (BN, STAGES, producer warps, measured ns per stage of one tile) of every
-// compiled variant.  The stage times were measured on GB300 on the MSCRED
+// (BN, STAGES, producer warps, measured ns per stage of one tile, resident
+// weights, producer groups, A in tensor memory) of every compiled variant.  The stage times were measured on GB300 on the MSCRED
 // encoder layers (fp32 NCHW, 3x3 / 2x2 filters); the producers' gather is
 // latency-bound, so more producer warps per SM run a stage faster.  The
 // 3-stage variant leaves shared memory for the tap tables of long
-// reductions (C*R*S up to about 9,000).  The resident-weight variants split
+// reductions (C*R*S up to about 9,000).  The last three keep the split input
+// in tensor memory (AT): correct, and measured within a few percent of their
+// shared-memory siblings on the MSCRED encoder layers, so their costs are set
+// just above those.  The resident-weight variants split
 // the weights once per CTA (C*R*S up to about 350 at BN = 64).  Two producer
 // groups (last four rows) took the encoder layers 5-10 % and the decoder's
 // 32-channel-wide residue classes 7-14 % below the best one-group variant.
-#define CONV2D_TF_VARIANTS(X)        \
-    X(32, 5, 4, 1240, false, 1)      \
-    X(64, 4, 4, 3850, false, 1)      \
-    X(128, 3, 4, 5000, false, 1)     \
-    X(32, 5, 8, 920, false, 1)       \
-    X(64, 4, 8, 1370, false, 1)      \
-    X(128, 3, 8, 3100, false, 1)     \
-    X(64, 4, 16, 1100, false, 1)     \
-    X(64, 3, 16, 1060, false, 1)     \
-    X(64, 2, 16, 1060, true, 1)      \
-    X(64, 3, 16, 1060, true, 1)      \
-    X(64, 4, 16, 990, false, 2)       \
-    X(64, 2, 16, 940, true, 2)         \
-    X(128, 2, 16, 2400, false, 2)    \
-    X(32, 5, 16, 820, false, 2)
+#define CONV2D_TF_VARIANTS(X)               \
+    X(32, 5, 4, 1240, false, 1, false)      \
+    X(64, 4, 4, 3850, false, 1, false)      \
+    X(128, 3, 4, 5000, false, 1, false)     \
+    X(32, 5, 8, 920, false, 1, false)       \
+    X(64, 4, 8, 1370, false, 1, false)      \
+    X(128, 3, 8, 3100, false, 1, false)     \
+    X(64, 4, 16, 1100, false, 1, false)     \
+    X(64, 3, 16, 1060, false, 1, false)     \
+    X(64, 2, 16, 1060, true, 1, false)      \
+    X(64, 3, 16, 1060, true, 1, false)      \
+    X(64, 4, 16, 990, false, 2, false)      \
+    X(64, 2, 16, 940, true, 2, false)       \
+    X(128, 2, 16, 2400, false, 2, false)    \
+    X(32, 5, 16, 820, false, 2, false)      \
+    X(64, 4, 16, 1000, true, 2, true)       \
+    X(64, 4, 16, 1000, false, 2, true)      \
+    X(32, 4, 16, 830, false, 2, true)
 
 }  // namespace
 
@@ -900,7 +974,7 @@ bool tf_lstm_variant(int id) { return tf_variant(id).nprod >= 8; }
 
 int tf_num_variants() {
     int n = 0;
-#define X(vbn, vst, vnp, vns, vrb, vng) ++n;
+#define X(vbn, vst, vnp, vns, vrb, vng, vat) ++n;
     CONV2D_TF_VARIANTS(X)
 #undef X
     return n;
@@ -908,9 +982,9 @@ int tf_num_variants() {
 
 TfTile tf_variant(int id) {
     int i = 0;
-    TfTile t{0, 0, 0, -1, 0, false, 1};
-#define X(vbn, vst, vnp, vns, vrb, vng)                        \
-    if (i == id) t = TfTile{vbn, vst, vnp, id, vns, vrb, vng}; \
+    TfTile t{0, 0, 0, -1, 0, false, 1, false};
+#define X(vbn, vst, vnp, vns, vrb, vng, vat)                        \
+    if (i == id) t = TfTile{vbn, vst, vnp, id, vns, vrb, vng, vat}; \
     ++i;
     CONV2D_TF_VARIANTS(X)
 #undef X
@@ -920,8 +994,12 @@ TfTile tf_variant(int id) {
 size_t tf_smem_bytes(const Shape &s, const TfTile &t) {
     const size_t kt = (size_t)((s.Kg + kTfBK - 1) / kTfBK);
     const size_t btile = (size_t)t.BN * kTfBK * 4;
-    const size_t stage = 2 * (size_t)kTfATile + (t.resb ? 0 : 2 * btile);
-    const size_t slots = t.BN >= 128 ? 2 : 6;
+    const size_t stage = (t.at ? 0 : 2 * (size_t)kTfATile) + (t.resb ? 0 : 2 * btile);
+    size_t slots = t.BN >= 128 ? 2 : 6;
+    if (t.at) {
+        const size_t fr = (512 - 2 * (size_t)t.BN - 64 * (size_t)t.stages) / t.BN;
+        slots = fr > 6 ? 6 : fr;
+    }
     const size_t bars = (2 * (size_t)t.stages + 2 * slots + 6) * 8;
     const size_t end = (size_t)t.stages * stage + bars + 16;
     const size_t taps = t.resb ? (end + 1023) / 1024 * 1024 + kt * 2 * btile : (end + 15) / 16 * 16;
@@ -956,12 +1034,12 @@ extern "C" int conv2d_tf_trace_dump(unsigned long long *out, unsigned int *count
 conv2d_status_t tf_launch(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st,
                           const TfLstm *lstm, const TfDeconv *dv) {
     int i = 0;
-#define X(vbn, vst, vnp, vns, vrb, vng)                                                   \
-    if (pl.tf.id == i) {                                                                  \
-        if (dv) return launch_tf<vbn, vst, vnp, false, vrb, vng>(s, pl, t, nullptr, st, dv); \
-        if (lstm) return launch_tf_lstm<vbn, vst, vnp, vrb, vng>(s, pl, t, lstm, st);      \
-        return launch_tf<vbn, vst, vnp, false, vrb, vng>(s, pl, t, nullptr, st);            \
-    }                                                                                     \
+#define X(vbn, vst, vnp, vns, vrb, vng, vat)                                                    \
+    if (pl.tf.id == i) {                                                                        \
+        if (dv) return launch_tf<vbn, vst, vnp, false, vrb, vng, vat>(s, pl, t, nullptr, st, dv); \
+        if (lstm) return launch_tf_lstm<vbn, vst, vnp, vrb, vng, vat>(s, pl, t, lstm, st);      \
+        return launch_tf<vbn, vst, vnp, false, vrb, vng, vat>(s, pl, t, nullptr, st);            \
+    }                                                                                           \
     ++i;
     CONV2D_TF_VARIANTS(X)
 #undef X

@@ -14,6 +14,11 @@ from cnn_convolution_gb300 import conv2d, workloads as wl
 
 TOL = {"f32": 1e-6, "f16": 4e-3, "bf16": 4e-3}
 
+# Compiled 3xTF32 variants (the library's table).  Tests parametrize over
+# range(N_TF_VARIANTS), and test_abi / test_gpu_fp32_tensor check that the
+# library reports the same count, so a variant added there cannot go untested.
+N_TF_VARIANTS = 17
+
 
 def run_gpu(spec, x, w, b, algo="auto", stream=None):
     d = conv2d.Conv2dDesc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride,

@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+from parity import N_TF_VARIANTS
 from oracle import convlstm as lstm_oracle
 from cnn_convolution_gb300 import conv2d, workloads as wl
 
@@ -116,7 +117,6 @@ def test_cell_argument_errors():
         conv2d.convlstm_cell(xh, w, None, c0, pad=1, c_next=c0)
 
 
-N_TF_VARIANTS = 14   # the 3xTF32 variant table of the library
 
 
 @pytest.mark.parametrize("variant", range(N_TF_VARIANTS))

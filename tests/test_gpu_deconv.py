@@ -8,7 +8,7 @@ import torch
 import oracle
 from oracle import deconv as dv_oracle
 from cnn_convolution_gb300 import conv2d
-from parity import TOL
+from parity import N_TF_VARIANTS, TOL
 
 pytestmark = pytest.mark.gpu
 
@@ -106,7 +106,7 @@ def test_deconv_argument_errors():
     assert conv2d.get_device_status() == 0
 
 
-@pytest.mark.parametrize("variant", range(14))
+@pytest.mark.parametrize("variant", range(N_TF_VARIANTS))
 def test_deconv_forced_variants(variant):
     """Each 3xTF32 variant in residue-class mode (a variant that cannot hold a
     class sends the layer to the gather kernel, which must agree too)."""

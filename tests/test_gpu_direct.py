@@ -47,6 +47,12 @@ SHAPES = [
     (1, 1, 1, 1, 3, 1, 1, 1, 0, 1, True),          # one pixel
     (2, 5, 11, 13, 9, 3, 2, 1, 1, 1, True),        # non-square filter (generic tap loop)
     (1, 2, 23, 40, 33, 4, 4, 2, 3, 1, False),      # 4x4, stride 2, 33 channels
+    # stride 1, dilation 1, K <= 32, 1x1 / 3x3 / 5x5: the register-blocked quad kernel
+    (3, 3, 17, 45, 20, 3, 3, 1, 1, 1, True),       # K = 20: second channel half partly empty
+    (2, 2, 9, 31, 7, 5, 5, 1, 2, 1, True),         # 5x5, Q not a multiple of 4
+    (2, 5, 13, 14, 32, 1, 1, 1, 0, 1, False),      # 1x1
+    (1, 6, 8, 33, 12, 3, 3, 1, 0, 1, True),        # no padding, a column block of 3
+    (2, 2, 30, 30, 16, 5, 5, 1, 3, 1, True),       # pad wider than the filter half-width
 ]
 
 

@@ -14,13 +14,11 @@ import pytest
 import torch
 
 from cnn_convolution_gb300 import conv2d, workloads as wl
-from parity import TOL, full_parity, run_gpu
+from parity import N_TF_VARIANTS, TOL, full_parity, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-# (BN, stages, producer warps, groups) table of the library; the count the
-# library reports must match, so a variant added there is not left untested
-N_VARIANTS = 14
+N_VARIANTS = N_TF_VARIANTS
 
 
 @pytest.fixture(scope="module", autouse=True)
