@@ -488,35 +488,37 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             if (pt == 0) TF_TRACE(0, 6);
             const int stage = f % STAGES;
             const uint32_t phase = (uint32_t)(f / STAGES) & 1u;
-            // lane 0 waits for the MMAs' release of the stage, the warp follows
-            // (one poller per warp instead of 32 keeps the barrier polling off
-            // the shared-memory bandwidth the tensor cores read operands with)
-            int okw = 1;
-            if (lane == 0) okw = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status) ? 1 : 0;
-            okw = __shfl_sync(0xffffffffu, okw, 0);
-            __syncwarp();
-            if (!okw) return false;
+            // every lane observes the MMAs' release of the stage itself before
+            // overwriting it (measured faster on the encoder layers than one
+            // waiting lane and a warp shuffle)
+            if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)))
+                return false;
             if (pt == 0) TF_TRACE(0, 2);
             if constexpr (AT) {
                 // this warp's 32 lanes are its pixels' accumulator rows; the
                 // thread writes its kChunks * 4 reduction elements of the
                 // stage into the A_hi and A_lo columns
                 tc_fence_after();
-                uint32_t hi[kChunks * 4], lo[kChunks * 4];
-#pragma unroll
-                for (int j = 0; j < kChunks; ++j) {
-                    uint32_t h4[4], l4[4];
-                    split4(va[j], h4, l4);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        hi[4 * j + e] = h4[e];
-                        lo[4 * j + e] = l4[e];
-                    }
-                }
+                // in pieces of at most 4 chunks (16 columns), to bound registers
+                constexpr int kPc = kChunks < 4 ? kChunks : 4;
                 const uint32_t ta = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) +
                                     (uint32_t)(TM::kACol0 + stage * 64 + chunk0 * 4);
-                tmem_st<kChunks * 4>(ta, hi);
-                tmem_st<kChunks * 4>(ta + 32u, lo);
+#pragma unroll
+                for (int j0 = 0; j0 < kChunks; j0 += kPc) {
+                    uint32_t hi[kPc * 4], lo[kPc * 4];
+#pragma unroll
+                    for (int j = 0; j < kPc; ++j) {
+                        uint32_t h4[4], l4[4];
+                        split4(va[j0 + j], h4, l4);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            hi[4 * j + e] = h4[e];
+                            lo[4 * j + e] = l4[e];
+                        }
+                    }
+                    tmem_st<kPc * 4>(ta + (uint32_t)(j0 * 4), hi);
+                    tmem_st<kPc * 4>(ta + 32u + (uint32_t)(j0 * 4), lo);
+                }
                 tmem_st_wait();
             } else {
 #pragma unroll
