@@ -462,6 +462,22 @@ def bench_main(args):
         run_encoder(descs, x_dev, ws, bs, outs)
     host_us = (time.perf_counter() - t0) / (n_calls // n_layers * n_layers) * 1e6
     torch.cuda.synchronize()
+    # the same through the raw C ABI (argument marshalling done once): the
+    # library's own host time per call (validation, plan lookup, launch)
+    import ctypes
+    lib = conv2d.load()
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    raw = []
+    for i, d in enumerate(descs):
+        src = x_dev if i == 0 else outs[i - 1]
+        raw.append((d.handle, src.data_ptr(), ws[i].data_ptr(), bs[i].data_ptr(), outs[i].data_ptr()))
+    torch.cuda._sleep(50_000_000)
+    t0 = time.perf_counter()
+    for _ in range(n_calls // n_layers):
+        for h, xp, wp, bp, yp in raw:
+            lib.conv2d_forward_desc(h, xp, wp, bp, yp, st)
+    host_us_c = (time.perf_counter() - t0) / (n_calls // n_layers * n_layers) * 1e6
+    torch.cuda.synchronize()
 
     # per-layer roofline; the dominant kernel is the layer with the largest time
     layers = []
@@ -581,6 +597,7 @@ def bench_main(args):
             "layers": layers,
             "eager_ms_per_step": round(statistics.mean(eager), 5),
             "host_us_per_call": round(host_us, 2),
+            "host_us_per_call_c_abi": round(host_us_c, 2),
             "e2e": e2e,
             "fp32_cuda_core_only": fp32_cuda_core_only,
             "single_signature_conv": single,

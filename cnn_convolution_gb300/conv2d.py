@@ -151,18 +151,31 @@ class Conv2dDesc:
         return buf.value.decode()
 
     def y_shape(self):
-        N, C, H, W, K = self.sizes[:5]
-        P, Q = self.output_dims()
-        return (N, K, P, Q) if self.layout == "NCHW" else (N, P, Q, K)
+        shape = getattr(self, "_y_shape", None)
+        if shape is None:
+            N, C, H, W, K = self.sizes[:5]
+            P, Q = self.output_dims()
+            shape = (N, K, P, Q) if self.layout == "NCHW" else (N, P, Q, K)
+            self._y_shape = shape
+        return shape
 
     def forward(self, x, w, bias=None, y=None, stream=None):
         if y is None:
             y = torch.empty(self.y_shape(), dtype=self.dtype, device=x.device)
-        _validate(x, w, bias, y, self.dtype)
-        st = _stream_handle(stream, x.device)
-        _check(self._lib.conv2d_forward_desc(self._h, x.data_ptr(), w.data_ptr(),
+        dt = self.dtype
+        # dtype and density are the caller's promise the library cannot see;
+        # device placement it checks itself (host pointers are rejected)
+        if not (x.dtype is dt and w.dtype is dt and y.dtype is dt and (bias is None or bias.dtype is dt)):
+            _validate(x, w, bias, y, dt)        # raises with the exact reason
+        if not (x.is_contiguous() and w.is_contiguous() and y.is_contiguous()
+                and (bias is None or bias.is_contiguous())):
+            _validate(x, w, bias, y, dt)
+        code = self._lib.conv2d_forward_desc(self._h, x.data_ptr(), w.data_ptr(),
                                              None if bias is None else bias.data_ptr(),
-                                             y.data_ptr(), st), "conv2d_forward_desc")
+                                             y.data_ptr(), _stream_handle(stream, x.device))
+        if code:
+            _validate(x, w, bias, y, dt)
+            _check(code, "conv2d_forward_desc")
         return y
 
 
@@ -176,10 +189,19 @@ def _validate(x, w, bias, y, dtype):
             raise ValueError(f"{name} must be contiguous")
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(stream, device):
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    """The cudaStream_t to launch on: `stream`'s, or the current stream of
+    `device` (read through torch's raw-stream query, which costs a fraction
+    of building a Stream object)."""
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:
+        idx = device.index if device.index is not None else torch.cuda.current_device()
+        return ctypes.c_void_p(_raw_stream(idx))
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
 def output_dims(H, W, R, S, stride=1, pad=0, dil=1) -> Tuple[int, int]:
