@@ -11,17 +11,22 @@
 //
 // out[b][c][i][j] = M_ij(t_first + b, windows[c]).
 //
-// One CTA per end time (grid.y splits the n*n pairs when there are more than
-// one CTA's worth).  The samples are staged in shared memory in chunks of
-// 64 time steps (rows padded to an odd stride, so the lanes of a warp, which
-// read different signals at one time step, hit different banks), walked
-// from the most recent backwards; because every window
-// ends at e, the windows are nested, so one pass over the longest window
-// emits every window's matrix as soon as its sample count is reached (the
-// windows are visited in increasing length).  Each thread accumulates its
-// pairs in fp32 with FMA in that fixed order and divides by w once.
+// One CTA per end time.  A thread owns one window and a 2x2 block of
+// (i, j) pairs -- rows i0, i0+1 against columns j0, j0+1, blocks with
+// j0 >= i0 only: the matrices are symmetric (s_i s_j = s_j s_i exactly), so
+// an off-diagonal block is also written transposed.  The end time's samples
+// (its longest window) are staged once in shared memory by asynchronous
+// copies, time-major ([position][signal], so one 8-byte read gives a signal
+// pair at one time step); windows too long for shared memory are read
+// through the read-only cache instead.  Each thread runs one plain loop over
+// its window, newest sample first: two 8-byte reads feed 4 FMAs into 4
+// fp32 accumulators that start from zero, then divides each by w once.
+// Threads of a warp share one window (the block count is padded to a
+// multiple of 32), so a warp's loop has one trip count.
 
 #include <algorithm>
+#include <atomic>
+#include <cmath>
 #include <cstdint>
 
 #include "internal.h"
@@ -30,88 +35,90 @@
 namespace conv2d {
 namespace {
 
-constexpr int kSigThreads = 256;
-constexpr int kSigChunk = 64;      // time steps staged per pass
-constexpr int kSigStride = kSigChunk + 1;   // odd row stride: lanes reading different rows hit different banks
-constexpr int kSigPairs = 4;       // (i, j) pairs per thread
+constexpr int kSigThreads = 384;
 constexpr int kSigMaxWindows = 8;
+constexpr int kSigSmemMax = 96 * 1024;   // larger windows are read from global memory
 
 struct SigParams {
     const float *series;   // [n][T]
     float *out;            // [n_steps][n_windows][n][n]
-    int n, T, n_win, t_first;
-    int win[kSigMaxWindows];    // window lengths, increasing
-    int chan[kSigMaxWindows];   // output channel of each
+    int n, T, n_win, t_first, wmax;
+    int sstride;           // staged floats per position: >= n rounded up to even, = 2 mod 32
+    int nblk, nblk_pad;    // 2x2 blocks with j0 >= i0; that count rounded up to a multiple of 32
+    int win[kSigMaxWindows];
 };
 
-__global__ void __launch_bounds__(kSigThreads) signature_kernel(const SigParams p) {
-    extern __shared__ float ss[];              // [n][kSigStride]
+// Signals i, i + 1 at one position; a signal index >= n reads as 0.
+template <bool kStaged>
+__device__ __forceinline__ float2 sig_pair(const float *ss, const SigParams &p, int64_t t_lo, int i, int pos) {
+    if constexpr (kStaged) {
+        return *reinterpret_cast<const float2 *>(ss + pos * p.sstride + i);
+    } else {
+        const float *g = p.series + t_lo + pos + (int64_t)i * p.T;
+        return make_float2(__ldg(g), i + 1 < p.n ? __ldg(g + p.T) : 0.f);
+    }
+}
+
+// Positions index the end time's samples: position 0 is time e - wmax, the
+// newest sample e - 1 is position wmax - 1; window w reads wmax - w .. wmax - 1.
+template <bool kStaged>
+__global__ void __launch_bounds__(kSigThreads) signature_kernel(const __grid_constant__ SigParams p) {
+    extern __shared__ __align__(16) float ss[];   // [position][sstride]
     // no early trigger: a kernel of many short CTAs lets the next one launch
     // at its exit, so the next grid is spread over idle SMs
     sm103a::pdl_wait();                        // the previous kernel's writes are visible
     const int b = blockIdx.x;
-    const int e = p.t_first + b;
-    const int nn = p.n * p.n;
-    const int pid0 = blockIdx.y * (kSigThreads * kSigPairs) + (int)threadIdx.x;
-    int pi[kSigPairs], pj[kSigPairs];
-#pragma unroll
-    for (int q = 0; q < kSigPairs; ++q) {
-        const int pid = pid0 + q * kSigThreads;
-        pi[q] = pid < nn ? pid / p.n : 0;
-        pj[q] = pid < nn ? pid - pi[q] * p.n : 0;
-    }
-    float acc[kSigPairs];
-#pragma unroll
-    for (int q = 0; q < kSigPairs; ++q) acc[q] = 0.f;
-
-    // the window table in shared memory; the next boundary stays in a register
-    __shared__ int s_win[kSigMaxWindows], s_chan[kSigMaxWindows];
-    if (threadIdx.x < kSigMaxWindows) {
-        s_win[threadIdx.x] = threadIdx.x < (unsigned)p.n_win ? p.win[threadIdx.x] : 0;
-        s_chan[threadIdx.x] = threadIdx.x < (unsigned)p.n_win ? p.chan[threadIdx.x] : 0;
+    const int64_t t_lo = (int64_t)p.t_first + b - p.wmax;
+    const int n_pad = (p.n + 1) & ~1;
+    if constexpr (kStaged) {
+        // one signal per warp at a time, consecutive positions across the
+        // lanes (coalesced reads); every copy in flight before the wait
+        const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+        const uint32_t ss_u = sm103a::smem_u32(ss);
+        for (int i = warp; i < n_pad; i += kSigThreads / 32) {
+            const float *row = p.series + (int64_t)min(i, p.n - 1) * p.T + t_lo;
+            for (int q = lane; q < p.wmax; q += 32)
+                sm103a::cp_async_f32(ss_u + 4u * (uint32_t)(q * p.sstride + i), row + q, i < p.n);
+        }
+        sm103a::cp_async_commit();
+        sm103a::cp_async_wait<0>();
     }
     __syncthreads();
-    const int wmax = s_win[p.n_win - 1];
-    int count = 0, next = 0;                   // samples summed so far, next window to emit
-    int next_w = s_win[0];
-    for (int t_hi = e; t_hi > e - wmax; t_hi -= kSigChunk) {
-        const int len = min(kSigChunk, t_hi - (e - wmax));
-        const int t_lo = t_hi - len;
-        __syncthreads();                       // the previous chunk is no longer read
-        // every load of the chunk is issued before any of them is stored
-        for (int k0 = 0; k0 < p.n * len; k0 += kSigThreads * 8) {
-            float v[8];
+
+    const int item = blockIdx.y * kSigThreads + (int)threadIdx.x;
+    const int c = item / p.nblk_pad, k = item - c * p.nblk_pad;
+    if (c >= p.n_win || k >= p.nblk) return;
+    // block k -> (bi, bj), bi <= bj, rows of the upper triangle in order:
+    // row bi starts at S(bi) = bi*nt - bi(bi-1)/2; the root of S(x) = k,
+    // then at most one step to correct its rounding
+    const int nt = n_pad / 2;
+    const int e2 = 2 * nt + 1;
+    int bi = (int)(((float)e2 - sqrtf((float)(e2 * e2 - 8 * k))) * 0.5f);
+    bi = max(0, min(bi, nt - 1));
+    if (bi > 0 && k < bi * nt - bi * (bi - 1) / 2) --bi;
+    if (bi + 1 < nt && k >= (bi + 1) * nt - (bi + 1) * bi / 2) ++bi;
+    const int i0 = 2 * bi, j0 = 2 * (bi + k - (bi * nt - bi * (bi - 1) / 2));
+
+    const int w = p.win[c];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};     // pair (i0 + u / 2, j0 + u % 2)
+#pragma unroll 4
+    for (int pos = p.wmax - 1; pos >= p.wmax - w; --pos) {
+        const float2 a = sig_pair<kStaged>(ss, p, t_lo, i0, pos);
+        const float2 v = sig_pair<kStaged>(ss, p, t_lo, j0, pos);
+        acc[0] = fmaf(a.x, v.x, acc[0]);
+        acc[1] = fmaf(a.x, v.y, acc[1]);
+        acc[2] = fmaf(a.y, v.x, acc[2]);
+        acc[3] = fmaf(a.y, v.y, acc[3]);
+    }
+    float *o = p.out + ((int64_t)b * p.n_win + c) * p.n * p.n;
+    const float wf = (float)w;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int k = k0 + u * kSigThreads + (int)threadIdx.x;
-                const int i = k / len, tt = k - i * len;
-                const bool in = k < p.n * len;
-                v[u] = sm103a::ldg_or_zero(p.series + (in ? (int64_t)i * p.T + t_lo + tt : 0), in);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int k = k0 + u * kSigThreads + (int)threadIdx.x;
-                const int i = k / len, tt = k - i * len;
-                if (k < p.n * len) ss[i * kSigStride + tt] = v[u];
-            }
-        }
-        __syncthreads();
-        for (int tt = len - 1; tt >= 0; --tt) {
-#pragma unroll
-            for (int q = 0; q < kSigPairs; ++q)
-                acc[q] = fmaf(ss[pi[q] * kSigStride + tt], ss[pj[q] * kSigStride + tt], acc[q]);
-            ++count;
-            while (count == next_w) {
-                const float w = (float)next_w;
-                float *o = p.out + ((int64_t)b * p.n_win + s_chan[next]) * nn;
-#pragma unroll
-                for (int q = 0; q < kSigPairs; ++q) {
-                    const int pid = pid0 + q * kSigThreads;
-                    if (pid < nn) o[pid] = acc[q] / w;
-                }
-                ++next;
-                next_w = next < p.n_win ? s_win[next] : 0;
-            }
+    for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u / 2, j = j0 + u % 2;
+        if (i < p.n && j < p.n) {
+            const float m = acc[u] / wf;
+            o[i * p.n + j] = m;
+            if (i0 != j0) o[j * p.n + i] = m;   // a diagonal block holds both (i, j) and (j, i)
         }
     }
 }
@@ -127,19 +134,41 @@ conv2d_status_t sig_launch(const float *series, int n, int T, const int *windows
     p.T = T;
     p.n_win = n_windows;
     p.t_first = t_first;
-    int order[kSigMaxWindows];
-    for (int c = 0; c < n_windows; ++c) order[c] = c;
-    std::sort(order, order + n_windows, [&](int a, int b) {
-        return windows[a] < windows[b] || (windows[a] == windows[b] && a < b);
-    });
+    p.wmax = 0;
     for (int c = 0; c < n_windows; ++c) {
-        p.win[c] = windows[order[c]];
-        p.chan[c] = order[c];
+        p.win[c] = windows[c];
+        p.wmax = std::max(p.wmax, windows[c]);
     }
-    const int per_cta = kSigThreads * kSigPairs;
-    const dim3 grid((unsigned)n_steps, (unsigned)((n * n + per_cta - 1) / per_cta));
-    const size_t smem = (size_t)n * kSigStride * sizeof(float);
-    if (launch_pdl(signature_kernel, grid, dim3(kSigThreads), smem, st, p) != cudaSuccess) {
+    const int n_pad = (n + 1) & ~1;
+    // = 2 mod 32: the staging writes (lanes on consecutive positions) spread over 16 banks
+    p.sstride = n_pad + (34 - n_pad % 32) % 32;
+    const int nt = n_pad / 2;
+    p.nblk = nt * (nt + 1) / 2;
+    p.nblk_pad = (p.nblk + 31) / 32 * 32;
+    const size_t smem = (size_t)p.wmax * p.sstride * sizeof(float);
+    const bool staged = smem <= (size_t)kSigSmemMax;
+    const int items = n_windows * p.nblk_pad;
+    const dim3 grid((unsigned)n_steps, (unsigned)((items + kSigThreads - 1) / kSigThreads));
+    cudaError_t e;
+    if (staged) {
+        if (smem > 48 * 1024) {
+            // the attribute once per device: setting it on every call stalls the host
+            static std::atomic<uint64_t> attr_done{0};
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+            const uint64_t bit = (uint64_t)1 << (dev & 63);
+            if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+                if (cudaFuncSetAttribute(signature_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSigSmemMax) != cudaSuccess)
+                    return CONV2D_ERR_CUDA;
+                attr_done.fetch_or(bit, std::memory_order_release);
+            }
+        }
+        e = launch_pdl(signature_kernel<true>, grid, dim3(kSigThreads), smem, st, p);
+    } else {
+        e = launch_pdl(signature_kernel<false>, grid, dim3(kSigThreads), 0, st, p);
+    }
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return CONV2D_ERR_CUDA;
     }

@@ -42,10 +42,14 @@ CASES = [
     (1, 10, [1], 1, 10),
     (2, 5, [1, 2, 5], 5, 1),
     (5, 100, [30, 10, 60], 60, 41),          # unsorted windows
-    (7, 200, [64, 65, 128, 3], 128, 73),     # windows across the 64-sample staging chunks
+    (7, 200, [64, 65, 128, 3], 128, 73),     # odd signal count: a padded signal in the last blocks
     (30, 80, [10, 10, 30], 30, 51),          # a repeated window
-    (40, 90, [17], 20, 70),                  # 1600 pairs: two CTAs per end time
-    (128, 50, [5, 50], 50, 1),               # the largest signal count
+    (40, 90, [17], 20, 70),                  # 210 pair blocks: padded to 224 per window
+    (128, 50, [5, 50], 50, 1),               # the largest signal count: 2080 pair blocks per window
+    (128, 120, [100, 3, 100], 100, 5),       # 52 KB of staged samples (above the default 48 KB)
+    (20, 1400, [1300, 2], 1300, 7),          # too long to stage: read from global memory
+    (128, 260, [7, 200], 200, 9),            # too long to stage at 128 signals
+    (3, 64, [1, 2, 3, 4, 5, 6, 7, 8], 8, 57),   # eight windows, every length up to the history
 ]
 
 
