@@ -113,7 +113,7 @@ const char *const kOverrideEnv[CONV2D_OVR_COUNT] = {
     "CONV2D_DIRECT",   "CONV2D_CC_TILE",   "CONV2D_CC_SPLIT",  "CONV2D_TC_BN",
     "CONV2D_TC_KSUB",  "CONV2D_TC_IM2COL", "CONV2D_TC_WINDOW", "CONV2D_TC_WINVAR",
     "CONV2D_TC_ROTATE", "CONV2D_TF_VAR",   "CONV2D_FP32_TC",   "CONV2D_DECONV_TC",
-    "CONV2D_GRID_CAP", "CONV2D_TEST_WITHHOLD", "CONV2D_TEST_WAIT_KCYCLES", "CONV2D_TC_PAIR"};
+    "CONV2D_GRID_CAP", "CONV2D_TEST_WITHHOLD", "CONV2D_TEST_WAIT_KCYCLES"};
 
 std::atomic<int> g_ovr[CONV2D_OVR_COUNT];
 std::atomic<int> g_ovr_gen{0};
@@ -291,23 +291,8 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
             }
         }
     }
-    // paired-CTA im2col / plain variants (each weight tile shared by two CTAs)
-    const int force_pair = ovr(CONV2D_OVR_TC_PAIR);
-    if (force_win != 1 && force_pair == 1) {
-        Cand pb{0, 0, -1, 1e300};
-        for (int bn : {128, 256}) {
-            if (tc_pair_stages(bn) == 0) continue;
-            if (force_bn > 0 && bn != force_bn) continue;
-            const double b_bytes = (double)bn * 64.0;   // this CTA's half of the weight tile
-            const double mem = kb * stage_ns(2, 16384.0 + b_bytes);
-            const double mma = kb * 2.0 * bn / 1.9;
-            const double cost = (double)rounds_for((s.M + 127) / 128, bn) * std::max(mem, mma);
-            if (cost < pb.cost) pb = Cand{bn, 1, -2, cost};
-        }
-        if (pb.bn) best = pb;   // forced: the best pair variant wins
-    }
     // window variants (stride-1 layers)
-    if (win_ok && force_win != 0 && best.win_variant != -2) {
+    if (win_ok && force_win != 0) {
         for (int id = 0; id < tc_window_variants(); ++id) {
             if (!tc_window_variant_ok(s, id)) continue;
             if (force_wv >= 0 && id != force_wv) continue;
@@ -330,11 +315,9 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     TcTile t;
     t.BN = best.bn;
     t.ksub = best.ks;
-    t.pair = best.win_variant == -2;
     t.window = best.win_variant >= 0;
-    t.win_variant = t.window ? best.win_variant : -1;
-    t.stages = t.window ? tc_window_variant(best.win_variant).stages
-               : t.pair ? tc_pair_stages(best.bn) : tc_stages(best.bn, best.ks);
+    t.win_variant = best.win_variant;
+    t.stages = t.window ? tc_window_variant(best.win_variant).stages : tc_stages(best.bn, best.ks);
     t.tma_store = true;
     t.force_im2col = ovr(CONV2D_OVR_TC_IM2COL) == 1;
     t.rotate = ovr(CONV2D_OVR_TC_ROTATE) != 0;
@@ -346,7 +329,6 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     const int64_t tiles = m_tiles * ((s.K + best.bn - 1) / best.bn);
     p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
     if (ovr(CONV2D_OVR_GRID_CAP) > 0) p->grid = std::min(p->grid, ovr(CONV2D_OVR_GRID_CAP));
-    if (t.pair) p->grid = std::max(2, p->grid / 2 * 2);   // whole clusters of two
     p->sm_count = d.sm_count;
     return CONV2D_OK;
 }
@@ -593,8 +575,8 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
     conv2d_status_t st = get_plan(desc->s, desc->algo, nullptr, &p);
     if (st != CONV2D_OK) return st;
     if (p.algo == Algo::TensorCore)
-        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 ksub=%d stages=%d grid=%d smem=%zu %sa=%s%s",
-                      p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes, p.tc.pair ? "pair " : "",
+        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 ksub=%d stages=%d grid=%d smem=%zu a=%s%s",
+                      p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes,
                       p.tc.window && tc_window_variant(p.tc.win_variant).resident ? "resident-w " : "",
                       p.tc.window ? "window"
                       : (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&

@@ -43,7 +43,6 @@ struct TcTile {
     bool window = false;         // stride-1 layers: one padded input window per channel block
     int win_variant = -1;        // index into the window-mode variant table
     bool rotate = true;          // CTA-dependent start of the k-loop
-    bool pair = false;           // clusters of two CTAs sharing each weight tile by multicast
 };
 
 // Variants of the fp32 split-precision (3xTF32) tensor-core kernel.
@@ -90,7 +89,6 @@ bool tc_shape_ok(const Shape &s, const Tensors *t);
 size_t tc_smem_bytes(const TcTile &t);
 int tc_stages(int bn, int ksub);   // 0 if the (BN, KSUB) variant does not exist
 int tc_num_variants();             // compiled (BN, KSUB) variants of the plain / im2col kernel
-int tc_pair_stages(int bn);        // stages of the paired-CTA variant of width bn, 0 if none
 bool tc_window_ok(const Shape &s);
 size_t tc_window_smem_bytes(const TcTile &t);
 struct TcWinVariant {

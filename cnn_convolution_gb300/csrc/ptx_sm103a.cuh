@@ -93,18 +93,6 @@ __device__ __forceinline__ void tma_load_tile_3d(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// 3-D tile load delivered to every CTA of the cluster in cta_mask, at the same
-// shared-memory offset, each completing bytes on its own mbarrier at `bar`'s
-// offset.
-__device__ __forceinline__ void tma_load_tile_3d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                    int c0, int c1, int c2, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_load_tile_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                                  int c0, int c1, int c2, int c3) {
     asm volatile(
@@ -227,26 +215,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
-}
-
-// Arrive on the mbarrier at `bar`'s offset in every CTA of cta_mask once all
-// tcgen05 operations issued so far by this thread complete.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// Rank of this CTA in its cluster, and a barrier over every thread of the cluster.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // 32 consecutive fp32 accumulator columns of this thread's lane.

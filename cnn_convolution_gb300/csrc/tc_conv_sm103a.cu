@@ -165,8 +165,6 @@ struct TcParams {
     // test hook (plain kernel): CTA 0 never issues the loads of its first
     // stage, so its MMA warp's wait on that stage runs out
     int withhold;
-    // CTA pairs: work units of two vertically adjacent M tiles (same N tile)
-    int pair_units;
 };
 
 // Shared-memory layout: STAGES stages, each holding KSUB k-blocks (the KSUB A
@@ -195,21 +193,10 @@ struct TcSmem {
 // A_TILE: the layer is a 1x1 / stride 1 / no padding convolution, so the A
 // operand is x itself viewed as the [N*H*W, C] matrix and is fetched with a
 // plain 2-D tiled map instead of an im2col one.
-//
-// PAIR: CTAs run in clusters of two that work on vertically adjacent M tiles
-// of the same output-channel tile, in lockstep.  Each CTA loads its own A
-// tile and one half of the stage's weight tile, multicast to both CTAs (the
-// halves land at the same offset in each), so each SM pulls 16 + BN*64 bytes
-// instead of 16 + BN*128 per k-block from L2.  A stage is free again only
-// when both CTAs' MMAs are done with it: each MMA warp's commit arrives on
-// the stage's empty barrier in both CTAs (count 2).  Cluster barriers after
-// the barrier set-up and before exit keep either CTA from touching the
-// other's shared memory when it is not running.
-template <typename T, int BN, int KSUB, int STAGES, bool A_TILE, bool PAIR>
+template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmY, const TcParams p) {
-    static_assert(!PAIR || KSUB == 1, "paired CTAs multicast one weight box per stage");
     using L = TcSmem<BN, KSUB, STAGES>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
@@ -242,7 +229,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), PAIR ? 2 : 1);   // paired: both CTAs' MMAs release a stage
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(accf_bar(a), 1);
@@ -263,19 +250,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the partner's barriers exist before any multicast load or commit reaches them
-    if (PAIR) cluster_sync_all();
     const uint32_t tmem_base = *tmem_holder;
     pdl_launch_dependents();
     pdl_wait();                                // the previous kernel's writes are visible
-
-    // Work units: one tile each, or (PAIR) two M tiles of one N tile, rank r
-    // of the cluster taking M tile 2 * (u / n_tiles_n) + r.
-    const int rank = PAIR ? (int)cluster_ctarank() : 0;
-    const int unit0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-    const int ustep = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
-    const int n_units = PAIR ? p.pair_units : p.total_tiles;
-    auto unit_tm = [&](int u) { return PAIR ? 2 * (u / p.n_tiles_n) + rank : u / p.n_tiles_n; };
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- TMA producer
@@ -292,9 +269,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int dil = p.dil;
         // test hook: CTA 0 leaves its first stage empty (nothing armed, nothing in flight)
         const bool held0 = p.withhold != 0 && blockIdx.x == 0;
-        for (int u = unit0; u < n_units && ok; u += ustep) {
-            const int tm = unit_tm(u);
-            const int tn = u % p.n_tiles_n;
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
+            const int tm = tile / p.n_tiles_n;
+            const int tn = tile - tm * p.n_tiles_n;
             const int64_t m0 = (int64_t)tm * kBM;
             const int n_img = (int)(m0 / p.PQ);
             const int pq = (int)(m0 - (int64_t)n_img * p.PQ);
@@ -307,13 +284,13 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // all hammering the same L2 lines.
             const int per_o = (p.n_inner + KSUB - 1) / KSUB;
             const int n_st = p.n_outer * per_o;
-            const int rot = p.rotate ? (int)((unsigned)unit0 % (unsigned)n_st) : 0;
+            const int rot = p.rotate ? (int)(blockIdx.x % (unsigned)n_st) : 0;
             if (A_TILE) {
                 // 1x1 layers read x once: warm L2 with the A rows of this CTA's
                 // next tile while this one streams (its boxes then hit L2)
-                const int uf = u + ustep;
-                if (uf < n_units) {
-                    const int mf = unit_tm(uf) * kBM;
+                const int tf = tile + (int)gridDim.x;
+                if (tf < p.total_tiles) {
+                    const int mf = (tf / p.n_tiles_n) * kBM;
                     if (p.chunked)
                         for (int i0 = 0; i0 < p.n_inner; i0 += KSUB) tma_prefetch_tile_3d(&tmA, 0, mf, i0);
                     else
@@ -346,11 +323,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             if (++s == p.S) { s = 0; ++r; }
                         }
                     }
-                    if (PAIR)   // this CTA's half of the weight tile, to both CTAs
-                        tma_load_tile_3d_mc(b_tile(stage, 0) + (uint32_t)(rank * (BN / 2) * 128), &tmB, fb, cx,
-                                            k0 + rank * (BN / 2), i0, (uint16_t)0x3);
-                    else
-                        tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
+                    tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
                 }
                 ++n_issued;
                 TC_TRACE(0, 1);
@@ -380,14 +353,14 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);   // 16-byte units
         constexpr uint64_t kADesc = (uint64_t)(kATileBytes >> 4);
         constexpr uint64_t kBDesc = (uint64_t)(L::kBTileBytes >> 4);
-        for (int u = unit0; u < n_units && ok; u += ustep) {
+        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
             TC_TRACE(1, 4);
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             const int per_o = (p.n_inner + KSUB - 1) / KSUB;
             const int n_st = p.n_outer * per_o;
-            const int rot = p.rotate ? (int)((unsigned)unit0 % (unsigned)n_st) : 0;
+            const int rot = p.rotate ? (int)(blockIdx.x % (unsigned)n_st) : 0;
             for (int j = 0; j < n_st; ++j) {
                 int sidx = rot + j;
                 if (sidx >= n_st) sidx -= n_st;
@@ -407,10 +380,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
                 any = true;
-                if (PAIR)
-                    mma_commit_mc(empty_bar(stage), (uint16_t)0x3);   // the stage holds the partner's half too
-                else
-                    mma_commit(empty_bar(stage));
+                mma_commit(empty_bar(stage));
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
@@ -447,7 +417,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t chunk = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = unit0; u < n_units; u += ustep) {
+        for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
             // One lane per warp waits, the whole warp follows (tcgen05.ld needs
             // a converged warp); then the four warps decide together, so that
             // if one warp's wait gave up they all leave the loop.
@@ -457,10 +427,9 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!epilogue_bar_all(ok != 0)) break;
             if (row == 0) TC_TRACE(2, 5);
             tc_fence_after();
-            const int tm = unit_tm(u);
-            const int tn = u % p.n_tiles_n;
+            const int tm = tile / p.n_tiles_n;
+            const int tn = tile - tm * p.n_tiles_n;
             const int m_warp = tm * kBM + quarter * 32;
-            const bool rows_in = (int64_t)m_warp < p.M;   // a paired CTA's second tile may lie past M
             const int k0 = tn * BN;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
@@ -499,7 +468,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                  o[4 * g + 2], o[4 * g + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && rows_in) {
+                if (lane == 0) {
                     tma_store_2d(&tmY, buf, kc, m_warp);
                     bulk_commit_group();
                 }
@@ -521,9 +490,6 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
-    // neither CTA of a pair leaves while its partner may still multicast into
-    // it or arrive on its barriers
-    if (PAIR) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ window (im2win) mode
@@ -1083,48 +1049,17 @@ void set_wait_hooks(TcParams *p, bool plain_kernel) {
     p->withhold = plain_kernel && ovr(CONV2D_OVR_TEST_WITHHOLD) == 1 ? 1 : 0;
 }
 
-// Largest number of 2-CTA clusters of a paired kernel resident at once on
-// this device (queried once per device and instantiation): a persistent
-// paired launch must not exceed it, or the extra clusters would run after
-// the others instead of beside them.
-int max_pair_clusters(const void *kern, size_t smem, std::atomic<uint64_t> &done, std::atomic<int> *cache) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    const uint64_t bit = (uint64_t)1 << dev;
-    if (done.load(std::memory_order_acquire) & bit) return cache[dev].load(std::memory_order_relaxed);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        n = 0;
-    }
-    cache[dev].store(n, std::memory_order_relaxed);
-    done.fetch_or(bit, std::memory_order_release);
-    return n;
-}
-
-template <typename T, int BN, int KSUB, int STAGES, bool A_TILE, bool PAIR>
+template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
 conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
     using L = TcSmem<BN, KSUB, STAGES>;
     const TcMaps *maps = nullptr;
-    // paired CTAs load half of each weight box: its map's box is BN / 2 rows
-    conv2d_status_t mst = cached_maps(s, PAIR ? BN / 2 : BN, KSUB, A_TILE ? 1 : 0, t, &maps);
+    conv2d_status_t mst = cached_maps(s, BN, KSUB, A_TILE ? 1 : 0, t, &maps);
     if (mst != CONV2D_OK) return mst;
     TcParams p;
     p.bias = t.bias;
     p.y = t.y;
     p.status = status_word_ptr();
-    set_wait_hooks(&p, !PAIR);
+    set_wait_hooks(&p, true);
     p.M = s.M;
     p.K = s.K;
     p.PQ = s.P * s.Q;
@@ -1140,40 +1075,16 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.n_inner = p.chunked ? p.CB : s.R * s.S;
     p.rotate = pl.tc.rotate ? 1 : 0;
     p.n_tiles_n = (s.K + BN - 1) / BN;
-    const int64_t m_tiles = (s.M + kBM - 1) / kBM;
-    const int64_t tiles = m_tiles * (int64_t)p.n_tiles_n;
+    const int64_t tiles = ((s.M + kBM - 1) / kBM) * (int64_t)p.n_tiles_n;
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     p.total_tiles = (int)tiles;
-    p.pair_units = (int)(((m_tiles + 1) / 2) * p.n_tiles_n);
-    auto kern = tc_conv_kernel<T, BN, KSUB, STAGES, A_TILE, PAIR>;
+    auto kern = tc_conv_kernel<T, BN, KSUB, STAGES, A_TILE>;
     static std::atomic<uint64_t> attr_done{0};   // this instantiation's per-device flags
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
         return CONV2D_ERR_CUDA;
-    int grid = pl.grid > 0 ? pl.grid : 1;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    int n_attr = 1;
-    if (PAIR) {
-        static std::atomic<uint64_t> occ_done{0};
-        static std::atomic<int> occ[64];
-        const int clusters = max_pair_clusters(reinterpret_cast<const void *>(kern), L::kBytes, occ_done, occ);
-        if (clusters < 1) return CONV2D_ERR_UNSUPPORTED;
-        grid = 2 * std::max(1, std::min(std::min(grid / 2, clusters), p.pair_units));
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        n_attr = 2;
-    }
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = L::kBytes;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = n_attr;
-    if (cudaLaunchKernelEx(&cfg, kern, maps->a, maps->b, maps->y, p) != cudaSuccess) {
+    const int grid = pl.grid > 0 ? pl.grid : 1;
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, maps->y, p) !=
+        cudaSuccess) {
         cudaGetLastError();
         return CONV2D_ERR_CUDA;
     }
@@ -1235,12 +1146,6 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     X(256, 1, 4)              \
     X(256, 2, 2)
 
-// Paired-CTA variants (KSUB = 1): (BN, STAGES).  Each CTA's stage is one
-// A tile and a full weight tile, half of it loaded by the partner.
-#define CONV2D_TC_PAIR_VARIANTS(X) \
-    X(128, 6)                      \
-    X(256, 4)
-
 // Window-mode variants: (BN, KSUB, STAGES, window slot KB, window slots,
 // resident weights, resident KB).  Id = position in this list.
 #define CONV2D_TC_WIN_VARIANTS(X)       \
@@ -1265,15 +1170,8 @@ conv2d_status_t dispatch_window(const Shape &s, const Plan &pl, const Tensors &t
 
 template <typename T, bool A_TILE>
 conv2d_status_t dispatch_bn(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
-    if (pl.tc.pair) {
-#define CONV2D_TC_PCASE(vbn, vst) \
-    if (pl.tc.BN == vbn) return launch_tc<T, vbn, 1, vst, A_TILE, true>(s, pl, t, st);
-        CONV2D_TC_PAIR_VARIANTS(CONV2D_TC_PCASE)
-#undef CONV2D_TC_PCASE
-        return CONV2D_ERR_INTERNAL;
-    }
 #define CONV2D_TC_CASE(vbn, vks, vst) \
-    if (pl.tc.BN == vbn && pl.tc.ksub == vks) return launch_tc<T, vbn, vks, vst, A_TILE, false>(s, pl, t, st);
+    if (pl.tc.BN == vbn && pl.tc.ksub == vks) return launch_tc<T, vbn, vks, vst, A_TILE>(s, pl, t, st);
     CONV2D_TC_VARIANTS(CONV2D_TC_CASE)
 #undef CONV2D_TC_CASE
     return CONV2D_ERR_INTERNAL;
@@ -1306,13 +1204,6 @@ bool tc_shape_ok(const Shape &s, const Tensors *t) {
 }
 
 size_t tc_smem_bytes(const TcTile &t) {
-    if (t.pair) {
-#define CONV2D_TC_PSMEM(vbn, vst) \
-    if (t.BN == vbn) return TcSmem<vbn, 1, vst>::kBytes;
-        CONV2D_TC_PAIR_VARIANTS(CONV2D_TC_PSMEM)
-#undef CONV2D_TC_PSMEM
-        return (size_t)1 << 30;
-    }
 #define CONV2D_TC_SMEM(vbn, vks, vst) \
     if (t.BN == vbn && t.ksub == vks) return TcSmem<vbn, vks, vst>::kBytes;
     CONV2D_TC_VARIANTS(CONV2D_TC_SMEM)
@@ -1378,14 +1269,6 @@ int tc_num_variants() {
     CONV2D_TC_VARIANTS(CONV2D_TC_COUNT)
 #undef CONV2D_TC_COUNT
     return n;
-}
-
-int tc_pair_stages(int bn) {
-#define CONV2D_TC_PST(vbn, vst) \
-    if (bn == vbn) return vst;
-    CONV2D_TC_PAIR_VARIANTS(CONV2D_TC_PST)
-#undef CONV2D_TC_PST
-    return 0;
 }
 
 int tc_stages(int bn, int ksub) {

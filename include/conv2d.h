@@ -256,8 +256,6 @@ typedef enum {
     CONV2D_OVR_TEST_WAIT_KCYCLES, /* [CONV2D_TEST_WAIT_KCYCLES] f16/bf16 tensor-core kernels: a bounded
                                      wait gives up after this many thousand SM cycles (default
                                      4,000,000, about 2 s) */
-    CONV2D_OVR_TC_PAIR,           /* [CONV2D_TC_PAIR] f16/bf16 im2col / plain kernel: 1 clusters of two
-                                     CTAs that share each weight tile (TMA multicast), 0 never */
     CONV2D_OVR_COUNT
 } conv2d_override_t;
 

@@ -170,7 +170,7 @@ def test_overrides_set_get_and_validation(lib):
     assert lib.conv2d_set_override(0, -2) == 1            # below -1
     assert lib.conv2d_get_override(99, ctypes.byref(v)) == 1
     assert lib.conv2d_get_override(0, None) == 1
-    assert len(conv2d.OVERRIDES) == 16                    # CONV2D_OVR_COUNT in the header
+    assert len(conv2d.OVERRIDES) == 15                    # CONV2D_OVR_COUNT in the header
     text = open(HEADER).read()
     body = text[text.index("typedef enum {\n    CONV2D_OVR_DIRECT"):text.index("CONV2D_OVR_COUNT")]
     names = re.findall(r"CONV2D_OVR_([A-Z0-9_]+)", body)

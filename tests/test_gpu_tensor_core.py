@@ -120,9 +120,9 @@ def test_full_grid_several_rounds_full_output(mode, dtype):
     assert err <= TOL[dtype], f"{d.plan()}: err={err}"
 
 
-PAIR_SHAPES = [
+IM2COL_SHAPES = [
     # N, C, H, W, K, R, S, stride, pad, dil, bias
-    (3, 64, 9, 7, 128, 3, 3, 2, 1, 1, True),       # 1 M tile: the second CTA's tile lies past M
+    (3, 64, 9, 7, 128, 3, 3, 2, 1, 1, True),       # one M tile
     (5, 72, 13, 11, 136, 3, 3, 1, 1, 1, False),    # odd number of M tiles, ragged C and K
     (4, 128, 14, 14, 256, 3, 3, 2, 1, 1, True),    # 2 N tiles of 128
     (6, 64, 20, 20, 96, 3, 3, 1, 1, 1, True),      # K < BN
@@ -135,30 +135,19 @@ PAIR_SHAPES = [
 @pytest.mark.parametrize("grid_cap", [None, 4])
 @pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_paired_ctas(dtype, bn, grid_cap):
-    """Clusters of two CTAs that share each weight tile by TMA multicast and
-    release a stage only when both MMAs are done with it; with a capped grid
-    each cluster runs many work units."""
-    with conv2d.overrides(tc_pair=1, tc_bn=bn, tc_window=0, grid_cap=grid_cap):
-        for i, (N, C, H, W, K, R, S, st, pad, dil, bias) in enumerate(PAIR_SHAPES):
-            spec = wl.ConvSpec(f"pair{i}", N, C, H, W, K, R, S, st, pad, dil, dtype=dtype,
+def test_im2col_plain_widths_and_rounds(dtype, bn, grid_cap):
+    """The im2col / plain kernel at each wide tile; with a capped grid every
+    CTA runs many tiles (both accumulators, both store buffers, phase flips)."""
+    with conv2d.overrides(tc_bn=bn, tc_window=0, grid_cap=grid_cap):
+        for i, (N, C, H, W, K, R, S, st, pad, dil, bias) in enumerate(IM2COL_SHAPES):
+            spec = wl.ConvSpec(f"i2c{i}", N, C, H, W, K, R, S, st, pad, dil, dtype=dtype,
                                layout="NHWC", bias=bias)
             x, w, b = wl.random_inputs(spec, seed=900 + i)
             y, d = run_gpu(spec, x, w, b, "tensor_core")
-            assert " pair " in d.plan(), d.plan()
+            assert f"BN={bn} " in d.plan() and "window" not in d.plan(), d.plan()
             err = full_parity(spec, x, w, b, algo="tensor_core")
             assert err <= TOL[dtype], f"{spec} BN={bn} grid_cap={grid_cap}: err={err}"
     assert conv2d.get_device_status() == 0
-
-
-def test_paired_ctas_full_grid_full_output():
-    spec = wl.ConvSpec("pair_full", 96, 64, 28, 28, 128, 3, 3, 1, 1, dtype="bf16", layout="NHWC")
-    x, w, b = wl.random_inputs(spec, seed=78)
-    with conv2d.overrides(tc_pair=1, tc_window=0):
-        y, d = run_gpu(spec, x, w, b, "tensor_core")
-        assert " pair " in d.plan(), d.plan()
-        err = full_parity(spec, x, w, b, algo="tensor_core")
-    assert err <= TOL["bf16"], f"{d.plan()}: err={err}"
 
 
 def test_plan_reports_tensor_core():
