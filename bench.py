@@ -85,7 +85,12 @@ def fp32_alu_peak_tflops(peaks=None):
 # DRAM bytes (read + write) per launch of a layer's kernel, from one ncu
 # capture of the kernel with the plan given here (profiles/ holds the summary
 # and command); a plan that differs gets null.
-DRAM_TRAFFIC = {}
+DRAM_TRAFFIC = {
+    # profiles/tf32x3_conv_kernel_mscred_encoder_l2.md
+    ("mscred_enc_l2_n256_c32_30x30_k64_3x3s2p1",
+     "tensor_core tcgen05 3xtf32 BM=128 BN=64 BK=32 stages=2 producers=512 groups=2 resident-w grid=152 "
+     "smem=218496"): 29629696,
+}
 
 # nominal dense TF32 / BF16 tensor rates of GB300 (1.1 and 2.25 PFLOP/s), used
 # only when the probe measurement is missing
@@ -771,10 +776,9 @@ def tensor_core_layers(device, peaks, flush, iters=50, names=None, keep_check=Fa
         by = layer_bytes(spec, P, Q)
         tf = fl / (med * 1e-3) / 1e12
         gbs = by / (med * 1e-3) / 1e9
-        cpeak = tc_peak if spec.dtype != "f32" else fp32_alu_peak_tflops(peaks)
+        unit, cpeak = ("tensor", tc_peak) if spec.dtype != "f32" else layer_peak(d.plan(), peaks)[:2]
         roof_t = max(fl / (cpeak * 1e12), by / (peaks["hbm_gbs"] * 1e9)) * 1e3
-        bound = ("tensor" if spec.dtype != "f32" else "alu") \
-            if fl / (cpeak * 1e12) >= by / (peaks["hbm_gbs"] * 1e9) else "hbm"
+        bound = unit if fl / (cpeak * 1e12) >= by / (peaks["hbm_gbs"] * 1e9) else "hbm"
         row = {"layer": spec.name, "plan": d.plan(), "ms_median": round(med, 5),
                "ms_mean": round(mean, 5), "ms_min": round(mn, 5), "tflops": round(tf, 2),
                "hbm_gbs": round(gbs, 1), "bound": bound, "roofline_frac": round(roof_t / med, 4),
@@ -913,7 +917,7 @@ def main():
     ap.add_argument("--layer-iters", type=int, default=50,
                     help="timed replays per single-layer measurement (median reported)")
     ap.add_argument("--layer", default=None,
-                    help="time one named layer only (for profiling) and print its line")
+                    help="time one named layer (or signature_matrices) only, for profiling, and print its line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.layer is None:
         ap.error("--warmup must be at least 3")
@@ -922,10 +926,20 @@ def main():
     if args.impl == "reference":
         return reference_main(args)
     if args.layer:
-        from cnn_convolution_gb300 import conv2d
+        from cnn_convolution_gb300 import conv2d, workloads as wl
         conv2d.load()
         peaks, _ = load_peaks()
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        if args.layer == "signature_matrices":
+            # the encoder batch's signature matrices alone (256 end times, 30 signals)
+            n, windows = 256, list(wl.MSCRED_WINDOWS)
+            series = wl.mscred_encoder_series(n).cuda()
+            x_sig = torch.empty((n, len(windows), 30, 30), dtype=torch.float32, device="cuda")
+            tg = TimedGraph(lambda: conv2d.signature_matrices(series, windows, 60, n, out=x_sig), flush)
+            med, mean, mn = time_graph(tg, args.steps)
+            print(json.dumps({"signature_matrices": {"us_median": round(med * 1e3, 3),
+                                                     "us_min": round(mn * 1e3, 3), "iters": args.steps}}))
+            return 0
         res = tensor_core_layers(torch.device("cuda", 0), peaks, flush, iters=args.steps,
                                  names={args.layer})
         print(json.dumps({"layers": res}))

@@ -115,13 +115,16 @@ def test_long_reduction_rebuilds_tap_table():
     assert full_parity(spec, x, w, b) <= TOL["f32"]
 
 
+@pytest.mark.parametrize("C,R,st", [(64, 3, 1), (256, 3, 2), (128, 7, 1)])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_all_positive_inputs(dtype):
-    """Every product has the same sign: |y| = den, the hardest case for the bound."""
-    spec = wl.ConvSpec("positive", 4, 64, 14, 14, 64, 3, 3, 1, 1, dtype=dtype, layout="NHWC")
+def test_all_positive_inputs(dtype, C, R, st):
+    """Every product has the same sign: |y| = den, the hardest case for the
+    bound (reductions of 576, 2304 and 6272 elements)."""
+    spec = wl.ConvSpec("positive", 4, C, 14, 14, 64, R, R, st, R // 2, dtype=dtype, layout="NHWC")
     x, w, b = wl.random_inputs(spec, seed=9, dist="positive")
     for algo in ALGOS_FOR[(dtype, "NHWC")]:
         err = full_parity(spec, x, w, b, algo)
+        print(f"all-positive {dtype} C*R*S={C * R * R} stride={st} {algo}: err={err:.3e}")
         assert err <= TOL[dtype], f"{algo}: err={err}"
 
 
