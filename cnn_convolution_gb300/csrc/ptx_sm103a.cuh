@@ -31,14 +31,22 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// A thread whose poll finds the phase incomplete is suspended until the phase
+// completes or this many nanoseconds pass.  Longer than the default limit:
+// waiting warps then poll (and take issue slots) less often; measured on
+// GB300 it shortened the 3xTF32 kernel on MSCRED encoder layer 2 from 34.5 to
+// 32.8 us and the bf16 7x7 layer from 89.7 to 88.1 us, and changed nothing
+// else (1 ms measured the same as 20 us).
+constexpr int kMbarSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred P;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, P;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kMbarSuspendNs)
         : "memory");
     return ok != 0;
 }
