@@ -979,7 +979,8 @@ def main():
     ap.add_argument("--layer-iters", type=int, default=50,
                     help="timed replays per single-layer measurement (median reported)")
     ap.add_argument("--layer", default=None,
-                    help="time one named layer (or signature_matrices) only, for profiling, and print its line")
+                    help="time one named layer (or signature_matrices, or mscred_encoder_step) only, for profiling, "
+                         "and print its line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.layer is None:
         ap.error("--warmup must be at least 3")
@@ -992,6 +993,23 @@ def main():
         conv2d.load()
         peaks, _ = load_peaks()
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        if args.layer == "mscred_encoder_step":
+            # the 4-layer encoder step alone, eager, L2 flushed before each step
+            specs, x_host, descs, ws, bs, outs, flops = encoder_setup(torch.device("cuda", 0))
+            x_dev = x_host.cuda()
+            ts = []
+            for _ in range(args.steps):
+                flush.zero_()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                run_encoder(descs, x_dev, ws, bs, outs)
+                e1.record()
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            print(json.dumps({"mscred_encoder_step": {"us_mean": round(statistics.mean(ts) * 1e3, 3),
+                                                      "plans": [d.plan() for d in descs], "steps": args.steps}}))
+            return 0
         if args.layer == "signature_matrices":
             # the encoder batch's signature matrices alone (256 end times, 30 signals)
             n, windows = 256, list(wl.MSCRED_WINDOWS)
