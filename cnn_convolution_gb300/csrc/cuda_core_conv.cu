@@ -213,11 +213,14 @@ cc_conv_kernel(const CcParams p) {
         }
     };
 
-    float acc[TM][TN];
+    // column pairs (2jj, 2jj + 1) of row i, packed for fma.rn.f32x2 (two fp32
+    // FMAs, each rounded as fmaf, in one issue slot)
+    static_assert(TN % 2 == 0, "packed accumulator pairs");
+    uint64_t acc2[TM][TN / 2];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+        for (int jj = 0; jj < TN / 2; ++jj) acc2[i][jj] = 0ull;
 
     const int tx = tid % (BN / TN);
     const int ty = tid / (BN / TN);
@@ -251,14 +254,24 @@ cc_conv_kernel(const CcParams p) {
                 const float4 t = *reinterpret_cast<const float4 *>(bs + kk * BS + v * (BN / TNV) + tx * 4);
                 b[4 * v] = t.x; b[4 * v + 1] = t.y; b[4 * v + 2] = t.z; b[4 * v + 3] = t.w;
             }
+            uint64_t b2[TN / 2];
 #pragma unroll
-            for (int i = 0; i < TM; ++i)
+            for (int jj = 0; jj < TN / 2; ++jj) b2[jj] = sm103a::pack_f32x2(b[2 * jj], b[2 * jj + 1]);
 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            for (int i = 0; i < TM; ++i) {
+                const uint64_t a2 = sm103a::pack_f32x2(a[i], a[i]);
+#pragma unroll
+                for (int jj = 0; jj < TN / 2; ++jj) acc2[i][jj] = sm103a::ffma2(a2, b2[jj], acc2[i][jj]);
+            }
         }
         if (kt + 1 < kt_end) store_tile(cur ^ 1);
         __syncthreads();
     }
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int jj = 0; jj < TN / 2; ++jj) sm103a::unpack_f32x2(acc2[i][jj], acc[i][2 * jj], acc[i][2 * jj + 1]);
 
     // Epilogue: stage the tile in shared memory, then write coalesced rows.
     // The tile's bias values go to shared memory first: a global load placed

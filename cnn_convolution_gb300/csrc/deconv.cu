@@ -296,11 +296,13 @@ __global__ void __launch_bounds__(kDvThreads, 3) deconv_s1_kernel(const DvParams
         sm103a::cp_async_commit();
     };
 
-    float acc[kDvS1Px][CB];
+    // channel pairs (2i, 2i + 1) of pixel j, packed for fma.rn.f32x2 (two
+    // fp32 FMAs, each rounded as fmaf, per instruction)
+    uint64_t acc2[kDvS1Px][CB / 2];
 #pragma unroll
     for (int j = 0; j < kDvS1Px; ++j)
 #pragma unroll
-        for (int c = 0; c < CB; ++c) acc[j][c] = 0.f;
+        for (int i = 0; i < CB / 2; ++i) acc2[j][i] = 0ull;
 
     stage(0, 0);
     int bf = 0;
@@ -322,24 +324,25 @@ __global__ void __launch_bounds__(kDvThreads, 3) deconv_s1_kernel(const DvParams
                 const int ih = h + p.pad - r;
                 const bool rv = active && (unsigned)ih < (unsigned)p.P;
                 const float *xr = xs + (kk * p.P + (rv ? ih : 0)) * p.Q;
-                float xv[kDvS1Px + ST - 1];
+                uint64_t xv2[kDvS1Px + ST - 1];   // each input value twice
 #pragma unroll
                 for (int m = 0; m < kDvS1Px + ST - 1; ++m) {
                     const int col = base + m;
-                    xv[m] = (rv && (unsigned)col < (unsigned)p.Q) ? xr[col] : 0.f;
+                    const float v = (rv && (unsigned)col < (unsigned)p.Q) ? xr[col] : 0.f;
+                    xv2[m] = sm103a::pack_f32x2(v, v);
                 }
 #pragma unroll
                 for (int s = 0; s < ST; ++s) {
 #pragma unroll
                     for (int q = 0; q < CB / 4; ++q) {
                         const float4 wv = ws4[(kk * RT * ST + r * ST + s) * (CB / 4) + q];
+                        const uint64_t w01 = sm103a::pack_f32x2(wv.x, wv.y);
+                        const uint64_t w23 = sm103a::pack_f32x2(wv.z, wv.w);
 #pragma unroll
                         for (int j = 0; j < kDvS1Px; ++j) {
-                            const float a = xv[ST - 1 - s + j];
-                            acc[j][4 * q] = fmaf(a, wv.x, acc[j][4 * q]);
-                            acc[j][4 * q + 1] = fmaf(a, wv.y, acc[j][4 * q + 1]);
-                            acc[j][4 * q + 2] = fmaf(a, wv.z, acc[j][4 * q + 2]);
-                            acc[j][4 * q + 3] = fmaf(a, wv.w, acc[j][4 * q + 3]);
+                            const uint64_t a2 = xv2[ST - 1 - s + j];
+                            acc2[j][2 * q] = sm103a::ffma2(a2, w01, acc2[j][2 * q]);
+                            acc2[j][2 * q + 1] = sm103a::ffma2(a2, w23, acc2[j][2 * q + 1]);
                         }
                     }
                 }
@@ -347,6 +350,11 @@ __global__ void __launch_bounds__(kDvThreads, 3) deconv_s1_kernel(const DvParams
         }
     }
     if (!active) return;
+    float acc[kDvS1Px][CB];
+#pragma unroll
+    for (int j = 0; j < kDvS1Px; ++j)
+#pragma unroll
+        for (int i = 0; i < CB / 2; ++i) sm103a::unpack_f32x2(acc2[j][i], acc[j][2 * i], acc[j][2 * i + 1]);
     float bv[CB];                               // all bias loads before the first store
 #pragma unroll
     for (int c = 0; c < CB; ++c) {

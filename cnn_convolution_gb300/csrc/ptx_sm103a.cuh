@@ -302,6 +302,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 // register is zeroed and then conditionally loaded inside one asm statement,
 // so nothing consumes the loaded value before it is used: a C++ `p ? ld : 0`
 // becomes a select right after the load and stalls on every load in turn.
+// Packed fp32 pairs: one fma.rn.f32x2 is two independent fp32 FMAs, each
+// rounded once exactly as fmaf, in one issue slot (the FMA rate is the same
+// as scalar FFMAs; the instruction count per FMA halves).
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
 __device__ __forceinline__ float ldg_or_zero(const float *ptr, bool pred) {
     float v;
     asm("{\n\t.reg .pred p;\n\t"
