@@ -704,14 +704,21 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
             // none of them follows a store of this tile.  (The tile's
             // coordinates are computed again after the main loop, so that
             // only the sums stay live across it.)
-            float a[kCpt];
+            // column pairs (2i, 2i + 1), added as add.rn.f32x2 (two fp32 adds,
+            // each rounded as a scalar add, per instruction)
+            uint64_t a2[kCpt / 2];
             const int kb0 = (tile % p.n_tiles_n) * BN + col0;
 #pragma unroll
-            for (int j = 0; j < kCpt; ++j) {
-                const int k = kb0 + j;
-                const int bk = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
-                const bool bin = p.bias != nullptr && k < p.K;
-                a[j] = ldg_or_zero(bin ? p.bias + bk : p.x, bin);
+            for (int j = 0; j < kCpt; j += 2) {
+                float bv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = kb0 + j + e;
+                    const int bk = LSTM ? (k & 3) * p.lstm_ch + (k >> 2) : k;
+                    const bool bin = p.bias != nullptr && k < p.K;
+                    bv[e] = ldg_or_zero(bin ? p.bias + bk : p.x, bin);
+                }
+                a2[j / 2] = pack_f32x2(bv[0], bv[1]);
             }
             for (int ks = 0; ks < p.KT; ++ks) {
                 int okw = 1;
@@ -725,7 +732,8 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                     uint32_t v[16];
                     tmem_ld_16cols(t_lane + (uint32_t)(2 * BN + slot * BN + col0 + c), v);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) a[c + j] += __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; j += 2)
+                        a2[(c + j) / 2] = fadd2(a2[(c + j) / 2], ((uint64_t)v[j + 1] << 32) | v[j]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -745,8 +753,12 @@ __global__ void __launch_bounds__(tf_threads<BN, NPROD>(), 1) tf32x3_conv_kernel
                 uint32_t v[16];
                 tmem_ld_16cols(t_lane + (uint32_t)(acc * BN + col0 + c), v);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a[c + j] += __uint_as_float(v[j]);
+                for (int j = 0; j < 16; j += 2)
+                    a2[(c + j) / 2] = fadd2(a2[(c + j) / 2], ((uint64_t)v[j + 1] << 32) | v[j]);
             }
+            float a[kCpt];
+#pragma unroll
+            for (int j = 0; j < kCpt; j += 2) unpack_f32x2(a2[j / 2], a[j], a[j + 1]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(corre_bar(acc));
