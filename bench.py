@@ -89,7 +89,7 @@ DRAM_TRAFFIC = {
     # profiles/tf32x3_conv_kernel_mscred_encoder_l2.md
     ("mscred_enc_l2_n256_c32_30x30_k64_3x3s2p1",
      "tensor_core tcgen05 3xtf32 BM=128 BN=64 BK=32 stages=2 producers=512 groups=2 resident-w grid=152 "
-     "smem=218496"): 29630720,
+     "smem=218496"): 29629184,
 }
 
 # nominal dense TF32 / BF16 tensor rates of GB300 (1.1 and 2.25 PFLOP/s), used
