@@ -338,8 +338,9 @@ def deconv_forward(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor
 OVERRIDES = {name: i for i, name in enumerate(
     ["direct", "cc_tile", "cc_split", "tc_bn", "tc_ksub", "tc_im2col", "tc_window", "tc_winvar",
      "tc_rotate", "tf_var", "fp32_tc", "deconv_tc", "grid_cap", "test_withhold",
-     "test_wait_kcycles"])}
-FAMILIES = {"cuda_core_tile": 0, "tensor_core": 1, "tensor_core_window": 2, "tf32x3": 3}
+     "test_wait_kcycles", "tc_cta2"])}
+FAMILIES = {"cuda_core_tile": 0, "tensor_core": 1, "tensor_core_window": 2, "tf32x3": 3,
+            "tensor_core_pair": 4}
 
 
 def set_override(name: str, value: Optional[int]):

@@ -113,7 +113,7 @@ const char *const kOverrideEnv[CONV2D_OVR_COUNT] = {
     "CONV2D_DIRECT",   "CONV2D_CC_TILE",   "CONV2D_CC_SPLIT",  "CONV2D_TC_BN",
     "CONV2D_TC_KSUB",  "CONV2D_TC_IM2COL", "CONV2D_TC_WINDOW", "CONV2D_TC_WINVAR",
     "CONV2D_TC_ROTATE", "CONV2D_TF_VAR",   "CONV2D_FP32_TC",   "CONV2D_DECONV_TC",
-    "CONV2D_GRID_CAP", "CONV2D_TEST_WITHHOLD", "CONV2D_TEST_WAIT_KCYCLES"};
+    "CONV2D_GRID_CAP", "CONV2D_TEST_WITHHOLD", "CONV2D_TEST_WAIT_KCYCLES", "CONV2D_TC_CTA2"};
 
 std::atomic<int> g_ovr[CONV2D_OVR_COUNT];
 std::atomic<int> g_ovr_gen{0};
@@ -291,8 +291,38 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
             }
         }
     }
+    // 2-CTA im2col / plain variants (M = 256 over a pair of SMs).  A pair's
+    // stage waits for the slower of its two CTAs' loads: measured per-SM
+    // ingest is about 0.8x a single CTA's, hence the 1.25 on their load time.
+    // Forced on, the best of them wins outright; forced off, none competes.
+    const int force_cta2 = ovr(CONV2D_OVR_TC_CTA2);
+    if (force_win != 1 && force_cta2 != 0) {
+        Cand cb2{0, 0, -1, 1e300};
+        for (int bn : {128, 256}) {
+            for (int ks : {2, 3, 4}) {
+                if (tc_cta2_stages(bn, ks) == 0) continue;
+                if (force_bn > 0 && bn != force_bn) continue;
+                if (force_ks > 0 && ks != force_ks) continue;
+                if (force_cta2 != 1 && wasteful(bn)) continue;
+                const double b_bytes = (double)bn * 64.0;   // this CTA's half of the weight tile
+                double mem;
+                if (plain) {
+                    mem = ((cb + ks - 1) / ks) * stage_ns(2, ks * (16384.0 + b_bytes));
+                } else {
+                    const int a_loads = (int)std::min<int64_t>(ks, rs);
+                    mem = cb * ((rs + ks - 1) / ks) *
+                          stage_ns(a_loads + 1, a_loads * 16384.0 + ks * b_bytes);
+                }
+                mem *= 1.25;
+                const double mma = kb * 2.0 * bn / 1.9;
+                const double cost = (double)rounds_for((s.M + 255) / 256 * 2, bn) * std::max(mem, mma);
+                if (cost < cb2.cost) cb2 = Cand{bn, ks, -2, cost};
+            }
+        }
+        if (cb2.bn && (force_cta2 == 1 || cb2.cost < best.cost)) best = cb2;
+    }
     // window variants (stride-1 layers)
-    if (win_ok && force_win != 0) {
+    if (win_ok && force_win != 0 && force_cta2 != 1) {
         for (int id = 0; id < tc_window_variants(); ++id) {
             if (!tc_window_variant_ok(s, id)) continue;
             if (force_wv >= 0 && id != force_wv) continue;
@@ -315,9 +345,11 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     TcTile t;
     t.BN = best.bn;
     t.ksub = best.ks;
+    t.cta2 = best.win_variant == -2;
     t.window = best.win_variant >= 0;
-    t.win_variant = best.win_variant;
-    t.stages = t.window ? tc_window_variant(best.win_variant).stages : tc_stages(best.bn, best.ks);
+    t.win_variant = t.window ? best.win_variant : -1;
+    t.stages = t.window ? tc_window_variant(best.win_variant).stages
+               : t.cta2 ? tc_cta2_stages(best.bn, best.ks) : tc_stages(best.bn, best.ks);
     t.tma_store = true;
     t.force_im2col = ovr(CONV2D_OVR_TC_IM2COL) == 1;
     t.rotate = ovr(CONV2D_OVR_TC_ROTATE) != 0;
@@ -329,6 +361,7 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
     const int64_t tiles = m_tiles * ((s.K + best.bn - 1) / best.bn);
     p->grid = (int)std::min<int64_t>(tiles, d.sm_count);
     if (ovr(CONV2D_OVR_GRID_CAP) > 0) p->grid = std::min(p->grid, ovr(CONV2D_OVR_GRID_CAP));
+    if (t.cta2) p->grid = std::max(2, p->grid / 2 * 2);   // whole clusters of two
     p->sm_count = d.sm_count;
     return CONV2D_OK;
 }
@@ -575,8 +608,8 @@ conv2d_status_t conv2d_desc_plan(conv2d_desc_t desc, char *buf, size_t len) {
     conv2d_status_t st = get_plan(desc->s, desc->algo, nullptr, &p);
     if (st != CONV2D_OK) return st;
     if (p.algo == Algo::TensorCore)
-        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 ksub=%d stages=%d grid=%d smem=%zu a=%s%s",
-                      p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes,
+        std::snprintf(buf, len, "tensor_core tcgen05 BM=128 BN=%d BK=64 ksub=%d stages=%d grid=%d smem=%zu %sa=%s%s",
+                      p.tc.BN, p.tc.ksub, p.tc.stages, p.grid, p.smem_bytes, p.tc.cta2 ? "cta2 " : "",
                       p.tc.window && tc_window_variant(p.tc.win_variant).resident ? "resident-w " : "",
                       p.tc.window ? "window"
                       : (desc->s.R == 1 && desc->s.S == 1 && desc->s.stride == 1 && desc->s.pad == 0 &&
@@ -821,6 +854,7 @@ conv2d_status_t conv2d_variant_count(conv2d_family_t family, int *count) {
         case CONV2D_FAMILY_TENSOR_CORE: *count = tc_num_variants(); return CONV2D_OK;
         case CONV2D_FAMILY_TENSOR_CORE_WINDOW: *count = tc_window_variants(); return CONV2D_OK;
         case CONV2D_FAMILY_TF32X3: *count = tf_num_variants(); return CONV2D_OK;
+        case CONV2D_FAMILY_TENSOR_CORE_PAIR: *count = tc_cta2_num_variants(); return CONV2D_OK;
     }
     return CONV2D_ERR_INVALID_ARG;
 }

@@ -43,6 +43,7 @@ struct TcTile {
     bool window = false;         // stride-1 layers: one padded input window per channel block
     int win_variant = -1;        // index into the window-mode variant table
     bool rotate = true;          // CTA-dependent start of the k-loop
+    bool cta2 = false;           // clusters of two CTAs issuing 2-CTA (M = 256) MMAs
 };
 
 // Variants of the fp32 split-precision (3xTF32) tensor-core kernel.
@@ -89,6 +90,8 @@ bool tc_shape_ok(const Shape &s, const Tensors *t);
 size_t tc_smem_bytes(const TcTile &t);
 int tc_stages(int bn, int ksub);   // 0 if the (BN, KSUB) variant does not exist
 int tc_num_variants();             // compiled (BN, KSUB) variants of the plain / im2col kernel
+int tc_cta2_stages(int bn, int ksub);
+int tc_cta2_num_variants();   // stages of the 2-CTA variant (BN, KSUB), 0 if none
 bool tc_window_ok(const Shape &s);
 size_t tc_window_smem_bytes(const TcTile &t);
 struct TcWinVariant {

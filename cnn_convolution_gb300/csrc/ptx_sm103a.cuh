@@ -51,6 +51,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, with acquire at cluster scope: for barriers that threads
+// of the partner CTA arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kMbarSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait on phase `parity` of an mbarrier.  Returns false (after setting
 // the abort flag and the status word) if it gave up after `limit` SM cycles,
 // or if another thread of the CTA already gave up.  The SM cycle counter is
@@ -62,6 +76,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     long long t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*abort_flag) return false;
+            const long long now = clock64();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit) {
+                *abort_flag = 1;
+                if (status) atomicOr(status, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+// mbar_wait for barriers the partner CTA arrives on (cluster-scope acquire).
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             unsigned int *status, long long limit = kWaitLimitCycles) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    long long t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_cl(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort_flag) return false;
             const long long now = clock64();
@@ -114,6 +149,37 @@ __device__ __forceinline__ void tma_load_tile_2d(uint32_t dst, const CUtensorMap
                                                  int c0, int c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// The same loads issued by either CTA of a 2-CTA pair (.cta_group::2): the
+// data lands in the issuing CTA's shared memory, the byte count is signalled
+// on `bar`, which may be the partner CTA's mbarrier (a shared::cluster address
+// from mapa).
+__device__ __forceinline__ void tma_load_im2col_4d_cg2(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                       int c, int w, int h, int n, uint16_t off_w,
+                                                       uint16_t off_h) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar), "h"(off_w),
+        "h"(off_h)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_tile_3d_cg2(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                     int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_tile_2d_cg2(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                     int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
@@ -216,6 +282,53 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
+}
+
+// 2-CTA (cta_group::2) forms, for kernels launched as clusters of two CTAs
+// on neighbouring SMs: one warp in each CTA of the pair allocates (the pair
+// gets the same tensor-memory address in both), and one thread of the even
+// CTA issues MMAs of M = 256 that read A's rows 0-127 and the first half of
+// B's N rows from its own shared memory, rows 128-255 and the second half of
+// B from the partner's (same offsets), and write each CTA's 128 rows of D
+// into that CTA's tensor memory.
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// Arrive on the mbarrier at shared::cluster address `bar` (this CTA's or the
+// partner's) once the pair's tcgen05 operations issued so far by this thread
+// complete.
+__device__ __forceinline__ void mma_commit2(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// One arrival on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Arrive on `bar` once all tcgen05 operations issued so far by this thread complete.

@@ -69,12 +69,22 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulate, A and B K-major.
-__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int n) {
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int n, int m = kBM) {
     return (1u << 4)                                   // D format: f32
            | ((bf16 ? 1u : 0u) << 7)                   // A format: f16 / bf16
            | ((bf16 ? 1u : 0u) << 10)                  // B format
            | ((uint32_t)(n >> 3) << 17)                // N / 8
-           | ((uint32_t)(kBM >> 4) << 24);             // M / 16
+           | ((uint32_t)(m >> 4) << 24);               // M / 16 (256: a 2-CTA MMA)
+}
+
+__device__ __forceinline__ void mma_f16_2cta(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // Accumulators in tensor memory: as many BN-column buffers as fit in 512
@@ -165,6 +175,8 @@ struct TcParams {
     // test hook (plain kernel): CTA 0 never issues the loads of its first
     // stage, so its MMA warp's wait on that stage runs out
     int withhold;
+    // 2-CTA kernel: work units of two vertically adjacent M tiles (same N tile)
+    int pair_units;
 };
 
 // Shared-memory layout: STAGES stages, each holding KSUB k-blocks (the KSUB A
@@ -173,9 +185,11 @@ struct TcParams {
 // consumer hand-off.  Measured on GB300, TMA cost is per instruction and per
 // stage rather than per byte, so a stage carries KSUB k-blocks and its B tiles
 // (and, for 1x1 layers, its A tiles) arrive in ONE 3-D box each.
-template <int BN, int KSUB, int STAGES>
+// CTA2: the 2-CTA kernel, whose CTAs each hold half of the weight tile's BN
+// rows and one more barrier per accumulator (the partner's relay).
+template <int BN, int KSUB, int STAGES, bool CTA2 = false>
 struct TcSmem {
-    static constexpr int kBTileBytes = BN * kBK * 2;
+    static constexpr int kBTileBytes = (CTA2 ? BN / 2 : BN) * kBK * 2;
     static constexpr int kStageBytes = KSUB * (kATileBytes + kBTileBytes);
     static constexpr int kAcc = tc_num_acc<BN>();
     // epilogue staging: per epilogue warp two buffers of 32 rows x 32 outputs
@@ -185,21 +199,37 @@ struct TcSmem {
     // the layer's bias as fp32
     static constexpr size_t kBiasOffset = kEpiOffset + 4 * 2 * kEpiBufBytes;
     static constexpr size_t kBarOffset = kBiasOffset + kBiasBytes;
-    // full[S], empty[S], acc_full[A], acc_empty[A], drain[1]; then tmem addr, abort flag
-    static constexpr size_t kBarBytes = (2 * STAGES + 2 * kAcc + 1) * 8;
+    // full[S], empty[S], acc_full[A], acc_empty[A], drain[1] (CTA2: +
+    // partner_acc_empty[A]); then tmem addr, abort flag
+    static constexpr size_t kBarBytes = (2 * STAGES + 2 * kAcc + 1 + (CTA2 ? kAcc : 0)) * 8;
     static constexpr size_t kBytes = kBarOffset + kBarBytes + 16 + 1024;   // +1024 for alignment
 };
 
 // A_TILE: the layer is a 1x1 / stride 1 / no padding convolution, so the A
 // operand is x itself viewed as the [N*H*W, C] matrix and is fetched with a
 // plain 2-D tiled map instead of an im2col one.
-template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
+//
+// CTA2: the kernel runs as clusters of two CTAs on neighbouring SMs that
+// compute vertically adjacent M tiles of the same output-channel tile with
+// 2-CTA MMAs (M = 256).  Each CTA loads its own A tile and its half of the
+// weight tile (BN / 2 rows), so each SM takes in and serves 25 % (BN = 128)
+// to 33 % (BN = 256) fewer bytes per k-block.  The even CTA's MMA thread
+// issues every MMA once both CTAs' stage is full: both CTAs' copies of a
+// stage (.cta_group::2 loads) count their bytes on the even CTA's full
+// barrier, which the even CTA arms with the pair's total; the odd CTA's MMA
+// warp, otherwise idle, relays its accumulator-empty events to the even CTA
+// (a remote mbarrier arrival per tile); the even CTA's commits arrive on both
+// CTAs' stage-empty and accumulator-full barriers.  Both CTAs walk
+// the same sequence of stages.  Cluster barriers after the set-up and before
+// the teardown keep either CTA from touching the other's barriers or
+// tensor memory while it is not running.
+template <typename T, int BN, int KSUB, int STAGES, bool A_TILE, bool CTA2>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmY, const TcParams p) {
-    using L = TcSmem<BN, KSUB, STAGES>;
+    using L = TcSmem<BN, KSUB, STAGES, CTA2>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    constexpr uint32_t kIdesc = make_idesc(kBf16, BN);
+    constexpr uint32_t kIdesc = make_idesc(kBf16, BN, CTA2 ? 256 : 128);
     constexpr int kAcc = L::kAcc;
     constexpr uint32_t kTmemCols = tc_tmem_cols<BN>();
 
@@ -213,6 +243,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
     auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + kAcc + a); };
     const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * kAcc);
+    // CTA2 only: in the even CTA, the odd CTA's relayed accumulator-empty events
+    auto pacce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 * kAcc + 1 + a); };
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + L::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBarOffset + L::kBarBytes + 4);
     auto a_tile = [&](int s, int j) {
@@ -234,6 +266,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(accf_bar(a), 1);
             mbar_init(acce_bar(a), 128);
+            if (CTA2) mbar_init(pacce_bar(a), 1);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -244,15 +277,30 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         prefetch_tensormap(&tmY);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
-        tmem_relinquish();
+        if (CTA2) {
+            tmem_alloc2(smem_u32(tmem_holder), kTmemCols);
+            tmem_relinquish2();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    // the partner's barriers exist before any remote arrival or commit reaches them
+    if (CTA2) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     pdl_launch_dependents();
     pdl_wait();                                // the previous kernel's writes are visible
+
+    // Work units: one tile each, or (CTA2) two M tiles of one N tile, CTA
+    // rank r of the pair taking M tile 2 * (u / n_tiles_n) + r.
+    const uint32_t rank = CTA2 ? cluster_ctarank() : 0u;
+    const int unit0 = CTA2 ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int ustep = CTA2 ? (int)gridDim.x / 2 : (int)gridDim.x;
+    const int n_units = CTA2 ? p.pair_units : p.total_tiles;
+    auto unit_tm = [&](int u) { return CTA2 ? 2 * (u / p.n_tiles_n) + (int)rank : u / p.n_tiles_n; };
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- TMA producer
@@ -267,30 +315,33 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t n_issued = 0;       // stages filled so far
         bool ok = true;
         const int dil = p.dil;
-        // test hook: CTA 0 leaves its first stage empty (nothing armed, nothing in flight)
+        // test hook: CTA 0 leaves its first stage empty (nothing armed, none of
+        // its own copies in flight; in a pair the odd CTA's copies still land
+        // on that barrier, whose phase then never completes)
         const bool held0 = p.withhold != 0 && blockIdx.x == 0;
-        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
-            const int tm = tile / p.n_tiles_n;
-            const int tn = tile - tm * p.n_tiles_n;
+        for (int u = unit0; u < n_units && ok; u += ustep) {
+            const int tm = unit_tm(u);
+            const int tn = u % p.n_tiles_n;
             const int64_t m0 = (int64_t)tm * kBM;
             const int n_img = (int)(m0 / p.PQ);
             const int pq = (int)(m0 - (int64_t)n_img * p.PQ);
             const int p0 = pq / p.Q, q0 = pq - p0 * p.Q;
             const int h0 = p0 * p.stride - p.pad;
             const int w0 = q0 * p.stride - p.pad;
-            const int k0 = tn * BN;
-            // Stages of a tile run in a CTA-dependent rotation, so that CTAs
-            // running at the same time fetch different weight tiles instead of
-            // all hammering the same L2 lines.
+            // this CTA's rows of the weight tile (CTA2: its half)
+            const int k0 = tn * BN + (int)rank * (BN / 2);
+            // Stages of a tile run in a CTA-dependent rotation (the same in
+            // both CTAs of a pair), so that CTAs running at the same time fetch
+            // different weight tiles instead of all hammering the same L2 lines.
             const int per_o = (p.n_inner + KSUB - 1) / KSUB;
             const int n_st = p.n_outer * per_o;
-            const int rot = p.rotate ? (int)(blockIdx.x % (unsigned)n_st) : 0;
+            const int rot = p.rotate ? (int)((unsigned)unit0 % (unsigned)n_st) : 0;
             if (A_TILE) {
                 // 1x1 layers read x once: warm L2 with the A rows of this CTA's
                 // next tile while this one streams (its boxes then hit L2)
-                const int tf = tile + (int)gridDim.x;
-                if (tf < p.total_tiles) {
-                    const int mf = (tf / p.n_tiles_n) * kBM;
+                const int uf = u + ustep;
+                if (uf < n_units && (int64_t)unit_tm(uf) * kBM < p.M) {
+                    const int mf = unit_tm(uf) * kBM;
                     if (p.chunked)
                         for (int i0 = 0; i0 < p.n_inner; i0 += KSUB) tma_prefetch_tile_3d(&tmA, 0, mf, i0);
                     else
@@ -306,31 +357,54 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int cx = p.chunked ? 0 : o * kBK;     // channel offset of this outer block
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
                 TC_TRACE(3, 8);
-                const uint32_t fb = full_bar(stage);
+                // CTA2: both CTAs' copies signal the even CTA's full barrier,
+                // which the even CTA arms with the pair's byte count
+                const uint32_t fb = CTA2 ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
                 const int a_tiles = (A_TILE && p.chunked) ? KSUB : nsub;
                 if (!(held0 && n_issued == 0)) {
-                    mbar_arrive_expect_tx(fb, (uint32_t)(a_tiles * kATileBytes + KSUB * L::kBTileBytes));
+                    const uint32_t bytes = (uint32_t)(a_tiles * kATileBytes + KSUB * L::kBTileBytes);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), CTA2 ? 2u * bytes : bytes);
                     if (A_TILE) {
-                        if (p.chunked)
-                            tma_load_tile_3d(a_tile(stage, 0), &tmA, fb, 0, (int)m0, i0);
-                        else
-                            tma_load_tile_2d(a_tile(stage, 0), &tmA, fb, cx, (int)m0);
+                        if (p.chunked) {
+                            if constexpr (CTA2)
+                                tma_load_tile_3d_cg2(a_tile(stage, 0), &tmA, fb, 0, (int)m0, i0);
+                            else
+                                tma_load_tile_3d(a_tile(stage, 0), &tmA, fb, 0, (int)m0, i0);
+                        } else {
+                            if constexpr (CTA2)
+                                tma_load_tile_2d_cg2(a_tile(stage, 0), &tmA, fb, cx, (int)m0);
+                            else
+                                tma_load_tile_2d(a_tile(stage, 0), &tmA, fb, cx, (int)m0);
+                        }
                     } else {
                         int r = i0 / p.S, s = i0 - r * p.S;
                         for (int jj = 0; jj < nsub; ++jj) {
-                            tma_load_im2col_4d(a_tile(stage, jj), &tmA, fb, cx, w0, h0, n_img,
-                                               (uint16_t)(s * dil), (uint16_t)(r * dil));
+                            if constexpr (CTA2)
+                                tma_load_im2col_4d_cg2(a_tile(stage, jj), &tmA, fb, cx, w0, h0, n_img,
+                                                       (uint16_t)(s * dil), (uint16_t)(r * dil));
+                            else
+                                tma_load_im2col_4d(a_tile(stage, jj), &tmA, fb, cx, w0, h0, n_img,
+                                                   (uint16_t)(s * dil), (uint16_t)(r * dil));
                             if (++s == p.S) { s = 0; ++r; }
                         }
                     }
-                    tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
+                    if constexpr (CTA2)
+                        tma_load_tile_3d_cg2(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
+                    else
+                        tma_load_tile_3d(b_tile(stage, 0), &tmB, fb, cx, k0, i0);
                 }
                 ++n_issued;
                 TC_TRACE(0, 1);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-        if (!ok) {
+        if (!ok && CTA2 && rank == 1) {
+            // This CTA's copies signal the even CTA's barriers: give the ones
+            // in flight time to land before the CTA goes away.
+            const long long t0 = clock64();
+            while (cycles_left(t0, p.wait_limit < (1ll << 20) ? p.wait_limit : (1ll << 20))) {
+            }
+        } else if (!ok) {
             // Let the copies already in flight land before the CTA goes away
             // (one time budget for all stages together).  Stage fill i went to
             // stage i % STAGES with phase (i / STAGES) & 1.
@@ -341,32 +415,57 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
         }
+    } else if (CTA2 && rank == 1 && warp == 1 && lane == 0) {
+        // ---------------------------------------------------------- relay (odd CTA)
+        // The even CTA issues the pair's MMAs; this CTA's MMA thread tells it,
+        // from the second use of each accumulator on, when this CTA's
+        // epilogue has freed it.  (Stage-full events need no relay: this
+        // CTA's copies signal the even CTA's barriers.)
+        const uint32_t leader = 0;
+        int acc = 0, n_tiles_done = 0;
+        uint32_t acc_phase = 0;
+        for (int u = unit0; u < n_units; u += ustep, ++n_tiles_done) {
+            if (n_tiles_done >= kAcc) {
+                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit)) break;
+                mbar_arrive_remote(mapa_shared(pacce_bar(acc), leader));
+            }
+            if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+        }
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------------- MMA issuer
+        // (CTA2: the even CTA's, for both CTAs)
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true, any = false;
+        const uint32_t partner = 1;
         const uint64_t a_desc0 = smem_desc_sw128(a_tile(0, 0));
         const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
         constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);   // 16-byte units
         constexpr uint64_t kADesc = (uint64_t)(kATileBytes >> 4);
         constexpr uint64_t kBDesc = (uint64_t)(L::kBTileBytes >> 4);
-        for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
-            if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
+        for (int u = unit0; u < n_units && ok; u += ustep) {
+            if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit) ||
+                (CTA2 && !mbar_wait_cl(pacce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit))) {
+                ok = false;
+                break;
+            }
             TC_TRACE(1, 4);
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             const int per_o = (p.n_inner + KSUB - 1) / KSUB;
             const int n_st = p.n_outer * per_o;
-            const int rot = p.rotate ? (int)(blockIdx.x % (unsigned)n_st) : 0;
+            const int rot = p.rotate ? (int)((unsigned)unit0 % (unsigned)n_st) : 0;
             for (int j = 0; j < n_st; ++j) {
                 int sidx = rot + j;
                 if (sidx >= n_st) sidx -= n_st;
                 const int o = sidx / per_o;
                 const int nsub = min(KSUB, p.n_inner - (sidx - o * per_o) * KSUB);
-                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
+                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.wait_limit)) {
+                    ok = false;
+                    break;
+                }
                 TC_TRACE(1, 2);
                 tc_fence_after();
                 for (int jj = 0; jj < nsub; ++jj) {
@@ -375,22 +474,40 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
                         // advance 16 elements (32 bytes) along K inside the swizzled rows
-                        mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
-                                (j | jj | k) != 0 ? 1u : 0u);
+                        if (CTA2)
+                            mma_f16_2cta(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
+                                         (j | jj | k) != 0 ? 1u : 0u);
+                        else
+                            mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
+                                    (j | jj | k) != 0 ? 1u : 0u);
                     }
                 }
                 any = true;
-                mma_commit(empty_bar(stage));
+                if (CTA2) {
+                    // the stage is free in both CTAs once these MMAs are done
+                    mma_commit2(empty_bar(stage));
+                    mma_commit2(mapa_shared(empty_bar(stage), partner));
+                } else {
+                    mma_commit(empty_bar(stage));
+                }
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
-            mma_commit(accf_bar(acc));
+            if (CTA2) {
+                mma_commit2(accf_bar(acc));
+                mma_commit2(mapa_shared(accf_bar(acc), partner));
+            } else {
+                mma_commit(accf_bar(acc));
+            }
             TC_TRACE(1, 3);
             if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
         }
         if (any) {
             // Make sure every MMA has retired before tensor memory is released.
-            mma_commit(drain_bar);
+            if (CTA2)
+                mma_commit2(drain_bar);
+            else
+                mma_commit(drain_bar);
             const long long t0 = clock64();
             while (!mbar_try_wait(drain_bar, 0) && cycles_left(t0, p.wait_limit)) {
             }
@@ -417,7 +534,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t chunk = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+        for (int u = unit0; u < n_units; u += ustep) {
             // One lane per warp waits, the whole warp follows (tcgen05.ld needs
             // a converged warp); then the four warps decide together, so that
             // if one warp's wait gave up they all leave the loop.
@@ -427,9 +544,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!epilogue_bar_all(ok != 0)) break;
             if (row == 0) TC_TRACE(2, 5);
             tc_fence_after();
-            const int tm = tile / p.n_tiles_n;
-            const int tn = tile - tm * p.n_tiles_n;
+            const int tm = unit_tm(u);
+            const int tn = u % p.n_tiles_n;
             const int m_warp = tm * kBM + quarter * 32;
+            const bool rows_in = (int64_t)m_warp < p.M;   // CTA2: the odd CTA's tile may lie past M
             const int k0 = tn * BN;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
@@ -468,7 +586,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                  o[4 * g + 2], o[4 * g + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
+                if (lane == 0 && rows_in) {
                     tma_store_2d(&tmY, buf, kc, m_warp);
                     bulk_commit_group();
                 }
@@ -485,10 +603,16 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     tc_fence_before();
     __syncthreads();
+    // CTA2: the even CTA's MMAs (which write this CTA's tensor memory) have
+    // drained and no arrival targets either CTA any more
+    if (CTA2) cluster_sync_all();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (CTA2)
+            tmem_dealloc2(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -1042,18 +1166,50 @@ bool ensure_smem_attr(const void *kern, size_t bytes, std::atomic<uint64_t> &don
     return true;
 }
 
-// Bounded-wait limit and the stall test hook of a launch, from the overrides.
-void set_wait_hooks(TcParams *p, bool plain_kernel) {
+// Bounded-wait limit and the stall test hook of a launch, from the overrides
+// (the hook exists in the im2col / plain kernels, single-CTA and 2-CTA).
+void set_wait_hooks(TcParams *p, bool has_withhold_hook) {
     const int kc = ovr(CONV2D_OVR_TEST_WAIT_KCYCLES);
     p->wait_limit = kc > 0 ? (long long)kc * 1000 : kWaitLimitCycles;
-    p->withhold = plain_kernel && ovr(CONV2D_OVR_TEST_WITHHOLD) == 1 ? 1 : 0;
+    p->withhold = has_withhold_hook && ovr(CONV2D_OVR_TEST_WITHHOLD) == 1 ? 1 : 0;
 }
 
-template <typename T, int BN, int KSUB, int STAGES, bool A_TILE>
+// Largest number of 2-CTA clusters of a kernel resident at once on this
+// device (queried once per device and instantiation): a persistent 2-CTA
+// launch must not exceed it, or the extra clusters would run after the others
+// instead of beside them.
+int max_pair_clusters(const void *kern, size_t smem, std::atomic<uint64_t> &done, std::atomic<int> *cache) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const uint64_t bit = (uint64_t)1 << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cache[dev].load(std::memory_order_relaxed);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cache[dev].store(n, std::memory_order_relaxed);
+    done.fetch_or(bit, std::memory_order_release);
+    return n;
+}
+
+template <typename T, int BN, int KSUB, int STAGES, bool A_TILE, bool CTA2>
 conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
-    using L = TcSmem<BN, KSUB, STAGES>;
+    using L = TcSmem<BN, KSUB, STAGES, CTA2>;
     const TcMaps *maps = nullptr;
-    conv2d_status_t mst = cached_maps(s, BN, KSUB, A_TILE ? 1 : 0, t, &maps);
+    // 2-CTA kernel: each CTA loads half of the weight tile, BN / 2 rows
+    conv2d_status_t mst = cached_maps(s, CTA2 ? BN / 2 : BN, KSUB, A_TILE ? 1 : 0, t, &maps);
     if (mst != CONV2D_OK) return mst;
     TcParams p;
     p.bias = t.bias;
@@ -1075,16 +1231,44 @@ conv2d_status_t launch_tc(const Shape &s, const Plan &pl, const Tensors &t, cuda
     p.n_inner = p.chunked ? p.CB : s.R * s.S;
     p.rotate = pl.tc.rotate ? 1 : 0;
     p.n_tiles_n = (s.K + BN - 1) / BN;
-    const int64_t tiles = ((s.M + kBM - 1) / kBM) * (int64_t)p.n_tiles_n;
+    const int64_t m_tiles = (s.M + kBM - 1) / kBM;
+    const int64_t tiles = m_tiles * (int64_t)p.n_tiles_n;
     if (tiles > INT32_MAX) return CONV2D_ERR_UNSUPPORTED;
     p.total_tiles = (int)tiles;
-    auto kern = tc_conv_kernel<T, BN, KSUB, STAGES, A_TILE>;
+    p.pair_units = (int)(((m_tiles + 1) / 2) * p.n_tiles_n);
+    auto kern = tc_conv_kernel<T, BN, KSUB, STAGES, A_TILE, CTA2>;
     static std::atomic<uint64_t> attr_done{0};   // this instantiation's per-device flags
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), L::kBytes, attr_done))
         return CONV2D_ERR_CUDA;
-    const int grid = pl.grid > 0 ? pl.grid : 1;
-    if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, maps->y, p) !=
-        cudaSuccess) {
+    int grid = pl.grid > 0 ? pl.grid : 1;
+    if (!CTA2) {
+        if (launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, st, maps->a, maps->b, maps->y, p) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return CONV2D_ERR_CUDA;
+        }
+        return CONV2D_OK;
+    }
+    static std::atomic<uint64_t> occ_done{0};
+    static std::atomic<int> occ[64];
+    const int clusters = max_pair_clusters(reinterpret_cast<const void *>(kern), L::kBytes, occ_done, occ);
+    if (clusters < 1) return CONV2D_ERR_UNSUPPORTED;
+    grid = 2 * std::max(1, std::min(std::min(grid / 2, clusters), p.pair_units));
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kBytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, maps->a, maps->b, maps->y, p) != cudaSuccess) {
         cudaGetLastError();
         return CONV2D_ERR_CUDA;
     }
@@ -1146,6 +1330,14 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     X(256, 1, 4)              \
     X(256, 2, 2)
 
+// 2-CTA variants of the im2col / plain kernel: (BN, KSUB, STAGES); a CTA's
+// stage holds KSUB A tiles and KSUB half weight tiles (BN / 2 rows).
+#define CONV2D_TC_CTA2_VARIANTS(X) \
+    X(128, 2, 4)                   \
+    X(128, 3, 2)                   \
+    X(128, 4, 2)                   \
+    X(256, 2, 3)
+
 // Window-mode variants: (BN, KSUB, STAGES, window slot KB, window slots,
 // resident weights, resident KB).  Id = position in this list.
 #define CONV2D_TC_WIN_VARIANTS(X)       \
@@ -1170,8 +1362,15 @@ conv2d_status_t dispatch_window(const Shape &s, const Plan &pl, const Tensors &t
 
 template <typename T, bool A_TILE>
 conv2d_status_t dispatch_bn(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {
+    if (pl.tc.cta2) {
+#define CONV2D_TC_C2CASE(vbn, vks, vst) \
+    if (pl.tc.BN == vbn && pl.tc.ksub == vks) return launch_tc<T, vbn, vks, vst, A_TILE, true>(s, pl, t, st);
+        CONV2D_TC_CTA2_VARIANTS(CONV2D_TC_C2CASE)
+#undef CONV2D_TC_C2CASE
+        return CONV2D_ERR_INTERNAL;
+    }
 #define CONV2D_TC_CASE(vbn, vks, vst) \
-    if (pl.tc.BN == vbn && pl.tc.ksub == vks) return launch_tc<T, vbn, vks, vst, A_TILE>(s, pl, t, st);
+    if (pl.tc.BN == vbn && pl.tc.ksub == vks) return launch_tc<T, vbn, vks, vst, A_TILE, false>(s, pl, t, st);
     CONV2D_TC_VARIANTS(CONV2D_TC_CASE)
 #undef CONV2D_TC_CASE
     return CONV2D_ERR_INTERNAL;
@@ -1204,6 +1403,13 @@ bool tc_shape_ok(const Shape &s, const Tensors *t) {
 }
 
 size_t tc_smem_bytes(const TcTile &t) {
+    if (t.cta2) {
+#define CONV2D_TC_C2SMEM(vbn, vks, vst) \
+    if (t.BN == vbn && t.ksub == vks) return TcSmem<vbn, vks, vst, true>::kBytes;
+        CONV2D_TC_CTA2_VARIANTS(CONV2D_TC_C2SMEM)
+#undef CONV2D_TC_C2SMEM
+        return (size_t)1 << 30;
+    }
 #define CONV2D_TC_SMEM(vbn, vks, vst) \
     if (t.BN == vbn && t.ksub == vks) return TcSmem<vbn, vks, vst>::kBytes;
     CONV2D_TC_VARIANTS(CONV2D_TC_SMEM)
@@ -1271,11 +1477,27 @@ int tc_num_variants() {
     return n;
 }
 
+int tc_cta2_num_variants() {
+    int n = 0;
+#define CONV2D_TC_C2COUNT(vbn, vks, vst) ++n;
+    CONV2D_TC_CTA2_VARIANTS(CONV2D_TC_C2COUNT)
+#undef CONV2D_TC_C2COUNT
+    return n;
+}
+
 int tc_stages(int bn, int ksub) {
 #define CONV2D_TC_ST(vbn, vks, vst) \
     if (bn == vbn && ksub == vks) return vst;
     CONV2D_TC_VARIANTS(CONV2D_TC_ST)
 #undef CONV2D_TC_ST
+    return 0;
+}
+
+int tc_cta2_stages(int bn, int ksub) {
+#define CONV2D_TC_C2ST(vbn, vks, vst) \
+    if (bn == vbn && ksub == vks) return vst;
+    CONV2D_TC_CTA2_VARIANTS(CONV2D_TC_C2ST)
+#undef CONV2D_TC_C2ST
     return 0;
 }
 

@@ -249,13 +249,18 @@ typedef enum {
                                      CTAs (so small layers run several tiles per CTA) */
     CONV2D_OVR_TEST_WITHHOLD,     /* [CONV2D_TEST_WITHHOLD] test hook, 1: in the f16/bf16 im2col /
                                      plain tensor-core kernel, CTA 0 never issues the loads of its
-                                     first pipeline stage, so a bounded wait runs out: that CTA writes
-                                     none of its tiles, the call's device status becomes
+                                     first pipeline stage, so a bounded wait runs out: that CTA (and,
+                                     in the 2-CTA kernel, its partner) writes none of its tiles, the
+                                     call's device status becomes
                                      CONV2D_ERR_TIMEOUT, the kernel still returns and the context
                                      stays usable */
     CONV2D_OVR_TEST_WAIT_KCYCLES, /* [CONV2D_TEST_WAIT_KCYCLES] f16/bf16 tensor-core kernels: a bounded
                                      wait gives up after this many thousand SM cycles (default
                                      4,000,000, about 2 s) */
+    CONV2D_OVR_TC_CTA2,           /* [CONV2D_TC_CTA2] f16/bf16 im2col / plain kernel: 1 only its 2-CTA
+                                     variants (clusters of two CTAs issuing 2-CTA MMAs, M = 256, each
+                                     CTA loading half of the weight tile), 0 never; unset, the
+                                     chooser weighs them against the single-CTA variants */
     CONV2D_OVR_COUNT
 } conv2d_override_t;
 
@@ -272,7 +277,8 @@ typedef enum {
     CONV2D_FAMILY_CUDA_CORE_TILE = 0,   /* FFMA implicit-GEMM tiles (CONV2D_OVR_CC_TILE ids) */
     CONV2D_FAMILY_TENSOR_CORE = 1,      /* f16/bf16 im2col / plain kernel: (BN, KSUB) pairs */
     CONV2D_FAMILY_TENSOR_CORE_WINDOW = 2, /* f16/bf16 window kernel (CONV2D_OVR_TC_WINVAR ids) */
-    CONV2D_FAMILY_TF32X3 = 3            /* fp32 3xTF32 kernel (CONV2D_OVR_TF_VAR ids) */
+    CONV2D_FAMILY_TF32X3 = 3,           /* fp32 3xTF32 kernel (CONV2D_OVR_TF_VAR ids) */
+    CONV2D_FAMILY_TENSOR_CORE_PAIR = 4  /* f16/bf16 2-CTA im2col / plain kernel: (BN, KSUB) pairs */
 } conv2d_family_t;
 
 /* Number of compiled variants of a family (tests cover every one). */

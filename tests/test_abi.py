@@ -170,7 +170,7 @@ def test_overrides_set_get_and_validation(lib):
     assert lib.conv2d_set_override(0, -2) == 1            # below -1
     assert lib.conv2d_get_override(99, ctypes.byref(v)) == 1
     assert lib.conv2d_get_override(0, None) == 1
-    assert len(conv2d.OVERRIDES) == 15                    # CONV2D_OVR_COUNT in the header
+    assert len(conv2d.OVERRIDES) == 16                    # CONV2D_OVR_COUNT in the header
     text = open(HEADER).read()
     body = text[text.index("typedef enum {\n    CONV2D_OVR_DIRECT"):text.index("CONV2D_OVR_COUNT")]
     names = re.findall(r"CONV2D_OVR_([A-Z0-9_]+)", body)
@@ -199,7 +199,7 @@ def test_variant_counts(lib):
     counts = {f: conv2d.variant_count(f) for f in conv2d.FAMILIES}
     import parity
     assert counts == {"cuda_core_tile": 8, "tensor_core": 7, "tensor_core_window": 9,
-                      "tf32x3": parity.N_TF_VARIANTS}
+                      "tf32x3": parity.N_TF_VARIANTS, "tensor_core_pair": 4}
     n = ctypes.c_int()
     assert lib.conv2d_variant_count(7, ctypes.byref(n)) == 1
     assert lib.conv2d_variant_count(0, None) == 1

@@ -29,12 +29,15 @@ def _lib():
 
 @pytest.fixture
 def force_bn():
+    """Force a single-CTA im2col / plain variant (BN, KSUB)."""
     def set_bn(bn, ksub=None):
         conv2d.set_override("tc_bn", bn)
         conv2d.set_override("tc_ksub", ksub)
+        conv2d.set_override("tc_cta2", 0)
     yield set_bn
     conv2d.set_override("tc_bn", None)
     conv2d.set_override("tc_ksub", None)
+    conv2d.set_override("tc_cta2", None)
 
 
 SHAPES = [
@@ -113,7 +116,7 @@ def test_full_grid_several_rounds_full_output(mode, dtype):
     output compared: every CTA runs three or more persistent rounds."""
     spec = wl.ConvSpec("rounds_full", 96, 8, 28, 28, 64, 3, 3, 1, 1, dtype=dtype, layout="NHWC")
     x, w, b = wl.random_inputs(spec, seed=77)
-    with conv2d.overrides(tc_window=1 if mode == "window" else 0):
+    with conv2d.overrides(tc_window=1 if mode == "window" else 0, tc_cta2=0):
         y, d = run_gpu(spec, x, w, b, "tensor_core")
         assert mode in d.plan(), d.plan()
         err = full_parity(spec, x, w, b, algo="tensor_core")
@@ -138,7 +141,7 @@ IM2COL_SHAPES = [
 def test_im2col_plain_widths_and_rounds(dtype, bn, grid_cap):
     """The im2col / plain kernel at each wide tile; with a capped grid every
     CTA runs many tiles (both accumulators, both store buffers, phase flips)."""
-    with conv2d.overrides(tc_bn=bn, tc_window=0, grid_cap=grid_cap):
+    with conv2d.overrides(tc_bn=bn, tc_window=0, tc_cta2=0, grid_cap=grid_cap):
         for i, (N, C, H, W, K, R, S, st, pad, dil, bias) in enumerate(IM2COL_SHAPES):
             spec = wl.ConvSpec(f"i2c{i}", N, C, H, W, K, R, S, st, pad, dil, dtype=dtype,
                                layout="NHWC", bias=bias)
@@ -147,6 +150,45 @@ def test_im2col_plain_widths_and_rounds(dtype, bn, grid_cap):
             assert f"BN={bn} " in d.plan() and "window" not in d.plan(), d.plan()
             err = full_parity(spec, x, w, b, algo="tensor_core")
             assert err <= TOL[dtype], f"{spec} BN={bn} grid_cap={grid_cap}: err={err}"
+    assert conv2d.get_device_status() == 0
+
+
+# (BN, k-blocks per stage) of every compiled 2-CTA variant
+PAIR_VARIANTS = [(128, 2), (128, 3), (128, 4), (256, 2)]
+
+
+def test_pair_variant_count_matches_library():
+    assert conv2d.variant_count("tensor_core_pair") == len(PAIR_VARIANTS)
+
+
+@pytest.mark.parametrize("grid_cap", [None, 4])
+@pytest.mark.parametrize("bn,ksub", PAIR_VARIANTS)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_two_cta_mma(dtype, bn, ksub, grid_cap):
+    """Clusters of two CTAs issuing 2-CTA MMAs (M = 256): each CTA loads its
+    own A tile and half of the weight tile; with a capped grid every pair
+    runs many work units, and an odd number of M tiles leaves the odd CTA's
+    last tile past M."""
+    with conv2d.overrides(tc_cta2=1, tc_bn=bn, tc_ksub=ksub, tc_window=0, grid_cap=grid_cap):
+        for i, (N, C, H, W, K, R, S, st, pad, dil, bias) in enumerate(IM2COL_SHAPES):
+            spec = wl.ConvSpec(f"c2{i}", N, C, H, W, K, R, S, st, pad, dil, dtype=dtype,
+                               layout="NHWC", bias=bias)
+            x, w, b = wl.random_inputs(spec, seed=950 + i)
+            y, d = run_gpu(spec, x, w, b, "tensor_core")
+            assert " cta2 " in d.plan() and f"BN={bn} " in d.plan() and f"ksub={ksub} " in d.plan(), d.plan()
+            err = full_parity(spec, x, w, b, algo="tensor_core")
+            assert err <= TOL[dtype], f"{spec} BN={bn} ksub={ksub} grid_cap={grid_cap}: err={err}"
+    assert conv2d.get_device_status() == 0
+
+
+def test_two_cta_mma_full_grid_full_output():
+    spec = wl.ConvSpec("c2_full", 96, 64, 28, 28, 128, 3, 3, 1, 1, dtype="bf16", layout="NHWC")
+    x, w, b = wl.random_inputs(spec, seed=79)
+    with conv2d.overrides(tc_cta2=1, tc_window=0):
+        y, d = run_gpu(spec, x, w, b, "tensor_core")
+        assert " cta2 " in d.plan(), d.plan()
+        err = full_parity(spec, x, w, b, algo="tensor_core")
+    assert err <= TOL["bf16"], f"{d.plan()}: err={err}"
     assert conv2d.get_device_status() == 0
 
 
@@ -175,11 +217,12 @@ def test_repeated_launches_are_deterministic():
     assert conv2d.get_device_status() == 0
 
 
+@pytest.mark.parametrize("pair", [0, 1])
 @pytest.mark.parametrize("im2col", ["0", "1"])
-def test_1x1_plain_and_im2col_maps(im2col, force_bn):
+def test_1x1_plain_and_im2col_maps(im2col, pair):
     """1x1 / stride 1 / pad 0 layers read x as a plain [N*H*W, C] matrix; the
-    im2col map must give the same answer."""
-    with conv2d.overrides(tc_im2col=int(im2col)):
+    im2col map must give the same answer (single-CTA and 2-CTA kernels)."""
+    with conv2d.overrides(tc_im2col=int(im2col), tc_cta2=pair):
         for i, (N, C, H, W, K) in enumerate([(3, 64, 7, 7, 264), (1, 72, 5, 9, 64),
                                              (4, 512, 7, 7, 256), (2, 8, 13, 11, 16)]):
             spec = wl.ConvSpec(f"p1x1_{i}", N, C, H, W, K, 1, 1, 1, 0, 1, dtype="bf16",

@@ -33,14 +33,19 @@ def _lib():
     oracle.build()
 
 
-def test_withheld_stage_times_out_and_the_context_stays_usable():
-    # stride 2: the im2col kernel (the window kernel is for stride-1 layers)
+@pytest.mark.parametrize("pair", [0, 1])
+def test_withheld_stage_times_out_and_the_context_stays_usable(pair):
+    # stride 2: the im2col kernel (the window kernel is for stride-1 layers);
+    # pair=1: its 2-CTA variant, where CTA 0 is the pair's MMA issuer and the
+    # odd CTA's copies of the withheld stage land on a barrier that never
+    # completes
     spec = wl.ConvSpec("stall", 4, 64, 14, 14, 128, 3, 3, 2, 1, dtype="bf16", layout="NHWC")
     x, w, b = wl.random_inputs(spec, seed=3)
     assert conv2d.get_device_status() == 0
-    with conv2d.overrides(test_withhold=1, test_wait_kcycles=20000):
+    with conv2d.overrides(test_withhold=1, test_wait_kcycles=20000, tc_cta2=pair):
         y, d = run_gpu(spec, x, w, b, "tensor_core")
         assert "a=im2col" in d.plan(), d.plan()
+        assert (" cta2 " in d.plan()) == bool(pair), d.plan()
     assert conv2d.get_device_status() == STATUS_TIMEOUT
     assert conv2d.get_device_status() == 0          # read and cleared
     err = full_parity(spec, x, w, b, algo="tensor_core")
@@ -48,11 +53,12 @@ def test_withheld_stage_times_out_and_the_context_stays_usable():
     assert conv2d.get_device_status() == 0
 
 
-def test_short_wait_limit_alone_changes_nothing():
+@pytest.mark.parametrize("pair", [0, 1])
+def test_short_wait_limit_alone_changes_nothing(pair):
     # the shortened limit without a withheld stage: every wait still succeeds
     spec = wl.ConvSpec("short_limit", 4, 64, 14, 14, 128, 3, 3, 2, 1, dtype="bf16", layout="NHWC")
     x, w, b = wl.random_inputs(spec, seed=4)
-    with conv2d.overrides(test_wait_kcycles=20000):
+    with conv2d.overrides(test_wait_kcycles=20000, tc_cta2=pair):
         err = full_parity(spec, x, w, b, algo="tensor_core")
     assert err <= TOL["bf16"], err
     assert conv2d.get_device_status() == 0
