@@ -23,7 +23,10 @@ fp16/bf16 layer timed alone (--layer-iters replays, 10 warm-ups, L2 flushed
 before each, median / mean / min), the single signature-matrix convolution
 and the 1x1 kernel-size-sweep layer also as a CUDA graph of 100 back-to-back
 launches (the per-call floor), the eager step and the host time of one C-ABI
-call, an end-to-end step with host<->device copies, the step with the fp32
+call, the end-to-end step (`e2e`: pinned-host x copied in, the 4 layers, y
+copied out to pinned host, all inside the timed region; one CUDA graph per
+step like `value`, and also as eager calls and as a pipelined stream of
+batches), the step with the fp32
 tensor-core (3xTF32) path off, the fp32 FFMA / TF32 / BF16 MMA peaks measured
 by the library's probe kernels (the fp32 roofline denominators), and the
 nvidia-smi clocks sampled across every GPU leg.
@@ -581,13 +584,46 @@ def bench_main(args):
         e1.synchronize()
         if it >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_t = max_over_ranks(statistics.mean(e2e_ms), world)
+    eager_t = max_over_ranks(statistics.mean(e2e_ms), world)
+    # the same step launched like `value`: one CUDA graph holding the copy-in,
+    # the 4 C-ABI calls and the copy-out, events inside it, L2 flushed first
+    def e2e_body():
+        x_buf.copy_(x_pin, non_blocking=True)
+        run_encoder(descs, x_buf, ws, bs, outs)
+        y_pin.copy_(outs[-1], non_blocking=True)
+    e2e_graph = TimedGraph(e2e_body, flush)
+    for _ in range(args.warmup):
+        e2e_graph.replay_ms()
+    e2e_t = max_over_ranks(statistics.mean([e2e_graph.replay_ms() for _ in range(args.steps)]), world)
     pipe_t = max_over_ranks(e2e_pipelined(descs, x_host, ws, bs, outs, args.steps, args.warmup), world)
+
+    # the two copies alone (CUDA events, median of 20): what the host link costs
+    def copy_us(fn):
+        ts = []
+        for it in range(25):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            if it >= 5:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+    h2d_us = copy_us(lambda: x_buf.copy_(x_pin, non_blocking=True))
+    d2h_us = copy_us(lambda: y_pin.copy_(outs[-1], non_blocking=True))
     e2e = {"value": round(step_flops * world / (e2e_t * 1e-3) / 1e12, 4), "unit": "TFLOPS",
            "ms_per_step": round(e2e_t, 5),
            "h2d_bytes_per_step": x_pin.numel() * 4, "d2h_bytes_per_step": y_pin.numel() * 4,
-           "launch": "eager C-ABI calls from Python (host overhead included); one step at a "
-                     "time, L2 flushed before each",
+           "launch": "one CUDA graph per step (as for `value`): pinned-host x copied in, the 4 "
+                     "C-ABI calls, y copied out to pinned host, timing events inside the graph; "
+                     "one step at a time, L2 flushed before each",
+           "copies_alone": {"h2d_us": round(h2d_us, 2), "d2h_us": round(d2h_us, 2),
+                            "h2d_gbs": round(x_pin.numel() * 4 / (h2d_us * 1e3), 1),
+                            "d2h_gbs": round(y_pin.numel() * 4 / (d2h_us * 1e3), 1)},
+           "eager": {"value": round(step_flops * world / (eager_t * 1e-3) / 1e12, 4),
+                     "unit": "TFLOPS", "ms_per_step": round(eager_t, 5),
+                     "note": "the same step as eager C-ABI calls from Python (host overhead "
+                             "included), events around it"},
            "pipelined": {"value": round(step_flops * world / (pipe_t * 1e-3) / 1e12, 4),
                          "unit": "TFLOPS", "ms_per_step": round(pipe_t, 5),
                          "note": "a stream of batches: batch i+1's H2D copy and batch i-1's D2H "
