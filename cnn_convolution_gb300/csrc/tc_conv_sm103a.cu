@@ -23,7 +23,11 @@
 //   * Persistent CTAs (one per SM) loop over output tiles; up to four
 //     accumulators in tensor memory let the main loop run ahead while the
 //     epilogue of earlier tiles (tcgen05.ld, + bias, one round-to-nearest-even
-//     cast, 16-byte stores of each pixel's outputs straight into y) drains.
+//     cast, then TMA stores of each warp's 32-row boxes, or in window mode
+//     16-byte stores of each pixel's outputs straight into y) drains.
+//   * 2-CTA variants of the im2col / plain kernel run as clusters of two
+//     CTAs issuing tcgen05.mma.cta_group::2 (M=256): each CTA loads its own
+//     A tile and half of the weight tile.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = tensor-memory
 // allocator and MMA issuer, warps 2..5 = epilogue (warp w reads accumulator
