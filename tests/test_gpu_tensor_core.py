@@ -192,6 +192,25 @@ def test_two_cta_mma_full_grid_full_output():
     assert conv2d.get_device_status() == 0
 
 
+@pytest.mark.parametrize("mode", ["single", "pair", "window"])
+def test_bias_beyond_shared_staging(mode):
+    """K > 2016: the epilogue reads the bias from global memory instead of its
+    shared-memory copy (ragged last output-channel tile included)."""
+    ovr = {"single": dict(tc_cta2=0, tc_window=0), "pair": dict(tc_cta2=1, tc_window=0),
+           "window": dict(tc_window=1, tc_cta2=0)}[mode]
+    with conv2d.overrides(**ovr):
+        for i, (R, pad) in enumerate([(1, 0), (3, 1)]):
+            spec = wl.ConvSpec(f"bigk{i}", 2, 64, 6, 7, 2072, R, R, 1, pad, 1, dtype="bf16",
+                               layout="NHWC", bias=True)
+            x, w, b = wl.random_inputs(spec, seed=990 + i)
+            y, d = run_gpu(spec, x, w, b, "tensor_core")
+            assert (" cta2 " in d.plan()) == (mode == "pair"), d.plan()
+            assert ("window" in d.plan()) == (mode == "window"), d.plan()
+            err = full_parity(spec, x, w, b, algo="tensor_core")
+            assert err <= TOL["bf16"], f"{spec} {mode}: err={err}"
+    assert conv2d.get_device_status() == 0
+
+
 def test_plan_reports_tensor_core():
     d = conv2d.Conv2dDesc(2, 64, 8, 8, 64, 3, 3, 1, 1, 1, torch.bfloat16, "NHWC")
     assert d.plan().startswith("tensor_core")
