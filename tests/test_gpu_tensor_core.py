@@ -161,7 +161,7 @@ def test_pair_variant_count_matches_library():
     assert conv2d.variant_count("tensor_core_pair") == len(PAIR_VARIANTS)
 
 
-@pytest.mark.parametrize("grid_cap", [None, 4])
+@pytest.mark.parametrize("grid_cap", [None, 1, 3, 4])
 @pytest.mark.parametrize("bn,ksub", PAIR_VARIANTS)
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_two_cta_mma(dtype, bn, ksub, grid_cap):
@@ -176,6 +176,9 @@ def test_two_cta_mma(dtype, bn, ksub, grid_cap):
             x, w, b = wl.random_inputs(spec, seed=950 + i)
             y, d = run_gpu(spec, x, w, b, "tensor_core")
             assert " cta2 " in d.plan() and f"BN={bn} " in d.plan() and f"ksub={ksub} " in d.plan(), d.plan()
+            if grid_cap is not None:   # whole clusters of two, within the cap (at least one cluster)
+                grid = int(d.plan().split("grid=")[1].split()[0])
+                assert grid % 2 == 0 and 2 <= grid <= max(2, grid_cap), d.plan()
             err = full_parity(spec, x, w, b, algo="tensor_core")
             assert err <= TOL[dtype], f"{spec} BN={bn} ksub={ksub} grid_cap={grid_cap}: err={err}"
     assert conv2d.get_device_status() == 0
