@@ -214,6 +214,42 @@ def test_bias_beyond_shared_staging(mode):
     assert conv2d.get_device_status() == 0
 
 
+def test_mixed_kernels_back_to_back():
+    """Four layers enqueued back to back on one stream with no host sync in
+    between, on different tensor-core kernels (2-CTA clusters, window,
+    single-CTA plain, 2-CTA clusters again): the programmatic dependent
+    launches must hand each layer's output to the next.  Every layer is compared with the oracle on
+    the input it actually received."""
+    from parity import sampled_parity
+    specs = [wl.ConvSpec("mix_a", 8, 128, 28, 28, 128, 7, 7, 1, 3, dtype="bf16", layout="NHWC", bias=True),
+             wl.ConvSpec("mix_b", 8, 128, 28, 28, 128, 3, 3, 1, 1, dtype="bf16", layout="NHWC", bias=True),
+             wl.ConvSpec("mix_c", 8, 128, 28, 28, 128, 1, 1, 1, 0, dtype="bf16", layout="NHWC", bias=True),
+             wl.ConvSpec("mix_d", 8, 128, 28, 28, 128, 3, 3, 1, 1, dtype="bf16", layout="NHWC", bias=True)]
+    modes = [dict(tc_cta2=1, tc_window=0), dict(tc_cta2=0, tc_window=1), dict(tc_cta2=0, tc_window=0),
+             dict(tc_cta2=1, tc_window=0)]
+    marks = [" cta2 ", "window", "a=tile", " cta2 "]
+    x0, _, _ = wl.random_inputs(specs[0], seed=1300)
+    cur = x0.cuda()
+    ins, outs, params, plans = [], [], [], []
+    for i, (spec, mode) in enumerate(zip(specs, modes)):
+        _, w, b = wl.random_inputs(spec, seed=1301 + i)
+        d = conv2d.Conv2dDesc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride,
+                              spec.pad, spec.dil, spec.torch_dtype, spec.layout)
+        with conv2d.overrides(**mode):
+            plans.append(d.plan())
+            y = d.forward(cur, w.cuda(), b.cuda())       # enqueued; no synchronisation
+        ins.append(cur)
+        outs.append(y)
+        params.append((w, b))
+        cur = y
+    torch.cuda.synchronize()
+    for spec, plan, mark, xin, y, (w, b) in zip(specs, plans, marks, ins, outs, params):
+        assert mark in plan and (mark == " cta2 " or " cta2 " not in plan), plan
+        err = sampled_parity(spec, xin.cpu(), w, b, y.cpu())
+        assert err <= TOL["bf16"], f"{spec.name} ({plan}): err={err}"
+    assert conv2d.get_device_status() == 0
+
+
 def test_plan_reports_tensor_core():
     d = conv2d.Conv2dDesc(2, 64, 8, 8, 64, 3, 3, 1, 1, 1, torch.bfloat16, "NHWC")
     assert d.plan().startswith("tensor_core")
