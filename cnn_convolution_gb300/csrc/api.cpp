@@ -333,8 +333,10 @@ conv2d_status_t choose_tc(const Shape &s, const DevInfo &d, Plan *p) {
             const double win_bytes = (double)(tr + (s.R - 1) * s.dil) * wp * 128.0;
             double mem = cb * stage_ns(1, win_bytes);
             if (!v.resident) mem += cb * ((rs + v.ksub - 1) / v.ksub) * stage_ns(1, v.ksub * v.bn * 128.0);
-            // few stages in flight: loads are latency-bound unless the weights stay resident
-            if (!v.resident) mem *= 1.25;
+            // few stages in flight: loads are latency-bound unless the weights stay
+            // resident; a third stage hides part of that (measured 2-5 % on the
+            // 3x3 and 5x5 sweep layers)
+            if (!v.resident) mem *= v.stages >= 3 ? 1.15 : 1.25;
             const double mma = kb * 2.0 * v.bn / 1.9;
             const double cost = (double)rounds_for((int64_t)s.N * ((s.P + tr - 1) / tr), v.bn) *
                                 std::max(mem, mma);

@@ -1343,7 +1343,9 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     X(256, 2, 3)
 
 // Window-mode variants: (BN, KSUB, STAGES, window slot KB, window slots,
-// resident weights, resident KB).  Id = position in this list.
+// resident weights, resident KB).  Id = position in this list.  The last two
+// size their window slots to 3x3 and 5x5 layers of rows up to 32 pixels so
+// that a third weight stage fits.
 #define CONV2D_TC_WIN_VARIANTS(X)       \
     X(0, 64, 4, 3, 48, 2, false, 0)     \
     X(1, 64, 6, 2, 48, 2, false, 0)     \
@@ -1353,7 +1355,9 @@ conv2d_status_t launch_tc_window(const Shape &s, const Plan &pl, const Tensors &
     X(5, 64, 4, 4, 32, 2, false, 0)     \
     X(6, 128, 2, 4, 32, 2, false, 0)    \
     X(7, 64, 1, 1, 32, 4, true, 72)     \
-    X(8, 128, 1, 1, 32, 4, true, 72)
+    X(8, 128, 1, 1, 32, 4, true, 72)    \
+    X(9, 128, 3, 3, 25, 2, false, 0)    \
+    X(10, 128, 3, 3, 33, 2, false, 0)
 
 template <typename T>
 conv2d_status_t dispatch_window(const Shape &s, const Plan &pl, const Tensors &t, cudaStream_t st) {

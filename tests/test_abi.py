@@ -198,7 +198,7 @@ def test_variant_counts(lib):
     from cnn_convolution_gb300 import conv2d
     counts = {f: conv2d.variant_count(f) for f in conv2d.FAMILIES}
     import parity
-    assert counts == {"cuda_core_tile": 8, "tensor_core": 7, "tensor_core_window": 9,
+    assert counts == {"cuda_core_tile": 8, "tensor_core": 7, "tensor_core_window": 11,
                       "tf32x3": parity.N_TF_VARIANTS, "tensor_core_pair": 4}
     n = ctypes.c_int()
     assert lib.conv2d_variant_count(7, ctypes.byref(n)) == 1

@@ -308,7 +308,7 @@ WINDOW_SHAPES = [
 # window-mode variants: (BN, window slot KB, resident weights), indexed as in the library
 WINDOW_VARIANTS = {0: (64, 48, False), 1: (64, 48, False), 2: (128, 48, False), 3: (128, 48, False),
                    4: (256, 48, False), 5: (64, 32, False), 6: (128, 32, False), 7: (64, 32, True),
-                   8: (128, 32, True)}
+                   8: (128, 32, True), 9: (128, 25, False), 10: (128, 33, False)}
 
 
 def _window_fits(shape, variant):
