@@ -61,14 +61,57 @@ constexpr int kBK = 64;             // channels per k-block (128 bytes of fp16/b
 constexpr int kThreads = 192;
 constexpr int kATileBytes = kBM * kBK * 2;
 
-// D(tmem) (+)= A(smem) * B(smem)^T, M=128, N from idesc, K=16.
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
+// The 64-bit shared-memory descriptor of smem_desc_sw128 as (low, high)
+// words: the high word is the same for every 128-byte-swizzled K-major tile
+// (stride 1024 B, version 1, swizzle mode 2); the low word holds the start
+// address >> 4 (bits 0-13, below 16384 for any shared-memory address) and the
+// leading byte offset.  Offsets of whole 16-byte units are added to the low
+// word alone: the address field never carries into the next field.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t addr) { return ((addr & 0x3FFFFu) >> 4) | (1u << 16); }
+
+// D(tmem) (+)= A(smem) * B(smem)^T, M=128, N from idesc, K=16 per MMA.
+// One 64-channel k-block: four MMAs (K = 16 each) at descriptor low words
+// a_lo, b_lo advanced by 32 bytes per step; the first accumulates only if
+// `accumulate` is set, the other three always.  One asm statement, 32-bit
+// descriptor arithmetic: the single issuing thread's loop is on the critical
+// path when an MMA takes ~50 cycles (N = 64).
+__device__ __forceinline__ void mma4_f16(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3, b1, b2, b3;\n\t"
+        ".reg .b64 da0, da1, da2, da3, db0, db1, db2, db3;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "setp.eq.b32 q, %3, %3;\n\t"
+        "add.u32 a1, %1, 2;\n\tadd.u32 a2, %1, 4;\n\tadd.u32 a3, %1, 6;\n\t"
+        "add.u32 b1, %2, 2;\n\tadd.u32 b2, %2, 4;\n\tadd.u32 b3, %2, 6;\n\t"
+        "mov.b64 da0, {%1, %5};\n\tmov.b64 da1, {a1, %5};\n\tmov.b64 da2, {a2, %5};\n\tmov.b64 da3, {a3, %5};\n\t"
+        "mov.b64 db0, {%2, %5};\n\tmov.b64 db1, {b1, %5};\n\tmov.b64 db2, {b2, %5};\n\tmov.b64 db3, {b3, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da0, db0, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da1, db1, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da2, db2, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da3, db3, %3, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHi)
+        : "memory");
+}
+
+// The same k-block for the 2-CTA (M = 256) MMA.
+__device__ __forceinline__ void mma4_f16_2cta(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3, b1, b2, b3;\n\t"
+        ".reg .b64 da0, da1, da2, da3, db0, db1, db2, db3;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, %3, %3;\n\t"
+        "add.u32 a1, %1, 2;\n\tadd.u32 a2, %1, 4;\n\tadd.u32 a3, %1, 6;\n\t"
+        "add.u32 b1, %2, 2;\n\tadd.u32 b2, %2, 4;\n\tadd.u32 b3, %2, 6;\n\t"
+        "mov.b64 da0, {%1, %5};\n\tmov.b64 da1, {a1, %5};\n\tmov.b64 da2, {a2, %5};\n\tmov.b64 da3, {a3, %5};\n\t"
+        "mov.b64 db0, {%2, %5};\n\tmov.b64 db1, {b1, %5};\n\tmov.b64 db2, {b2, %5};\n\tmov.b64 db3, {b3, %5};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da0, db0, %3, p;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da1, db1, %3, q;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da2, db2, %3, q;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da3, db3, %3, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHi)
         : "memory");
 }
 
@@ -79,16 +122,6 @@ __host__ __device__ constexpr uint32_t make_idesc(bool bf16, int n, int m = kBM)
            | ((bf16 ? 1u : 0u) << 10)                  // B format
            | ((uint32_t)(n >> 3) << 17)                // N / 8
            | ((uint32_t)(m >> 4) << 24);               // M / 16 (256: a 2-CTA MMA)
-}
-
-__device__ __forceinline__ void mma_f16_2cta(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 // Accumulators in tensor memory: as many BN-column buffers as fit in 512
@@ -444,11 +477,11 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t acc_phase = 0;
         bool ok = true, any = false;
         const uint32_t partner = 1;
-        const uint64_t a_desc0 = smem_desc_sw128(a_tile(0, 0));
-        const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
-        constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);   // 16-byte units
-        constexpr uint64_t kADesc = (uint64_t)(kATileBytes >> 4);
-        constexpr uint64_t kBDesc = (uint64_t)(L::kBTileBytes >> 4);
+        const uint32_t a_lo0 = desc_lo(a_tile(0, 0));
+        const uint32_t b_lo0 = desc_lo(b_tile(0, 0));
+        constexpr uint32_t kStageDesc = (uint32_t)(L::kStageBytes >> 4);   // 16-byte units
+        constexpr uint32_t kADesc = (uint32_t)(kATileBytes >> 4);
+        constexpr uint32_t kBDesc = (uint32_t)(L::kBTileBytes >> 4);
         for (int u = unit0; u < n_units && ok; u += ustep) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit) ||
                 (CTA2 && !mbar_wait_cl(pacce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit))) {
@@ -473,18 +506,13 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 TC_TRACE(1, 2);
                 tc_fence_after();
                 for (int jj = 0; jj < nsub; ++jj) {
-                    const uint64_t ad = a_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)jj * kADesc;
-                    const uint64_t bd = b_desc0 + (uint64_t)stage * kStageDesc + (uint64_t)jj * kBDesc;
-#pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // advance 16 elements (32 bytes) along K inside the swizzled rows
-                        if (CTA2)
-                            mma_f16_2cta(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
-                                         (j | jj | k) != 0 ? 1u : 0u);
-                        else
-                            mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc,
-                                    (j | jj | k) != 0 ? 1u : 0u);
-                    }
+                    const uint32_t a_lo = a_lo0 + (uint32_t)stage * kStageDesc + (uint32_t)jj * kADesc;
+                    const uint32_t b_lo = b_lo0 + (uint32_t)stage * kStageDesc + (uint32_t)jj * kBDesc;
+                    // four K = 16 steps, 32 bytes apart inside the swizzled rows
+                    if constexpr (CTA2)
+                        mma4_f16_2cta(d_tmem, a_lo, b_lo, kIdesc, (j | jj) != 0 ? 1u : 0u);
+                    else
+                        mma4_f16(d_tmem, a_lo, b_lo, kIdesc, (j | jj) != 0 ? 1u : 0u);
                 }
                 any = true;
                 if (CTA2) {
@@ -804,12 +832,10 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         int stage = 0, wslot = 0, acc = 0;
         uint32_t phase = 0, wphase = 0, acc_phase = 0;
         bool ok = true, any = false;
-        const uint64_t b_desc0 = smem_desc_sw128(b_tile(0, 0));
-        constexpr uint64_t kStageDesc = (uint64_t)(L::kStageBytes >> 4);
-        constexpr uint64_t kSubDesc = (uint64_t)(L::kBTileBytes >> 4);
+        constexpr uint32_t kSubDesc32 = (uint32_t)(L::kBTileBytes >> 4);
         // window row shifts in descriptor units (16 bytes; a row is 128 bytes)
-        const uint64_t a_col_step = (uint64_t)(p.dil * 8);
-        const uint64_t a_row_step = (uint64_t)(p.dil * p.Wp * 8 - p.S * p.dil * 8);
+        const uint32_t a_col_step = (uint32_t)(p.dil * 8);
+        const uint32_t a_row_step = (uint32_t)(p.dil * p.Wp * 8 - p.S * p.dil * 8);
         if (RES && !mbar_wait(res_bar, 0, abort_flag, p.status, p.wait_limit)) ok = false;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
@@ -828,10 +854,10 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 // shared-memory address bits, so the base-offset field stays 0.
                 // The issuing thread's loop is on the critical path for N = 64
                 // tiles (an MMA every ~50 cycles), so it does no multiplications.
-                const uint64_t a_desc_w = smem_desc_sw128(win_slot(wslot));
-                uint64_t a_tap = 0;                              // row shift of the tap, descriptor units
+                const uint32_t a_lo_w = desc_lo(win_slot(wslot));
+                uint32_t a_tap = 0;                              // row shift of the tap, descriptor units
                 int s = 0;
-                uint64_t bd_res = RES ? smem_desc_sw128(res_tile(cb, 0)) : 0;
+                uint32_t b_lo_res = RES ? desc_lo(res_tile(cb, 0)) : 0u;
                 for (int t0 = 0; t0 < RS; t0 += KSUB) {
                     const int nsub = min(KSUB, RS - t0);
                     if (!RES) {
@@ -839,17 +865,12 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                         TC_TRACE(1, 2);
                         tc_fence_after();
                     }
-                    const uint64_t bd_stage = b_desc0 + (uint64_t)stage * kStageDesc;
+                    const uint32_t b_lo_stage = desc_lo(b_tile(stage, 0));
 #pragma unroll 3
                     for (int j = 0; j < nsub; ++j) {
-                        const uint64_t ad = a_desc_w + a_tap;
-                        const uint64_t bd = RES ? bd_res : bd_stage + (uint64_t)j * kSubDesc;
-                        const uint32_t first = (cb | (t0 + j)) == 0 ? 1u : 0u;
-                        mma_f16(d_tmem, ad, bd, kIdesc, first ^ 1u);
-#pragma unroll
-                        for (int k = 1; k < kBK / 16; ++k)
-                            mma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), kIdesc, 1u);
-                        if (RES) bd_res += kSubDesc;
+                        const uint32_t b_lo = RES ? b_lo_res : b_lo_stage + (uint32_t)j * kSubDesc32;
+                        mma4_f16(d_tmem, a_lo_w + a_tap, b_lo, kIdesc, (cb | (t0 + j)) != 0 ? 1u : 0u);
+                        if (RES) b_lo_res += kSubDesc32;
                         a_tap += a_col_step;
                         if (++s == p.S) { s = 0; a_tap += a_row_step; }
                     }
