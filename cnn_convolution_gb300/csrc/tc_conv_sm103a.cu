@@ -836,6 +836,12 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         // window row shifts in descriptor units (16 bytes; a row is 128 bytes)
         const uint32_t a_col_step = (uint32_t)(p.dil * 8);
         const uint32_t a_row_step = (uint32_t)(p.dil * p.Wp * 8 - p.S * p.dil * 8);
+        // 3x3 filters with resident weights: the nine taps' row shifts, once
+        // per CTA, for a fully unrolled issue of each window's 36 MMAs
+        const bool taps9 = RES && p.R == 3 && p.S == 3;
+        uint32_t tap_off[9];
+#pragma unroll
+        for (int t = 0; t < 9; ++t) tap_off[t] = (uint32_t)(((t / 3) * p.Wp + (t % 3)) * p.dil * 8);
         if (RES && !mbar_wait(res_bar, 0, abort_flag, p.status, p.wait_limit)) ok = false;
         for (int tile = blockIdx.x; tile < p.total_tiles && ok; tile += gridDim.x) {
             if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
@@ -858,7 +864,14 @@ tc_conv_window_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 uint32_t a_tap = 0;                              // row shift of the tap, descriptor units
                 int s = 0;
                 uint32_t b_lo_res = RES ? desc_lo(res_tile(cb, 0)) : 0u;
-                for (int t0 = 0; t0 < RS; t0 += KSUB) {
+                if (taps9) {
+#pragma unroll
+                    for (int t = 0; t < 9; ++t)
+                        mma4_f16(d_tmem, a_lo_w + tap_off[t], b_lo_res + (uint32_t)t * kSubDesc32, kIdesc,
+                                 (cb | t) != 0 ? 1u : 0u);
+                    any = true;
+                }
+                for (int t0 = 0; t0 < RS && !taps9; t0 += KSUB) {
                     const int nsub = min(KSUB, RS - t0);
                     if (!RES) {
                         if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.wait_limit)) { ok = false; break; }
