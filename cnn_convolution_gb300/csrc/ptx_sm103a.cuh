@@ -411,6 +411,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     return d;
 }
 
+// The same descriptor as (low, high) 32-bit words: the high word is the same
+// for every 128-byte-swizzled K-major tile (stride 1024 B, version 1,
+// swizzle mode 2); the low word holds the start address >> 4 (bits 0-13,
+// below 16384 for any shared-memory address) and the leading byte offset.
+// Offsets of whole 16-byte units are added to the low word alone: the address
+// field never carries into the next field.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t addr) { return ((addr & 0x3FFFFu) >> 4) | (1u << 16); }
+
 // Predicated read-only loads that leave 0 where the predicate is false.  The
 // register is zeroed and then conditionally loaded inside one asm statement,
 // so nothing consumes the loaded value before it is used: a C++ `p ? ld : 0`

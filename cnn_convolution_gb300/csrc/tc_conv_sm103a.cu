@@ -61,15 +61,6 @@ constexpr int kBK = 64;             // channels per k-block (128 bytes of fp16/b
 constexpr int kThreads = 192;
 constexpr int kATileBytes = kBM * kBK * 2;
 
-// The 64-bit shared-memory descriptor of smem_desc_sw128 as (low, high)
-// words: the high word is the same for every 128-byte-swizzled K-major tile
-// (stride 1024 B, version 1, swizzle mode 2); the low word holds the start
-// address >> 4 (bits 0-13, below 16384 for any shared-memory address) and the
-// leading byte offset.  Offsets of whole 16-byte units are added to the low
-// word alone: the address field never carries into the next field.
-constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
-__device__ __forceinline__ uint32_t desc_lo(uint32_t addr) { return ((addr & 0x3FFFFu) >> 4) | (1u << 16); }
-
 // D(tmem) (+)= A(smem) * B(smem)^T, M=128, N from idesc, K=16 per MMA.
 // One 64-channel k-block: four MMAs (K = 16 each) at descriptor low words
 // a_lo, b_lo advanced by 32 bytes per step; the first accumulates only if
