@@ -3,7 +3,7 @@
 // the GPU's attainable fp32 FFMA, TF32 and BF16 MMA rates.  They give the
 // roofline denominators of the fp32 kernels (FFMA for the direct / implicit
 // GEMM kernels, TF32 for the 3xTF32 kernel) a measured value beside the
-// measured HBM and cuBLAS BF16 figures.
+// separately measured HBM copy bandwidth and cuBLAS BF16 throughput.
 
 #include <cuda.h>
 
